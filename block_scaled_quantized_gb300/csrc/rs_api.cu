@@ -1,0 +1,256 @@
+// Host entry points of librs (include/rs.h): argument validation, workspace
+// layout, the device error word, and the launch sequence of each call.
+#include <mutex>
+
+#include "rs.h"
+#include "rs_device.cuh"
+#include "rs_internal.h"
+
+namespace rs {
+
+// Written by kernels whose bounded waits ran out (or on a non-finite tensor
+// amax); read and cleared by rs_get_device_error().
+__device__ uint32_t g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    uint32_t* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Properties of the current device, queried once per device.
+const DeviceInfo* current_device(cudaError_t* why) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *why = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+            *why = e;
+            return nullptr;
+        }
+        d.supported = (major == 10 && minor == 3);  // kernels are built for sm_103a only
+        if (d.supported) {
+            void* p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_device_error)) != cudaSuccess) {
+                *why = e;
+                return nullptr;
+            }
+            d.err = static_cast<uint32_t*>(p);
+        }
+        d.ready = true;
+    }
+    *why = cudaSuccess;
+    return &d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool fmt_ok(int fmt) { return fmt == RS_NVFP4 || fmt == RS_MXFP4; }
+bool k_ok(int K) { return K > 0 && K % 32 == 0; }
+
+rs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? RS_OK : RS_ERR_CUDA; }
+
+// Common checks of the quantizer entry points.
+rs_status check_quant(int fmt, int rows, int K, const void* x, int64_t ldx, const float* alpha, const void* q) {
+    if (!fmt_ok(fmt) || rows < 0) return RS_ERR_INVALID_ARG;
+    if (!k_ok(K)) return RS_ERR_SHAPE;
+    if (rows == 0) return RS_OK;
+    if (!x || !q) return RS_ERR_INVALID_ARG;
+    if (ldx < K) return RS_ERR_INVALID_ARG;
+    if (fmt == RS_NVFP4 && !alpha) return RS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || (ldx % 8) != 0) return RS_ERR_ALIGNMENT;
+    if (fmt == RS_NVFP4 && !aligned4(alpha)) return RS_ERR_ALIGNMENT;
+    if ((int64_t)rows * 2 > (int64_t)0x7FFFFFFF) return RS_ERR_SHAPE;
+    return RS_OK;
+}
+
+rs_status linear_impl(int fmt, bool compensated, int M, int N, int K, const void* x, const void* xq,
+                      const float* alpha_x, const void* wq, const float* alpha_w, void* y, int out_dtype,
+                      void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!fmt_ok(fmt) || M < 0 || N < 0) return RS_ERR_INVALID_ARG;
+    if (out_dtype != RS_OUT_BF16 && out_dtype != RS_OUT_F32) return RS_ERR_INVALID_ARG;
+    if (!k_ok(K)) return RS_ERR_SHAPE;
+    if ((int64_t)M * 2 > (int64_t)0x7FFFFFFF) return RS_ERR_SHAPE;
+    if (M == 0 || N == 0) return RS_OK;
+    if ((x == nullptr) == (xq == nullptr)) return RS_ERR_INVALID_ARG;
+    if (!wq || !y) return RS_ERR_INVALID_ARG;
+    if (fmt == RS_NVFP4 && (!alpha_x || !alpha_w)) return RS_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || (xq && !aligned16(xq)) || !aligned16(wq) || !aligned16(y) ||
+        (ws && !aligned16(ws)))
+        return RS_ERR_ALIGNMENT;
+    if (fmt == RS_NVFP4 && (!aligned4(alpha_x) || !aligned4(alpha_w))) return RS_ERR_ALIGNMENT;
+    const bool quantize_input = x != nullptr;
+    const WorkspaceLayout L = workspace_layout(fmt, compensated, M, N, K, quantize_input);
+    if (L.total > 0 && (!ws || ws_bytes < L.total)) return RS_ERR_WORKSPACE;
+
+    cudaError_t why;
+    const DeviceInfo* dev = current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+
+    const GemmPlan plan = make_gemm_plan(fmt, compensated, M, N, K, dev->num_sms);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    const void* act = xq;
+    if (quantize_input) {
+        void* act_buf = w + L.act_off;
+        cudaError_t e = launch_quantize(fmt, compensated, M, K, x, K, alpha_x, act_buf, stream, dev->num_sms,
+                                        /*pdl=*/true);
+        if (e != cudaSuccess) return RS_ERR_CUDA;
+        act = act_buf;
+    }
+    GemmCall c{};
+    c.xq = act;
+    c.wq = wq;
+    c.alpha_x = alpha_x;
+    c.alpha_w = alpha_w;
+    c.y = y;
+    c.out_f32 = out_dtype == RS_OUT_F32 ? 1 : 0;
+    c.partials = plan.splits > 1 ? reinterpret_cast<float*>(w + L.part_off) : nullptr;
+    c.counters = reinterpret_cast<uint32_t*>(w + L.cnt_off);
+    c.err = dev->err;
+    c.pdl = quantize_input;  // overlap the weight prefetch with our own quantizer only
+    return from_cuda(launch_gemm(plan, c, stream));
+}
+
+}  // namespace
+
+WorkspaceLayout workspace_layout(int fmt, bool compensated, int M, int N, int K, bool quantize_input) {
+    WorkspaceLayout L{};
+    const int rows = compensated ? 2 * M : M;
+    L.act_off = 0;
+    L.act_bytes = quantize_input ? align_up(operand_bytes(fmt, rows, K), 1024) : 0;
+    const GemmPlan worst = make_gemm_plan(fmt, compensated, M, N, K, 0);
+    L.part_off = L.act_bytes;
+    L.part_bytes = align_up(worst.partial_bytes, 1024);
+    L.cnt_off = L.part_off + L.part_bytes;
+    L.cnt_bytes = align_up(worst.counter_bytes, 256);
+    L.total = L.cnt_off + L.cnt_bytes;
+    return L;
+}
+
+uint32_t* device_error_word() {
+    cudaError_t why;
+    const DeviceInfo* d = current_device(&why);
+    return d ? d->err : nullptr;
+}
+
+}  // namespace rs
+
+using namespace rs;
+
+extern "C" {
+
+const char* rs_status_string(rs_status s) {
+    switch (s) {
+        case RS_OK: return "RS_OK";
+        case RS_ERR_INVALID_ARG: return "RS_ERR_INVALID_ARG";
+        case RS_ERR_ALIGNMENT: return "RS_ERR_ALIGNMENT";
+        case RS_ERR_SHAPE: return "RS_ERR_SHAPE";
+        case RS_ERR_UNSUPPORTED: return "RS_ERR_UNSUPPORTED";
+        case RS_ERR_WORKSPACE: return "RS_ERR_WORKSPACE";
+        case RS_ERR_CUDA: return "RS_ERR_CUDA";
+        case RS_ERR_DEVICE_TIMEOUT: return "RS_ERR_DEVICE_TIMEOUT";
+    }
+    return "RS_ERR_UNKNOWN";
+}
+
+int rs_version(void) { return 1; }
+
+size_t rs_operand_bytes(rs_format fmt, int rows, int K) {
+    if (!fmt_ok(fmt) || rows < 0 || !k_ok(K)) return 0;
+    return operand_bytes(fmt, rows, K);
+}
+
+size_t rs_operand_sf_offset(rs_format fmt, int rows, int K) {
+    if (!fmt_ok(fmt) || rows < 0 || !k_ok(K)) return 0;
+    return operand_sf_offset(fmt, rows, K);
+}
+
+size_t rs_act_bytes(rs_format fmt, int rows, int K) { return rs_operand_bytes(fmt, rows, K); }
+
+size_t rs_weight_bytes(rs_format fmt, int N, int K) { return rs_operand_bytes(fmt, N, K); }
+
+size_t rs_workspace_bytes(rs_format fmt, int M, int N, int K, int compensated) {
+    if (!fmt_ok(fmt) || M < 0 || N < 0 || !k_ok(K)) return 0;
+    if (M == 0 || N == 0) return 0;
+    return workspace_layout(fmt, compensated != 0, M, N, K, true).total;
+}
+
+rs_status rs_compute_tensor_scale(const void* x_bf16, int64_t n, float* alpha_out, rs_stream_t stream) {
+    if (n < 0 || !alpha_out || (n > 0 && !x_bf16)) return RS_ERR_INVALID_ARG;
+    if ((x_bf16 && (reinterpret_cast<uintptr_t>(x_bf16) & 1u)) || !aligned4(alpha_out)) return RS_ERR_ALIGNMENT;
+    cudaError_t why;
+    const DeviceInfo* dev = current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    return from_cuda(launch_tensor_scale(x_bf16, n, alpha_out, dev->err, (cudaStream_t)stream, dev->num_sms));
+}
+
+rs_status rs_quantize_fp4(rs_format fmt, int rows, int K, const void* x_bf16, int64_t ldx, const float* alpha,
+                          void* q_out, rs_stream_t stream) {
+    rs_status s = check_quant(fmt, rows, K, x_bf16, ldx, alpha, q_out);
+    if (s != RS_OK || rows == 0) return s;
+    cudaError_t why;
+    const DeviceInfo* dev = current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    return from_cuda(launch_quantize(fmt, false, rows, K, x_bf16, ldx, alpha, q_out, (cudaStream_t)stream,
+                                     dev->num_sms, /*pdl=*/false));
+}
+
+rs_status rs_quantize_residue(rs_format fmt, int M, int K, const void* x_bf16, int64_t ldx, const float* alpha,
+                              void* q_paired_out, rs_stream_t stream) {
+    rs_status s = check_quant(fmt, M, K, x_bf16, ldx, alpha, q_paired_out);
+    if (s != RS_OK || M == 0) return s;
+    cudaError_t why;
+    const DeviceInfo* dev = current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    return from_cuda(launch_quantize(fmt, true, M, K, x_bf16, ldx, alpha, q_paired_out, (cudaStream_t)stream,
+                                     dev->num_sms, /*pdl=*/false));
+}
+
+rs_status rs_linear_w4a4(rs_format fmt, int M, int N, int K, const void* x_bf16, const void* xq,
+                         const float* alpha_x, const void* wq, const float* alpha_w, void* y,
+                         rs_out_dtype out_dtype, void* workspace, size_t ws_bytes, rs_stream_t stream) {
+    return linear_impl(fmt, false, M, N, K, x_bf16, xq, alpha_x, wq, alpha_w, y, out_dtype, workspace, ws_bytes,
+                       (cudaStream_t)stream);
+}
+
+rs_status rs_linear_compensated(rs_format fmt, int M, int N, int K, const void* x_bf16, const void* xq_paired,
+                                const float* alpha_x, const void* wq, const float* alpha_w, void* y,
+                                rs_out_dtype out_dtype, void* workspace, size_t ws_bytes, rs_stream_t stream) {
+    return linear_impl(fmt, true, M, N, K, x_bf16, xq_paired, alpha_x, wq, alpha_w, y, out_dtype, workspace,
+                       ws_bytes, (cudaStream_t)stream);
+}
+
+rs_status rs_get_device_error(rs_stream_t stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return RS_ERR_CUDA;
+    uint32_t* p = device_error_word();
+    if (!p) return RS_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return RS_ERR_CUDA;
+    if (v != 0) {
+        const uint32_t zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return RS_ERR_CUDA;
+    }
+    return (rs_status)v;
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Internal host-side interfaces shared by the librs translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rs {
+
+// Layout of an rs operand (see include/rs.h): codes first, scale atoms at a
+// 1024-byte aligned offset.
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int atom_k_host(int fmt) { return fmt == 0 ? 64 : 128; }
+inline int n_atoms_k_host(int fmt, int K) { return (K + atom_k_host(fmt) - 1) / atom_k_host(fmt); }
+inline size_t operand_sf_offset(int fmt, int rows, int K) {
+    (void)fmt;
+    return align_up((size_t)rows * (size_t)(K / 2), 1024);
+}
+inline size_t operand_sf_bytes(int fmt, int rows, int K) {
+    return (size_t)((rows + 127) / 128) * (size_t)n_atoms_k_host(fmt, K) * 512;
+}
+inline size_t operand_bytes(int fmt, int rows, int K) {
+    return operand_sf_offset(fmt, rows, K) + operand_sf_bytes(fmt, rows, K);
+}
+
+// GEMM launch plan for one linear call.
+struct GemmPlan {
+    int fmt, fold;
+    int M, N, K;
+    int Rb;          // rows of the activation operand (M, or 2M when folded)
+    int bn;          // MMA N: 16, 32, 64, 128 or 256
+    int n_tiles;     // ceil(N / 128)
+    int b_tiles;     // ceil(Rb / bn)
+    int chunks;      // ceil(K / 256)
+    int splits;      // K splits per output tile
+    int stages;      // pipeline depth
+    int tmem_cols;   // tensor-memory columns to allocate
+    size_t smem_bytes;
+    size_t partial_bytes;  // split-K partial sums (0 when splits == 1)
+    size_t counter_bytes;  // one uint32 per output tile
+};
+
+constexpr int kMaxSplits = 32;
+
+// Plan for a given SM count (num_sms <= 0: the worst case used for sizing).
+GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms);
+
+// Workspace layout shared by rs_workspace_bytes and the linear entry points.
+struct WorkspaceLayout {
+    size_t act_off, act_bytes;      // quantized activations (when x_bf16 is given)
+    size_t part_off, part_bytes;    // split-K partials
+    size_t cnt_off, cnt_bytes;      // tile counters
+    size_t total;
+};
+WorkspaceLayout workspace_layout(int fmt, bool compensated, int M, int N, int K, bool quantize_input);
+
+cudaError_t launch_tensor_scale(const void* x, int64_t n, float* alpha, uint32_t* err,
+                                cudaStream_t stream, int num_sms);
+// pdl: launch with programmatic stream serialization and let the dependent
+// GEMM start (its weight prefetch) as soon as this kernel's own wait on the
+// previous grid has returned.  Only for activations consumed by our GEMM.
+cudaError_t launch_quantize(int fmt, bool paired, int rows, int K, const void* x, int64_t ldx,
+                            const float* alpha, void* q_out, cudaStream_t stream, int num_sms, bool pdl);
+
+struct GemmCall {
+    const void* xq;        // activation operand (Rb rows)
+    const void* wq;        // weight operand (N rows)
+    const float* alpha_x;
+    const float* alpha_w;
+    void* y;
+    int out_f32;
+    float* partials;
+    uint32_t* counters;
+    uint32_t* err;
+    bool pdl;              // launch with programmatic stream serialization
+};
+// Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
+cudaError_t launch_gemm(const GemmPlan& plan, const GemmCall& call, cudaStream_t stream);
+
+// Device error word of the current device.
+uint32_t* device_error_word();
+
+}  // namespace rs

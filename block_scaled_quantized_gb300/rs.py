@@ -1,0 +1,175 @@
+"""ctypes binding of librs (include/rs.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls.  Tensors are
+torch tensors on the current CUDA device; their data pointers and the current
+torch stream are passed straight through, and a non-OK status raises
+``RsError``.  All arithmetic runs in librs's CUDA kernels; there is no CPU
+fallback, and importing the binding fails loudly when librs.so is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+NVFP4 = 0
+MXFP4 = 1
+OUT_BF16 = 0
+OUT_F32 = 1
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "librs.so")
+
+STATUS = {0: "RS_OK", 1: "RS_ERR_INVALID_ARG", 2: "RS_ERR_ALIGNMENT", 3: "RS_ERR_SHAPE",
+          4: "RS_ERR_UNSUPPORTED", 5: "RS_ERR_WORKSPACE", 6: "RS_ERR_CUDA", 7: "RS_ERR_DEVICE_TIMEOUT"}
+
+# Every symbol include/rs.h declares.
+EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_offset", "rs_act_bytes",
+           "rs_weight_bytes", "rs_workspace_bytes", "rs_compute_tensor_scale", "rs_quantize_fp4",
+           "rs_quantize_residue", "rs_linear_w4a4", "rs_linear_compensated", "rs_get_device_error"]
+
+
+class RsError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"librs.so not found at {path}: build it with "
+                           "block_scaled_quantized_gb300.build.build() (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "rs_status_string": ([I], ctypes.c_char_p),
+        "rs_version": ([], I),
+        "rs_operand_bytes": ([I, I, I], SZ),
+        "rs_operand_sf_offset": ([I, I, I], SZ),
+        "rs_act_bytes": ([I, I, I], SZ),
+        "rs_weight_bytes": ([I, I, I], SZ),
+        "rs_workspace_bytes": ([I, I, I, I, I], SZ),
+        "rs_compute_tensor_scale": ([P, I64, P, P], I),
+        "rs_quantize_fp4": ([I, I, I, P, I64, P, P, P], I),
+        "rs_quantize_residue": ([I, I, I, P, I64, P, P, P], I),
+        "rs_linear_w4a4": ([I, I, I, I, P, P, P, P, P, P, I, P, SZ, P], I),
+        "rs_linear_compensated": ([I, I, I, I, P, P, P, P, P, P, I, P, SZ, P], I),
+        "rs_get_device_error": ([P], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = load_library()
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("librs takes CUDA tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise RsError(fn, status)
+
+
+# -------------------------------------------------------------- sizes ----
+
+def rs_operand_bytes(fmt: int, rows: int, K: int) -> int:
+    return lib().rs_operand_bytes(fmt, rows, K)
+
+
+def rs_operand_sf_offset(fmt: int, rows: int, K: int) -> int:
+    return lib().rs_operand_sf_offset(fmt, rows, K)
+
+
+def rs_act_bytes(fmt: int, rows: int, K: int) -> int:
+    return lib().rs_act_bytes(fmt, rows, K)
+
+
+def rs_weight_bytes(fmt: int, N: int, K: int) -> int:
+    return lib().rs_weight_bytes(fmt, N, K)
+
+
+def rs_workspace_bytes(fmt: int, M: int, N: int, K: int, compensated: bool) -> int:
+    return lib().rs_workspace_bytes(fmt, M, N, K, int(bool(compensated)))
+
+
+def rs_version() -> int:
+    return lib().rs_version()
+
+
+# -------------------------------------------------------- entry points ----
+
+def rs_compute_tensor_scale(x: torch.Tensor, alpha_out: torch.Tensor, stream=None):
+    _check("rs_compute_tensor_scale",
+           lib().rs_compute_tensor_scale(_ptr(x), x.numel(), _ptr(alpha_out), _stream(stream)))
+
+
+def rs_quantize_fp4(fmt: int, x: torch.Tensor, alpha: torch.Tensor | None, q_out: torch.Tensor,
+                    stream=None):
+    rows, K = x.shape
+    _check("rs_quantize_fp4", lib().rs_quantize_fp4(fmt, rows, K, _ptr(x), x.stride(0), _ptr(alpha),
+                                                    _ptr(q_out), _stream(stream)))
+
+
+def rs_quantize_residue(fmt: int, x: torch.Tensor, alpha: torch.Tensor | None, q_paired_out: torch.Tensor,
+                        stream=None):
+    M, K = x.shape
+    _check("rs_quantize_residue", lib().rs_quantize_residue(fmt, M, K, _ptr(x), x.stride(0), _ptr(alpha),
+                                                            _ptr(q_paired_out), _stream(stream)))
+
+
+def _linear(name: str, fmt: int, M: int, N: int, K: int, x, xq, alpha_x, wq, alpha_w, y, workspace,
+            stream):
+    out = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    fn = getattr(lib(), name)
+    _check(name, fn(fmt, M, N, K, _ptr(x), _ptr(xq), _ptr(alpha_x), _ptr(wq), _ptr(alpha_w), _ptr(y), out,
+                    _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def rs_linear_w4a4(fmt: int, M: int, N: int, K: int, x=None, xq=None, alpha_x=None, wq=None, alpha_w=None,
+                   y=None, workspace=None, stream=None):
+    _linear("rs_linear_w4a4", fmt, M, N, K, x, xq, alpha_x, wq, alpha_w, y, workspace, stream)
+
+
+def rs_linear_compensated(fmt: int, M: int, N: int, K: int, x=None, xq_paired=None, alpha_x=None, wq=None,
+                          alpha_w=None, y=None, workspace=None, stream=None):
+    _linear("rs_linear_compensated", fmt, M, N, K, x, xq_paired, alpha_x, wq, alpha_w, y, workspace, stream)
+
+
+def rs_get_device_error(stream=None) -> int:
+    return lib().rs_get_device_error(_stream(stream))
+
+
+# -------------------------------------------------- buffer conveniences ----
+
+def empty_operand(fmt: int, rows: int, K: int, device=None) -> torch.Tensor:
+    """Uninitialised byte buffer for an rs operand of rows x K."""
+    return torch.empty(rs_operand_bytes(fmt, rows, K), dtype=torch.uint8, device=device or "cuda")
+
+
+def zeros_workspace(fmt: int, M: int, N: int, K: int, compensated: bool, device=None) -> torch.Tensor:
+    """Zero-filled workspace (the split-K tile counters must start at zero)."""
+    n = max(rs_workspace_bytes(fmt, M, N, K, compensated), 16)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")

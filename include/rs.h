@@ -1,0 +1,188 @@
+/*
+ * rs.h - C ABI of librs: residue-compensated block-scaled FP4 linear layers
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The method is ResServe ("ResServe: Accurate and Efficient FP4 LLM Inference
+ * with Residue Compensation", arXiv 2611.08713): activations X are quantized
+ * to NVFP4 or MXFP4 at run time, the quantization residue R = X - QDQ(X) is
+ * quantized to the same format, and a linear layer against offline-quantized
+ * FP4 weights computes Y = X^ W^T + R^ W^T (Sec. 4.2 Eq. 1, full
+ * compensation), with base and residue stacked as paired activation rows of
+ * one block-scaled GEMM and folded on chip (Sec. 4.3 Eq. 2, Sec. 5.1).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers marked (device) are CUDA device pointers on the current device;
+ *   the caller owns and allocates every buffer.  librs never allocates device
+ *   memory and keeps no per-call state beyond a small host-side cache of
+ *   device properties and kernel attributes.
+ * - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream) and is asynchronous.  Host-checkable errors are returned before
+ *   anything is enqueued; a failed launch returns RS_ERR_CUDA.  Device-side
+ *   problems (a bounded wait that ran out, a non-finite tensor amax) set a
+ *   device error word that rs_get_device_error() reads.
+ * - Every device pointer must be 16-byte aligned.  K must be a positive
+ *   multiple of 32 (two E2M1 codes per byte, 16-byte row pitch of the code
+ *   array).  Row counts may be 0 (nothing is enqueued) and need no padding.
+ * - No exception crosses the ABI.
+ *
+ * Formats (Sec. 2, Fig. 1; App. B.2 Eq. 8-10)
+ * -------------------------------------------
+ *   RS_NVFP4: E2M1 codes, one E4M3 block scale per 16 elements along K and
+ *             one fp32 tensor scale alpha.
+ *   RS_MXFP4: E2M1 codes, one E8M0 block scale per 32 elements along K, no
+ *             tensor scale (alpha pointers are ignored and may be NULL).
+ *
+ * Quantization rule (the one the oracle follows): per block, Max = max|x|,
+ * s = fl(Max/6), NVFP4 scale byte = E4M3 round-to-nearest-even of fl(s/alpha)
+ * saturated to 448 (0 when alpha == 0), s~ = fl(alpha * dec(byte)); MXFP4
+ * scale = 2^e with e = floor(log2 Max) - 2 clamped to [-127, 127] (Max == 0
+ * gives e = -127), byte = e + 127.  Elements: v = fl(x * fl(1/s~)) (NVFP4) or
+ * fl(x * 2^-e) (MXFP4), code = E2M1 round-to-nearest-even with saturation at
+ * +-6 and the sign kept.  x^ = fl(s~ * dec(code)); residue r = fl(x - x^),
+ * quantized by the same rule with its own block scales and the same alpha.
+ *
+ * Device layout of a quantized operand ("rs operand", `rows` x K)
+ * ---------------------------------------------------------------
+ * One buffer of rs_operand_bytes(fmt, rows, K) bytes:
+ *   [0, rows*K/2)          codes, row-major, row pitch K/2 bytes, element 2j
+ *                          of a row in the low nibble of byte j.
+ *   [sf_off, +sf_bytes)    block scales, sf_off = rs_operand_sf_offset().
+ *                          Stored as 512-byte atoms.  An atom holds the scales
+ *                          of 128 consecutive rows and 4 consecutive blocks
+ *                          (64 elements of K for NVFP4, 128 for MXFP4).  The
+ *                          atom for row tile t = r/128 and block group
+ *                          g = b/4 is atom number t * ceil(K/(4*bs)) + g; the
+ *                          byte for row r and block b within it is at
+ *                          (r % 32) * 16 + ((r / 32) % 4) * 4 + (b % 4).
+ *                          Rows are padded to a multiple of 128 and blocks to
+ *                          a multiple of 4 with zero bytes.
+ * This is the scale layout the tcgen05 block-scaled MMA reads from tensor
+ * memory after a 32x128b.warpx4 copy, so the quantizer writes what the GEMM
+ * reads and no reordering pass sits between them (App. B.2, Sec. 4.4).
+ *
+ * A paired operand (compensated input; the row-pair layout of Sec. 5.1 and
+ * Fig. 5a) is an rs operand with 2*M rows: row 2j holds the base X^ of token
+ * j and row 2j+1 its residue R^.
+ */
+#ifndef RS_H
+#define RS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RS_API __attribute__((visibility("default")))
+#else
+#define RS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *rs_stream_t; /* binary-compatible with cudaStream_t */
+
+typedef enum {
+    RS_OK = 0,
+    RS_ERR_INVALID_ARG = 1,    /* bad enum, NULL pointer, negative size, ldx < K */
+    RS_ERR_ALIGNMENT = 2,      /* pointer or row pitch not 16-byte aligned */
+    RS_ERR_SHAPE = 3,          /* K not a positive multiple of 32, size limits */
+    RS_ERR_UNSUPPORTED = 4,    /* no GPU with tcgen05 (sm_100 family) */
+    RS_ERR_WORKSPACE = 5,      /* workspace NULL or smaller than rs_workspace_bytes() */
+    RS_ERR_CUDA = 6,           /* a CUDA runtime/driver call or launch failed */
+    RS_ERR_DEVICE_TIMEOUT = 7  /* a bounded device wait ran out (reported later) */
+} rs_status;
+
+typedef enum { RS_NVFP4 = 0, RS_MXFP4 = 1 } rs_format;
+typedef enum { RS_OUT_BF16 = 0, RS_OUT_F32 = 1 } rs_out_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+RS_API const char *rs_status_string(rs_status s);
+
+/* Library ABI version (incremented on incompatible changes). */
+RS_API int rs_version(void);
+
+/* ---- sizes (host only, no CUDA calls) ----------------------------------- */
+
+/* Bytes of an rs operand of `rows` x K (layout above); 0 on invalid input. */
+RS_API size_t rs_operand_bytes(rs_format fmt, int rows, int K);
+/* Byte offset of the scale atoms inside an rs operand. */
+RS_API size_t rs_operand_sf_offset(rs_format fmt, int rows, int K);
+/* Activation operand sizes: `rows` tokens quantized alone (W4A4 input) or,
+ * for rs_quantize_residue, pass rows = 2*M. */
+RS_API size_t rs_act_bytes(rs_format fmt, int rows, int K);
+/* Weight operand size, W [N][K] (nn.Linear layout). */
+RS_API size_t rs_weight_bytes(rs_format fmt, int N, int K);
+/* Workspace that rs_linear_w4a4 / rs_linear_compensated need for these sizes
+ * when given a bf16 input (quantized activations plus split-K partial sums
+ * and tile counters).  The workspace must be zero-filled once before its
+ * first use; every completed call leaves its counter region zeroed again. */
+RS_API size_t rs_workspace_bytes(rs_format fmt, int M, int N, int K, int compensated);
+
+/* ---- tensor scale (App. B.2 Eq. 8) -------------------------------------- */
+
+/* alpha = fl(amax / 2688) over n bf16 values (device); writes one float to
+ * alpha_out (device).  A non-finite amax sets the device error word to
+ * RS_ERR_INVALID_ARG.  The paper computes this scale offline or outside its
+ * timed region (App. C.1); it is a separate call for that reason. */
+RS_API rs_status rs_compute_tensor_scale(const void *x_bf16, int64_t n, float *alpha_out,
+                                  rs_stream_t stream);
+
+/* ---- quantizers (Sec. 4.4, App. B.2 Algorithm 1) ------------------------- */
+
+/* Quantize bf16 rows x[rows][ldx] (device, first K columns used) into an rs
+ * operand q_out (device, rs_operand_bytes(fmt, rows, K) bytes).  Used for the
+ * offline weight quantization (Fig. 1c) and for W4A4 activations.  alpha
+ * (device, one float) is the NVFP4 tensor scale; ignored for MXFP4. */
+RS_API rs_status rs_quantize_fp4(rs_format fmt, int rows, int K, const void *x_bf16, int64_t ldx,
+                          const float *alpha, void *q_out, rs_stream_t stream);
+
+/* Fused base + residue quantizer (Alg. 1; Sec. 4.4): one pass over x[M][ldx]
+ * forms X^, the residue R = X - X^ in registers and R^, and writes the paired
+ * rs operand with 2*M rows (row 2j = X^ of token j, row 2j+1 = R^ of token j)
+ * to q_paired_out (device, rs_act_bytes(fmt, 2*M, K) bytes). */
+RS_API rs_status rs_quantize_residue(rs_format fmt, int M, int K, const void *x_bf16, int64_t ldx,
+                              const float *alpha, void *q_paired_out, rs_stream_t stream);
+
+/* ---- linear layers (Sec. 4.3 Eq. 2, Sec. 5.1 Eq. 4) ----------------------- */
+
+/* Uncompensated W4A4 linear (Fig. 1c): Y[M][N] = alpha_x alpha_w * X^ W^T.
+ * Exactly one of x_bf16 (device, [M][K] contiguous, quantized inside the
+ * call into the workspace) and xq (device, rs operand with M rows) is
+ * non-NULL.  wq: rs operand of W [N][K].  alpha_x / alpha_w (device floats)
+ * are required for NVFP4.  y (device): [M][N] row-major, bf16 or fp32.
+ * workspace (device): at least rs_workspace_bytes(fmt, M, N, K, 0) bytes. */
+RS_API rs_status rs_linear_w4a4(rs_format fmt, int M, int N, int K,
+                         const void *x_bf16, const void *xq, const float *alpha_x,
+                         const void *wq, const float *alpha_w,
+                         void *y, rs_out_dtype out_dtype,
+                         void *workspace, size_t ws_bytes, rs_stream_t stream);
+
+/* Fully compensated linear (M-Ext, Sec. 4.3 Eq. 2):
+ *   Y[M][N] = alpha_x alpha_w * (X^ W^T + R^ W^T).
+ * The GEMM runs in the swapped orientation Z^T = W^ [X^; R^]^T (Eq. 4) with
+ * base and residue as adjacent accumulator columns, and each output is folded
+ * (Y_j = Z_2j + Z_2j+1) in fp32 registers before the scale and the store, so
+ * no expanded result leaves the SM.  Exactly one of x_bf16 (device, [M][K])
+ * and xq_paired (device, paired rs operand, 2*M rows) is non-NULL. */
+RS_API rs_status rs_linear_compensated(rs_format fmt, int M, int N, int K,
+                                const void *x_bf16, const void *xq_paired, const float *alpha_x,
+                                const void *wq, const float *alpha_w,
+                                void *y, rs_out_dtype out_dtype,
+                                void *workspace, size_t ws_bytes, rs_stream_t stream);
+
+/* ---- device error word --------------------------------------------------- */
+
+/* Synchronizes `stream`, then returns and clears the device error word of the
+ * current device: RS_OK, RS_ERR_DEVICE_TIMEOUT (a kernel's bounded wait ran
+ * out; its outputs are invalid and the workspace must be zero-filled again)
+ * or RS_ERR_INVALID_ARG (non-finite tensor amax).  Returns RS_ERR_CUDA if the
+ * synchronization itself fails. */
+RS_API rs_status rs_get_device_error(rs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RS_H */

@@ -1,0 +1,109 @@
+"""librs loads and exports every entry point include/rs.h declares, its size
+functions follow the documented layout, and host-side argument checks reject
+bad calls before anything reaches a GPU (no compute call needs a device here:
+every call below fails validation first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+import layout
+
+
+@pytest.fixture(scope="module")
+def librs():
+    from block_scaled_quantized_gb300 import build, rs
+    build.build()
+    return rs.load_library()
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "rs.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(rs_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for want in ["rs_quantize_fp4", "rs_quantize_residue", "rs_linear_w4a4", "rs_linear_compensated"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(librs):
+    from block_scaled_quantized_gb300 import rs
+    names = _declared_functions()
+    for name in names:
+        assert hasattr(librs, name), name
+    assert sorted(rs.EXPORTS) == names
+
+
+def test_status_strings(librs):
+    for code, name in [(0, b"RS_OK"), (3, b"RS_ERR_SHAPE"), (7, b"RS_ERR_DEVICE_TIMEOUT")]:
+        assert librs.rs_status_string(code) == name
+    assert librs.rs_version() >= 1
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("rows,K", [(1, 32), (3, 96), (16, 4096), (130, 288), (4096, 8192), (28672, 4096)])
+def test_operand_sizes_follow_documented_layout(librs, fmt, rows, K):
+    assert librs.rs_operand_bytes(fmt, rows, K) == layout.operand_bytes(fmt, rows, K)
+    assert librs.rs_operand_sf_offset(fmt, rows, K) == layout.sf_offset(rows, K)
+    assert librs.rs_act_bytes(fmt, rows, K) == librs.rs_weight_bytes(fmt, rows, K)
+
+
+def test_size_functions_reject_bad_shapes(librs):
+    assert librs.rs_operand_bytes(0, 4, 48) == 0       # K % 32 != 0
+    assert librs.rs_operand_bytes(2, 4, 64) == 0       # bad format
+    assert librs.rs_operand_bytes(0, -1, 64) == 0
+    assert librs.rs_workspace_bytes(0, 0, 128, 64, 1) == 0
+    assert librs.rs_workspace_bytes(0, 8, 4096, 4096, 1) >= librs.rs_act_bytes(0, 16, 4096)
+
+
+FAKE = 1 << 20          # 16-byte aligned fake device address (never dereferenced)
+FAKE_ODD = FAKE + 8
+
+
+def _lin(librs, fn="rs_linear_compensated", fmt=0, M=8, N=256, K=256, x=FAKE, xq=None, ax=FAKE, w=FAKE,
+         aw=FAKE, y=FAKE, out=0, ws=FAKE, wsb=None):
+    if wsb is None:
+        wsb = librs.rs_workspace_bytes(fmt, M, N, K, 1)
+    return getattr(librs, fn)(fmt, M, N, K, x, xq, ax, w, aw, y, out, ws, wsb, None)
+
+
+def test_linear_argument_checks(librs):
+    assert _lin(librs, fmt=5) == 1                            # bad format
+    assert _lin(librs, K=48) == 3                             # K % 32
+    assert _lin(librs, K=0) == 3
+    assert _lin(librs, M=-1) == 1
+    assert _lin(librs, M=0) == 0                              # nothing to do
+    assert _lin(librs, N=0) == 0
+    assert _lin(librs, x=None, xq=None) == 1                  # need exactly one input
+    assert _lin(librs, x=FAKE, xq=FAKE) == 1
+    assert _lin(librs, w=None) == 1
+    assert _lin(librs, y=None) == 1
+    assert _lin(librs, ax=None) == 1                          # NVFP4 needs alpha
+    assert _lin(librs, out=3) == 1
+    assert _lin(librs, x=FAKE_ODD) == 2                       # alignment
+    assert _lin(librs, y=FAKE_ODD) == 2
+    assert _lin(librs, w=FAKE_ODD) == 2
+    assert _lin(librs, wsb=16) == 5                           # workspace too small
+    assert _lin(librs, ws=None) == 5
+    assert _lin(librs, fn="rs_linear_w4a4", wsb=0) == 5
+
+
+def test_quantizer_argument_checks(librs):
+    q = librs.rs_quantize_residue
+    assert q(3, 4, 64, FAKE, 64, FAKE, FAKE, None) == 1
+    assert q(0, 4, 40, FAKE, 64, FAKE, FAKE, None) == 3
+    assert q(0, 4, 64, FAKE, 32, FAKE, FAKE, None) == 1       # ldx < K
+    assert q(0, 4, 64, FAKE, 68, FAKE, FAKE, None) == 2       # row pitch not 16-byte aligned
+    assert q(0, 4, 64, FAKE_ODD, 64, FAKE, FAKE, None) == 2
+    assert q(0, 4, 64, FAKE, 64, None, FAKE, None) == 1       # NVFP4 needs alpha
+    assert q(0, 0, 64, None, 64, None, None, None) == 0       # empty input
+    f = librs.rs_quantize_fp4
+    assert f(0, 4, 64, None, 64, FAKE, FAKE, None) == 1
+    assert f(1, 4, 64, FAKE, 64, None, FAKE_ODD, None) == 2
+    assert librs.rs_compute_tensor_scale(FAKE, -1, FAKE, None) == 1
+    assert librs.rs_compute_tensor_scale(FAKE, 16, None, None) == 1

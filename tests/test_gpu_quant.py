@@ -1,0 +1,123 @@
+"""GPU parity of the quantizers through the C ABI: codes and scale bytes
+bit-exact against the oracle (ResServe App. B.2 Eq. 8-10, Alg. 1), padding
+scale bytes zero, tensor scale bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import layout
+from gpu_util import DEV, gpu_quantize, gpu_tensor_scale, unpack
+from block_scaled_quantized_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from block_scaled_quantized_gb300 import build
+    build.build()
+    import oracle
+    oracle.build()
+
+
+@pytest.mark.parametrize("recipe", ["gauss_outlier_k2048", "attn_proj_k4096", "mlp_down",
+                                    "mx_k5120_n27648", "prefill_k8192"])
+def test_tensor_scale_bit_exact(recipe):
+    import oracle
+    x = workloads.make_x(recipe, 8)
+    a = gpu_tensor_scale(x.to(DEV)).cpu().numpy()[0]
+    assert a == oracle.tensor_scale(workloads.bf16_bits(x))
+    w = workloads.make_w(recipe, N=256)
+    a = gpu_tensor_scale(w.to(DEV)).cpu().numpy()[0]
+    assert a == oracle.tensor_scale(workloads.bf16_bits(w))
+
+
+def _check(fmt, x, paired, alpha=None):
+    import oracle
+    rows, K = x.shape
+    xb = workloads.bf16_bits(x.cpu())
+    a_or = oracle.tensor_scale(xb) if (fmt == 0 and alpha is None) else np.float32(alpha or 0)
+    a_gpu = torch.tensor([a_or], dtype=torch.float32, device=DEV) if fmt == 0 else None
+    buf = gpu_quantize(fmt, x.to(DEV) if not x.is_cuda else x, a_gpu, paired)
+    host = buf.cpu().numpy()
+    if paired:
+        ref = oracle.quantize_residue(fmt, xb, a_or)
+        codes, sf = layout.unpack_operand(host, fmt, 2 * rows, K)
+        np.testing.assert_array_equal(codes[0::2], ref["codes_x"])
+        np.testing.assert_array_equal(sf[0::2], ref["sf_x"])
+        np.testing.assert_array_equal(codes[1::2], ref["codes_r"])
+        np.testing.assert_array_equal(sf[1::2], ref["sf_r"])
+        assert not np.any(layout.padding_sf_bytes(host, fmt, 2 * rows, K))
+    else:
+        cx, sx, _ = oracle.quantize(fmt, xb, a_or)
+        codes, sf = layout.unpack_operand(host, fmt, rows, K)
+        np.testing.assert_array_equal(codes, cx)
+        np.testing.assert_array_equal(sf, sx)
+        assert not np.any(layout.padding_sf_bytes(host, fmt, rows, K))
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("paired", [False, True])
+@pytest.mark.parametrize("rows,K", [(1, 32), (1, 2048), (2, 96), (3, 288), (7, 1024), (8, 4096),
+                                    (64, 160), (130, 512), (257, 64)])
+def test_quantizer_bit_exact_ragged(fmt, paired, rows, K):
+    x = workloads.make_x("attn_proj_k4096", rows, K=K, seed=rows * 1000 + K)
+    _check(fmt, x, paired)
+
+
+@pytest.mark.parametrize("fmt,recipe,M", [(0, "gauss_outlier_k2048", 1), (0, "attn_proj_k4096", 8),
+                                          (0, "mlp_gate_up", 8), (0, "mlp_down", 8),
+                                          (1, "mx_k5120_n27648", 128), (0, "prefill_k8192", 64)])
+def test_quantizer_bit_exact_workloads(fmt, recipe, M):
+    x = workloads.make_x(recipe, M)
+    _check(fmt, x, True)
+    _check(fmt, x, False)
+
+
+@pytest.mark.parametrize("fmt,recipe", [(0, "attn_proj_k4096"), (0, "mlp_gate_up"), (1, "mx_k5120_n27648"),
+                                        (0, "prefill_k8192")])
+def test_weight_quantization_bit_exact(fmt, recipe):
+    w = workloads.make_w(recipe, N=384)
+    _check(fmt, w, False)
+
+
+def test_quantizer_strided_rows_and_edge_values():
+    import oracle
+    # rows of a wider buffer (ldx > K), plus zeros, -0, tiny and huge values
+    wide = workloads.random_bf16((5, 320), seed=3).to(DEV)
+    x = wide[:, :256]
+    assert x.stride(0) == 320
+    xc = x.cpu().clone()
+    xc[0, :16] = 0.0
+    xc[1, :16] = -0.0
+    xc[2, 16] = 1e-30
+    xc[2, 17] = 3e30
+    xc[3, 32:64] = 1.0
+    wide[:, :256] = xc.to(DEV)
+    for fmt in (0, 1):
+        for paired in (False, True):
+            xb = workloads.bf16_bits(xc)
+            a = oracle.tensor_scale(xb) if fmt == 0 else np.float32(0)
+            ag = torch.tensor([a], device=DEV) if fmt == 0 else None
+            buf = gpu_quantize(fmt, x, ag, paired)
+            rows_out = 10 if paired else 5
+            codes, sf = unpack(buf, fmt, rows_out, 256)
+            if paired:
+                ref = oracle.quantize_residue(fmt, xb, a)
+                np.testing.assert_array_equal(codes[0::2], ref["codes_x"])
+                np.testing.assert_array_equal(codes[1::2], ref["codes_r"])
+                np.testing.assert_array_equal(sf[0::2], ref["sf_x"])
+                np.testing.assert_array_equal(sf[1::2], ref["sf_r"])
+            else:
+                cx, sx, _ = oracle.quantize(fmt, xb, a)
+                np.testing.assert_array_equal(codes, cx)
+                np.testing.assert_array_equal(sf, sx)
+
+
+def test_alpha_zero_gives_zero_operand():
+    x = torch.zeros((4, 64), dtype=torch.bfloat16, device=DEV)
+    a = gpu_tensor_scale(x)
+    assert a.item() == 0.0
+    buf = gpu_quantize(0, x, a, paired=True)
+    codes, sf = unpack(buf, 0, 8, 64)
+    assert not codes.any() and not sf.any()
