@@ -141,14 +141,14 @@ class Linear:
             rs.rs_compute_tensor_scale(self.x, self.ax)   # calibrated activation scale
             rs.rs_compute_tensor_scale(wg, self.aw)
         wq = torch.empty(rs.rs_weight_bytes(fmt, self.N, self.K), dtype=torch.uint8, device=dev)
-        rs.rs_quantize_fp4(fmt, wg, self.aw if fmt == rs.NVFP4 else None, wq)
+        rs.rs_quantize_weight(fmt, wg, self.aw if fmt == rs.NVFP4 else None, wq)
         del wg
         self.wq_bytes = wq.numel()
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         n = max(2, math.ceil(2 * l2 / self.wq_bytes) + 1) if copies_for_l2 else 1
         self.wqs = [wq] + [wq.clone() for _ in range(n - 1)]
         self.y = torch.empty((M, self.N), dtype=out_dtype or torch.bfloat16, device=dev)
-        self.ws = rs.zeros_workspace(fmt, M, self.N, self.K, compensated)
+        self.ws = rs.empty_workspace(fmt, M, self.N, self.K, compensated)
         rows = 2 * M if compensated else M
         self.xq = torch.empty(rs.rs_act_bytes(fmt, rows, self.K), dtype=torch.uint8, device=dev)
         quant = rs.rs_quantize_residue if compensated else rs.rs_quantize_fp4

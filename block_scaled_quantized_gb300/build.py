@@ -45,20 +45,24 @@ def _digest(extra: list[str]) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile librs.so if its sources changed; returns the library path."""
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          name: str = "librs") -> str:
+    """Compile <name>.so if its sources changed; returns the library path.
+    ``name``/``extra`` select a variant, e.g. the trace build
+    (``name="librs_trace", extra=["-DRS_TRACE"]``)."""
     extra = list(extra or [])
     os.makedirs(BUILD, exist_ok=True)
-    stamp = os.path.join(BUILD, "librs.stamp")
+    lib_path = os.path.join(BUILD, name + ".so")
+    stamp = os.path.join(BUILD, name + ".stamp")
     digest = _digest(extra)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
+                return lib_path
     cc = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, name + "_" + src.replace(".cu", ".o"))
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -71,15 +75,15 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -1,5 +1,5 @@
-// Host entry points of librs (include/rs.h): argument validation, workspace
-// layout, the device error word, and the launch sequence of each call.
+// Host entry points of librs (include/rs.h): argument validation, the device
+// error word, and the launch sequence of each call.
 #include <mutex>
 
 #include "rs.h"
@@ -96,53 +96,36 @@ rs_status linear_impl(int fmt, bool compensated, int M, int N, int K, const void
         return RS_ERR_ALIGNMENT;
     if (fmt == RS_NVFP4 && (!aligned4(alpha_x) || !aligned4(alpha_w))) return RS_ERR_ALIGNMENT;
     const bool quantize_input = x != nullptr;
-    const WorkspaceLayout L = workspace_layout(fmt, compensated, M, N, K, quantize_input);
-    if (L.total > 0 && (!ws || ws_bytes < L.total)) return RS_ERR_WORKSPACE;
+    if (quantize_input && (!ws || ws_bytes < workspace_bytes(fmt, compensated, M, K))) return RS_ERR_WORKSPACE;
 
     cudaError_t why;
     const DeviceInfo* dev = current_device(&why);
     if (!dev) return RS_ERR_CUDA;
     if (!dev->supported) return RS_ERR_UNSUPPORTED;
 
-    const GemmPlan plan = make_gemm_plan(fmt, compensated, M, N, K, dev->num_sms);
-    uint8_t* w = static_cast<uint8_t*>(ws);
-    const void* act = xq;
-    if (quantize_input) {
-        void* act_buf = w + L.act_off;
-        cudaError_t e = launch_quantize(fmt, compensated, M, K, x, K, alpha_x, act_buf, stream, dev->num_sms,
-                                        /*pdl=*/true);
-        if (e != cudaSuccess) return RS_ERR_CUDA;
-        act = act_buf;
-    }
+    const GemmPlan plan = make_gemm_plan(fmt, compensated, M, N, K, dev->num_sms, /*allow_fused=*/quantize_input);
     GemmCall c{};
-    c.xq = act;
     c.wq = wq;
     c.alpha_x = alpha_x;
     c.alpha_w = alpha_w;
     c.y = y;
     c.out_f32 = out_dtype == RS_OUT_F32 ? 1 : 0;
-    c.partials = plan.splits > 1 ? reinterpret_cast<float*>(w + L.part_off) : nullptr;
-    c.counters = reinterpret_cast<uint32_t*>(w + L.cnt_off);
     c.err = dev->err;
-    c.pdl = quantize_input;  // overlap the weight prefetch with our own quantizer only
+    if (quantize_input && plan.fused) {
+        c.x = x;  // the GEMM quantizes its own K slices: one launch
+    } else if (quantize_input) {
+        void* act = ws;
+        cudaError_t e = launch_quantize(fmt, compensated, M, K, x, K, alpha_x, act, stream, dev->num_sms,
+                                        /*pdl=*/true);
+        if (e != cudaSuccess) return RS_ERR_CUDA;
+        c.xq = act;
+    } else {
+        c.xq = xq;
+    }
     return from_cuda(launch_gemm(plan, c, stream));
 }
 
 }  // namespace
-
-WorkspaceLayout workspace_layout(int fmt, bool compensated, int M, int N, int K, bool quantize_input) {
-    WorkspaceLayout L{};
-    const int rows = compensated ? 2 * M : M;
-    L.act_off = 0;
-    L.act_bytes = quantize_input ? align_up(operand_bytes(fmt, rows, K), 1024) : 0;
-    const GemmPlan worst = make_gemm_plan(fmt, compensated, M, N, K, 0);
-    L.part_off = L.act_bytes;
-    L.part_bytes = align_up(worst.partial_bytes, 1024);
-    L.cnt_off = L.part_off + L.part_bytes;
-    L.cnt_bytes = align_up(worst.counter_bytes, 256);
-    L.total = L.cnt_off + L.cnt_bytes;
-    return L;
-}
 
 uint32_t* device_error_word() {
     cudaError_t why;
@@ -184,12 +167,15 @@ size_t rs_operand_sf_offset(rs_format fmt, int rows, int K) {
 
 size_t rs_act_bytes(rs_format fmt, int rows, int K) { return rs_operand_bytes(fmt, rows, K); }
 
-size_t rs_weight_bytes(rs_format fmt, int N, int K) { return rs_operand_bytes(fmt, N, K); }
+size_t rs_weight_bytes(rs_format fmt, int N, int K) {
+    if (!fmt_ok(fmt) || N < 0 || !k_ok(K)) return 0;
+    return weight_bytes(fmt, N, K);
+}
 
 size_t rs_workspace_bytes(rs_format fmt, int M, int N, int K, int compensated) {
     if (!fmt_ok(fmt) || M < 0 || N < 0 || !k_ok(K)) return 0;
     if (M == 0 || N == 0) return 0;
-    return workspace_layout(fmt, compensated != 0, M, N, K, true).total;
+    return workspace_bytes(fmt, compensated != 0, M, K);
 }
 
 rs_status rs_compute_tensor_scale(const void* x_bf16, int64_t n, float* alpha_out, rs_stream_t stream) {
@@ -212,6 +198,18 @@ rs_status rs_quantize_fp4(rs_format fmt, int rows, int K, const void* x_bf16, in
     if (!dev->supported) return RS_ERR_UNSUPPORTED;
     return from_cuda(launch_quantize(fmt, false, rows, K, x_bf16, ldx, alpha, q_out, (cudaStream_t)stream,
                                      dev->num_sms, /*pdl=*/false));
+}
+
+rs_status rs_quantize_weight(rs_format fmt, int N, int K, const void* w_bf16, int64_t ldw, const float* alpha,
+                             void* wq_out, rs_stream_t stream) {
+    rs_status s = check_quant(fmt, N, K, w_bf16, ldw, alpha, wq_out);
+    if (s != RS_OK || N == 0) return s;
+    cudaError_t why;
+    const DeviceInfo* dev = current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    return from_cuda(launch_quantize_weight(fmt, N, K, w_bf16, ldw, alpha, wq_out, (cudaStream_t)stream,
+                                            dev->num_sms));
 }
 
 rs_status rs_quantize_residue(rs_format fmt, int M, int K, const void* x_bf16, int64_t ldx, const float* alpha,

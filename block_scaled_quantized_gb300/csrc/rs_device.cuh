@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace rs {
@@ -29,6 +30,15 @@ __host__ __device__ constexpr int block_elems(int fmt) { return fmt == 0 ? kNvBl
 
 // Elements of K covered by one scale atom (4 blocks).
 __host__ __device__ constexpr int atom_k(int fmt) { return kAtomBlocks * block_elems(fmt); }
+
+// Tiled weight operand: one block per (128 output channels, 256 K) holding
+// the codes (128 rows x 128 bytes, 128-byte-swizzled shared-memory image)
+// followed by the block's scale atoms.
+constexpr int kWeightCodeBytes = 128 * 128;
+__host__ __device__ constexpr int weight_atoms_per_block(int fmt) { return 256 / atom_k(fmt); }
+__host__ __device__ constexpr uint32_t weight_block_bytes(int fmt) {
+    return (uint32_t)kWeightCodeBytes + (uint32_t)weight_atoms_per_block(fmt) * (uint32_t)kAtomBytes;
+}
 
 // Byte offset of the scale of (row r, block b) inside the scale region of an
 // operand whose atoms per row tile along K is n_atoms_k.
@@ -56,6 +66,41 @@ __device__ __forceinline__ float e2m1_decode(uint32_t c) {
     const uint32_t twice = i < 2u ? i : ((2u + (i & 1u)) << ((i >> 1) - 1u));
     const float m = (float)twice * 0.5f;
     return (c & 8u) ? -m : m;
+}
+
+// Eight fp32 values -> eight E2M1 codes (element e in bits 4e..4e+3) with the
+// hardware conversion (round to nearest even, saturating to +-6, sign kept;
+// identical to e2m1_encode on every input, including ties and signed zero).
+__device__ __forceinline__ uint32_t e2m1_encode8(const float (&v)[8]) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return r;
+}
+
+// Eight E2M1 codes (as packed by e2m1_encode8) -> eight exact fp32 values.
+__device__ __forceinline__ void e2m1_decode8(uint32_t codes, float (&v)[8]) {
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(codes));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 p = *reinterpret_cast<const __half2*>(&h[i]);
+        v[2 * i] = __low2float(p);
+        v[2 * i + 1] = __high2float(p);
+    }
 }
 
 // 2^e as fp32 for e in [-126, 127].
@@ -308,11 +353,62 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// --------------------------------------------------- clusters and DSMEM --
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Whole-cluster barrier; every thread of every CTA in the cluster executes
+// it (warp-converged).  Release/acquire order shared-memory traffic.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_dsmem(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------ named CTA barriers --
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+
+// ------------------------------------------------------ trace build only --
+// Built with -DRS_TRACE, kernels stamp the global timer at phase boundaries
+// into a caller-provided buffer (16 slots per CTA); a normal build compiles
+// the marks away.
+#ifdef RS_TRACE
+#define RS_TRACE_MARK(buf, slot)                                                              \
+    do {                                                                                      \
+        if (buf) {                                                                            \
+            const size_t cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x; \
+            (buf)[cta * 16 + (slot)] = rs::globaltimer_ns();                                  \
+        }                                                                                     \
+    } while (0)
+#define RS_TRACE_VALUE(buf, slot, v)                                                          \
+    do {                                                                                      \
+        if (buf) {                                                                            \
+            const size_t cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x; \
+            (buf)[cta * 16 + (slot)] = (uint64_t)(v);                                         \
+        }                                                                                     \
+    } while (0)
+#else
+#define RS_TRACE_MARK(buf, slot) do { } while (0)
+#define RS_TRACE_VALUE(buf, slot, v) do { } while (0)
+#endif
 
 // ---------------------------------------------- programmatic launch (PDL) --
 

@@ -2,28 +2,43 @@
 // the W4A4 and the residue-compensated linear layer.
 //
 // Swapped orientation (ResServe Sec. 5.1, Eq. 4): the MMA's 128-row A
-// operand is a tile of 128 output channels of W^ [N][K]; the narrow B operand
-// is the activation operand (M token rows, or 2M rows when base and residue
-// are paired as adjacent rows, Sec. 5.1 "row-pair" layout), so Z^T tiles are
-// 128 channels x bn activation rows.  Block scales travel as 512-byte atoms:
-// TMA brings them into shared memory next to the code tiles and
-// tcgen05.cp (32x128b.warpx4) moves them into tensor memory, where the
-// kind::mxf4nvf4 block-scaled MMA reads them.
+// operand is a tile of 128 output channels of W^; the narrow B operand holds
+// the activation rows (M tokens, or 2M rows when base and residue are paired
+// as adjacent rows, the row-pair layout of Sec. 5.1 / Fig. 5a), so each
+// accumulator tile is Z^T: 128 channels x bn activation rows.
 //
-// Fold (Sec. 4.3 Eq. 2; Sec. 5.1): with paired rows, the base and residue
-// products of token j land in accumulator columns 2j and 2j+1; a 32x32b
-// tensor-memory load hands both to the same thread, which adds them in fp32
-// before scaling and storing, so the expanded Z never leaves the SM.
+// Data movement:
+//  * weights are stored offline as contiguous (128 channels x 256 K) blocks
+//    that already hold the 128-byte-swizzled shared-memory image of the codes
+//    plus their scale atoms, so each pipeline stage is one bulk copy of
+//    18 KB (NVFP4) / 17 KB (MXFP4) of consecutive bytes;
+//  * activation codes come either from a TMA tensor load of the row-major
+//    activation operand, or, for small M, from a quantizing prologue that
+//    converts the CTA's slice of the bf16 input straight into shared memory
+//    (Alg. 1 fused into the GEMM: one launch per linear layer);
+//  * scale atoms go shared memory -> tensor memory with tcgen05.cp
+//    (32x128b.warpx4), where the kind::mxf4nvf4 block-scaled MMA reads them.
 //
-// Split-K: when the output tiles alone cannot occupy every SM, each tile's K
-// range is split; every split stores its folded fp32 partial to the
-// workspace, and the last split to finish (a per-tile counter, no waiting)
-// sums the partials in split order and writes Y, then re-arms the counter.
+// Fold (Sec. 4.3 Eq. 2): with paired rows, the base and residue products of
+// token j are accumulator columns 2j and 2j+1; a 32x32b tensor-memory load
+// gives both to one thread, which adds them in fp32 before scaling and
+// storing, so the expanded Z never leaves the SM.
 //
-// Warp roles (192 threads): warps 0-3 epilogue (tensor-memory lane quarters
-// 0-3), warp 4 TMA producer, warp 5 TMEM allocator and MMA issuer.  Every
-// wait is bounded (about one second); a wait that runs out sets the device
-// error word and an abort flag, and the CTA drains its copies and exits.
+// Split-K: when the output tiles alone cannot keep every SM streaming
+// weights, the K range of each tile is split across the CTAs of a thread-
+// block cluster (up to 8); each CTA leaves its folded fp32 partial in shared
+// memory and, after a cluster barrier, every CTA sums one slice of the
+// outputs over all partners' shared memory (DSMEM) in a fixed order.
+//
+// Programmatic dependent launch: the kernel releases its dependents at once
+// and starts streaming weights before waiting for the previous grid; only
+// the activation / output accesses come after that wait.
+//
+// Warp roles (192 threads): warps 0-3 quantizer (fused plans) and epilogue
+// (tensor-memory lane quarters 0-3), warp 4 bulk/TMA producer, warp 5 TMEM
+// allocator and MMA issuer.  Every wait is bounded (about one second); a wait
+// that runs out sets the device error word and an abort flag, and the CTA
+// drains its copies and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -32,89 +47,110 @@
 
 #include "rs_device.cuh"
 #include "rs_internal.h"
+#include "rs_quant_core.cuh"
 
 namespace rs {
 
 constexpr int kThreads = 192;
 constexpr int kMaxStages = 8;
-constexpr uint32_t kTileA = 128 * 128;  // 128 channels x 128 bytes (256 K)
 constexpr size_t kSmemLimit = 232448;   // 227 KB opt-in per block
-
-__host__ __device__ constexpr int atoms_per_chunk(int fmt) { return 256 / (fmt == 0 ? 64 : 128); }
-__host__ __device__ constexpr int b_atom_tiles(int bn) { return (bn + 127) / 128; }
-__host__ __device__ constexpr uint32_t stage_bytes(int fmt, int bn) {
-    return (kTileA + (uint32_t)bn * 128u + (uint32_t)atoms_per_chunk(fmt) * 512u * (1u + (uint32_t)b_atom_tiles(bn)) + 1023u) /
-           1024u * 1024u;
-}
-__host__ __device__ constexpr int sf_cols_per_stage(int fmt, int bn) {
-    return atoms_per_chunk(fmt) * 4 * (1 + b_atom_tiles(bn));
-}
 constexpr uint32_t kCtrlBytes = 256;
 
+__host__ __device__ constexpr int b_atom_tiles(int bn) { return (bn + 127) / 128; }
+// Shared-memory bytes of one activation stage: codes (bn rows x 128 bytes)
+// plus its scale atoms, rounded to the 1024-byte swizzle period.
+__host__ __device__ constexpr uint32_t b_stage_bytes(int fmt, int bn) {
+    return ((uint32_t)bn * 128u + (uint32_t)weight_atoms_per_block(fmt) * (uint32_t)b_atom_tiles(bn) * 512u + 1023u) /
+           1024u * 1024u;
+}
+__host__ __device__ constexpr int sfa_cols(int fmt) { return weight_atoms_per_block(fmt) * 4; }
+__host__ __device__ constexpr int sf_cols_per_stage(int fmt, int bn) {
+    return weight_atoms_per_block(fmt) * 4 * (1 + b_atom_tiles(bn));
+}
+
 struct GemmArgs {
-    const uint8_t* sfa;     // weight scale atoms
-    const uint8_t* sfb;     // activation scale atoms
+    const uint8_t* wq;      // tiled weight operand
+    const uint16_t* x;      // fused: bf16 activations [M][K]
+    const uint8_t* sfb;     // TMA plans: activation scale atoms
     void* y;
     const float* alpha_x;
     const float* alpha_w;
-    float* partials;
-    uint32_t* counters;
     uint32_t* err;
-    int N, K, Rb, M;
-    int n_atoms_k;
+    uint64_t* trace;        // trace builds only: 16 timer stamps per CTA
+    int N, K, M, Rb;
+    int n_atoms_k;          // activation operand atoms per row tile along K
     int b_row_tiles;        // scale-atom row tiles of the activation operand
     int chunks;
     int splits;
     int fold;
     int out_f32;
     int stages;
+    int slots;              // fused: resident activation chunks
     int tmem_cols;
 };
 
-template <int FMT, int BN>
+template <int FMT, int BN, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                const GemmArgs g) {
-    constexpr int APC = atoms_per_chunk(FMT);
+    gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs g) {
+    constexpr int APC = weight_atoms_per_block(FMT);
     constexpr int BT = b_atom_tiles(BN);
+    constexpr int LPA = lanes_per_atom<FMT>();
+    constexpr uint32_t WB = weight_block_bytes(FMT);
     constexpr uint32_t B_BYTES = BN * 128;
-    constexpr uint32_t SFA_BYTES = APC * 512;
-    constexpr uint32_t STAGE = stage_bytes(FMT, BN);
-    constexpr int SFA_COLS = APC * 4;
+    constexpr uint32_t BSTAGE = b_stage_bytes(FMT, BN);
+    constexpr int SFA_COLS = sfa_cols(FMT);
     constexpr int SF_COLS = sf_cols_per_stage(FMT, BN);
+    static_assert(!FUSED || BT == 1, "fused plans keep the activation tile within one scale atom");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = g.stages;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STAGE);
+    uint8_t* wring = smem;                                   // S x WB
+    uint8_t* bregion = smem + (size_t)S * WB;                // S (or slots) x BSTAGE
+    const int nbslots = FUSED ? g.slots : S;
+    uint64_t* full = reinterpret_cast<uint64_t*>(bregion + (size_t)nbslots * BSTAGE);
     uint64_t* empty = full + kMaxStages;
     uint64_t* accum_full = empty + kMaxStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_full + 1);
+    uint64_t* b_ready = accum_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_ready + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
-    volatile uint32_t* last_flag = tmem_slot + 2;
-    volatile uint32_t* consumed = tmem_slot + 3;
-    volatile uint32_t* issued = tmem_slot + 4;
+    volatile uint32_t* consumed = tmem_slot + 2;
+    volatile uint32_t* issued = tmem_slot + 3;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) RS_TRACE_MARK(g.trace, 0);
     const int n_tile = blockIdx.x, b_tile = blockIdx.y, split = blockIdx.z;
     const int per = g.chunks / g.splits, rem = g.chunks % g.splits;
     const int c0 = split * per + (split < rem ? split : rem);
     const int nck = per + (split < rem ? 1 : 0);
+    const int pre = nck < S ? nck : S;
+    const uint8_t* wsrc = g.wq + ((size_t)n_tile * g.chunks + c0) * WB;
 
+    // Producer: barriers, then start streaming weights right away (they do
+    // not depend on the previous kernel in the stream).
+    uint64_t pol_w = 0;
     if (warp == 4 && lane == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
         mbar_init(smem_u32(accum_full), 1);
+        mbar_init(smem_u32(b_ready), 1);
         *abort_flag = 0;
-        *last_flag = 0;
         *consumed = 0;
         *issued = 0;
         fence_mbarrier_init();
-        tma_prefetch_desc(&tmap_a);
-        tma_prefetch_desc(&tmap_b);
+        pol_w = l2_policy_evict_first();  // weights are streamed once per call
+        const int nb_tiles = FUSED ? 0 : min(BT, g.b_row_tiles - b_tile * BT);
+        for (int i = 0; i < pre; ++i) {
+            const uint32_t fb = smem_u32(&full[i]);
+            const int na = min(APC, g.n_atoms_k - (c0 + i) * APC);
+            const uint32_t b_tx = FUSED ? 0u : B_BYTES + (uint32_t)na * 512u * (uint32_t)nb_tiles;
+            mbar_arrive_expect_tx(fb, WB + b_tx);
+            bulk_load(smem_u32(wring + (size_t)i * WB), wsrc + (size_t)i * WB, WB, fb, pol_w);
+        }
+        RS_TRACE_MARK(g.trace, 2);
     }
     if (warp == 5) {
         tmem_alloc(smem_u32(tmem_slot), (uint32_t)g.tmem_cols);
@@ -124,91 +160,97 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) {
+        RS_TRACE_MARK(g.trace, 1);
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        RS_TRACE_VALUE(g.trace, 12, smid);
+    }
     const uint32_t tm_acc = tmem;
     const uint32_t tm_sf = tmem + BN;
 
-    // Let the next kernel in the stream start its prologue; it waits for
-    // this grid's completion before touching our outputs.
+    // Dependents may start their prologue now; they wait for our completion
+    // before they touch anything we read or write.
     pdl_launch_dependents();
 
+    const int outs = g.fold ? BN / 2 : BN;
+    const int m0 = b_tile * outs;
+    const int row = warp * 32 + lane;  // epilogue: accumulator lane = channel within the tile
+    const int n = n_tile * 128 + row;
+
     if (warp == 4) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ producer
         if (lane == 0) {
-            const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
-            const uint64_t pol_x = l2_policy_evict_last();   // activations: re-read by every tile
-            const int nb_tiles = min(BT, g.b_row_tiles - b_tile * BT);
-            auto atoms_in = [&](int chunk) { return min(APC, g.n_atoms_k - chunk * APC); };
-            auto load_w = [&](int i) {
-                const int chunk = c0 + i, s = i % S, na = atoms_in(chunk);
-                uint8_t* st = smem + (size_t)s * STAGE;
+            const uint64_t pol_x = l2_policy_evict_last();  // activations: re-read by every tile
+            const int nb_tiles = FUSED ? 0 : min(BT, g.b_row_tiles - b_tile * BT);
+            auto load_b = [&](int i) {
+                if (FUSED) return;
+                const int chunk = c0 + i, s = i % S;
+                uint8_t* st = bregion + (size_t)s * BSTAGE;
                 const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, kTileA + B_BYTES + (uint32_t)na * 512u * (1u + (uint32_t)nb_tiles));
-                tma_load_2d(smem_u32(st), &tmap_a, fb, chunk * 128, n_tile * 128, pol_w);
-                bulk_load(smem_u32(st + kTileA + B_BYTES),
-                          g.sfa + ((size_t)n_tile * g.n_atoms_k + (size_t)chunk * APC) * 512, (uint32_t)na * 512u, fb,
-                          pol_w);
-            };
-            auto load_x = [&](int i) {
-                const int chunk = c0 + i, s = i % S, na = atoms_in(chunk);
-                uint8_t* st = smem + (size_t)s * STAGE;
-                const uint32_t fb = smem_u32(&full[s]);
-                tma_load_2d(smem_u32(st + kTileA), &tmap_b, fb, chunk * 128, b_tile * BN, pol_x);
+                tma_load_2d(smem_u32(st), &tmap_b, fb, chunk * 128, b_tile * BN, pol_x);
+                const int na = min(APC, g.n_atoms_k - chunk * APC);
                 for (int t = 0; t < nb_tiles; ++t)
-                    bulk_load(smem_u32(st + kTileA + B_BYTES + SFA_BYTES + (uint32_t)t * APC * 512u),
+                    bulk_load(smem_u32(st + B_BYTES + (uint32_t)t * APC * 512u),
                               g.sfb + ((size_t)(b_tile * BT + t) * g.n_atoms_k + (size_t)chunk * APC) * 512,
                               (uint32_t)na * 512u, fb, pol_x);
             };
-            // Weights do not depend on the previous kernel: start them first.
-            const int pre = min(S, nck);
-            for (int i = 0; i < pre; ++i) load_w(i);
             pdl_wait_prior_grid();
-            for (int i = 0; i < pre; ++i) load_x(i);
+            for (int i = 0; i < pre; ++i) load_b(i);
             int i = pre;
             for (; i < nck; ++i) {
                 const int s = i % S;
                 const uint32_t ph = (uint32_t)(i / S) & 1u;
                 if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag, g.err)) break;
-                load_w(i);
-                load_x(i);
+                const uint32_t fb = smem_u32(&full[s]);
+                const int na = min(APC, g.n_atoms_k - (c0 + i) * APC);
+                const uint32_t b_tx = FUSED ? 0u : B_BYTES + (uint32_t)na * 512u * (uint32_t)nb_tiles;
+                mbar_arrive_expect_tx(fb, WB + b_tx);
+                bulk_load(smem_u32(wring + (size_t)s * WB), wsrc + (size_t)i * WB, WB, fb, pol_w);
+                load_b(i);
             }
             *issued = (uint32_t)i;
+            RS_TRACE_MARK(g.trace, 3);
         }
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
+            bool ok = true;
+            if (FUSED) ok = mbar_wait_bounded(smem_u32(b_ready), 0, abort_flag, g.err);
             int i = 0;
-            for (; i < nck; ++i) {
+            for (; ok && i < nck; ++i) {
                 const int s = i % S;
                 const uint32_t ph = (uint32_t)(i / S) & 1u;
                 if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err)) break;
+                if (i == 0) RS_TRACE_MARK(g.trace, 4);
+                if (i == nck - 1) RS_TRACE_MARK(g.trace, 5);
                 tc_fence_after();
                 const int chunk = c0 + i;
-                const int na = min(APC, g.n_atoms_k - chunk * APC);
-                const int nb_tiles = min(BT, g.b_row_tiles - b_tile * BT);
-                const uint32_t sa = smem_u32(smem + (size_t)s * STAGE);
-                const uint32_t sb = sa + kTileA;
-                const uint32_t ssfa = sb + B_BYTES;
-                const uint32_t ssfb = ssfa + SFA_BYTES;
+                const uint32_t sa = smem_u32(wring + (size_t)s * WB);
+                const uint32_t sb = smem_u32(bregion + (size_t)(FUSED ? i : s) * BSTAGE);
                 const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS);
                 const uint32_t tsfb = tsfa + SFA_COLS;
-                for (int a = 0; a < na; ++a) tc_cp_sf_atom(tsfa + a * 4, sf_atom_desc(ssfa + a * 512));
-                for (int t = 0; t < nb_tiles; ++t)
-                    for (int a = 0; a < na; ++a)
-                        tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sf_atom_desc(ssfb + (t * APC + a) * 512));
                 const int kleft = g.K - chunk * 256;
                 const int nks = min(4, (kleft + 63) / 64);
+                const int na = FMT == 0 ? nks : (nks + 1) / 2;  // atoms the issued k-steps read
+                const int nb_tiles = FUSED ? 1 : min(BT, g.b_row_tiles - b_tile * BT);
+                for (int a = 0; a < na; ++a)
+                    tc_cp_sf_atom(tsfa + a * 4, sf_atom_desc(sa + kWeightCodeBytes + a * 512));
+                for (int t = 0; t < nb_tiles; ++t)
+                    for (int a = 0; a < na; ++a)
+                        tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sf_atom_desc(sb + B_BYTES + (t * APC + a) * 512));
                 for (int ks = 0; ks < nks; ++ks) {
                     const uint64_t adesc = kmajor_sw128_desc(sa + ks * 32);
                     const uint64_t bdesc = kmajor_sw128_desc(sb + ks * 32);
-                    const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
+                    const uint32_t accum = (i > 0 || ks > 0) ? 1u : 0u;
                     if (FMT == 0) {
                         mma_nvfp4(tm_acc, adesc, bdesc, mxf4_idesc(BN, false, 0), tsfa + ks * 4, tsfb + ks * BT * 4,
-                                  acc);
+                                  accum);
                     } else {
                         const int a = ks >> 1;
                         const uint32_t sf_id = (uint32_t)(ks & 1) * 2u;
-                        mma_mxfp4(tm_acc, adesc, bdesc, mxf4_idesc(BN, true, sf_id), tsfa + a * 4,
-                                  tsfb + a * BT * 4, acc);
+                        mma_mxfp4(tm_acc, adesc, bdesc, mxf4_idesc(BN, true, sf_id), tsfa + a * 4, tsfb + a * BT * 4,
+                                  accum);
                     }
                 }
                 tc_commit(smem_u32(&empty[s]));
@@ -217,30 +259,74 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(smem_u32(accum_full));  // fires once every issued MMA is done
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 0-3)
-        pdl_wait_prior_grid();
+        // ------------------------------------------------ warps 0-3
+        const int ctid = threadIdx.x;  // 0..127
+        if (FUSED) {
+            // Quantizing prologue (Alg. 1): this CTA's K slice of every token
+            // -> base (row 2j) and residue (row 2j+1) codes in the swizzled
+            // B tiles, block scales in the B scale atoms.
+            const uint32_t bbytes = (uint32_t)nck * BSTAGE;
+            for (uint32_t off = (uint32_t)ctid * 16u; off < bbytes; off += 128u * 16u)
+                *reinterpret_cast<uint4*>(bregion + off) = make_uint4(0u, 0u, 0u, 0u);
+            named_bar_sync(1, 128);
+            pdl_wait_prior_grid();
+            const float alpha = FMT == 0 ? *g.alpha_x : 0.0f;
+            const int tasks = g.M * nck;
+            for (int task = warp; task < tasks; task += 4) {
+                const int j = task / nck, ci = task % nck;
+                const int k0 = (c0 + ci) * 256 + lane * 8;
+                const bool valid = k0 < g.K;
+                float xf[8];
+                load8_bf16(g.x + (size_t)j * g.K + k0, valid, xf);
+                uint32_t sfq;
+                float xh[8];
+                const uint32_t codes = quant_lane<FMT>(xf, alpha, sfq, xh);
+                const uint32_t sfw = gather_sf_word<FMT>(sfq, lane);
+                uint8_t* slot = bregion + (size_t)ci * BSTAGE;
+                const uint32_t rb = g.fold ? 2u * (uint32_t)j : (uint32_t)j;
+                *reinterpret_cast<uint32_t*>(slot + sw128_offset(rb, (uint32_t)lane * 4u)) = codes;
+                if ((lane % LPA) == 0)
+                    *reinterpret_cast<uint32_t*>(slot + B_BYTES + (lane / LPA) * 512 + (rb % 32) * 16 + (rb / 32) * 4) = sfw;
+                if (g.fold) {
+                    float r[8];
+                    residue8(xf, xh, r);
+                    uint32_t sfr;
+                    float rh[8];
+                    const uint32_t rcodes = quant_lane<FMT>(r, alpha, sfr, rh);
+                    const uint32_t sfrw = gather_sf_word<FMT>(sfr, lane);
+                    const uint32_t rr = rb + 1u;
+                    *reinterpret_cast<uint32_t*>(slot + sw128_offset(rr, (uint32_t)lane * 4u)) = rcodes;
+                    if ((lane % LPA) == 0)
+                        *reinterpret_cast<uint32_t*>(slot + B_BYTES + (lane / LPA) * 512 + (rr % 32) * 16 + (rr / 32) * 4) =
+                            sfrw;
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (ctid == 0) mbar_arrive(smem_u32(b_ready));
+        } else {
+            pdl_wait_prior_grid();  // before writing the output
+        }
+
+        // ---------------------------------------------- epilogue
         bool ok = mbar_wait_bounded(smem_u32(accum_full), 0, abort_flag, g.err);
+        if (ctid == 0) RS_TRACE_MARK(g.trace, 6);
         named_bar_sync(1, 128);
         ok = ok && (*abort_flag == 0);
         ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
         tc_fence_after();
-        const int row = warp * 32 + lane;  // accumulator lane = channel within the tile
-        const int n = n_tile * 128 + row;
-        const int outs = g.fold ? BN / 2 : BN;
-        const int m0 = b_tile * outs;
-        const int tile_id = b_tile * (int)gridDim.x + n_tile;
         const float gsc = FMT == 0 ? __fmul_rn(*g.alpha_x, *g.alpha_w) : 1.0f;
-        float* part = g.partials + ((size_t)tile_id * g.splits + split) * (size_t)outs * 128;
-
-        auto store_out = [&](int j, float val) {
-            const int m = m0 + j;
-            if (m < g.M && n < g.N) {
-                const size_t idx = (size_t)m * g.N + n;
+        float* red = reinterpret_cast<float*>(wring);  // split-K partial (the weight ring is idle now)
+        auto emit = [&](int j, float z) {
+            if (g.splits > 1) {
+                red[j * 128 + row] = z;
+            } else if (n < g.N && m0 + j < g.M) {
+                const float val = __fmul_rn(gsc, z);
+                const size_t idx = (size_t)(m0 + j) * g.N + n;
                 if (g.out_f32) reinterpret_cast<float*>(g.y)[idx] = val;
                 else reinterpret_cast<__nv_bfloat16*>(g.y)[idx] = __float2bfloat16_rn(val);
             }
         };
-
         if (ok) {
 #pragma unroll 1
             for (int c = 0; c < BN; c += 16) {
@@ -248,44 +334,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld16(tm_acc + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
                 if (g.fold) {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const float z = __fadd_rn(v[2 * u], v[2 * u + 1]);  // Fold: base + residue
-                        const int j = c / 2 + u;
-                        if (g.splits == 1) store_out(j, __fmul_rn(gsc, z));
-                        else part[(size_t)j * 128 + row] = z;
-                    }
+                    for (int u = 0; u < 8; ++u) emit(c / 2 + u, __fadd_rn(v[2 * u], v[2 * u + 1]));  // Fold
                 } else {
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int j = c + u;
-                        if (g.splits == 1) store_out(j, __fmul_rn(gsc, v[u]));
-                        else part[(size_t)j * 128 + row] = v[u];
-                    }
+                    for (int u = 0; u < 16; ++u) emit(c + u, v[u]);
                 }
             }
+        } else if (g.splits > 1) {
+            for (int j = 0; j < outs; ++j) red[j * 128 + row] = 0.0f;
         }
-        if (g.splits > 1) {
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (threadIdx.x == 0) {
-                uint32_t prev = 0;
-                if (ok) prev = atomicAdd(&g.counters[tile_id], 1u);
-                *last_flag = (ok && prev == (uint32_t)g.splits - 1u) ? 1u : 0u;
-            }
-            named_bar_sync(1, 128);
-            if (*last_flag) {
-                __threadfence();
-                const float* base = g.partials + (size_t)tile_id * g.splits * (size_t)outs * 128;
-                for (int j = 0; j < outs && m0 + j < g.M; ++j) {
-                    float acc = 0.0f;
-                    for (int s = 0; s < g.splits; ++s)
-                        acc = __fadd_rn(acc, __ldcg(base + ((size_t)s * outs + j) * 128 + row));
-                    store_out(j, __fmul_rn(gsc, acc));
-                }
-                if (threadIdx.x == 0) g.counters[tile_id] = 0u;  // re-arm for the next call
-            }
-        }
+        if (ctid == 0) RS_TRACE_MARK(g.trace, 7);
     }
+
+    // ---------------------------------------------------- split-K reduction
+    __syncwarp();
+    if (g.splits > 1) {
+        cluster_sync_all();  // partials of every CTA in the cluster are visible
+        if (warp < 4) {
+            const float gsc = FMT == 0 ? __fmul_rn(*g.alpha_x, *g.alpha_w) : 1.0f;
+            const int per_cta = (outs + g.splits - 1) / g.splits;
+            const uint32_t red0 = smem_u32(wring);
+            for (int jj = 0; jj < per_cta; ++jj) {
+                const int j = split * per_cta + jj;
+                const int m = m0 + j;
+                if (j >= outs || m >= g.M) break;
+                const uint32_t off = red0 + (uint32_t)(j * 128 + row) * 4u;
+                float part[kMaxSplits];
+#pragma unroll
+                for (int r = 0; r < kMaxSplits; ++r)
+                    part[r] = r < g.splits ? ld_dsmem_f32(map_dsmem(off, (uint32_t)r)) : 0.0f;
+                float acc = 0.0f;
+#pragma unroll
+                for (int r = 0; r < kMaxSplits; ++r)
+                    if (r < g.splits) acc = __fadd_rn(acc, part[r]);
+                if (n < g.N && *abort_flag == 0) {
+                    const float val = __fmul_rn(gsc, acc);
+                    const size_t idx = (size_t)m * g.N + n;
+                    if (g.out_f32) reinterpret_cast<float*>(g.y)[idx] = val;
+                    else reinterpret_cast<__nv_bfloat16*>(g.y)[idx] = __float2bfloat16_rn(val);
+                }
+            }
+        }
+        cluster_sync_all();  // nobody leaves while partners still read its partial
+    }
+    if (threadIdx.x == 0) RS_TRACE_MARK(g.trace, 9);
 
     // ---------------------------------------------------- teardown
     tc_fence_before();
@@ -302,12 +394,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, (uint32_t)g.tmem_cols);
+        if (lane == 0) RS_TRACE_MARK(g.trace, 10);
     }
 }
 
 // ------------------------------------------------------------------- host --
 
-GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms) {
+static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots) {
+    const size_t b = fused ? (size_t)slots * b_stage_bytes(fmt, bn) : (size_t)stages * b_stage_bytes(fmt, bn);
+    return 1024 + (size_t)stages * weight_block_bytes(fmt) + b + kCtrlBytes;
+}
+
+static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, int split_cap, bool allow_fused) {
     GemmPlan p{};
     p.fmt = fmt;
     p.fold = fold ? 1 : 0;
@@ -320,24 +418,60 @@ GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms) {
     p.b_tiles = (p.Rb + p.bn - 1) / p.bn;
     p.chunks = (K + 255) / 256;
     const int tiles = p.n_tiles * p.b_tiles;
-    int splits;
-    if (num_sms <= 0) splits = std::min(p.chunks, kMaxSplits);  // sizing bound
-    else splits = tiles >= num_sms ? 1 : std::max(1, std::min({p.chunks, kMaxSplits, num_sms / tiles}));
-    p.splits = splits;
-    const int max_chunks = (p.chunks + splits - 1) / splits;
-    const uint32_t st = stage_bytes(fmt, p.bn);
-    int stages = (int)((kSmemLimit - 1024 - kCtrlBytes) / st);
-    stages = std::min({stages, kMaxStages, max_chunks});
+    const int sms = num_sms > 0 ? num_sms : 148;
+    // Split count: minimise the chunks the busiest SM streams (CTAs are
+    // spread round-robin over the SMs); prefer fewer splits on a tie.
+    int best_s = 1;
+    long best_load = -1;
+    const int smax = std::min({p.chunks, kMaxSplits, split_cap});
+    for (int s = 1; s <= smax; ++s) {
+        const long ctas = (long)tiles * s;
+        const long load = ((ctas + sms - 1) / sms) * (long)((p.chunks + s - 1) / s);
+        if (best_load < 0 || load < best_load) {
+            best_load = load;
+            best_s = s;
+        }
+    }
+    p.splits = best_s;
+    const int max_chunks = (p.chunks + p.splits - 1) / p.splits;
+    p.fused = (allow_fused && p.b_tiles == 1 && p.bn <= 32) ? 1 : 0;
+    int stages = std::min(kMaxStages, max_chunks);
+    while (stages > 1 && plan_smem(fmt, p.bn, stages, p.fused, max_chunks) > kSmemLimit) --stages;
+    if (p.fused && plan_smem(fmt, p.bn, stages, true, max_chunks) > kSmemLimit) {
+        p.fused = 0;
+        stages = std::min(kMaxStages, max_chunks);
+        while (stages > 1 && plan_smem(fmt, p.bn, stages, false, 0) > kSmemLimit) --stages;
+    }
     p.stages = std::max(stages, 1);
-    const int cols = p.bn + p.stages * sf_cols_per_stage(fmt, p.bn);
+    const int outs = fold ? p.bn / 2 : p.bn;
+    if (p.splits > 1 && (size_t)outs * 128 * sizeof(float) > (size_t)p.stages * weight_block_bytes(fmt)) {
+        // the split-K partial lives in the idle weight ring; without room, no split
+        return plan_impl(fmt, fold, M, N, K, num_sms, 1, allow_fused);
+    }
+    p.slots = p.fused ? max_chunks : 0;
+    // Two CTAs can share an SM when the shared memory allows it; keep the
+    // tensor-memory allocation within half of the SM's 512 columns then.
+    p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots);
+    int cols = p.bn + p.stages * sf_cols_per_stage(fmt, p.bn);
+    if (p.smem_bytes <= kSmemLimit / 2) {
+        while (cols > 256 && p.stages > 1) {
+            --p.stages;
+            cols = p.bn + p.stages * sf_cols_per_stage(fmt, p.bn);
+        }
+        p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots);
+    }
     int alloc = 32;
     while (alloc < cols) alloc *= 2;
     p.tmem_cols = alloc;
-    p.smem_bytes = 1024 + (size_t)p.stages * st + kCtrlBytes;
-    const int outs = fold ? p.bn / 2 : p.bn;
-    p.partial_bytes = splits > 1 ? (size_t)tiles * splits * outs * 128 * sizeof(float) : 0;
-    p.counter_bytes = (size_t)tiles * sizeof(uint32_t);
     return p;
+}
+
+GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused) {
+    return plan_impl(fmt, fold, M, N, K, num_sms, kMaxSplits, allow_fused);
+}
+
+size_t workspace_bytes(int fmt, bool compensated, int M, int K) {
+    return align_up(operand_bytes(fmt, compensated ? 2 * M : M, K), 1024);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -359,7 +493,8 @@ static EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// Code tiles: [rows][K/2] bytes, box = 128 bytes (256 K) x box_rows, 128B swizzle.
+// Activation codes: [rows][K/2] bytes, box = 128 bytes (256 K) x box_rows,
+// 128-byte swizzle (the image the K-major SW128 descriptor reads).
 static bool encode_codes_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;
@@ -374,55 +509,70 @@ static bool encode_codes_map(CUtensorMap* m, const void* base, int rows, int K, 
 
 // The dynamic shared-memory opt-in is set once per kernel and device (to the
 // maximum, so later calls never need it again, e.g. during graph capture).
-template <int FMT, int BN>
+template <int FMT, int BN, bool FUSED>
 static cudaError_t ensure_smem_attr() {
     static bool done[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+    e = cudaFuncSetAttribute(gemm_kernel<FMT, BN, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemLimit);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return e;
 }
 
-template <int FMT, int BN>
-static cudaError_t launch_typed(const GemmPlan& p, const GemmCall& c, const CUtensorMap& ta,
-                                const CUtensorMap& tb, const GemmArgs& args, cudaStream_t stream) {
-    auto kern = gemm_kernel<FMT, BN>;
-    cudaError_t e = ensure_smem_attr<FMT, BN>();
+template <int FMT, int BN, bool FUSED>
+static cudaError_t launch_typed(const GemmPlan& p, const CUtensorMap& tb, const GemmArgs& args, cudaStream_t stream) {
+    cudaError_t e = ensure_smem_attr<FMT, BN, FUSED>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)p.n_tiles, (unsigned)p.b_tiles, (unsigned)p.splits);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = p.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (p.splits > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = (unsigned)p.splits;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = c.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<FMT, BN, FUSED>, tb, args);
 }
 
+#ifdef RS_TRACE
+static uint64_t* g_trace = nullptr;
+#endif
+
 cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t stream) {
-    alignas(64) CUtensorMap ta;
     alignas(64) CUtensorMap tb;
-    if (!encode_codes_map(&ta, c.wq, p.N, p.K, 128)) return cudaErrorInvalidValue;
-    if (!encode_codes_map(&tb, c.xq, p.Rb, p.K, p.bn)) return cudaErrorInvalidValue;
+    std::memset(&tb, 0, sizeof tb);
+    if (!p.fused && !encode_codes_map(&tb, c.xq, p.Rb, p.K, p.bn)) return cudaErrorInvalidValue;
     GemmArgs a{};
-    a.sfa = static_cast<const uint8_t*>(c.wq) + operand_sf_offset(p.fmt, p.N, p.K);
-    a.sfb = static_cast<const uint8_t*>(c.xq) + operand_sf_offset(p.fmt, p.Rb, p.K);
+    a.wq = static_cast<const uint8_t*>(c.wq);
+    a.x = static_cast<const uint16_t*>(c.x);
+    a.sfb = p.fused ? nullptr : static_cast<const uint8_t*>(c.xq) + operand_sf_offset(p.fmt, p.Rb, p.K);
     a.y = c.y;
     a.alpha_x = c.alpha_x;
     a.alpha_w = c.alpha_w;
-    a.partials = c.partials;
-    a.counters = c.counters;
     a.err = c.err;
+#ifdef RS_TRACE
+    a.trace = g_trace;
+#else
+    a.trace = nullptr;
+#endif
     a.N = p.N;
     a.K = p.K;
-    a.Rb = p.Rb;
     a.M = p.M;
+    a.Rb = p.Rb;
     a.n_atoms_k = n_atoms_k_host(p.fmt, p.K);
     a.b_row_tiles = (p.Rb + 127) / 128;
     a.chunks = p.chunks;
@@ -430,13 +580,23 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
     a.fold = p.fold;
     a.out_f32 = c.out_f32;
     a.stages = p.stages;
+    a.slots = p.slots;
     a.tmem_cols = p.tmem_cols;
-#define RS_CASE(F, B)                                                   \
-    if (p.fmt == F && p.bn == B) return launch_typed<F, B>(p, c, ta, tb, a, stream);
-    RS_CASE(0, 16) RS_CASE(0, 32) RS_CASE(0, 64) RS_CASE(0, 128) RS_CASE(0, 256)
-    RS_CASE(1, 16) RS_CASE(1, 32) RS_CASE(1, 64) RS_CASE(1, 128) RS_CASE(1, 256)
+#define RS_CASE(F, B, FU)                                                      \
+    if (p.fmt == F && p.bn == B && (p.fused != 0) == FU) return launch_typed<F, B, FU>(p, tb, a, stream);
+    RS_CASE(0, 16, true) RS_CASE(0, 32, true) RS_CASE(1, 16, true) RS_CASE(1, 32, true)
+    RS_CASE(0, 16, false) RS_CASE(0, 32, false) RS_CASE(0, 64, false) RS_CASE(0, 128, false) RS_CASE(0, 256, false)
+    RS_CASE(1, 16, false) RS_CASE(1, 32, false) RS_CASE(1, 64, false) RS_CASE(1, 128, false) RS_CASE(1, 256, false)
 #undef RS_CASE
     return cudaErrorInvalidValue;
 }
 
 }  // namespace rs
+
+#ifdef RS_TRACE
+// Trace builds only: set the device buffer (16 uint64 per CTA) that the next
+// GEMM launches stamp; NULL turns tracing off.
+extern "C" __attribute__((visibility("default"))) void rs_debug_set_trace(void* buf) {
+    rs::g_trace = static_cast<uint64_t*>(buf);
+}
+#endif

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "rs_device.cuh"
+
 namespace rs {
 
 // Layout of an rs operand (see include/rs.h): codes first, scale atoms at a
@@ -23,6 +25,11 @@ inline size_t operand_bytes(int fmt, int rows, int K) {
     return operand_sf_offset(fmt, rows, K) + operand_sf_bytes(fmt, rows, K);
 }
 
+// Tiled weight operand (see rs_device.cuh): ceil(N/128) x ceil(K/256) blocks.
+inline size_t weight_bytes(int fmt, int N, int K) {
+    return (size_t)((N + 127) / 128) * (size_t)((K + 255) / 256) * weight_block_bytes(fmt);
+}
+
 // GEMM launch plan for one linear call.
 struct GemmPlan {
     int fmt, fold;
@@ -32,27 +39,24 @@ struct GemmPlan {
     int n_tiles;     // ceil(N / 128)
     int b_tiles;     // ceil(Rb / bn)
     int chunks;      // ceil(K / 256)
-    int splits;      // K splits per output tile
+    int splits;      // K splits per output tile (= cluster size when > 1)
     int stages;      // pipeline depth
+    int fused;       // quantize the activations inside the GEMM
+    int slots;       // fused: activation chunks resident in shared memory
     int tmem_cols;   // tensor-memory columns to allocate
     size_t smem_bytes;
-    size_t partial_bytes;  // split-K partial sums (0 when splits == 1)
-    size_t counter_bytes;  // one uint32 per output tile
 };
 
-constexpr int kMaxSplits = 32;
+constexpr int kMaxSplits = 8;   // portable thread-block cluster size
 
-// Plan for a given SM count (num_sms <= 0: the worst case used for sizing).
-GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms);
+// Plan for a given SM count.  allow_fused: the caller passes bf16 input, so
+// small-M plans may quantize inside the GEMM.
+GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused);
 
-// Workspace layout shared by rs_workspace_bytes and the linear entry points.
-struct WorkspaceLayout {
-    size_t act_off, act_bytes;      // quantized activations (when x_bf16 is given)
-    size_t part_off, part_bytes;    // split-K partials
-    size_t cnt_off, cnt_bytes;      // tile counters
-    size_t total;
-};
-WorkspaceLayout workspace_layout(int fmt, bool compensated, int M, int N, int K, bool quantize_input);
+// Workspace of a linear call given a bf16 input: the quantized activation
+// operand when the plan quantizes in a separate kernel (sized for the worst
+// case so that it does not depend on the device).
+size_t workspace_bytes(int fmt, bool compensated, int M, int K);
 
 cudaError_t launch_tensor_scale(const void* x, int64_t n, float* alpha, uint32_t* err,
                                 cudaStream_t stream, int num_sms);
@@ -61,18 +65,18 @@ cudaError_t launch_tensor_scale(const void* x, int64_t n, float* alpha, uint32_t
 // previous grid has returned.  Only for activations consumed by our GEMM.
 cudaError_t launch_quantize(int fmt, bool paired, int rows, int K, const void* x, int64_t ldx,
                             const float* alpha, void* q_out, cudaStream_t stream, int num_sms, bool pdl);
+cudaError_t launch_quantize_weight(int fmt, int N, int K, const void* w, int64_t ldw, const float* alpha,
+                                   void* wq_out, cudaStream_t stream, int num_sms);
 
 struct GemmCall {
-    const void* xq;        // activation operand (Rb rows)
-    const void* wq;        // weight operand (N rows)
+    const void* x;         // fused plans: bf16 activations [M][K]
+    const void* xq;        // other plans: activation operand (Rb rows)
+    const void* wq;        // tiled weight operand
     const float* alpha_x;
     const float* alpha_w;
     void* y;
     int out_f32;
-    float* partials;
-    uint32_t* counters;
     uint32_t* err;
-    bool pdl;              // launch with programmatic stream serialization
 };
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmCall& call, cudaStream_t stream);

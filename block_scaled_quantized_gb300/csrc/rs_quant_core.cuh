@@ -1,0 +1,117 @@
+// Per-lane quantization core shared by the standalone quantizer kernels and
+// the quantizing prologue of the fused GEMM, so that both produce identical
+// codes and scale bytes.
+//
+// ResServe App. B.2 Eq. 8-10 and Algorithm 1 (eight inputs per lane): the
+// lanes that share one scale block (2 for NVFP4's 16-element blocks, 4 for
+// MXFP4's 32-element blocks) combine their maxima with shuffles, every lane
+// derives the block scale and the fp32 multiplier, converts its eight values
+// to E2M1, and decodes them again to form the reconstruction x^ (and from it
+// the residue) in registers.
+#pragma once
+
+#include "rs_device.cuh"
+
+namespace rs {
+
+// NVFP4 block scale from the block amax (Eq. 8-9, Alg. 1 line 3):
+// byte = E4M3(fl(fl(amax/6)/alpha)), s~ = fl(alpha * dec(byte)), mul = fl(1/s~).
+__device__ __forceinline__ uint32_t nv_block_scale(float amax, float alpha, float& st, float& mul) {
+    const float s = __fdiv_rn(amax, kE2M1Max);
+    const float t = alpha > 0.0f ? __fdiv_rn(s, alpha) : 0.0f;
+    const uint32_t sf = e4m3_encode_satfinite(t);
+    st = __fmul_rn(alpha, e4m3_decode(sf));
+    mul = st == 0.0f ? 0.0f : __fdiv_rn(1.0f, st);
+    return sf;
+}
+
+// MXFP4 block scale: byte = max(E - 2, 0) where E is the biased fp32
+// exponent of amax, i.e. e = floor(log2 amax) - 2 clamped at -127 (amax == 0
+// and fp32-subnormal amax give byte 0).  st = 2^e, mul = 2^-e, both exact.
+__device__ __forceinline__ uint32_t mx_block_scale(float amax, float& st, float& mul) {
+    const int E = (int)(__float_as_uint(amax) >> 23);
+    const uint32_t byte = E >= 2 ? (uint32_t)(E - 2) : 0u;
+    st = byte >= 1u ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);  // 2^(byte-127)
+    mul = __uint_as_float((254u - byte) << 23);                                      // 2^(127-byte)
+    return byte;
+}
+
+// Shuffle-max over the lanes that share one scale block (full warp active).
+template <int FMT>
+__device__ __forceinline__ float block_amax(float a) {
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+    if (FMT == 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+    return a;
+}
+
+// Quantize this lane's eight values; returns the packed codes (element e in
+// bits 4e..4e+3, i.e. element 2j in the low nibble of byte j), the block's
+// scale byte in `sf`, and the reconstruction fl(s~ * dec(q)) in `xh`.
+template <int FMT>
+__device__ __forceinline__ uint32_t quant_lane(const float (&xf)[8], float alpha, uint32_t& sf, float (&xh)[8]) {
+    float am = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(xf[e]));
+    am = block_amax<FMT>(am);
+    float st, mul;
+    sf = FMT == 0 ? nv_block_scale(am, alpha, st, mul) : mx_block_scale(am, st, mul);
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(xf[e], mul);
+    const uint32_t codes = e2m1_encode8(v);
+    float d[8];
+    e2m1_decode8(codes, d);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xh[e] = __fmul_rn(st, d[e]);
+    return codes;
+}
+
+// Residue of this lane's eight values, r = fl(x - x^) (Alg. 1 line 6).
+__device__ __forceinline__ void residue8(const float (&xf)[8], const float (&xh)[8], float (&r)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = __fsub_rn(xf[e], xh[e]);
+}
+
+// Gather the four scale bytes of one atom row (4 consecutive blocks) into the
+// first lane of its group: NVFP4 groups are 8 lanes (2 per block), MXFP4
+// groups 16 lanes (4 per block).  Returns the word on every lane; only the
+// group leader's copy is meaningful.
+template <int FMT>
+__device__ __forceinline__ uint32_t gather_sf_word(uint32_t sfbyte, int lane) {
+    constexpr int kLanesPerBlock = FMT == 0 ? 2 : 4;
+    constexpr int kLanesPerAtom = 4 * kLanesPerBlock;
+    const int base = lane & ~(kLanesPerAtom - 1);
+    const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, sfbyte, base);
+    const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, sfbyte, base + kLanesPerBlock);
+    const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, sfbyte, base + 2 * kLanesPerBlock);
+    const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, sfbyte, base + 3 * kLanesPerBlock);
+    return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+}
+
+template <int FMT>
+__host__ __device__ constexpr int lanes_per_atom() { return FMT == 0 ? 8 : 16; }
+
+// Load eight bf16 values (16 bytes) as fp32, or zeros when !valid.
+__device__ __forceinline__ void load8_bf16(const uint16_t* p, bool valid, float (&xf)[8]) {
+    if (valid) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            xf[2 * i] = __uint_as_float(w[i] << 16);
+            xf[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xf[e] = 0.0f;
+    }
+}
+
+// Byte offset of code byte b (0..127) of row r (0..127) in a 128-row x
+// 128-byte tile stored in the 128-byte-swizzled shared-memory image that the
+// tcgen05 K-major SW128 descriptor reads: 16-byte chunk index XOR (r % 8).
+__host__ __device__ constexpr uint32_t sw128_offset(uint32_t r, uint32_t b) {
+    return r * 128u + ((((b >> 4) ^ (r & 7u))) << 4) + (b & 15u);
+}
+
+}  // namespace rs

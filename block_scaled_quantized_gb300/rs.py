@@ -26,7 +26,8 @@ STATUS = {0: "RS_OK", 1: "RS_ERR_INVALID_ARG", 2: "RS_ERR_ALIGNMENT", 3: "RS_ERR
 # Every symbol include/rs.h declares.
 EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_offset", "rs_act_bytes",
            "rs_weight_bytes", "rs_workspace_bytes", "rs_compute_tensor_scale", "rs_quantize_fp4",
-           "rs_quantize_residue", "rs_linear_w4a4", "rs_linear_compensated", "rs_get_device_error"]
+           "rs_quantize_weight", "rs_quantize_residue", "rs_linear_w4a4", "rs_linear_compensated",
+           "rs_get_device_error"]
 
 
 class RsError(RuntimeError):
@@ -51,6 +52,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_workspace_bytes": ([I, I, I, I, I], SZ),
         "rs_compute_tensor_scale": ([P, I64, P, P], I),
         "rs_quantize_fp4": ([I, I, I, P, I64, P, P, P], I),
+        "rs_quantize_weight": ([I, I, I, P, I64, P, P, P], I),
         "rs_quantize_residue": ([I, I, I, P, I64, P, P, P], I),
         "rs_linear_w4a4": ([I, I, I, I, P, P, P, P, P, P, I, P, SZ, P], I),
         "rs_linear_compensated": ([I, I, I, I, P, P, P, P, P, P, I, P, SZ, P], I),
@@ -132,6 +134,13 @@ def rs_quantize_fp4(fmt: int, x: torch.Tensor, alpha: torch.Tensor | None, q_out
                                                     _ptr(q_out), _stream(stream)))
 
 
+def rs_quantize_weight(fmt: int, w: torch.Tensor, alpha: torch.Tensor | None, wq_out: torch.Tensor,
+                       stream=None):
+    N, K = w.shape
+    _check("rs_quantize_weight", lib().rs_quantize_weight(fmt, N, K, _ptr(w), w.stride(0), _ptr(alpha),
+                                                          _ptr(wq_out), _stream(stream)))
+
+
 def rs_quantize_residue(fmt: int, x: torch.Tensor, alpha: torch.Tensor | None, q_paired_out: torch.Tensor,
                         stream=None):
     M, K = x.shape
@@ -169,7 +178,12 @@ def empty_operand(fmt: int, rows: int, K: int, device=None) -> torch.Tensor:
     return torch.empty(rs_operand_bytes(fmt, rows, K), dtype=torch.uint8, device=device or "cuda")
 
 
-def zeros_workspace(fmt: int, M: int, N: int, K: int, compensated: bool, device=None) -> torch.Tensor:
-    """Zero-filled workspace (the split-K tile counters must start at zero)."""
+def empty_weight(fmt: int, N: int, K: int, device=None) -> torch.Tensor:
+    """Uninitialised byte buffer for an rs weight of W [N][K]."""
+    return torch.empty(rs_weight_bytes(fmt, N, K), dtype=torch.uint8, device=device or "cuda")
+
+
+def empty_workspace(fmt: int, M: int, N: int, K: int, compensated: bool, device=None) -> torch.Tensor:
+    """Workspace for a linear call with bf16 input (no initialisation needed)."""
     n = max(rs_workspace_bytes(fmt, M, N, K, compensated), 16)
-    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")

@@ -64,6 +64,23 @@
  * A paired operand (compensated input; the row-pair layout of Sec. 5.1 and
  * Fig. 5a) is an rs operand with 2*M rows: row 2j holds the base X^ of token
  * j and row 2j+1 its residue R^.
+ *
+ * Device layout of a quantized weight ("rs weight", W [N][K], offline)
+ * --------------------------------------------------------------------
+ * rs_weight_bytes(fmt, N, K) bytes made of ceil(N/128) x ceil(K/256) blocks,
+ * block (t, c) at byte ((t * ceil(K/256)) + c) * B with B = 18432 (NVFP4) or
+ * 17408 (MXFP4).  A block covers output channels [128t, 128t+128) and K
+ * elements [256c, 256c+256):
+ *   [0, 16384)     codes of the 128 channels, 128 bytes each (element 2j of
+ *                  the block in the low nibble of byte j), stored as the
+ *                  128-byte-swizzled image: byte j of channel r at
+ *                  r*128 + ((j/16) XOR (r%8))*16 + j%16.
+ *   [16384, B)     the block's scale atoms (4 for NVFP4, 2 for MXFP4), each
+ *                  512 bytes laid out as in an rs operand (channel r, block b
+ *                  of the atom at (r%32)*16 + ((r/32)%4)*4 + b).
+ * Channels beyond N and elements beyond K hold zero codes and zero scales.
+ * The GEMM streams one whole block per pipeline stage with a single bulk
+ * copy of consecutive bytes.
  */
 #ifndef RS_H
 #define RS_H
@@ -112,12 +129,13 @@ RS_API size_t rs_operand_sf_offset(rs_format fmt, int rows, int K);
 /* Activation operand sizes: `rows` tokens quantized alone (W4A4 input) or,
  * for rs_quantize_residue, pass rows = 2*M. */
 RS_API size_t rs_act_bytes(rs_format fmt, int rows, int K);
-/* Weight operand size, W [N][K] (nn.Linear layout). */
+/* Weight operand size, W [N][K] (nn.Linear layout), rs weight layout. */
 RS_API size_t rs_weight_bytes(rs_format fmt, int N, int K);
-/* Workspace that rs_linear_w4a4 / rs_linear_compensated need for these sizes
- * when given a bf16 input (quantized activations plus split-K partial sums
- * and tile counters).  The workspace must be zero-filled once before its
- * first use; every completed call leaves its counter region zeroed again. */
+/* Workspace that rs_linear_w4a4 / rs_linear_compensated need when given a
+ * bf16 input: room for the quantized activation operand, which plans with
+ * larger M produce in a separate quantizer kernel (small-M plans quantize
+ * inside the GEMM and leave the workspace untouched).  No initialisation is
+ * needed; calls that share a workspace must be ordered (same stream). */
 RS_API size_t rs_workspace_bytes(rs_format fmt, int M, int N, int K, int compensated);
 
 /* ---- tensor scale (App. B.2 Eq. 8) -------------------------------------- */
@@ -132,11 +150,18 @@ RS_API rs_status rs_compute_tensor_scale(const void *x_bf16, int64_t n, float *a
 /* ---- quantizers (Sec. 4.4, App. B.2 Algorithm 1) ------------------------- */
 
 /* Quantize bf16 rows x[rows][ldx] (device, first K columns used) into an rs
- * operand q_out (device, rs_operand_bytes(fmt, rows, K) bytes).  Used for the
- * offline weight quantization (Fig. 1c) and for W4A4 activations.  alpha
- * (device, one float) is the NVFP4 tensor scale; ignored for MXFP4. */
+ * operand q_out (device, rs_operand_bytes(fmt, rows, K) bytes), the W4A4
+ * activation input (Fig. 1c).  alpha (device, one float) is the NVFP4 tensor
+ * scale; ignored for MXFP4. */
 RS_API rs_status rs_quantize_fp4(rs_format fmt, int rows, int K, const void *x_bf16, int64_t ldx,
                           const float *alpha, void *q_out, rs_stream_t stream);
+
+/* Offline weight quantization (Fig. 1c): W[N][ldw] (device, bf16, first K
+ * columns) into the rs weight layout wq_out (device, rs_weight_bytes(fmt, N,
+ * K) bytes), same quantization rule as the activations; alpha (device) is
+ * the weight's NVFP4 tensor scale (ignored for MXFP4). */
+RS_API rs_status rs_quantize_weight(rs_format fmt, int N, int K, const void *w_bf16, int64_t ldw,
+                                    const float *alpha, void *wq_out, rs_stream_t stream);
 
 /* Fused base + residue quantizer (Alg. 1; Sec. 4.4): one pass over x[M][ldx]
  * forms X^, the residue R = X - X^ in registers and R^, and writes the paired
@@ -149,10 +174,19 @@ RS_API rs_status rs_quantize_residue(rs_format fmt, int M, int K, const void *x_
 
 /* Uncompensated W4A4 linear (Fig. 1c): Y[M][N] = alpha_x alpha_w * X^ W^T.
  * Exactly one of x_bf16 (device, [M][K] contiguous, quantized inside the
- * call into the workspace) and xq (device, rs operand with M rows) is
- * non-NULL.  wq: rs operand of W [N][K].  alpha_x / alpha_w (device floats)
- * are required for NVFP4.  y (device): [M][N] row-major, bf16 or fp32.
- * workspace (device): at least rs_workspace_bytes(fmt, M, N, K, 0) bytes. */
+ * call) and xq (device, rs operand with M rows) is non-NULL.  wq: rs weight
+ * of W [N][K] from rs_quantize_weight.  alpha_x / alpha_w (device floats) are
+ * required for NVFP4.  y (device): [M][N] row-major, bf16 or fp32.
+ * workspace (device): at least rs_workspace_bytes(fmt, M, N, K, 0) bytes when
+ * x_bf16 is given; may be NULL with xq.
+ *
+ * The GEMM is launched with programmatic stream serialization: it may start
+ * while the previous kernel in the stream is still running and begins
+ * streaming wq before it waits for that kernel.  wq must therefore not be
+ * written by a kernel that signals early completion (griddepcontrol
+ * launch_dependents) right before this call; librs's own kernels that write
+ * weights never do.  Inputs x / xq / alpha and the output y are touched only
+ * after the previous kernel has completed. */
 RS_API rs_status rs_linear_w4a4(rs_format fmt, int M, int N, int K,
                          const void *x_bf16, const void *xq, const float *alpha_x,
                          const void *wq, const float *alpha_w,

@@ -37,7 +37,9 @@ def prepare_weight(fmt, w_bf16):
     N, K = w_bf16.shape
     w_gpu = w_bf16.to(DEV)
     aw = gpu_tensor_scale(w_gpu) if fmt == 0 else None
-    wq = gpu_quantize(fmt, w_gpu, aw, paired=False)
+    wq = torch.full((rs.rs_weight_bytes(fmt, N, K),), 0xCD, dtype=torch.uint8, device=DEV)
+    rs.rs_quantize_weight(fmt, w_gpu, aw, wq)
+    torch.cuda.synchronize()
     wb = workloads.bf16_bits(w_bf16)
     aw_or = oracle.tensor_scale(wb) if fmt == 0 else np.float32(0)
     cw, sw, _ = oracle.quantize(fmt, wb, aw_or)
@@ -51,7 +53,7 @@ def gpu_linear(fmt, compensated, x_bf16, wprep, out_dtype=torch.float32, prequan
     if fmt == 0 and ax is None:
         ax = gpu_tensor_scale(x_gpu)
     y = torch.full((M, N), float("nan"), dtype=out_dtype, device=DEV)
-    ws = rs.zeros_workspace(fmt, M, N, K, compensated)
+    ws = rs.empty_workspace(fmt, M, N, K, compensated)
     fn = rs.rs_linear_compensated if compensated else rs.rs_linear_w4a4
     if prequantized:
         xq = gpu_quantize(fmt, x_gpu, ax, paired=compensated)

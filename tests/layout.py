@@ -50,3 +50,42 @@ def padding_sf_bytes(buf, fmt, rows, K):
             atom = (r // 128) * na + b // 4
             out.append(buf[off + atom * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)])
     return np.array(out, np.uint8)
+
+
+def weight_block_bytes(fmt):
+    return 16384 + (4 if fmt == 0 else 2) * 512
+
+
+def weight_bytes(fmt, N, K):
+    return (N + 127) // 128 * ((K + 255) // 256) * weight_block_bytes(fmt)
+
+
+def unpack_weight(buf, fmt, N, K):
+    """rs weight (tiled, swizzled) -> logical codes [N][K/2], scales [N][K/bs];
+    also returns whether every padding byte is zero."""
+    buf = np.asarray(buf, np.uint8)
+    wb = weight_block_bytes(fmt)
+    nt, nc = (N + 127) // 128, (K + 255) // 256
+    blocks = buf[: nt * nc * wb].reshape(nt, nc, wb)
+    codes_img = blocks[:, :, :16384].reshape(nt, nc, 128, 128)
+    r = np.arange(128)[:, None]
+    j = np.arange(128)[None, :]
+    src = ((j // 16) ^ (r % 8)) * 16 + j % 16           # position of byte j of row r
+    codes_full = np.take_along_axis(codes_img, np.broadcast_to(src, codes_img.shape), axis=3)
+    codes_full = codes_full.transpose(0, 2, 1, 3).reshape(nt * 128, nc * 128)
+    bs = block_size(fmt)
+    apb = 256 // (4 * bs)                                  # atoms per block
+    atoms = blocks[:, :, 16384:].reshape(nt, nc, apb, 512)
+    nb_full = nc * 256 // bs
+    rr = np.arange(nt * 128)[:, None]
+    bb = np.arange(nb_full)[None, :]
+    t = rr // 128
+    c = bb // (256 // bs)
+    a = (bb % (256 // bs)) // 4
+    off = (rr % 32) * 16 + ((rr % 128) // 32) * 4 + bb % 4
+    sf_full = atoms[t, c, a, off]
+    codes = codes_full[:N, : K // 2].copy()
+    sf = sf_full[:N, : K // bs].copy()
+    pad_ok = (not codes_full[N:].any() and not codes_full[:, K // 2:].any()
+              and not sf_full[N:].any() and not sf_full[:, K // bs:].any())
+    return codes, sf, pad_ok

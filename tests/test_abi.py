@@ -50,7 +50,8 @@ def test_status_strings(librs):
 def test_operand_sizes_follow_documented_layout(librs, fmt, rows, K):
     assert librs.rs_operand_bytes(fmt, rows, K) == layout.operand_bytes(fmt, rows, K)
     assert librs.rs_operand_sf_offset(fmt, rows, K) == layout.sf_offset(rows, K)
-    assert librs.rs_act_bytes(fmt, rows, K) == librs.rs_weight_bytes(fmt, rows, K)
+    assert librs.rs_act_bytes(fmt, rows, K) == librs.rs_operand_bytes(fmt, rows, K)
+    assert librs.rs_weight_bytes(fmt, rows, K) == layout.weight_bytes(fmt, rows, K)
 
 
 def test_size_functions_reject_bad_shapes(librs):
@@ -91,6 +92,7 @@ def test_linear_argument_checks(librs):
     assert _lin(librs, wsb=16) == 5                           # workspace too small
     assert _lin(librs, ws=None) == 5
     assert _lin(librs, fn="rs_linear_w4a4", wsb=0) == 5
+    assert _lin(librs, x=None, xq=FAKE, ws=None, wsb=0, w=FAKE_ODD) == 2  # xq path needs no workspace
 
 
 def test_quantizer_argument_checks(librs):
@@ -104,6 +106,11 @@ def test_quantizer_argument_checks(librs):
     assert q(0, 0, 64, None, 64, None, None, None) == 0       # empty input
     f = librs.rs_quantize_fp4
     assert f(0, 4, 64, None, 64, FAKE, FAKE, None) == 1
+    wq = librs.rs_quantize_weight
+    assert wq(0, 4, 48, FAKE, 64, FAKE, FAKE, None) == 3
+    assert wq(0, 4, 64, FAKE, 64, None, FAKE, None) == 1
+    assert wq(1, 4, 64, FAKE, 64, None, FAKE_ODD, None) == 2
+    assert wq(0, 0, 64, None, 64, None, None, None) == 0
     assert f(1, 4, 64, FAKE, 64, None, FAKE_ODD, None) == 2
     assert librs.rs_compute_tensor_scale(FAKE, -1, FAKE, None) == 1
     assert librs.rs_compute_tensor_scale(FAKE, 16, None, None) == 1

@@ -102,9 +102,9 @@ def _sampled_parity(fmt, compensated, recipe, M, n_rows=256, n_tok=None, seed=0)
     ax = gpu_tensor_scale(x_gpu) if fmt == 0 else None
     aw = gpu_tensor_scale(w_gpu) if fmt == 0 else None
     wq = torch.empty(rs.rs_weight_bytes(fmt, N, K), dtype=torch.uint8, device=DEV)
-    rs.rs_quantize_fp4(fmt, w_gpu, aw, wq)
+    rs.rs_quantize_weight(fmt, w_gpu, aw, wq)
     y = torch.empty((M, N), dtype=torch.float32, device=DEV)
-    ws = rs.zeros_workspace(fmt, M, N, K, compensated)
+    ws = rs.empty_workspace(fmt, M, N, K, compensated)
     fn = rs.rs_linear_compensated if compensated else rs.rs_linear_w4a4
     fn(fmt, M, N, K, x=x_gpu, alpha_x=ax, wq=wq, alpha_w=aw, y=y, workspace=ws)
     torch.cuda.synchronize()

@@ -74,11 +74,34 @@ def test_quantizer_bit_exact_workloads(fmt, recipe, M):
     _check(fmt, x, False)
 
 
+def _check_weight(fmt, w):
+    import oracle
+    from block_scaled_quantized_gb300 import rs
+    N, K = w.shape
+    wb = workloads.bf16_bits(w)
+    a_or = oracle.tensor_scale(wb) if fmt == 0 else np.float32(0)
+    a_gpu = torch.tensor([a_or], dtype=torch.float32, device=DEV) if fmt == 0 else None
+    buf = torch.full((rs.rs_weight_bytes(fmt, N, K),), 0xAB, dtype=torch.uint8, device=DEV)
+    assert buf.numel() == layout.weight_bytes(fmt, N, K)
+    rs.rs_quantize_weight(fmt, w.to(DEV), a_gpu, buf)
+    torch.cuda.synchronize()
+    codes, sf, pad_ok = layout.unpack_weight(buf.cpu().numpy(), fmt, N, K)
+    cw, sw, _ = oracle.quantize(fmt, wb, a_or)
+    np.testing.assert_array_equal(codes, cw)
+    np.testing.assert_array_equal(sf, sw)
+    assert pad_ok
+
+
 @pytest.mark.parametrize("fmt,recipe", [(0, "attn_proj_k4096"), (0, "mlp_gate_up"), (1, "mx_k5120_n27648"),
                                         (0, "prefill_k8192")])
 def test_weight_quantization_bit_exact(fmt, recipe):
-    w = workloads.make_w(recipe, N=384)
-    _check(fmt, w, False)
+    _check_weight(fmt, workloads.make_w(recipe, N=384))
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("N,K", [(1, 32), (100, 288), (129, 96), (256, 1024), (300, 4128)])
+def test_weight_quantization_ragged(fmt, N, K):
+    _check_weight(fmt, workloads.random_bf16((N, K), seed=N + K, scale=0.02))
 
 
 def test_quantizer_strided_rows_and_edge_values():
