@@ -374,35 +374,82 @@ __device__ __forceinline__ uint32_t map_dsmem(uint32_t addr, uint32_t rank) {
     return r;
 }
 
+// Bulk copy from this CTA's shared memory into another CTA's shared memory
+// in the cluster, completing bytes on that CTA's mbarrier (both cluster
+// addresses from map_dsmem); 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst_cluster),
+        "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until every committed bulk copy of this thread has finished reading
+// its source.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
 
+// Store 4 / 8 / 16 consecutive 32-bit columns of this warp's lane quarter
+// (lane l of the warp -> tensor-memory lane quarter*32 + l).
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint4 v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint4 (&v)[2]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z),
+                 "r"(v[1].w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint4 (&v)[4]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w),
+        "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ------------------------------------------------------ named CTA barriers --
 
+// Named barrier over `nthreads` threads (non-aligned form: callers may reach
+// it from divergent paths within a warp).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------------ trace build only --
 // Built with -DRS_TRACE, kernels stamp the global timer at phase boundaries
-// into a caller-provided buffer (16 slots per CTA); a normal build compiles
+// into a caller-provided buffer (32 slots per CTA); a normal build compiles
 // the marks away.
 #ifdef RS_TRACE
 #define RS_TRACE_MARK(buf, slot)                                                              \
     do {                                                                                      \
         if (buf) {                                                                            \
             const size_t cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x; \
-            (buf)[cta * 16 + (slot)] = rs::globaltimer_ns();                                  \
+            (buf)[cta * 32 + (slot)] = rs::globaltimer_ns();                                  \
         }                                                                                     \
     } while (0)
 #define RS_TRACE_VALUE(buf, slot, v)                                                          \
     do {                                                                                      \
         if (buf) {                                                                            \
             const size_t cta = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x; \
-            (buf)[cta * 16 + (slot)] = (uint64_t)(v);                                         \
+            (buf)[cta * 32 + (slot)] = (uint64_t)(v);                                         \
         }                                                                                     \
     } while (0)
 #else

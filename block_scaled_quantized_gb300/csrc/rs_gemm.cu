@@ -16,8 +16,10 @@
 //    activation operand, or, for small M, from a quantizing prologue that
 //    converts the CTA's slice of the bf16 input straight into shared memory
 //    (Alg. 1 fused into the GEMM: one launch per linear layer);
-//  * scale atoms go shared memory -> tensor memory with tcgen05.cp
-//    (32x128b.warpx4), where the kind::mxf4nvf4 block-scaled MMA reads them.
+//  * scale atoms go shared memory -> tensor memory through the four epilogue
+//    warps (each writes its lane quarter with tcgen05.st, the image a
+//    32x128b.warpx4 copy would make), where the kind::mxf4nvf4 block-scaled
+//    MMA reads them; the tensor pipe then only runs MMAs.
 //
 // Fold (Sec. 4.3 Eq. 2): with paired rows, the base and residue products of
 // token j are accumulator columns 2j and 2j+1; a 32x32b tensor-memory load
@@ -26,19 +28,22 @@
 //
 // Split-K: when the output tiles alone cannot keep every SM streaming
 // weights, the K range of each tile is split across the CTAs of a thread-
-// block cluster (up to 8); each CTA leaves its folded fp32 partial in shared
-// memory and, after a cluster barrier, every CTA sums one slice of the
-// outputs over all partners' shared memory (DSMEM) in a fixed order.
+// block cluster (up to 8); each CTA owns a slice of the outputs, every CTA
+// writes its folded fp32 partial to its own shared memory and bulk-copies
+// each owner's slice into that owner's receive buffer (DSMEM), completing on
+// the owner's mbarrier; each owner sums its slice in a fixed partner order
+// and writes Y.
 //
 // Programmatic dependent launch: the kernel releases its dependents at once
 // and starts streaming weights before waiting for the previous grid; only
 // the activation / output accesses come after that wait.
 //
-// Warp roles (192 threads): warps 0-3 quantizer (fused plans) and epilogue
-// (tensor-memory lane quarters 0-3), warp 4 bulk/TMA producer, warp 5 TMEM
-// allocator and MMA issuer.  Every wait is bounded (about one second); a wait
-// that runs out sets the device error word and an abort flag, and the CTA
-// drains its copies and exits.
+// Warp roles (384 threads): warp 4 bulk/TMA producer; warp 5 TMEM allocator
+// and MMA issuer; warps 0-3 (tensor-memory lane quarters 0-3) write each
+// stage's scale atoms into tensor memory and then run the epilogue; in fused
+// plans warps 0-3 and 6-11 first run the quantizing prologue.  Every wait is
+// bounded (about one second); a wait that runs out sets the device error
+// word and an abort flag, and the CTA drains its copies and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -51,10 +56,12 @@
 
 namespace rs {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;       // 12 warps
+constexpr int kQuantWarps = 10;     // warps 0-3 and 6-11 quantize in fused plans
+constexpr int kQuantThreads = kQuantWarps * 32;
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;   // 227 KB opt-in per block
-constexpr uint32_t kCtrlBytes = 256;
+constexpr uint32_t kCtrlBytes = 512;
 
 __host__ __device__ constexpr int b_atom_tiles(int bn) { return (bn + 127) / 128; }
 // Shared-memory bytes of one activation stage: codes (bn rows x 128 bytes)
@@ -76,7 +83,7 @@ struct GemmArgs {
     const float* alpha_x;
     const float* alpha_w;
     uint32_t* err;
-    uint64_t* trace;        // trace builds only: 16 timer stamps per CTA
+    uint64_t* trace;        // trace builds only: 32 timer stamps per CTA
     int N, K, M, Rb;
     int n_atoms_k;          // activation operand atoms per row tile along K
     int b_row_tiles;        // scale-atom row tiles of the activation operand
@@ -86,6 +93,7 @@ struct GemmArgs {
     int out_f32;
     int stages;
     int slots;              // fused: resident activation chunks
+    int recv_bytes;         // split-K receive buffer (0 without split)
     int tmem_cols;
 };
 
@@ -94,7 +102,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs g) {
     constexpr int APC = weight_atoms_per_block(FMT);
     constexpr int BT = b_atom_tiles(BN);
-    constexpr int LPA = lanes_per_atom<FMT>();
     constexpr uint32_t WB = weight_block_bytes(FMT);
     constexpr uint32_t B_BYTES = BN * 128;
     constexpr uint32_t BSTAGE = b_stage_bytes(FMT, BN);
@@ -108,11 +115,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* wring = smem;                                   // S x WB
     uint8_t* bregion = smem + (size_t)S * WB;                // S (or slots) x BSTAGE
     const int nbslots = FUSED ? g.slots : S;
-    uint64_t* full = reinterpret_cast<uint64_t*>(bregion + (size_t)nbslots * BSTAGE);
+    uint8_t* recv_region = bregion + (size_t)nbslots * BSTAGE;  // split-K partials from partners
+    const uint32_t recv_base = smem_u32(recv_region);
+    uint64_t* full = reinterpret_cast<uint64_t*>(recv_region + g.recv_bytes);
     uint64_t* empty = full + kMaxStages;
-    uint64_t* accum_full = empty + kMaxStages;
-    uint64_t* b_ready = accum_full + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_ready + 1);
+    uint64_t* sf_ready = empty + kMaxStages;   // per stage: scales in tensor memory
+    uint64_t* accum_full = sf_ready + kMaxStages;
+    uint64_t* red_full = accum_full + 1;       // split-K: all partners' partials received
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_full + 1);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     volatile uint32_t* consumed = tmem_slot + 2;
     volatile uint32_t* issued = tmem_slot + 3;
@@ -134,9 +144,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&sf_ready[s]), 4);  // one arrival per scale-writer warp
         }
         mbar_init(smem_u32(accum_full), 1);
-        mbar_init(smem_u32(b_ready), 1);
+        mbar_init(smem_u32(red_full), 1);
+        if (g.splits > 1) {
+            const int outs0 = g.fold ? BN / 2 : BN;
+            const int per_cta0 = (outs0 + g.splits - 1) / g.splits;
+            mbar_arrive_expect_tx(smem_u32(red_full), (uint32_t)(g.splits * per_cta0 * 512));
+        }
         *abort_flag = 0;
         *consumed = 0;
         *issued = 0;
@@ -168,6 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t tm_acc = tmem;
     const uint32_t tm_sf = tmem + BN;
+    // split-K partners copy into our receive buffer and signal red_full:
+    // every barrier of the cluster must be initialised before that
+    if (g.splits > 1) cluster_sync_all();
 
     // Dependents may start their prologue now; they wait for our completion
     // before they touch anything we read or write.
@@ -215,13 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            bool ok = true;
-            if (FUSED) ok = mbar_wait_bounded(smem_u32(b_ready), 0, abort_flag, g.err);
             int i = 0;
-            for (; ok && i < nck; ++i) {
+            for (; i < nck; ++i) {
                 const int s = i % S;
                 const uint32_t ph = (uint32_t)(i / S) & 1u;
-                if (!mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err)) break;
+                // chunk i's scales are in tensor memory (and, in fused plans,
+                // its activation tile is in shared memory)
+                if (!mbar_wait_bounded(smem_u32(&sf_ready[s]), ph, abort_flag, g.err)) break;
                 if (i == 0) RS_TRACE_MARK(g.trace, 4);
                 if (i == nck - 1) RS_TRACE_MARK(g.trace, 5);
                 tc_fence_after();
@@ -232,13 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tsfb = tsfa + SFA_COLS;
                 const int kleft = g.K - chunk * 256;
                 const int nks = min(4, (kleft + 63) / 64);
-                const int na = FMT == 0 ? nks : (nks + 1) / 2;  // atoms the issued k-steps read
-                const int nb_tiles = FUSED ? 1 : min(BT, g.b_row_tiles - b_tile * BT);
-                for (int a = 0; a < na; ++a)
-                    tc_cp_sf_atom(tsfa + a * 4, sf_atom_desc(sa + kWeightCodeBytes + a * 512));
-                for (int t = 0; t < nb_tiles; ++t)
-                    for (int a = 0; a < na; ++a)
-                        tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sf_atom_desc(sb + B_BYTES + (t * APC + a) * 512));
                 for (int ks = 0; ks < nks; ++ks) {
                     const uint64_t adesc = kmajor_sw128_desc(sa + ks * 32);
                     const uint64_t bdesc = kmajor_sw128_desc(sb + ks * 32);
@@ -255,128 +267,230 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_commit(smem_u32(&empty[s]));
             }
-            *consumed = (uint32_t)i;
             tc_commit(smem_u32(accum_full));  // fires once every issued MMA is done
         }
     } else {
-        // ------------------------------------------------ warps 0-3
-        const int ctid = threadIdx.x;  // 0..127
+        // ------------------------------------------------ warps 0-3, 6-11
+        const bool epi = warp < 4;
+        const int qw = warp < 4 ? warp : warp - 2;  // quantizer warp 0..kQuantWarps-1
+        const int qtid = qw * 32 + lane;
         if (FUSED) {
-            // Quantizing prologue (Alg. 1): this CTA's K slice of every token
-            // -> base (row 2j) and residue (row 2j+1) codes in the swizzled
-            // B tiles, block scales in the B scale atoms.
+            // Quantizing prologue (Alg. 1), one scale block per thread: this
+            // CTA's K slice of every token -> base (row 2j) and residue
+            // (row 2j+1) codes in the swizzled B tiles, scales in the B atoms.
+            constexpr int E = block_elems(FMT);  // 16 (NVFP4) or 32 (MXFP4)
             const uint32_t bbytes = (uint32_t)nck * BSTAGE;
-            for (uint32_t off = (uint32_t)ctid * 16u; off < bbytes; off += 128u * 16u)
+            for (uint32_t off = (uint32_t)qtid * 16u; off < bbytes; off += (uint32_t)kQuantThreads * 16u)
                 *reinterpret_cast<uint4*>(bregion + off) = make_uint4(0u, 0u, 0u, 0u);
-            named_bar_sync(1, 128);
+            named_bar_sync(2, kQuantThreads);
             pdl_wait_prior_grid();
             const float alpha = FMT == 0 ? *g.alpha_x : 0.0f;
-            const int tasks = g.M * nck;
-            for (int task = warp; task < tasks; task += 4) {
-                const int j = task / nck, ci = task % nck;
-                const int k0 = (c0 + ci) * 256 + lane * 8;
-                const bool valid = k0 < g.K;
-                float xf[8];
-                load8_bf16(g.x + (size_t)j * g.K + k0, valid, xf);
-                uint32_t sfq;
-                float xh[8];
-                const uint32_t codes = quant_lane<FMT>(xf, alpha, sfq, xh);
-                const uint32_t sfw = gather_sf_word<FMT>(sfq, lane);
+            const int kbeg = c0 * 256, kend = min(g.K, (c0 + nck) * 256);
+            // codes of one block (element offset kk of the slice) and, gathered
+            // over four consecutive lanes, one scale-atom word
+            auto put = [&](uint32_t rowb, int kk, const uint32_t (&codes)[E / 8], uint32_t sfbyte, bool live) {
+                const int ci = kk / 256;
+                const uint32_t b = (uint32_t)(kk % 256) / 2u;  // byte within the 128-byte row
                 uint8_t* slot = bregion + (size_t)ci * BSTAGE;
-                const uint32_t rb = g.fold ? 2u * (uint32_t)j : (uint32_t)j;
-                *reinterpret_cast<uint32_t*>(slot + sw128_offset(rb, (uint32_t)lane * 4u)) = codes;
-                if ((lane % LPA) == 0)
-                    *reinterpret_cast<uint32_t*>(slot + B_BYTES + (lane / LPA) * 512 + (rb % 32) * 16 + (rb / 32) * 4) = sfw;
-                if (g.fold) {
-                    float r[8];
-                    residue8(xf, xh, r);
-                    uint32_t sfr;
-                    float rh[8];
-                    const uint32_t rcodes = quant_lane<FMT>(r, alpha, sfr, rh);
-                    const uint32_t sfrw = gather_sf_word<FMT>(sfr, lane);
-                    const uint32_t rr = rb + 1u;
-                    *reinterpret_cast<uint32_t*>(slot + sw128_offset(rr, (uint32_t)lane * 4u)) = rcodes;
-                    if ((lane % LPA) == 0)
-                        *reinterpret_cast<uint32_t*>(slot + B_BYTES + (lane / LPA) * 512 + (rr % 32) * 16 + (rr / 32) * 4) =
-                            sfrw;
+                if (live) {
+                    if constexpr (E == 16) {
+                        *reinterpret_cast<uint2*>(slot + sw128_offset(rowb, b)) = make_uint2(codes[0], codes[1]);
+                    } else {
+                        *reinterpret_cast<uint4*>(slot + sw128_offset(rowb, b)) =
+                            make_uint4(codes[0], codes[E / 8 - 3], codes[E / 8 - 2], codes[E / 8 - 1]);
+                    }
+                }
+                const int base = lane & ~3;
+                const uint32_t w = __shfl_sync(0xFFFFFFFFu, sfbyte, base) |
+                                   (__shfl_sync(0xFFFFFFFFu, sfbyte, base + 1) << 8) |
+                                   (__shfl_sync(0xFFFFFFFFu, sfbyte, base + 2) << 16) |
+                                   (__shfl_sync(0xFFFFFFFFu, sfbyte, base + 3) << 24);
+                if (live && (lane & 3) == 0) {
+                    const int a = (kk % 256) / atom_k(FMT);
+                    *reinterpret_cast<uint32_t*>(slot + B_BYTES + a * 512 + (rowb % 32) * 16 + (rowb / 32) * 4) = w;
+                }
+            };
+            // flat mapping: thread qtid takes scale blocks qtid, qtid + T, ...
+            // (T = quantizer threads); four consecutive lanes hold the four
+            // blocks of one scale-atom word.  All loads of a batch go out
+            // before any arithmetic.
+            const int bpr = nck * 256 / E;  // blocks per token row in this slice
+            const int total = g.M * bpr;
+            constexpr int kBatch = 32 / E;  // blocks per thread per batch
+            // the loop bound is per warp (fw): put() shuffles across all 32 lanes
+            for (int fw = qw * 32; fw < total; fw += kBatch * kQuantThreads) {
+                const int f0 = fw + lane;
+                float xs[kBatch][E];
+#pragma unroll
+                for (int r = 0; r < kBatch; ++r) {
+                    const int f = f0 + r * kQuantThreads;
+                    const int j = f / bpr, kk = (f % bpr) * E;
+                    const bool live = f < total && kbeg + kk < kend;
+#pragma unroll
+                    for (int q = 0; q < E / 8; ++q) {
+                        float v8[8];
+                        load8_bf16(g.x + (size_t)j * g.K + kbeg + kk + 8 * q, live, v8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) xs[r][8 * q + e] = v8[e];
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < kBatch; ++r) {
+                    if (fw + r * kQuantThreads >= total) break;  // whole warp past the end
+                    const int f = f0 + r * kQuantThreads;
+                    const int j = f / bpr, kk = (f % bpr) * E;
+                    const bool live = f < total && kbeg + kk < kend;
+                    uint32_t sfq, codes[E / 8];
+                    float xh[E];
+                    quant_block<FMT, E>(xs[r], alpha, sfq, codes, xh);
+                    const uint32_t rb = g.fold ? 2u * (uint32_t)j : (uint32_t)j;
+                    put(rb, kk, codes, sfq, live);
+                    if (g.fold) {
+                        float rr[E];
+#pragma unroll
+                        for (int e = 0; e < E; ++e) rr[e] = __fsub_rn(xs[r][e], xh[e]);  // residue (Alg. 1 line 6)
+                        uint32_t sfr, rcodes[E / 8];
+                        float rh[E];
+                        quant_block<FMT, E>(rr, alpha, sfr, rcodes, rh);
+                        put(rb + 1u, kk, rcodes, sfr, live);
+                    }
                 }
             }
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (ctid == 0) mbar_arrive(smem_u32(b_ready));
-        } else {
+            named_bar_sync(2, kQuantThreads);
+            if (qtid == 0) RS_TRACE_MARK(g.trace, 8);
+        } else if (epi) {
             pdl_wait_prior_grid();  // before writing the output
         }
 
-        // ---------------------------------------------- epilogue
-        bool ok = mbar_wait_bounded(smem_u32(accum_full), 0, abort_flag, g.err);
-        if (ctid == 0) RS_TRACE_MARK(g.trace, 6);
-        named_bar_sync(1, 128);
-        ok = ok && (*abort_flag == 0);
-        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-        tc_fence_after();
-        const float gsc = FMT == 0 ? __fmul_rn(*g.alpha_x, *g.alpha_w) : 1.0f;
-        float* red = reinterpret_cast<float*>(wring);  // split-K partial (the weight ring is idle now)
-        auto emit = [&](int j, float z) {
-            if (g.splits > 1) {
-                red[j * 128 + row] = z;
-            } else if (n < g.N && m0 + j < g.M) {
-                const float val = __fmul_rn(gsc, z);
-                const size_t idx = (size_t)(m0 + j) * g.N + n;
-                if (g.out_f32) reinterpret_cast<float*>(g.y)[idx] = val;
-                else reinterpret_cast<__nv_bfloat16*>(g.y)[idx] = __float2bfloat16_rn(val);
-            }
-        };
-        if (ok) {
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 16) {
-                float v[16];
-                tmem_ld16(tm_acc + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
-                if (g.fold) {
+        if (epi) {
+            // ---------------------------------------------- scales -> TMEM
+            // Each warp writes its own lane quarter with the 32 x 16-byte rows
+            // of every scale atom (the image a 32x128b.warpx4 copy makes).
+            const uint32_t quarter = (uint32_t)(warp * 32) << 16;
+            int i = 0;
+            for (; i < nck; ++i) {
+                const int s = i % S;
+                const uint32_t ph = (uint32_t)(i / S) & 1u;
+                // warp-uniform outcome: the tcgen05.st below are warp-collective
+                const bool landed = mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err);
+                if (!__all_sync(0xFFFFFFFFu, landed)) break;
+                const uint8_t* wst = wring + (size_t)s * WB + kWeightCodeBytes;
+                const uint8_t* bst = bregion + (size_t)(FUSED ? i : s) * BSTAGE + B_BYTES;
+                const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS) + quarter;
+                const uint32_t tsfb = tsfa + SFA_COLS;
+                if constexpr (BT == 1) {
+                    // every atom of the chunk in one store per operand (atoms a
+                    // ragged K tail does not read are stale but never used)
+                    uint4 va[APC], vb[APC];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) emit(c / 2 + u, __fadd_rn(v[2 * u], v[2 * u + 1]));  // Fold
+                    for (int a = 0; a < APC; ++a) {
+                        va[a] = *reinterpret_cast<const uint4*>(wst + a * 512 + lane * 16);
+                        vb[a] = *reinterpret_cast<const uint4*>(bst + a * 512 + lane * 16);
+                    }
+                    if constexpr (APC == 4) {
+                        tmem_st16(tsfa, va);
+                        tmem_st16(tsfb, vb);
+                    } else {
+                        tmem_st8(tsfa, va);
+                        tmem_st8(tsfb, vb);
+                    }
                 } else {
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) emit(c + u, v[u]);
+                    const int kleft = g.K - (c0 + i) * 256;
+                    const int nks = min(4, (kleft + 63) / 64);
+                    const int na = FMT == 0 ? nks : (nks + 1) / 2;
+                    const int nb_tiles = min(BT, g.b_row_tiles - b_tile * BT);
+                    for (int a = 0; a < na; ++a)
+                        tmem_st4(tsfa + a * 4, *reinterpret_cast<const uint4*>(wst + a * 512 + lane * 16));
+                    for (int t = 0; t < nb_tiles; ++t)
+                        for (int a = 0; a < na; ++a)
+                            tmem_st4(tsfb + (a * BT + t) * 4,
+                                     *reinterpret_cast<const uint4*>(bst + (t * APC + a) * 512 + lane * 16));
                 }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sf_ready[s]));
             }
-        } else if (g.splits > 1) {
-            for (int j = 0; j < outs; ++j) red[j * 128 + row] = 0.0f;
-        }
-        if (ctid == 0) RS_TRACE_MARK(g.trace, 7);
-    }
+            if (warp == 0 && lane == 0) *consumed = (uint32_t)i;
 
-    // ---------------------------------------------------- split-K reduction
-    __syncwarp();
-    if (g.splits > 1) {
-        cluster_sync_all();  // partials of every CTA in the cluster are visible
-        if (warp < 4) {
+            // ---------------------------------------------- epilogue
+            const int ctid = threadIdx.x;  // 0..127
+            bool ok = mbar_wait_bounded(smem_u32(accum_full), 0, abort_flag, g.err);
+            if (ctid == 0) RS_TRACE_MARK(g.trace, 6);
+            named_bar_sync(1, 128);
+            ok = ok && (*abort_flag == 0);
+            ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+            tc_fence_after();
             const float gsc = FMT == 0 ? __fmul_rn(*g.alpha_x, *g.alpha_w) : 1.0f;
             const int per_cta = (outs + g.splits - 1) / g.splits;
-            const uint32_t red0 = smem_u32(wring);
-            for (int jj = 0; jj < per_cta; ++jj) {
-                const int j = split * per_cta + jj;
-                const int m = m0 + j;
-                if (j >= outs || m >= g.M) break;
-                const uint32_t off = red0 + (uint32_t)(j * 128 + row) * 4u;
-                float part[kMaxSplits];
-#pragma unroll
-                for (int r = 0; r < kMaxSplits; ++r)
-                    part[r] = r < g.splits ? ld_dsmem_f32(map_dsmem(off, (uint32_t)r)) : 0.0f;
-                float acc = 0.0f;
-#pragma unroll
-                for (int r = 0; r < kMaxSplits; ++r)
-                    if (r < g.splits) acc = __fadd_rn(acc, part[r]);
-                if (n < g.N && *abort_flag == 0) {
-                    const float val = __fmul_rn(gsc, acc);
-                    const size_t idx = (size_t)m * g.N + n;
+            // split-K: this CTA's partial, [j][channel], in the idle weight ring
+            float* part = reinterpret_cast<float*>(wring);
+            auto emit = [&](int j, float z) {
+                if (g.splits > 1) {
+                    part[j * 128 + row] = z;
+                } else if (n < g.N && m0 + j < g.M) {
+                    const float val = __fmul_rn(gsc, z);
+                    const size_t idx = (size_t)(m0 + j) * g.N + n;
                     if (g.out_f32) reinterpret_cast<float*>(g.y)[idx] = val;
                     else reinterpret_cast<__nv_bfloat16*>(g.y)[idx] = __float2bfloat16_rn(val);
                 }
+            };
+            if (ok) {
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    float v[16];
+                    tmem_ld16(tm_acc + quarter + (uint32_t)c, v);
+                    if (g.fold) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) emit(c / 2 + u, __fadd_rn(v[2 * u], v[2 * u + 1]));  // Fold
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) emit(c + u, v[u]);
+                    }
+                }
+            } else if (g.splits > 1) {
+                for (int j = 0; j < outs; ++j) emit(j, 0.0f);
+            }
+            if (g.splits > 1) {
+                // send each owner its slice of outputs: one bulk copy per owner
+                // into its receive buffer at our rank's slot
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                if (ctid == 0) {
+                    const uint32_t slice = (uint32_t)per_cta * 128u * 4u;
+                    for (int o = 0; o < g.splits; ++o) {
+                        const uint32_t dst = map_dsmem(recv_base + (uint32_t)split * slice, (uint32_t)o);
+                        const uint32_t bar = map_dsmem(smem_u32(red_full), (uint32_t)o);
+                        bulk_copy_to_cluster(dst, smem_u32(part) + (uint32_t)o * slice, slice, bar);
+                    }
+                    bulk_commit_group();
+                }
+            }
+            if (ctid == 0) RS_TRACE_MARK(g.trace, 7);
+            if (g.splits > 1) {
+                // own slice: sum the partners' partials in rank order
+                const bool got = mbar_wait_bounded(smem_u32(red_full), 0, abort_flag, g.err);
+                const float* recv = reinterpret_cast<const float*>(recv_region);
+                for (int jj = 0; got && jj < per_cta; ++jj) {
+                    const int j = split * per_cta + jj;
+                    const int m = m0 + j;
+                    if (j >= outs || m >= g.M) break;
+                    float acc = 0.0f;
+                    for (int r = 0; r < g.splits; ++r) acc = __fadd_rn(acc, recv[(r * per_cta + jj) * 128 + row]);
+                    if (n < g.N && *abort_flag == 0) {
+                        const float val = __fmul_rn(gsc, acc);
+                        const size_t idx = (size_t)m * g.N + n;
+                        if (g.out_f32) reinterpret_cast<float*>(g.y)[idx] = val;
+                        else reinterpret_cast<__nv_bfloat16*>(g.y)[idx] = __float2bfloat16_rn(val);
+                    }
+                }
+                if (ctid == 0) bulk_wait_group_read0();  // our outgoing copies have read their source
             }
         }
-        cluster_sync_all();  // nobody leaves while partners still read its partial
     }
+
+    __syncwarp();
     if (threadIdx.x == 0) RS_TRACE_MARK(g.trace, 9);
 
     // ---------------------------------------------------- teardown
@@ -400,9 +514,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------- host --
 
-static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots) {
+static size_t recv_bytes_for(int splits, int outs) {
+    if (splits <= 1) return 0;
+    const int per_cta = (outs + splits - 1) / splits;
+    return align_up((size_t)splits * per_cta * 128 * sizeof(float), 1024);
+}
+
+static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots, size_t recv) {
     const size_t b = fused ? (size_t)slots * b_stage_bytes(fmt, bn) : (size_t)stages * b_stage_bytes(fmt, bn);
-    return 1024 + (size_t)stages * weight_block_bytes(fmt) + b + kCtrlBytes;
+    return 1024 + (size_t)stages * weight_block_bytes(fmt) + b + recv + kCtrlBytes;
 }
 
 static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, int split_cap, bool allow_fused) {
@@ -434,31 +554,34 @@ static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, 
     }
     p.splits = best_s;
     const int max_chunks = (p.chunks + p.splits - 1) / p.splits;
+    const int outs = fold ? p.bn / 2 : p.bn;
+    const size_t recv = recv_bytes_for(p.splits, outs);
     p.fused = (allow_fused && p.b_tiles == 1 && p.bn <= 32) ? 1 : 0;
     int stages = std::min(kMaxStages, max_chunks);
-    while (stages > 1 && plan_smem(fmt, p.bn, stages, p.fused, max_chunks) > kSmemLimit) --stages;
-    if (p.fused && plan_smem(fmt, p.bn, stages, true, max_chunks) > kSmemLimit) {
+    while (stages > 1 && plan_smem(fmt, p.bn, stages, p.fused, max_chunks, recv) > kSmemLimit) --stages;
+    if (p.fused && plan_smem(fmt, p.bn, stages, true, max_chunks, recv) > kSmemLimit) {
         p.fused = 0;
         stages = std::min(kMaxStages, max_chunks);
-        while (stages > 1 && plan_smem(fmt, p.bn, stages, false, 0) > kSmemLimit) --stages;
+        while (stages > 1 && plan_smem(fmt, p.bn, stages, false, 0, recv) > kSmemLimit) --stages;
     }
     p.stages = std::max(stages, 1);
-    const int outs = fold ? p.bn / 2 : p.bn;
-    if (p.splits > 1 && (size_t)outs * 128 * sizeof(float) > (size_t)p.stages * weight_block_bytes(fmt)) {
-        // the split-K partial lives in the idle weight ring; without room, no split
+    // the split-K partial is sent from the idle weight ring; without room
+    // for it (or for the receive buffer), no split
+    if (p.splits > 1 && (plan_smem(fmt, p.bn, p.stages, p.fused, p.fused ? max_chunks : 0, recv) > kSmemLimit ||
+                         recv > (size_t)p.stages * weight_block_bytes(fmt)))
         return plan_impl(fmt, fold, M, N, K, num_sms, 1, allow_fused);
-    }
     p.slots = p.fused ? max_chunks : 0;
+    p.recv_bytes = (int)recv;
     // Two CTAs can share an SM when the shared memory allows it; keep the
     // tensor-memory allocation within half of the SM's 512 columns then.
-    p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots);
+    p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots, recv);
     int cols = p.bn + p.stages * sf_cols_per_stage(fmt, p.bn);
     if (p.smem_bytes <= kSmemLimit / 2) {
         while (cols > 256 && p.stages > 1) {
             --p.stages;
             cols = p.bn + p.stages * sf_cols_per_stage(fmt, p.bn);
         }
-        p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots);
+        p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots, recv);
     }
     int alloc = 32;
     while (alloc < cols) alloc *= 2;
@@ -581,6 +704,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
     a.out_f32 = c.out_f32;
     a.stages = p.stages;
     a.slots = p.slots;
+    a.recv_bytes = p.recv_bytes;
     a.tmem_cols = p.tmem_cols;
 #define RS_CASE(F, B, FU)                                                      \
     if (p.fmt == F && p.bn == B && (p.fused != 0) == FU) return launch_typed<F, B, FU>(p, tb, a, stream);
@@ -594,8 +718,8 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
 }  // namespace rs
 
 #ifdef RS_TRACE
-// Trace builds only: set the device buffer (16 uint64 per CTA) that the next
-// GEMM launches stamp; NULL turns tracing off.
+// Trace builds only: set the device buffer (32 uint64 per CTA) that the next
+// GEMM launches stamp (32 per CTA); NULL turns tracing off.
 extern "C" __attribute__((visibility("default"))) void rs_debug_set_trace(void* buf) {
     rs::g_trace = static_cast<uint64_t*>(buf);
 }

@@ -43,6 +43,7 @@ struct GemmPlan {
     int stages;      // pipeline depth
     int fused;       // quantize the activations inside the GEMM
     int slots;       // fused: activation chunks resident in shared memory
+    int recv_bytes;  // split-K receive buffer in shared memory
     int tmem_cols;   // tensor-memory columns to allocate
     size_t smem_bytes;
 };

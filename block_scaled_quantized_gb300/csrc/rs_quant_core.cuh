@@ -91,6 +91,36 @@ __device__ __forceinline__ uint32_t gather_sf_word(uint32_t sfbyte, int lane) {
 template <int FMT>
 __host__ __device__ constexpr int lanes_per_atom() { return FMT == 0 ? 8 : 16; }
 
+// One whole scale block per thread (16 elements NVFP4, 32 MXFP4): the block
+// amax, scale and multiplier are computed once, and the E element codes come
+// back packed 8 per 32-bit word (element e of the block in bits 4(e%8).. of
+// word e/8).  Same arithmetic per element as quant_lane; the amax is a max,
+// so its evaluation order does not change it.
+template <int FMT, int E>
+__device__ __forceinline__ void quant_block(const float (&xf)[E], float alpha, uint32_t& sf, uint32_t (&codes)[E / 8],
+                                            float (&xh)[E]) {
+    float am0 = 0.0f, am1 = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+        am0 = fmaxf(am0, fabsf(xf[e]));
+        am1 = fmaxf(am1, fabsf(xf[e + 1]));
+    }
+    const float am = fmaxf(am0, am1);
+    float st, mul;
+    sf = FMT == 0 ? nv_block_scale(am, alpha, st, mul) : mx_block_scale(am, st, mul);
+#pragma unroll
+    for (int w = 0; w < E / 8; ++w) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(xf[8 * w + e], mul);
+        codes[w] = e2m1_encode8(v);
+        float d[8];
+        e2m1_decode8(codes[w], d);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xh[8 * w + e] = __fmul_rn(st, d[e]);
+    }
+}
+
 // Load eight bf16 values (16 bytes) as fp32, or zeros when !valid.
 __device__ __forceinline__ void load8_bf16(const uint16_t* p, bool valid, float (&xf)[8]) {
     if (valid) {
