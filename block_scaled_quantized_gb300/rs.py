@@ -27,7 +27,7 @@ STATUS = {0: "RS_OK", 1: "RS_ERR_INVALID_ARG", 2: "RS_ERR_ALIGNMENT", 3: "RS_ERR
 EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_offset", "rs_act_bytes",
            "rs_weight_bytes", "rs_workspace_bytes", "rs_compute_tensor_scale", "rs_quantize_fp4",
            "rs_quantize_weight", "rs_quantize_residue", "rs_linear_w4a4", "rs_linear_compensated",
-           "rs_get_device_error"]
+           "rs_linear_compensated_noalloc", "rs_get_device_error"]
 
 
 class RsError(RuntimeError):
@@ -56,6 +56,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_quantize_residue": ([I, I, I, P, I64, P, P, P], I),
         "rs_linear_w4a4": ([I, I, I, I, P, P, P, P, P, P, I, P, SZ, P], I),
         "rs_linear_compensated": ([I, I, I, I, P, P, P, P, P, P, I, P, SZ, P], I),
+        "rs_linear_compensated_noalloc": ([I, I, I, I, P, P, P, P, P, I, P], I),
         "rs_get_device_error": ([P], I),
     }
     for name, (args, res) in sig.items():
@@ -165,6 +166,17 @@ def rs_linear_w4a4(fmt: int, M: int, N: int, K: int, x=None, xq=None, alpha_x=No
 def rs_linear_compensated(fmt: int, M: int, N: int, K: int, x=None, xq_paired=None, alpha_x=None, wq=None,
                           alpha_w=None, y=None, workspace=None, stream=None):
     _linear("rs_linear_compensated", fmt, M, N, K, x, xq_paired, alpha_x, wq, alpha_w, y, workspace, stream)
+
+
+def rs_linear_compensated_noalloc(fmt: int, M: int, N: int, K: int, x=None, alpha_x=None, wq=None,
+                                  alpha_w=None, y=None, stream=None):
+    """Compensated linear without a workspace, for callers that cannot
+    allocate device memory: the quantized activations go to librs's fixed
+    device array (see include/rs.h)."""
+    out = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
+    _check("rs_linear_compensated_noalloc",
+           lib().rs_linear_compensated_noalloc(fmt, M, N, K, _ptr(x), _ptr(alpha_x), _ptr(wq), _ptr(alpha_w),
+                                               _ptr(y), out, _stream(stream)))
 
 
 def rs_get_device_error(stream=None) -> int:

@@ -206,6 +206,38 @@ RS_API rs_status rs_linear_compensated(rs_format fmt, int M, int N, int K,
                                 void *y, rs_out_dtype out_dtype,
                                 void *workspace, size_t ws_bytes, rs_stream_t stream);
 
+/* ---- compensated linear without any device allocation -------------------- */
+
+/* Size of the fixed device array that rs_linear_compensated_noalloc uses in
+ * place of a workspace (4 MiB).  Every GPU that loads librs holds it until the
+ * process exits. */
+#define RS_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* The paper has no counterpart to this entry point: it exists for callers
+ * that cannot allocate device memory, such as a plugin that another
+ * framework hands only its input and output buffers, or a process whose
+ * device footprint must stay fixed after start-up.
+ *
+ * Same result as rs_linear_compensated with a bf16 input x_bf16 ([M][K],
+ * device, contiguous), but the quantized activations (the paired base and
+ * residue operand, rs_act_bytes(fmt, 2*M, K) bytes) go to a fixed device
+ * array of RS_NOALLOC_SCRATCH_BYTES inside librs instead of a caller
+ * workspace.  Nothing is allocated: no cudaMalloc, no cudaFree.
+ *   - Sizes whose operand does not fit the array are rejected with
+ *     RS_ERR_WORKSPACE before anything is enqueued (NVFP4, K = 4096: up to
+ *     M = 904 fits; rs_act_bytes(fmt, 2*M, K) gives the exact size).
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array per device, which keeps the last
+ *     call's contents; calls that overlap on the GPU (different streams
+ *     without ordering between them) race on it.  Calls ordered on one
+ *     stream are safe: each call rewrites every byte it later reads.
+ * Other arguments, alignment rules and errors as for rs_linear_compensated. */
+RS_API rs_status rs_linear_compensated_noalloc(rs_format fmt, int M, int N, int K, const void *x_bf16,
+                                               const float *alpha_x, const void *wq, const float *alpha_w,
+                                               void *y, rs_out_dtype out_dtype, rs_stream_t stream);
+
 /* ---- device error word --------------------------------------------------- */
 
 /* Synchronizes `stream`, then returns and clears the device error word of the
