@@ -157,7 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *consumed = 0;
         *issued = 0;
         fence_mbarrier_init();
-        pol_w = l2_policy_evict_first();  // weights are streamed once per call
+        // a single activation tile reads each weight block once: stream it;
+        // several activation tiles re-read every weight block: keep it
+        pol_w = gridDim.y == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
         const int nb_tiles = FUSED ? 0 : min(BT, g.b_row_tiles - b_tile * BT);
         for (int i = 0; i < pre; ++i) {
             const uint32_t fb = smem_u32(&full[i]);
@@ -200,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 4) {
         // ------------------------------------------------ producer
         if (lane == 0) {
-            const uint64_t pol_x = l2_policy_evict_last();  // activations: re-read by every tile
+            // activations are re-read by every channel tile of their row block
+            const uint64_t pol_x = gridDim.y == 1 ? l2_policy_evict_last() : l2_policy_evict_normal();
             const int nb_tiles = FUSED ? 0 : min(BT, g.b_row_tiles - b_tile * BT);
             auto load_b = [&](int i) {
                 if (FUSED) return;
@@ -274,6 +277,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool epi = warp < 4;
         const int qw = warp < 4 ? warp : warp - 2;  // quantizer warp 0..kQuantWarps-1
         const int qtid = qw * 32 + lane;
+        const uint32_t quarter = (uint32_t)(warp * 32) << 16;
+        // weight scales of one stage into this warp's lane quarter
+        auto write_sfa = [&](int s) {
+            const uint8_t* wst = wring + (size_t)s * WB + kWeightCodeBytes;
+            const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS) + quarter;
+            uint4 va[APC];
+#pragma unroll
+            for (int a = 0; a < APC; ++a) va[a] = *reinterpret_cast<const uint4*>(wst + a * 512 + lane * 16);
+            if constexpr (APC == 4) tmem_st16(tsfa, va);
+            else tmem_st8(tsfa, va);
+        };
+        const int sfa_early = 0;
         if (FUSED) {
             // Quantizing prologue (Alg. 1), one scale block per thread: this
             // CTA's K slice of every token -> base (row 2j) and residue
@@ -284,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint4*>(bregion + off) = make_uint4(0u, 0u, 0u, 0u);
             named_bar_sync(2, kQuantThreads);
             pdl_wait_prior_grid();
+            if (qtid == 0) RS_TRACE_MARK(g.trace, 16);
             const float alpha = FMT == 0 ? *g.alpha_x : 0.0f;
             const int kbeg = c0 * 256, kend = min(g.K, (c0 + nck) * 256);
             // codes of one block (element offset kk of the slice) and, gathered
@@ -351,11 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < E; ++e) rr[e] = __fsub_rn(xs[r][e], xh[e]);  // residue (Alg. 1 line 6)
                         uint32_t sfr, rcodes[E / 8];
                         float rh[E];
-                        quant_block<FMT, E>(rr, alpha, sfr, rcodes, rh);
+                        quant_block<FMT, E, false>(rr, alpha, sfr, rcodes, rh);
                         put(rb + 1u, kk, rcodes, sfr, live);
                     }
                 }
             }
+            if (qtid == 0) RS_TRACE_MARK(g.trace, 17);
+            if (qtid == kQuantThreads - 1) RS_TRACE_MARK(g.trace, 18);
             fence_proxy_async_smem();
             named_bar_sync(2, kQuantThreads);
             if (qtid == 0) RS_TRACE_MARK(g.trace, 8);
@@ -367,7 +385,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------------------------------------- scales -> TMEM
             // Each warp writes its own lane quarter with the 32 x 16-byte rows
             // of every scale atom (the image a 32x128b.warpx4 copy makes).
-            const uint32_t quarter = (uint32_t)(warp * 32) << 16;
             int i = 0;
             for (; i < nck; ++i) {
                 const int s = i % S;
@@ -382,19 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (BT == 1) {
                     // every atom of the chunk in one store per operand (atoms a
                     // ragged K tail does not read are stale but never used)
-                    uint4 va[APC], vb[APC];
+                    if (i >= sfa_early) write_sfa(s);
+                    uint4 vb[APC];
 #pragma unroll
-                    for (int a = 0; a < APC; ++a) {
-                        va[a] = *reinterpret_cast<const uint4*>(wst + a * 512 + lane * 16);
-                        vb[a] = *reinterpret_cast<const uint4*>(bst + a * 512 + lane * 16);
-                    }
-                    if constexpr (APC == 4) {
-                        tmem_st16(tsfa, va);
-                        tmem_st16(tsfb, vb);
-                    } else {
-                        tmem_st8(tsfa, va);
-                        tmem_st8(tsfb, vb);
-                    }
+                    for (int a = 0; a < APC; ++a) vb[a] = *reinterpret_cast<const uint4*>(bst + a * 512 + lane * 16);
+                    if constexpr (APC == 4) tmem_st16(tsfb, vb);
+                    else tmem_st8(tsfb, vb);
                 } else {
                     const int kleft = g.K - (c0 + i) * 256;
                     const int nks = min(4, (kleft + 63) / 64);

@@ -96,7 +96,7 @@ __host__ __device__ constexpr int lanes_per_atom() { return FMT == 0 ? 8 : 16; }
 // back packed 8 per 32-bit word (element e of the block in bits 4(e%8).. of
 // word e/8).  Same arithmetic per element as quant_lane; the amax is a max,
 // so its evaluation order does not change it.
-template <int FMT, int E>
+template <int FMT, int E, bool kRecon = true>
 __device__ __forceinline__ void quant_block(const float (&xf)[E], float alpha, uint32_t& sf, uint32_t (&codes)[E / 8],
                                             float (&xh)[E]) {
     float am0 = 0.0f, am1 = 0.0f;
@@ -114,10 +114,12 @@ __device__ __forceinline__ void quant_block(const float (&xf)[E], float alpha, u
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(xf[8 * w + e], mul);
         codes[w] = e2m1_encode8(v);
-        float d[8];
-        e2m1_decode8(codes[w], d);
+        if constexpr (kRecon) {  // the reconstruction is only needed to form a residue
+            float d[8];
+            e2m1_decode8(codes[w], d);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) xh[8 * w + e] = __fmul_rn(st, d[e]);
+            for (int e = 0; e < 8; ++e) xh[8 * w + e] = __fmul_rn(st, d[e]);
+        }
     }
 }
 
