@@ -170,18 +170,41 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with cluster-scope acquire: for phases completed by arrivals
+// from other CTAs of the cluster (mbar_arrive_remote).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (address from
+// map_dsmem), releasing this thread's prior shared-memory accesses at
+// cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 // Bounded wait for the phase with the given parity to complete.  Gives up
 // after `limit_ns` of wall-clock time or as soon as *abort becomes non-zero;
 // on a timeout it records kErrTimeout in the device error word and raises
 // the CTA's abort flag so that the other roles stop too.  Returns true when
 // the phase completed.
+// With `cluster` the wait acquires at cluster scope.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile uint32_t* abort, uint32_t* err,
-                                                  uint64_t limit_ns = 1000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                                  uint64_t limit_ns = 1000000000ull, bool cluster = false) {
+    auto try_once = [&]() { return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (try_once()) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_once()) return true;
         if ((it & 63u) == 0u) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > limit_ns) {

@@ -26,13 +26,22 @@
 // gives both to one thread, which adds them in fp32 before scaling and
 // storing, so the expanded Z never leaves the SM.
 //
+// Persistent tiles: the grid has at most one CTA per SM and K split; CTA x
+// takes output tiles x, x + gridDim.x, ... with its K slice fixed, so the
+// weight ring streams across tile boundaries without a gap, a fused plan
+// quantizes its activation slice once, and with two tensor-memory
+// accumulators the epilogue of one tile overlaps the MMAs of the next.
+//
 // Split-K: when the output tiles alone cannot keep every SM streaming
 // weights, the K range of each tile is split across the CTAs of a thread-
 // block cluster (up to 8); each CTA owns a slice of the outputs, every CTA
 // writes its folded fp32 partial to its own shared memory and bulk-copies
 // each owner's slice into that owner's receive buffer (DSMEM), completing on
 // the owner's mbarrier; each owner sums its slice in a fixed partner order
-// and writes Y.
+// and writes Y.  With several tiles per CTA the receive buffers alternate
+// with the accumulators, and an owner that has summed a buffer re-arms it
+// and signals every partner (remote mbarrier arrive) before they send into
+// it again.
 //
 // Programmatic dependent launch: the kernel releases its dependents at once
 // and starts streaming weights before waiting for the previous grid; only
@@ -40,8 +49,9 @@
 //
 // Warp roles (384 threads): warp 4 bulk/TMA producer; warp 5 TMEM allocator
 // and MMA issuer; warps 0-3 (tensor-memory lane quarters 0-3) write each
-// stage's scale atoms into tensor memory and then run the epilogue; in fused
-// plans warps 0-3 and 6-11 first run the quantizing prologue.  Every wait is
+// stage's scale atoms into tensor memory; warps 8-11 (lane quarters 0-3)
+// run the epilogue; in fused plans warps 0-3 and 6-11 first run the
+// quantizing prologue.  Every wait is
 // bounded (about one second); a wait that runs out sets the device error
 // word and an abort flag, and the CTA drains its copies and exits.
 #include <cuda.h>
@@ -87,13 +97,17 @@ struct GemmArgs {
     int N, K, M, Rb;
     int n_atoms_k;          // activation operand atoms per row tile along K
     int b_row_tiles;        // scale-atom row tiles of the activation operand
+    int n_tiles;            // 128-channel output tiles
+    int b_tiles;            // bn-row activation tiles
     int chunks;
     int splits;
     int fold;
     int out_f32;
     int stages;
     int slots;              // fused: resident activation chunks
-    int recv_bytes;         // split-K receive buffer (0 without split)
+    int nacc;               // accumulator buffers in tensor memory (1 or 2)
+    int part_bytes;         // split-K: this CTA's partial
+    int recv_bytes;         // split-K: one receive buffer (0 without split)
     int tmem_cols;
 };
 
@@ -115,14 +129,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* wring = smem;                                   // S x WB
     uint8_t* bregion = smem + (size_t)S * WB;                // S (or slots) x BSTAGE
     const int nbslots = FUSED ? g.slots : S;
-    uint8_t* recv_region = bregion + (size_t)nbslots * BSTAGE;  // split-K partials from partners
+    uint8_t* part_region = bregion + (size_t)nbslots * BSTAGE;    // split-K: our partial
+    uint8_t* recv_region = part_region + g.part_bytes;            // split-K: nacc receive buffers
     const uint32_t recv_base = smem_u32(recv_region);
-    uint64_t* full = reinterpret_cast<uint64_t*>(recv_region + g.recv_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(recv_region + (size_t)g.nacc * g.recv_bytes);
     uint64_t* empty = full + kMaxStages;
     uint64_t* sf_ready = empty + kMaxStages;   // per stage: scales in tensor memory
-    uint64_t* accum_full = sf_ready + kMaxStages;
-    uint64_t* red_full = accum_full + 1;       // split-K: all partners' partials received
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_full + 1);
+    uint64_t* accum_full = sf_ready + kMaxStages;  // per accumulator: tile's MMAs done
+    uint64_t* accum_empty = accum_full + 2;        // per accumulator: drained by the epilogue
+    uint64_t* red_full = accum_empty + 2;          // split-K: all partials of a tile received
+    uint64_t* recv_free = red_full + 2;            // split-K: every owner's receive buffer free again
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_free + 2);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     volatile uint32_t* consumed = tmem_slot + 2;
     volatile uint32_t* issued = tmem_slot + 3;
@@ -130,12 +147,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) RS_TRACE_MARK(g.trace, 0);
-    const int n_tile = blockIdx.x, b_tile = blockIdx.y, split = blockIdx.z;
+    // Persistent over output tiles: tile t = blockIdx.x + j * gridDim.x, with
+    // the channel tile varying fastest so that neighbouring CTAs share the
+    // activation tile.  The K slice (split) of a CTA is the same for all of
+    // its tiles, so fused plans quantize it once.
+    const int split = blockIdx.z;
+    const int total_tiles = g.n_tiles * g.b_tiles;
+    const int ntl = (total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     const int per = g.chunks / g.splits, rem = g.chunks % g.splits;
     const int c0 = split * per + (split < rem ? split : rem);
     const int nck = per + (split < rem ? 1 : 0);
-    const int pre = nck < S ? nck : S;
-    const uint8_t* wsrc = g.wq + ((size_t)n_tile * g.chunks + c0) * WB;
+    const int nu = ntl * nck;  // (tile, chunk) units, tile-major
+    const int pre = nu < S ? nu : S;
+    const int nacc = g.nacc;
+    const int outs = g.fold ? BN / 2 : BN;
+    const int per_cta = (outs + g.splits - 1) / g.splits;  // split-K: outputs each CTA owns
+    const uint32_t slice_bytes = (uint32_t)per_cta * 128u * 4u;
+    const uint32_t red_bytes = (uint32_t)g.splits * slice_bytes;
+    auto n_tile_of = [&](int j) { return ((int)blockIdx.x + j * (int)gridDim.x) % g.n_tiles; };
+    auto b_tile_of = [&](int j) { return ((int)blockIdx.x + j * (int)gridDim.x) / g.n_tiles; };
+    auto wsrc_of = [&](int u) {
+        const int j = u / nck, i = u - j * nck;
+        return g.wq + ((size_t)n_tile_of(j) * g.chunks + c0 + i) * WB;
+    };
+    auto b_tx_of = [&](int u) -> uint32_t {
+        if (FUSED) return 0u;
+        const int j = u / nck, i = u - j * nck;
+        const int nb_tiles = min(BT, g.b_row_tiles - b_tile_of(j) * BT);
+        const int na = min(APC, g.n_atoms_k - (c0 + i) * APC);
+        return B_BYTES + (uint32_t)na * 512u * (uint32_t)nb_tiles;
+    };
 
     // Producer: barriers, then start streaming weights right away (they do
     // not depend on the previous kernel in the stream).
@@ -146,27 +187,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&empty[s]), 1);
             mbar_init(smem_u32(&sf_ready[s]), 4);  // one arrival per scale-writer warp
         }
-        mbar_init(smem_u32(accum_full), 1);
-        mbar_init(smem_u32(red_full), 1);
-        if (g.splits > 1) {
-            const int outs0 = g.fold ? BN / 2 : BN;
-            const int per_cta0 = (outs0 + g.splits - 1) / g.splits;
-            mbar_arrive_expect_tx(smem_u32(red_full), (uint32_t)(g.splits * per_cta0 * 512));
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&accum_full[b]), 1);
+            mbar_init(smem_u32(&accum_empty[b]), 4);          // one arrival per epilogue warp
+            mbar_init(smem_u32(&red_full[b]), 1);
+            mbar_init(smem_u32(&recv_free[b]), (uint32_t)g.splits);  // one arrival per owner
         }
+        // the first use of each receive buffer is armed before any partner
+        // can send (they send only after the cluster barrier below)
+        if (g.splits > 1)
+            for (int b = 0; b < nacc && b < ntl; ++b) mbar_arrive_expect_tx(smem_u32(&red_full[b]), red_bytes);
         *abort_flag = 0;
         *consumed = 0;
         *issued = 0;
         fence_mbarrier_init();
         // a single activation tile reads each weight block once: stream it;
         // several activation tiles re-read every weight block: keep it
-        pol_w = gridDim.y == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
-        const int nb_tiles = FUSED ? 0 : min(BT, g.b_row_tiles - b_tile * BT);
-        for (int i = 0; i < pre; ++i) {
-            const uint32_t fb = smem_u32(&full[i]);
-            const int na = min(APC, g.n_atoms_k - (c0 + i) * APC);
-            const uint32_t b_tx = FUSED ? 0u : B_BYTES + (uint32_t)na * 512u * (uint32_t)nb_tiles;
-            mbar_arrive_expect_tx(fb, WB + b_tx);
-            bulk_load(smem_u32(wring + (size_t)i * WB), wsrc + (size_t)i * WB, WB, fb, pol_w);
+        pol_w = g.b_tiles == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
+        for (int u = 0; u < pre; ++u) {
+            const uint32_t fb = smem_u32(&full[u]);
+            mbar_arrive_expect_tx(fb, WB + b_tx_of(u));
+            bulk_load(smem_u32(wring + (size_t)u * WB), wsrc_of(u), WB, fb, pol_w);
         }
         RS_TRACE_MARK(g.trace, 2);
     }
@@ -184,9 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
         RS_TRACE_VALUE(g.trace, 12, smid);
     }
-    const uint32_t tm_acc = tmem;
-    const uint32_t tm_sf = tmem + BN;
-    // split-K partners copy into our receive buffer and signal red_full:
+    const uint32_t tm_sf = tmem + (uint32_t)(nacc * BN);
+    // split-K partners copy into our receive buffers and signal red_full:
     // every barrier of the cluster must be initialised before that
     if (g.splits > 1) cluster_sync_all();
 
@@ -194,101 +234,99 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before they touch anything we read or write.
     pdl_launch_dependents();
 
-    const int outs = g.fold ? BN / 2 : BN;
-    const int m0 = b_tile * outs;
-    const int row = warp * 32 + lane;  // epilogue: accumulator lane = channel within the tile
-    const int n = n_tile * 128 + row;
-
     if (warp == 4) {
         // ------------------------------------------------ producer
         if (lane == 0) {
             // activations are re-read by every channel tile of their row block
-            const uint64_t pol_x = gridDim.y == 1 ? l2_policy_evict_last() : l2_policy_evict_normal();
-            const int nb_tiles = FUSED ? 0 : min(BT, g.b_row_tiles - b_tile * BT);
-            auto load_b = [&](int i) {
+            const uint64_t pol_x = g.b_tiles == 1 ? l2_policy_evict_last() : l2_policy_evict_normal();
+            auto load_b = [&](int u) {
                 if (FUSED) return;
-                const int chunk = c0 + i, s = i % S;
+                const int j = u / nck, i = u - j * nck;
+                const int chunk = c0 + i, s = u % S, bt = b_tile_of(j);
+                const int nb_tiles = min(BT, g.b_row_tiles - bt * BT);
                 uint8_t* st = bregion + (size_t)s * BSTAGE;
                 const uint32_t fb = smem_u32(&full[s]);
-                tma_load_2d(smem_u32(st), &tmap_b, fb, chunk * 128, b_tile * BN, pol_x);
+                tma_load_2d(smem_u32(st), &tmap_b, fb, chunk * 128, bt * BN, pol_x);
                 const int na = min(APC, g.n_atoms_k - chunk * APC);
                 for (int t = 0; t < nb_tiles; ++t)
                     bulk_load(smem_u32(st + B_BYTES + (uint32_t)t * APC * 512u),
-                              g.sfb + ((size_t)(b_tile * BT + t) * g.n_atoms_k + (size_t)chunk * APC) * 512,
+                              g.sfb + ((size_t)(bt * BT + t) * g.n_atoms_k + (size_t)chunk * APC) * 512,
                               (uint32_t)na * 512u, fb, pol_x);
             };
             pdl_wait_prior_grid();
-            for (int i = 0; i < pre; ++i) load_b(i);
-            int i = pre;
-            for (; i < nck; ++i) {
-                const int s = i % S;
-                const uint32_t ph = (uint32_t)(i / S) & 1u;
+            for (int u = 0; u < pre; ++u) load_b(u);
+            int u = pre;
+            for (; u < nu; ++u) {
+                const int s = u % S;
+                const uint32_t ph = (uint32_t)(u / S) & 1u;
                 if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag, g.err)) break;
                 const uint32_t fb = smem_u32(&full[s]);
-                const int na = min(APC, g.n_atoms_k - (c0 + i) * APC);
-                const uint32_t b_tx = FUSED ? 0u : B_BYTES + (uint32_t)na * 512u * (uint32_t)nb_tiles;
-                mbar_arrive_expect_tx(fb, WB + b_tx);
-                bulk_load(smem_u32(wring + (size_t)s * WB), wsrc + (size_t)i * WB, WB, fb, pol_w);
-                load_b(i);
+                mbar_arrive_expect_tx(fb, WB + b_tx_of(u));
+                bulk_load(smem_u32(wring + (size_t)s * WB), wsrc_of(u), WB, fb, pol_w);
+                load_b(u);
             }
-            *issued = (uint32_t)i;
+            *issued = (uint32_t)u;
             RS_TRACE_MARK(g.trace, 3);
         }
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int i = 0;
-            for (; i < nck; ++i) {
-                const int s = i % S;
-                const uint32_t ph = (uint32_t)(i / S) & 1u;
-                // chunk i's scales are in tensor memory (and, in fused plans,
-                // its activation tile is in shared memory)
-                if (!mbar_wait_bounded(smem_u32(&sf_ready[s]), ph, abort_flag, g.err)) break;
-                if (i == 0) RS_TRACE_MARK(g.trace, 4);
-                if (i == nck - 1) RS_TRACE_MARK(g.trace, 5);
-                tc_fence_after();
-                const int chunk = c0 + i;
-                const uint32_t sa = smem_u32(wring + (size_t)s * WB);
-                const uint32_t sb = smem_u32(bregion + (size_t)(FUSED ? i : s) * BSTAGE);
-                const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS);
-                const uint32_t tsfb = tsfa + SFA_COLS;
-                const int kleft = g.K - chunk * 256;
-                const int nks = min(4, (kleft + 63) / 64);
-                for (int ks = 0; ks < nks; ++ks) {
-                    const uint64_t adesc = kmajor_sw128_desc(sa + ks * 32);
-                    const uint64_t bdesc = kmajor_sw128_desc(sb + ks * 32);
-                    const uint32_t accum = (i > 0 || ks > 0) ? 1u : 0u;
-                    if (FMT == 0) {
-                        mma_nvfp4(tm_acc, adesc, bdesc, mxf4_idesc(BN, false, 0), tsfa + ks * 4, tsfb + ks * BT * 4,
-                                  accum);
-                    } else {
-                        const int a = ks >> 1;
-                        const uint32_t sf_id = (uint32_t)(ks & 1) * 2u;
-                        mma_mxfp4(tm_acc, adesc, bdesc, mxf4_idesc(BN, true, sf_id), tsfa + a * 4, tsfb + a * BT * 4,
-                                  accum);
-                    }
+            int u = 0;
+            bool ok = true;
+            for (int j = 0; ok && j < ntl; ++j) {
+                const int b = j % nacc;
+                if (j >= nacc) {
+                    // the epilogue has read this accumulator's previous tile
+                    if (!mbar_wait_bounded(smem_u32(&accum_empty[b]), (uint32_t)(j / nacc - 1) & 1u, abort_flag,
+                                           g.err))
+                        break;
+                    tc_fence_after();
                 }
-                tc_commit(smem_u32(&empty[s]));
+                const uint32_t tm_acc = tmem + (uint32_t)(b * BN);
+                for (int i = 0; i < nck; ++i, ++u) {
+                    const int s = u % S;
+                    const uint32_t ph = (uint32_t)(u / S) & 1u;
+                    // unit u's scales are in tensor memory (and, in fused plans,
+                    // its activation tile is in shared memory)
+                    if (!mbar_wait_bounded(smem_u32(&sf_ready[s]), ph, abort_flag, g.err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (u == 0) RS_TRACE_MARK(g.trace, 4);
+                    if (u == nu - 1) RS_TRACE_MARK(g.trace, 5);
+                    tc_fence_after();
+                    const int chunk = c0 + i;
+                    const uint32_t sa = smem_u32(wring + (size_t)s * WB);
+                    const uint32_t sb = smem_u32(bregion + (size_t)(FUSED ? i : s) * BSTAGE);
+                    const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS);
+                    const uint32_t tsfb = tsfa + SFA_COLS;
+                    const int kleft = g.K - chunk * 256;
+                    const int nks = min(4, (kleft + 63) / 64);
+                    for (int ks = 0; ks < nks; ++ks) {
+                        const uint64_t adesc = kmajor_sw128_desc(sa + ks * 32);
+                        const uint64_t bdesc = kmajor_sw128_desc(sb + ks * 32);
+                        const uint32_t accum = (i > 0 || ks > 0) ? 1u : 0u;
+                        if (FMT == 0) {
+                            mma_nvfp4(tm_acc, adesc, bdesc, mxf4_idesc(BN, false, 0), tsfa + ks * 4,
+                                      tsfb + ks * BT * 4, accum);
+                        } else {
+                            const int a = ks >> 1;
+                            const uint32_t sf_id = (uint32_t)(ks & 1) * 2u;
+                            mma_mxfp4(tm_acc, adesc, bdesc, mxf4_idesc(BN, true, sf_id), tsfa + a * 4,
+                                      tsfb + a * BT * 4, accum);
+                        }
+                    }
+                    tc_commit(smem_u32(&empty[s]));
+                }
+                if (ok) tc_commit(smem_u32(&accum_full[b]));  // fires once the tile's MMAs are done
             }
-            tc_commit(smem_u32(accum_full));  // fires once every issued MMA is done
         }
     } else {
         // ------------------------------------------------ warps 0-3, 6-11
-        const bool epi = warp < 4;
+        const bool sfw = warp < 4;             // scale writers: tensor-memory lane quarter = warp
+        const bool epi = warp >= 8;            // epilogue: lane quarter = warp - 8
         const int qw = warp < 4 ? warp : warp - 2;  // quantizer warp 0..kQuantWarps-1
         const int qtid = qw * 32 + lane;
-        const uint32_t quarter = (uint32_t)(warp * 32) << 16;
-        // weight scales of one stage into this warp's lane quarter
-        auto write_sfa = [&](int s) {
-            const uint8_t* wst = wring + (size_t)s * WB + kWeightCodeBytes;
-            const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS) + quarter;
-            uint4 va[APC];
-#pragma unroll
-            for (int a = 0; a < APC; ++a) va[a] = *reinterpret_cast<const uint4*>(wst + a * 512 + lane * 16);
-            if constexpr (APC == 4) tmem_st16(tsfa, va);
-            else tmem_st8(tsfa, va);
-        };
-        const int sfa_early = 0;
         if (FUSED) {
             // Quantizing prologue (Alg. 1), one scale block per thread: this
             // CTA's K slice of every token -> base (row 2j) and residue
@@ -381,14 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             pdl_wait_prior_grid();  // before writing the output
         }
 
-        if (epi) {
+        if (sfw) {
             // ---------------------------------------------- scales -> TMEM
             // Each warp writes its own lane quarter with the 32 x 16-byte rows
             // of every scale atom (the image a 32x128b.warpx4 copy makes).
-            int i = 0;
-            for (; i < nck; ++i) {
-                const int s = i % S;
-                const uint32_t ph = (uint32_t)(i / S) & 1u;
+            const uint32_t quarter = (uint32_t)(warp * 32) << 16;
+            int u = 0;
+            for (; u < nu; ++u) {
+                const int j = u / nck, i = u - j * nck;
+                const int s = u % S;
+                const uint32_t ph = (uint32_t)(u / S) & 1u;
                 // warp-uniform outcome: the tcgen05.st below are warp-collective
                 const bool landed = mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err);
                 if (!__all_sync(0xFFFFFFFFu, landed)) break;
@@ -399,17 +439,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (BT == 1) {
                     // every atom of the chunk in one store per operand (atoms a
                     // ragged K tail does not read are stale but never used)
-                    if (i >= sfa_early) write_sfa(s);
-                    uint4 vb[APC];
+                    uint4 va[APC], vb[APC];
 #pragma unroll
-                    for (int a = 0; a < APC; ++a) vb[a] = *reinterpret_cast<const uint4*>(bst + a * 512 + lane * 16);
-                    if constexpr (APC == 4) tmem_st16(tsfb, vb);
-                    else tmem_st8(tsfb, vb);
+                    for (int a = 0; a < APC; ++a) {
+                        va[a] = *reinterpret_cast<const uint4*>(wst + a * 512 + lane * 16);
+                        vb[a] = *reinterpret_cast<const uint4*>(bst + a * 512 + lane * 16);
+                    }
+                    if constexpr (APC == 4) {
+                        tmem_st16(tsfa, va);
+                        tmem_st16(tsfb, vb);
+                    } else {
+                        tmem_st8(tsfa, va);
+                        tmem_st8(tsfb, vb);
+                    }
                 } else {
                     const int kleft = g.K - (c0 + i) * 256;
                     const int nks = min(4, (kleft + 63) / 64);
                     const int na = FMT == 0 ? nks : (nks + 1) / 2;
-                    const int nb_tiles = min(BT, g.b_row_tiles - b_tile * BT);
+                    const int nb_tiles = min(BT, g.b_row_tiles - b_tile_of(j) * BT);
                     for (int a = 0; a < na; ++a)
                         tmem_st4(tsfa + a * 4, *reinterpret_cast<const uint4*>(wst + a * 512 + lane * 16));
                     for (int t = 0; t < nb_tiles; ++t)
@@ -422,81 +469,110 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sf_ready[s]));
             }
-            if (warp == 0 && lane == 0) *consumed = (uint32_t)i;
+            if (warp == 0 && lane == 0) *consumed = (uint32_t)u;
+        }
 
+        if (epi) {
             // ---------------------------------------------- epilogue
-            const int ctid = threadIdx.x;  // 0..127
-            bool ok = mbar_wait_bounded(smem_u32(accum_full), 0, abort_flag, g.err);
-            if (ctid == 0) RS_TRACE_MARK(g.trace, 6);
-            named_bar_sync(1, 128);
-            ok = ok && (*abort_flag == 0);
-            ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-            tc_fence_after();
+            const int ew = warp - 8;                       // lane quarter
+            const uint32_t quarter = (uint32_t)(ew * 32) << 16;
+            const int row = ew * 32 + lane;                // accumulator lane = channel within the tile
+            const int ctid = row;                          // 0..127
             const float gsc = FMT == 0 ? __fmul_rn(*g.alpha_x, *g.alpha_w) : 1.0f;
-            const int per_cta = (outs + g.splits - 1) / g.splits;
-            // split-K: this CTA's partial, [j][channel], in the idle weight ring
-            float* part = reinterpret_cast<float*>(wring);
-            auto emit = [&](int j, float z) {
-                if (g.splits > 1) {
-                    part[j * 128 + row] = z;
-                } else if (n < g.N && m0 + j < g.M) {
-                    const float val = __fmul_rn(gsc, z);
-                    const size_t idx = (size_t)(m0 + j) * g.N + n;
-                    if (g.out_f32) reinterpret_cast<float*>(g.y)[idx] = val;
-                    else reinterpret_cast<__nv_bfloat16*>(g.y)[idx] = __float2bfloat16_rn(val);
-                }
-            };
-            if (ok) {
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
-                    float v[16];
-                    tmem_ld16(tm_acc + quarter + (uint32_t)c, v);
-                    if (g.fold) {
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) emit(c / 2 + u, __fadd_rn(v[2 * u], v[2 * u + 1]));  // Fold
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < 16; ++u) emit(c + u, v[u]);
-                    }
-                }
-            } else if (g.splits > 1) {
-                for (int j = 0; j < outs; ++j) emit(j, 0.0f);
-            }
-            if (g.splits > 1) {
-                // send each owner its slice of outputs: one bulk copy per owner
-                // into its receive buffer at our rank's slot
-                fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (ctid == 0) {
-                    const uint32_t slice = (uint32_t)per_cta * 128u * 4u;
-                    for (int o = 0; o < g.splits; ++o) {
-                        const uint32_t dst = map_dsmem(recv_base + (uint32_t)split * slice, (uint32_t)o);
-                        const uint32_t bar = map_dsmem(smem_u32(red_full), (uint32_t)o);
-                        bulk_copy_to_cluster(dst, smem_u32(part) + (uint32_t)o * slice, slice, bar);
-                    }
-                    bulk_commit_group();
-                }
-            }
-            if (ctid == 0) RS_TRACE_MARK(g.trace, 7);
-            if (g.splits > 1) {
-                // own slice: sum the partners' partials in rank order
-                const bool got = mbar_wait_bounded(smem_u32(red_full), 0, abort_flag, g.err);
-                const float* recv = reinterpret_cast<const float*>(recv_region);
-                for (int jj = 0; got && jj < per_cta; ++jj) {
-                    const int j = split * per_cta + jj;
-                    const int m = m0 + j;
-                    if (j >= outs || m >= g.M) break;
-                    float acc = 0.0f;
-                    for (int r = 0; r < g.splits; ++r) acc = __fadd_rn(acc, recv[(r * per_cta + jj) * 128 + row]);
-                    if (n < g.N && *abort_flag == 0) {
-                        const float val = __fmul_rn(gsc, acc);
+            float* part = reinterpret_cast<float*>(part_region);  // split-K: [j][channel]
+            const uint32_t my_rank = (uint32_t)split;
+            for (int j = 0; j < ntl; ++j) {
+                const int b = j % nacc;
+                const uint32_t use_ph = (uint32_t)(j / nacc) & 1u;
+                const int n = n_tile_of(j) * 128 + row;
+                const int m0 = b_tile_of(j) * outs;
+                auto store_y = [&](int m, float z) {
+                    if (n < g.N && m < g.M) {
+                        const float val = __fmul_rn(gsc, z);
                         const size_t idx = (size_t)m * g.N + n;
                         if (g.out_f32) reinterpret_cast<float*>(g.y)[idx] = val;
                         else reinterpret_cast<__nv_bfloat16*>(g.y)[idx] = __float2bfloat16_rn(val);
                     }
+                };
+                auto emit = [&](int jj, float z) {
+                    if (g.splits > 1) part[jj * 128 + row] = z;
+                    else store_y(m0 + jj, z);
+                };
+                bool ok = mbar_wait_bounded(smem_u32(&accum_full[b]), use_ph, abort_flag, g.err);
+                if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 6);
+                ok = __all_sync(0xFFFFFFFFu, ok && *abort_flag == 0);  // warp-uniform for tcgen05.ld
+                tc_fence_after();
+                if (g.splits > 1 && j > 0) {
+                    // the previous tile's outgoing copies have read our partial
+                    if (ctid == 0) bulk_wait_group_read0();
+                    named_bar_sync(1, 128);
                 }
-                if (ctid == 0) bulk_wait_group_read0();  // our outgoing copies have read their source
+                if (ok) {
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 16) {
+                        float v[16];
+                        tmem_ld16(tmem + (uint32_t)(b * BN) + quarter + (uint32_t)c, v);
+                        if (g.fold) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) emit(c / 2 + q, __fadd_rn(v[2 * q], v[2 * q + 1]));  // Fold
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) emit(c + q, v[q]);
+                        }
+                    }
+                } else if (g.splits > 1) {
+                    for (int jj = 0; jj < outs; ++jj) emit(jj, 0.0f);
+                }
+                // accumulator b drained: the MMA warp may start its next tile
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&accum_empty[b]));
+                if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 7);
+                if (g.splits > 1) {
+                    // send each owner its slice of outputs: one bulk copy per
+                    // owner into its receive buffer b at our rank's slot
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, 128);
+                    if (ctid == 0) {
+                        // every owner has consumed what was sent into buffer b
+                        // for tile j - nacc
+                        const bool free_ok = j < nacc || mbar_wait_bounded(smem_u32(&recv_free[b]),
+                                                                           (uint32_t)(j / nacc - 1) & 1u, abort_flag,
+                                                                           g.err, 1000000000ull, true);
+                        if (free_ok && *abort_flag == 0) {
+                            const uint32_t rbuf = recv_base + (uint32_t)(b * g.recv_bytes);
+                            for (int o = 0; o < g.splits; ++o) {
+                                const uint32_t dst = map_dsmem(rbuf + my_rank * slice_bytes, (uint32_t)o);
+                                const uint32_t bar = map_dsmem(smem_u32(&red_full[b]), (uint32_t)o);
+                                bulk_copy_to_cluster(dst, smem_u32(part) + (uint32_t)o * slice_bytes, slice_bytes,
+                                                     bar);
+                            }
+                            bulk_commit_group();
+                        }
+                    }
+                    // own slice: sum the partners' partials in rank order
+                    const bool got = mbar_wait_bounded(smem_u32(&red_full[b]), use_ph, abort_flag, g.err);
+                    const float* recv = reinterpret_cast<const float*>(recv_region + (size_t)b * g.recv_bytes);
+                    for (int jj = 0; got && jj < per_cta; ++jj) {
+                        const int jo = split * per_cta + jj;
+                        if (jo >= outs) break;
+                        float acc = 0.0f;
+                        for (int r = 0; r < g.splits; ++r) acc = __fadd_rn(acc, recv[(r * per_cta + jj) * 128 + row]);
+                        if (*abort_flag == 0) store_y(m0 + jo, acc);
+                    }
+                    if (j + nacc < ntl) {
+                        // buffer b is read: re-arm it for tile j + nacc, then
+                        // tell every partner it may send into it again
+                        named_bar_sync(1, 128);
+                        if (ctid == 0 && *abort_flag == 0) {
+                            mbar_arrive_expect_tx(smem_u32(&red_full[b]), red_bytes);
+                            for (int p = 0; p < g.splits; ++p)
+                                mbar_arrive_remote(map_dsmem(smem_u32(&recv_free[b]), (uint32_t)p));
+                        }
+                    }
+                }
             }
+            if (g.splits > 1 && ctid == 0) bulk_wait_group_read0();  // our outgoing copies have read their source
         }
     }
 
@@ -508,10 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (*abort_flag && warp == 4 && lane == 0) {
         // Let every copy still in flight land before the CTA exits.
-        for (uint32_t i = *consumed; i < *issued; ++i) {
-            const uint32_t s = i % (uint32_t)S;
+        for (uint32_t u = *consumed; u < *issued; ++u) {
+            const uint32_t s = u % (uint32_t)S;
             volatile uint32_t no_abort = 0;
-            (void)mbar_wait_bounded(smem_u32(&full[s]), (i / (uint32_t)S) & 1u, &no_abort, nullptr, 100000000ull);
+            (void)mbar_wait_bounded(smem_u32(&full[s]), (u / (uint32_t)S) & 1u, &no_abort, nullptr, 100000000ull);
         }
     }
     __syncthreads();
@@ -524,18 +600,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------- host --
 
-static size_t recv_bytes_for(int splits, int outs) {
+// Split-K buffers: this CTA's partial and each receive buffer hold `splits`
+// slices of ceil(outs / splits) outputs x 128 channels (fp32).
+static size_t split_buf_bytes(int splits, int outs) {
     if (splits <= 1) return 0;
     const int per_cta = (outs + splits - 1) / splits;
     return align_up((size_t)splits * per_cta * 128 * sizeof(float), 1024);
 }
 
-static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots, size_t recv) {
+static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots, size_t splitbuf, int nacc) {
     const size_t b = fused ? (size_t)slots * b_stage_bytes(fmt, bn) : (size_t)stages * b_stage_bytes(fmt, bn);
-    return 1024 + (size_t)stages * weight_block_bytes(fmt) + b + recv + kCtrlBytes;
+    return 1024 + (size_t)stages * weight_block_bytes(fmt) + b + splitbuf * (size_t)(1 + nacc) + kCtrlBytes;
 }
 
-static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, int split_cap, bool allow_fused) {
+// Complete plan for a given split count s; stages == 0 when it does not fit.
+static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms, int s, bool allow_fused) {
     GemmPlan p{};
     p.fmt = fmt;
     p.fold = fold ? 1 : 0;
@@ -548,50 +627,59 @@ static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, 
     p.b_tiles = (p.Rb + p.bn - 1) / p.bn;
     p.chunks = (K + 255) / 256;
     const int tiles = p.n_tiles * p.b_tiles;
-    const int sms = num_sms > 0 ? num_sms : 148;
-    // Split count: minimise the chunks the busiest SM streams (CTAs are
-    // spread round-robin over the SMs); prefer fewer splits on a tie.
-    int best_s = 1;
-    long best_load = -1;
-    const int smax = std::min({p.chunks, kMaxSplits, split_cap});
-    for (int s = 1; s <= smax; ++s) {
-        const long ctas = (long)tiles * s;
-        const long load = ((ctas + sms - 1) / sms) * (long)((p.chunks + s - 1) / s);
-        if (best_load < 0 || load < best_load) {
-            best_load = load;
-            best_s = s;
+    // persistent grid: gridDim.x CTAs per K split, CTA x taking tiles x,
+    // x + gridDim.x, ...; one CTA per SM
+    p.splits = s;
+    p.grid_x = std::min(tiles, std::max(1, sms / s));
+    const int max_chunks = (p.chunks + s - 1) / s;
+    const int ntl = (tiles + p.grid_x - 1) / p.grid_x;
+    const int nu = ntl * max_chunks;
+    const int outs = fold ? p.bn / 2 : p.bn;
+    const size_t splitbuf = split_buf_bytes(s, outs);
+    const int sfc = sf_cols_per_stage(fmt, p.bn);
+    bool fused = allow_fused && p.b_tiles == 1 && p.bn <= 32;
+    // two accumulators let the epilogue of one tile overlap the next tile's
+    // MMAs when a CTA has several tiles
+    int nacc = ntl > 1 ? 2 : 1;
+    auto fits = [&](int st, bool fu, int na) {
+        return plan_smem(fmt, p.bn, st, fu, fu ? max_chunks : 0, splitbuf, na) <= kSmemLimit &&
+               na * p.bn + st * sfc <= 512;
+    };
+    auto best_stages = [&](bool fu, int na) {
+        int st = std::min(kMaxStages, nu);
+        while (st > 1 && !fits(st, fu, na)) --st;
+        return fits(st, fu, na) ? st : 0;
+    };
+    int stages = best_stages(fused, nacc);
+    if (nacc == 2 && stages < std::min(4, nu)) {
+        const int st1 = best_stages(fused, 1);
+        if (st1 > stages) {
+            nacc = 1;
+            stages = st1;
         }
     }
-    p.splits = best_s;
-    const int max_chunks = (p.chunks + p.splits - 1) / p.splits;
-    const int outs = fold ? p.bn / 2 : p.bn;
-    const size_t recv = recv_bytes_for(p.splits, outs);
-    p.fused = (allow_fused && p.b_tiles == 1 && p.bn <= 32) ? 1 : 0;
-    int stages = std::min(kMaxStages, max_chunks);
-    while (stages > 1 && plan_smem(fmt, p.bn, stages, p.fused, max_chunks, recv) > kSmemLimit) --stages;
-    if (p.fused && plan_smem(fmt, p.bn, stages, true, max_chunks, recv) > kSmemLimit) {
-        p.fused = 0;
-        stages = std::min(kMaxStages, max_chunks);
-        while (stages > 1 && plan_smem(fmt, p.bn, stages, false, 0, recv) > kSmemLimit) --stages;
+    if (fused && stages == 0) {
+        fused = false;
+        stages = best_stages(false, nacc);
     }
-    p.stages = std::max(stages, 1);
-    // the split-K partial is sent from the idle weight ring; without room
-    // for it (or for the receive buffer), no split
-    if (p.splits > 1 && (plan_smem(fmt, p.bn, p.stages, p.fused, p.fused ? max_chunks : 0, recv) > kSmemLimit ||
-                         recv > (size_t)p.stages * weight_block_bytes(fmt)))
-        return plan_impl(fmt, fold, M, N, K, num_sms, 1, allow_fused);
+    p.fused = fused ? 1 : 0;
+    p.nacc = nacc;
+    p.stages = stages;
     p.slots = p.fused ? max_chunks : 0;
-    p.recv_bytes = (int)recv;
-    // Two CTAs can share an SM when the shared memory allows it; keep the
-    // tensor-memory allocation within half of the SM's 512 columns then.
-    p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots, recv);
-    int cols = p.bn + p.stages * sf_cols_per_stage(fmt, p.bn);
+    p.part_bytes = (int)splitbuf;
+    p.recv_bytes = (int)splitbuf;
+    if (stages == 0) return p;
+    // Two CTAs can share an SM when the shared memory allows it (a dependent
+    // launch starting early); keep the tensor-memory allocation within half
+    // of the SM's 512 columns then.
+    p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots, splitbuf, p.nacc);
+    int cols = p.nacc * p.bn + p.stages * sfc;
     if (p.smem_bytes <= kSmemLimit / 2) {
         while (cols > 256 && p.stages > 1) {
             --p.stages;
-            cols = p.bn + p.stages * sf_cols_per_stage(fmt, p.bn);
+            cols = p.nacc * p.bn + p.stages * sfc;
         }
-        p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots, recv);
+        p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots, splitbuf, p.nacc);
     }
     int alloc = 32;
     while (alloc < cols) alloc *= 2;
@@ -599,8 +687,35 @@ static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, 
     return p;
 }
 
+// Split count: minimise the chunks the busiest CTA streams; prefer fewer
+// splits on a tie.  A split plan must keep a pipeline of at least four
+// stages (or all of its units) next to its split-K buffers.
+static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused) {
+    const int sms = num_sms > 0 ? num_sms : 148;
+    const int chunks = (K + 255) / 256;
+    GemmPlan best = plan_for_splits(fmt, fold, M, N, K, sms, 1, allow_fused);
+    if (best.stages == 0) best.stages = 1;  // cannot happen for the supported tile shapes
+    auto load_of = [&](const GemmPlan& p) {
+        const int tiles = p.n_tiles * p.b_tiles;
+        return (long)((tiles + p.grid_x - 1) / p.grid_x) * (long)((p.chunks + p.splits - 1) / p.splits);
+    };
+    long best_load = load_of(best);
+    for (int s = 2; s <= std::min(chunks, kMaxSplits); ++s) {
+        const GemmPlan p = plan_for_splits(fmt, fold, M, N, K, sms, s, allow_fused);
+        const int tiles = p.n_tiles * p.b_tiles;
+        const int nu = ((tiles + p.grid_x - 1) / p.grid_x) * ((chunks + s - 1) / s);
+        if (p.stages < std::min(4, nu)) continue;
+        const long load = load_of(p);
+        if (load < best_load) {
+            best = p;
+            best_load = load;
+        }
+    }
+    return best;
+}
+
 GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused) {
-    return plan_impl(fmt, fold, M, N, K, num_sms, kMaxSplits, allow_fused);
+    return plan_impl(fmt, fold, M, N, K, num_sms, allow_fused);
 }
 
 size_t workspace_bytes(int fmt, bool compensated, int M, int K) {
@@ -660,7 +775,7 @@ static cudaError_t launch_typed(const GemmPlan& p, const CUtensorMap& tb, const 
     cudaError_t e = ensure_smem_attr<FMT, BN, FUSED>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)p.n_tiles, (unsigned)p.b_tiles, (unsigned)p.splits);
+    cfg.gridDim = dim3((unsigned)p.grid_x, 1u, (unsigned)p.splits);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = p.smem_bytes;
     cfg.stream = stream;
@@ -714,6 +829,10 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
     a.out_f32 = c.out_f32;
     a.stages = p.stages;
     a.slots = p.slots;
+    a.n_tiles = p.n_tiles;
+    a.b_tiles = p.b_tiles;
+    a.nacc = p.nacc;
+    a.part_bytes = p.part_bytes;
     a.recv_bytes = p.recv_bytes;
     a.tmem_cols = p.tmem_cols;
 #define RS_CASE(F, B, FU)                                                      \

@@ -40,10 +40,13 @@ struct GemmPlan {
     int b_tiles;     // ceil(Rb / bn)
     int chunks;      // ceil(K / 256)
     int splits;      // K splits per output tile (= cluster size when > 1)
+    int grid_x;      // persistent CTAs per K split; CTA x takes tiles x, x + grid_x, ...
+    int nacc;        // accumulator buffers in tensor memory (2: epilogue overlaps the next tile)
+    int part_bytes;  // split-K: partial buffer in shared memory
     int stages;      // pipeline depth
     int fused;       // quantize the activations inside the GEMM
     int slots;       // fused: activation chunks resident in shared memory
-    int recv_bytes;  // split-K receive buffer in shared memory
+    int recv_bytes;  // split-K: one receive buffer in shared memory
     int tmem_cols;   // tensor-memory columns to allocate
     size_t smem_bytes;
 };

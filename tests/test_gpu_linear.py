@@ -40,6 +40,25 @@ def test_linear_parity_small(fmt, compensated, M, N, K):
     assert_close_f32(y, ref)
 
 
+# More 128-channel tiles than a GB300 has SMs per K split, so that CTAs run
+# several tiles (double-buffered accumulators, per-tile split-K exchange):
+# fused and TMA-fed activations, ragged channel and K tails, two activation
+# row tiles.
+SHAPES_MULTI_TILE = [(3, 20416, 512), (8, 40960, 288), (40, 20480, 768), (300, 12800, 256)]
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("compensated", [False, True])
+@pytest.mark.parametrize("M,N,K", SHAPES_MULTI_TILE)
+def test_linear_parity_multi_tile(fmt, compensated, M, N, K):
+    x = workloads.make_x("gauss_outlier_k2048", M, K=K, seed=M + N + K)
+    w = workloads.make_w("gauss_outlier_k2048", N=N, K=K, seed=N * 7 + K)
+    wp = prepare_weight(fmt, w)
+    y, _ = gpu_linear(fmt, compensated, x, wp)
+    ref = oracle_linear(fmt, compensated, x, wp)
+    assert_close_f32(y, ref)
+
+
 @pytest.mark.parametrize("fmt", [0, 1])
 @pytest.mark.parametrize("compensated", [False, True])
 def test_prequantized_input_matches(fmt, compensated):
