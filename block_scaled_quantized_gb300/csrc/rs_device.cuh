@@ -137,7 +137,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t elect_one_lane() { return (threadIdx.x & 31u) == 0u; }
+// One lane of the (converged) warp is elected.  Work issued by the elected
+// lane inside a warp-wide loop keeps its operands warp-uniform, which the
+// tensor-pipe issue of tcgen05.mma / tcgen05.cp needs to run at full rate.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .b32 r;\n\t.reg .pred p;\n\t"
+        "elect.sync r|p, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
 
 // ---------------------------------------------------------------- mbarrier --
 

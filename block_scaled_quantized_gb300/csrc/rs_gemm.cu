@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t recv_base = smem_u32(recv_region);
     uint64_t* full = reinterpret_cast<uint64_t*>(recv_region + (size_t)g.nacc * g.recv_bytes);
     uint64_t* empty = full + kMaxStages;
-    uint64_t* sf_ready = empty + kMaxStages;   // per stage: scales in tensor memory
-    uint64_t* accum_full = sf_ready + kMaxStages;  // per accumulator: tile's MMAs done
+    uint64_t* qdone = empty + kMaxStages;      // fused: activation slice quantized into shared memory
+    uint64_t* accum_full = qdone + 1;              // per accumulator: tile's MMAs done
     uint64_t* accum_empty = accum_full + 2;        // per accumulator: drained by the epilogue
     uint64_t* red_full = accum_empty + 2;          // split-K: all partials of a tile received
     uint64_t* recv_free = red_full + 2;            // split-K: every owner's receive buffer free again
@@ -180,13 +180,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Producer: barriers, then start streaming weights right away (they do
     // not depend on the previous kernel in the stream).
+    // a single activation tile reads each weight block once: stream it;
+    // several activation tiles re-read every weight block: keep it
     uint64_t pol_w = 0;
+    if (warp == 4) pol_w = g.b_tiles == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
     if (warp == 4 && lane == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
-            mbar_init(smem_u32(&sf_ready[s]), 4);  // one arrival per scale-writer warp
         }
+        mbar_init(smem_u32(qdone), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accum_full[b]), 1);
             mbar_init(smem_u32(&accum_empty[b]), 4);          // one arrival per epilogue warp
@@ -201,9 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         *consumed = 0;
         *issued = 0;
         fence_mbarrier_init();
-        // a single activation tile reads each weight block once: stream it;
-        // several activation tiles re-read every weight block: keep it
-        pol_w = g.b_tiles == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
         for (int u = 0; u < pre; ++u) {
             const uint32_t fb = smem_u32(&full[u]);
             mbar_arrive_expect_tx(fb, WB + b_tx_of(u));
@@ -236,72 +236,88 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 4) {
         // ------------------------------------------------ producer
-        if (lane == 0) {
-            // activations are re-read by every channel tile of their row block
-            const uint64_t pol_x = g.b_tiles == 1 ? l2_policy_evict_last() : l2_policy_evict_normal();
-            auto load_b = [&](int u) {
-                if (FUSED) return;
-                const int j = u / nck, i = u - j * nck;
-                const int chunk = c0 + i, s = u % S, bt = b_tile_of(j);
-                const int nb_tiles = min(BT, g.b_row_tiles - bt * BT);
-                uint8_t* st = bregion + (size_t)s * BSTAGE;
-                const uint32_t fb = smem_u32(&full[s]);
-                tma_load_2d(smem_u32(st), &tmap_b, fb, chunk * 128, bt * BN, pol_x);
-                const int na = min(APC, g.n_atoms_k - chunk * APC);
-                for (int t = 0; t < nb_tiles; ++t)
-                    bulk_load(smem_u32(st + B_BYTES + (uint32_t)t * APC * 512u),
-                              g.sfb + ((size_t)(bt * BT + t) * g.n_atoms_k + (size_t)chunk * APC) * 512,
-                              (uint32_t)na * 512u, fb, pol_x);
-            };
-            pdl_wait_prior_grid();
+        // whole warp runs the loop, one elected lane issues the copies
+        // activations are re-read by every channel tile of their row block
+        const uint64_t pol_x = g.b_tiles == 1 ? l2_policy_evict_last() : l2_policy_evict_normal();
+        auto load_b = [&](int u) {
+            if (FUSED) return;
+            const int j = u / nck, i = u - j * nck;
+            const int chunk = c0 + i, s = u % S, bt = b_tile_of(j);
+            const int nb_tiles = min(BT, g.b_row_tiles - bt * BT);
+            uint8_t* st = bregion + (size_t)s * BSTAGE;
+            const uint32_t fb = smem_u32(&full[s]);
+            tma_load_2d(smem_u32(st), &tmap_b, fb, chunk * 128, bt * BN, pol_x);
+            const int na = min(APC, g.n_atoms_k - chunk * APC);
+            for (int t = 0; t < nb_tiles; ++t)
+                bulk_load(smem_u32(st + B_BYTES + (uint32_t)t * APC * 512u),
+                          g.sfb + ((size_t)(bt * BT + t) * g.n_atoms_k + (size_t)chunk * APC) * 512,
+                          (uint32_t)na * 512u, fb, pol_x);
+        };
+        pdl_wait_prior_grid();
+        if (elect_one_sync())
             for (int u = 0; u < pre; ++u) load_b(u);
-            int u = pre;
-            for (; u < nu; ++u) {
-                const int s = u % S;
-                const uint32_t ph = (uint32_t)(u / S) & 1u;
-                if (!mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag, g.err)) break;
+        __syncwarp();
+        int u = pre;
+        for (; u < nu; ++u) {
+            const int s = u % S;
+            const uint32_t ph = (uint32_t)(u / S) & 1u;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag, g.err))) break;
+            if (elect_one_sync()) {
                 const uint32_t fb = smem_u32(&full[s]);
                 mbar_arrive_expect_tx(fb, WB + b_tx_of(u));
                 bulk_load(smem_u32(wring + (size_t)s * WB), wsrc_of(u), WB, fb, pol_w);
                 load_b(u);
             }
+            __syncwarp();
+        }
+        if (lane == 0) {
             *issued = (uint32_t)u;
             RS_TRACE_MARK(g.trace, 3);
         }
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int u = 0;
-            bool ok = true;
-            for (int j = 0; ok && j < ntl; ++j) {
-                const int b = j % nacc;
-                if (j >= nacc) {
-                    // the epilogue has read this accumulator's previous tile
-                    if (!mbar_wait_bounded(smem_u32(&accum_empty[b]), (uint32_t)(j / nacc - 1) & 1u, abort_flag,
-                                           g.err))
-                        break;
-                    tc_fence_after();
-                }
-                const uint32_t tm_acc = tmem + (uint32_t)(b * BN);
-                for (int i = 0; i < nck; ++i, ++u) {
-                    const int s = u % S;
-                    const uint32_t ph = (uint32_t)(u / S) & 1u;
-                    // unit u's scales are in tensor memory (and, in fused plans,
-                    // its activation tile is in shared memory)
-                    if (!mbar_wait_bounded(smem_u32(&sf_ready[s]), ph, abort_flag, g.err)) {
-                        ok = false;
-                        break;
+        // The whole warp runs the loop; one elected lane copies the unit's
+        // scale atoms shared -> tensor memory (tcgen05.cp, ordered before the
+        // MMAs that read them in the tensor pipe) and issues the MMAs.  A
+        // stage's scale columns are rewritten only after its full barrier,
+        // which the producer re-arms after that stage's previous MMAs are done.
+        int u = 0;
+        bool ok = true;
+        if (FUSED) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(qdone), 0, abort_flag, g.err));
+        for (int j = 0; ok && j < ntl; ++j) {
+            const int b = j % nacc;
+            if (j >= nacc) {
+                // the epilogue has read this accumulator's previous tile
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&accum_empty[b]),
+                                                               (uint32_t)(j / nacc - 1) & 1u, abort_flag, g.err));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            const uint32_t tm_acc = tmem + (uint32_t)(b * BN);
+            const int nb_tiles = min(BT, g.b_row_tiles - b_tile_of(j) * BT);
+            for (int i = 0; i < nck; ++i, ++u) {
+                const int s = u % S;
+                const uint32_t ph = (uint32_t)(u / S) & 1u;
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err));
+                if (!ok) break;
+                if (lane == 0) *consumed = (uint32_t)(u + 1);
+                if (u == 0 && lane == 0) RS_TRACE_MARK(g.trace, 4);
+                if (u == nu - 1 && lane == 0) RS_TRACE_MARK(g.trace, 5);
+                tc_fence_after();
+                const int chunk = c0 + i;
+                const uint32_t sa = smem_u32(wring + (size_t)s * WB);
+                const uint32_t sb = smem_u32(bregion + (size_t)(FUSED ? i : s) * BSTAGE);
+                const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS);
+                const uint32_t tsfb = tsfa + SFA_COLS;
+                const int kleft = g.K - chunk * 256;
+                const int nks = min(4, (kleft + 63) / 64);
+                const int na = FMT == 0 ? nks : (nks + 1) / 2;  // scale atoms the chunk uses
+                if (elect_one_sync()) {
+                    for (int a = 0; a < na; ++a) {
+                        tc_cp_sf_atom(tsfa + a * 4, sf_atom_desc(sa + kWeightCodeBytes + a * 512));
+                        for (int t = 0; t < nb_tiles; ++t)
+                            tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sf_atom_desc(sb + B_BYTES + (t * APC + a) * 512));
                     }
-                    if (u == 0) RS_TRACE_MARK(g.trace, 4);
-                    if (u == nu - 1) RS_TRACE_MARK(g.trace, 5);
-                    tc_fence_after();
-                    const int chunk = c0 + i;
-                    const uint32_t sa = smem_u32(wring + (size_t)s * WB);
-                    const uint32_t sb = smem_u32(bregion + (size_t)(FUSED ? i : s) * BSTAGE);
-                    const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS);
-                    const uint32_t tsfb = tsfa + SFA_COLS;
-                    const int kleft = g.K - chunk * 256;
-                    const int nks = min(4, (kleft + 63) / 64);
                     for (int ks = 0; ks < nks; ++ks) {
                         const uint64_t adesc = kmajor_sw128_desc(sa + ks * 32);
                         const uint64_t bdesc = kmajor_sw128_desc(sb + ks * 32);
@@ -318,12 +334,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_commit(smem_u32(&empty[s]));
                 }
-                if (ok) tc_commit(smem_u32(&accum_full[b]));  // fires once the tile's MMAs are done
+                __syncwarp();
             }
+            if (ok) {
+                if (elect_one_sync()) tc_commit(smem_u32(&accum_full[b]));  // fires once the tile's MMAs are done
+                __syncwarp();
+            }
+            if (j < 3 && lane == 0) RS_TRACE_MARK(g.trace, 19 + j);
         }
     } else {
         // ------------------------------------------------ warps 0-3, 6-11
-        const bool sfw = warp < 4;             // scale writers: tensor-memory lane quarter = warp
         const bool epi = warp >= 8;            // epilogue: lane quarter = warp - 8
         const int qw = warp < 4 ? warp : warp - 2;  // quantizer warp 0..kQuantWarps-1
         const int qtid = qw * 32 + lane;
@@ -414,62 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (qtid == kQuantThreads - 1) RS_TRACE_MARK(g.trace, 18);
             fence_proxy_async_smem();
             named_bar_sync(2, kQuantThreads);
-            if (qtid == 0) RS_TRACE_MARK(g.trace, 8);
+            if (qtid == 0) {
+                mbar_arrive(smem_u32(qdone));  // the MMA warp may read the activation slice
+                RS_TRACE_MARK(g.trace, 8);
+            }
         } else if (epi) {
             pdl_wait_prior_grid();  // before writing the output
-        }
-
-        if (sfw) {
-            // ---------------------------------------------- scales -> TMEM
-            // Each warp writes its own lane quarter with the 32 x 16-byte rows
-            // of every scale atom (the image a 32x128b.warpx4 copy makes).
-            const uint32_t quarter = (uint32_t)(warp * 32) << 16;
-            int u = 0;
-            for (; u < nu; ++u) {
-                const int j = u / nck, i = u - j * nck;
-                const int s = u % S;
-                const uint32_t ph = (uint32_t)(u / S) & 1u;
-                // warp-uniform outcome: the tcgen05.st below are warp-collective
-                const bool landed = mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err);
-                if (!__all_sync(0xFFFFFFFFu, landed)) break;
-                const uint8_t* wst = wring + (size_t)s * WB + kWeightCodeBytes;
-                const uint8_t* bst = bregion + (size_t)(FUSED ? i : s) * BSTAGE + B_BYTES;
-                const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS) + quarter;
-                const uint32_t tsfb = tsfa + SFA_COLS;
-                if constexpr (BT == 1) {
-                    // every atom of the chunk in one store per operand (atoms a
-                    // ragged K tail does not read are stale but never used)
-                    uint4 va[APC], vb[APC];
-#pragma unroll
-                    for (int a = 0; a < APC; ++a) {
-                        va[a] = *reinterpret_cast<const uint4*>(wst + a * 512 + lane * 16);
-                        vb[a] = *reinterpret_cast<const uint4*>(bst + a * 512 + lane * 16);
-                    }
-                    if constexpr (APC == 4) {
-                        tmem_st16(tsfa, va);
-                        tmem_st16(tsfb, vb);
-                    } else {
-                        tmem_st8(tsfa, va);
-                        tmem_st8(tsfb, vb);
-                    }
-                } else {
-                    const int kleft = g.K - (c0 + i) * 256;
-                    const int nks = min(4, (kleft + 63) / 64);
-                    const int na = FMT == 0 ? nks : (nks + 1) / 2;
-                    const int nb_tiles = min(BT, g.b_row_tiles - b_tile_of(j) * BT);
-                    for (int a = 0; a < na; ++a)
-                        tmem_st4(tsfa + a * 4, *reinterpret_cast<const uint4*>(wst + a * 512 + lane * 16));
-                    for (int t = 0; t < nb_tiles; ++t)
-                        for (int a = 0; a < na; ++a)
-                            tmem_st4(tsfb + (a * BT + t) * 4,
-                                     *reinterpret_cast<const uint4*>(bst + (t * APC + a) * 512 + lane * 16));
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sf_ready[s]));
-            }
-            if (warp == 0 && lane == 0) *consumed = (uint32_t)u;
         }
 
         if (epi) {
@@ -500,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 bool ok = mbar_wait_bounded(smem_u32(&accum_full[b]), use_ph, abort_flag, g.err);
                 if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 6);
+                if (j < 3 && ctid == 0) RS_TRACE_MARK(g.trace, 22 + j);
                 ok = __all_sync(0xFFFFFFFFu, ok && *abort_flag == 0);  // warp-uniform for tcgen05.ld
                 tc_fence_after();
                 if (g.splits > 1 && j > 0) {
@@ -560,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int r = 0; r < g.splits; ++r) acc = __fadd_rn(acc, recv[(r * per_cta + jj) * 128 + row]);
                         if (*abort_flag == 0) store_y(m0 + jo, acc);
                     }
+                    if (j < 3 && ctid == 0) RS_TRACE_MARK(g.trace, 25 + j);
                     if (j + nacc < ntl) {
                         // buffer b is read: re-arm it for tile j + nacc, then
                         // tell every partner it may send into it again
