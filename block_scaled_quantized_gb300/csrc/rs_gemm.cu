@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t pol_w = 0;
     if (warp == 4) pol_w = g.b_tiles == 1 ? l2_policy_evict_first() : l2_policy_evict_last();
     if (warp == 4 && lane == 0) {
+        RS_TRACE_MARK(g.trace, 31);
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
@@ -203,13 +204,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         *consumed = 0;
         *issued = 0;
+        RS_TRACE_MARK(g.trace, 28);
         fence_mbarrier_init();
-        for (int u = 0; u < pre; ++u) {
-            const uint32_t fb = smem_u32(&full[u]);
-            mbar_arrive_expect_tx(fb, WB + b_tx_of(u));
-            bulk_load(smem_u32(wring + (size_t)u * WB), wsrc_of(u), WB, fb, pol_w);
+    }
+    if (warp == 4) {
+        __syncwarp();
+        if (elect_one_sync()) {
+            for (int u = 0; u < pre; ++u) {
+                const uint32_t fb = smem_u32(&full[u]);
+                mbar_arrive_expect_tx(fb, WB + b_tx_of(u));
+                bulk_load(smem_u32(wring + (size_t)u * WB), wsrc_of(u), WB, fb, pol_w);
+                if (u == 0) RS_TRACE_MARK(g.trace, 30);
+            }
+            RS_TRACE_MARK(g.trace, 2);
         }
-        RS_TRACE_MARK(g.trace, 2);
+        __syncwarp();
     }
     if (warp == 5) {
         tmem_alloc(smem_u32(tmem_slot), (uint32_t)g.tmem_cols);
@@ -258,17 +267,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < pre; ++u) load_b(u);
         __syncwarp();
         int u = pre;
+        // stage, phase, and the unit's (tile, chunk) advance incrementally
+        int s = pre % S, jj = pre / nck, ii = pre - jj * nck;
+        uint32_t ph = (uint32_t)(pre / S) & 1u;
+        const uint8_t* wtile = g.wq + ((size_t)n_tile_of(jj) * g.chunks + c0) * WB;
         for (; u < nu; ++u) {
-            const int s = u % S;
-            const uint32_t ph = (uint32_t)(u / S) & 1u;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag, g.err))) break;
             if (elect_one_sync()) {
                 const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, WB + b_tx_of(u));
-                bulk_load(smem_u32(wring + (size_t)s * WB), wsrc_of(u), WB, fb, pol_w);
+                mbar_arrive_expect_tx(fb, WB + (FUSED ? 0u : b_tx_of(u)));
+                bulk_load(smem_u32(wring + (size_t)s * WB), wtile + (size_t)ii * WB, WB, fb, pol_w);
                 load_b(u);
             }
             __syncwarp();
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (++ii == nck) {
+                ii = 0;
+                ++jj;
+                wtile = g.wq + ((size_t)n_tile_of(jj) * g.chunks + c0) * WB;
+            }
         }
         if (lane == 0) {
             *issued = (uint32_t)u;
@@ -281,11 +301,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MMAs that read them in the tensor pipe) and issues the MMAs.  A
         // stage's scale columns are rewritten only after its full barrier,
         // which the producer re-arms after that stage's previous MMAs are done.
-        int u = 0;
+        // Descriptors are formed once and advanced by adding (offset >> 4) to
+        // their start-address field (shared addresses stay below 2^18, so the
+        // 14-bit field never carries); stage and phase advance incrementally.
+        const uint64_t adesc0 = kmajor_sw128_desc(smem_u32(wring));
+        const uint64_t bdesc0 = kmajor_sw128_desc(smem_u32(bregion));
+        const uint64_t sfadesc0 = sf_atom_desc(smem_u32(wring) + kWeightCodeBytes);
+        const uint64_t sfbdesc0 = sf_atom_desc(smem_u32(bregion) + B_BYTES);
+        constexpr uint32_t kIdesc = mxf4_idesc(BN, FMT == 1, 0);
+        int u = 0, s = 0;
+        uint32_t ph = 0;
         bool ok = true;
-        if (FUSED) ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(qdone), 0, abort_flag, g.err));
         for (int j = 0; ok && j < ntl; ++j) {
-            const int b = j % nacc;
+            const int b = j & (nacc - 1);
             if (j >= nacc) {
                 // the epilogue has read this accumulator's previous tile
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&accum_empty[b]),
@@ -296,45 +324,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tm_acc = tmem + (uint32_t)(b * BN);
             const int nb_tiles = min(BT, g.b_row_tiles - b_tile_of(j) * BT);
             for (int i = 0; i < nck; ++i, ++u) {
-                const int s = u % S;
-                const uint32_t ph = (uint32_t)(u / S) & 1u;
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err));
+                if (u == 0 && lane == 0) RS_TRACE_MARK(g.trace, 15);
+                bool landed = mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err);
+                if (u == 0 && lane == 0) RS_TRACE_MARK(g.trace, 29);
+                // fused plans: the activation slice is quantized (waited for
+                // here, after the loop set-up, which overlaps the quantizer)
+                if (FUSED && u == 0) landed = landed && mbar_wait_bounded(smem_u32(qdone), 0, abort_flag, g.err);
+                if (u == 0 && lane == 0) RS_TRACE_MARK(g.trace, 11);
+                ok = __all_sync(0xFFFFFFFFu, landed);
                 if (!ok) break;
                 if (lane == 0) *consumed = (uint32_t)(u + 1);
                 if (u == 0 && lane == 0) RS_TRACE_MARK(g.trace, 4);
                 if (u == nu - 1 && lane == 0) RS_TRACE_MARK(g.trace, 5);
                 tc_fence_after();
-                const int chunk = c0 + i;
-                const uint32_t sa = smem_u32(wring + (size_t)s * WB);
-                const uint32_t sb = smem_u32(bregion + (size_t)(FUSED ? i : s) * BSTAGE);
+                const uint32_t aoff = (uint32_t)s * (WB >> 4);
+                const uint32_t boff = (uint32_t)(FUSED ? i : s) * (BSTAGE >> 4);
+                const uint64_t ad = adesc0 + aoff, bd = bdesc0 + boff;
+                const uint64_t sad = sfadesc0 + aoff, sbd = sfbdesc0 + boff;
                 const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS);
                 const uint32_t tsfb = tsfa + SFA_COLS;
-                const int kleft = g.K - chunk * 256;
-                const int nks = min(4, (kleft + 63) / 64);
-                const int na = FMT == 0 ? nks : (nks + 1) / 2;  // scale atoms the chunk uses
+                const bool whole = c0 + i < g.chunks - 1 || (g.K & 255) == 0;  // all four k-steps
                 if (elect_one_sync()) {
-                    for (int a = 0; a < na; ++a) {
-                        tc_cp_sf_atom(tsfa + a * 4, sf_atom_desc(sa + kWeightCodeBytes + a * 512));
-                        for (int t = 0; t < nb_tiles; ++t)
-                            tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sf_atom_desc(sb + B_BYTES + (t * APC + a) * 512));
-                    }
-                    for (int ks = 0; ks < nks; ++ks) {
-                        const uint64_t adesc = kmajor_sw128_desc(sa + ks * 32);
-                        const uint64_t bdesc = kmajor_sw128_desc(sb + ks * 32);
-                        const uint32_t accum = (i > 0 || ks > 0) ? 1u : 0u;
-                        if (FMT == 0) {
-                            mma_nvfp4(tm_acc, adesc, bdesc, mxf4_idesc(BN, false, 0), tsfa + ks * 4,
-                                      tsfb + ks * BT * 4, accum);
-                        } else {
-                            const int a = ks >> 1;
-                            const uint32_t sf_id = (uint32_t)(ks & 1) * 2u;
-                            mma_mxfp4(tm_acc, adesc, bdesc, mxf4_idesc(BN, true, sf_id), tsfa + a * 4,
-                                      tsfb + a * BT * 4, accum);
+                    if (whole) {
+#pragma unroll
+                        for (int a = 0; a < APC; ++a) {
+                            tc_cp_sf_atom(tsfa + a * 4, sad + (uint32_t)a * 32u);
+                            for (int t = 0; t < nb_tiles; ++t)
+                                tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sbd + (uint32_t)(t * APC + a) * 32u);
+                        }
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t accum = (i > 0 || ks > 0) ? 1u : 0u;
+                            if (FMT == 0)
+                                mma_nvfp4(tm_acc, ad + (uint32_t)ks * 2u, bd + (uint32_t)ks * 2u, kIdesc,
+                                          tsfa + ks * 4, tsfb + ks * BT * 4, accum);
+                            else
+                                mma_mxfp4(tm_acc, ad + (uint32_t)ks * 2u, bd + (uint32_t)ks * 2u,
+                                          kIdesc | ((uint32_t)(ks & 1) * 2u << 4) | ((uint32_t)(ks & 1) * 2u << 29),
+                                          tsfa + (ks >> 1) * 4, tsfb + (ks >> 1) * BT * 4, accum);
+                        }
+                    } else {
+                        // ragged K tail: the k-steps (and scale atoms) it covers
+                        const int nks = (g.K - (c0 + i) * 256 + 63) / 64;
+                        const int na = FMT == 0 ? nks : (nks + 1) / 2;
+                        for (int a = 0; a < na; ++a) {
+                            tc_cp_sf_atom(tsfa + a * 4, sad + (uint32_t)a * 32u);
+                            for (int t = 0; t < nb_tiles; ++t)
+                                tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sbd + (uint32_t)(t * APC + a) * 32u);
+                        }
+                        for (int ks = 0; ks < nks; ++ks) {
+                            const uint32_t accum = (i > 0 || ks > 0) ? 1u : 0u;
+                            if (FMT == 0)
+                                mma_nvfp4(tm_acc, ad + (uint32_t)ks * 2u, bd + (uint32_t)ks * 2u, kIdesc,
+                                          tsfa + ks * 4, tsfb + ks * BT * 4, accum);
+                            else
+                                mma_mxfp4(tm_acc, ad + (uint32_t)ks * 2u, bd + (uint32_t)ks * 2u,
+                                          kIdesc | ((uint32_t)(ks & 1) * 2u << 4) | ((uint32_t)(ks & 1) * 2u << 29),
+                                          tsfa + (ks >> 1) * 4, tsfb + (ks >> 1) * BT * 4, accum);
                         }
                     }
                     tc_commit(smem_u32(&empty[s]));
                 }
                 __syncwarp();
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             if (ok) {
                 if (elect_one_sync()) tc_commit(smem_u32(&accum_full[b]));  // fires once the tile's MMAs are done
@@ -417,8 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t sfq, codes[E / 8];
                     float xh[E];
                     quant_block<FMT, E>(xs[r], alpha, sfq, codes, xh);
+                    if (qtid == 0 && fw == 0 && r == 0) RS_TRACE_VALUE(g.trace, 13, globaltimer_ns() + (codes[0] & 1u));
                     const uint32_t rb = g.fold ? 2u * (uint32_t)j : (uint32_t)j;
                     put(rb, kk, codes, sfq, live);
+                    if (qtid == 0 && fw == 0 && r == 0) RS_TRACE_MARK(g.trace, 14);
                     if (g.fold) {
                         float rr[E];
 #pragma unroll
