@@ -125,6 +125,24 @@ __device__ __forceinline__ uint32_t e4m3_encode_satfinite(float t) {
     return ((uint32_t)(e + 7) << 3) + ni - 8u;             // 16 carries into the exponent
 }
 
+// Hardware E4M3 conversions: cvt.rn.satfinite.e4m3x2.f32 (round to nearest
+// even, finite inputs above 448 saturate to 448) and cvt.rn.f16x2.e4m3x2
+// (exact).  On every non-negative finite float and every finite byte they
+// agree with e4m3_encode_satfinite / e4m3_decode above.
+// Two floats -> two bytes: `a` in bits 8-15, `b` in bits 0-7.
+__device__ __forceinline__ uint32_t e4m3x2_encode_hw(float a, float b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ float e4m3_decode_hw(uint32_t byte) {
+    uint32_t h2;
+    const uint16_t b16 = (uint16_t)byte;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(b16));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
 // ------------------------------------------------------------ misc helpers --
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

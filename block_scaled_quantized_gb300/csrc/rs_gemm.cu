@@ -413,7 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync(2, kQuantThreads);
             pdl_wait_prior_grid();
             if (qtid == 0) RS_TRACE_MARK(g.trace, 16);
-            const float alpha = FMT == 0 ? *g.alpha_x : 0.0f;
+            const NvScaleConst ksc = nv_scale_const(FMT == 0 ? *g.alpha_x : 0.0f);
+            if (FMT == 0 && qtid == 0 && blockIdx.x == 0 && blockIdx.z == 0 && !nv_alpha_supported(ksc.alpha))
+                atomicExch(g.err, kErrInvalidArg);
             const int kbeg = c0 * 256, kend = min(g.K, (c0 + nck) * 256);
             // codes of one block (element offset kk of the slice) and, gathered
             // over four consecutive lanes, one scale-atom word
@@ -471,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool live = f < total && kbeg + kk < kend;
                     uint32_t sfq, codes[E / 8];
                     float xh[E];
-                    quant_block<FMT, E>(xs[r], alpha, sfq, codes, xh);
+                    quant_block<FMT, E>(xs[r], ksc, sfq, codes, xh);
                     if (qtid == 0 && fw == 0 && r == 0) RS_TRACE_VALUE(g.trace, 13, globaltimer_ns() + (codes[0] & 1u));
                     const uint32_t rb = g.fold ? 2u * (uint32_t)j : (uint32_t)j;
                     put(rb, kk, codes, sfq, live);
@@ -482,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int e = 0; e < E; ++e) rr[e] = __fsub_rn(xs[r][e], xh[e]);  // residue (Alg. 1 line 6)
                         uint32_t sfr, rcodes[E / 8];
                         float rh[E];
-                        quant_block<FMT, E, false>(rr, alpha, sfr, rcodes, rh);
+                        quant_block<FMT, E, false>(rr, ksc, sfr, rcodes, rh);
                         put(rb + 1u, kk, rcodes, sfr, live);
                     }
                 }

@@ -51,7 +51,9 @@ __global__ void tensor_scale_finalize_kernel(float* __restrict__ alpha, uint32_t
         *alpha = __uint_as_float(0x7FC00000u);
         return;
     }
-    *alpha = __fdiv_rn(__uint_as_float(bits), 2688.0f);
+    const float a = __fdiv_rn(__uint_as_float(bits), 2688.0f);
+    if (!nv_alpha_supported(a)) atomicExch(err, kErrInvalidArg);  // tensor amax below about 4e-32
+    *alpha = a;
 }
 
 // ------------------------------------------------------------- quantizer --
@@ -72,6 +74,7 @@ struct QuantArgs {
     int n_atoms_k;       // ceil(K / atom_k)
     int chunks;          // ceil(K / 256)
     int early_trigger;   // release the dependent grid once the prior grid is done
+    uint32_t* err;       // device error word
 };
 
 template <int FMT, int MODE>
@@ -84,7 +87,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps_total = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t tasks = (int64_t)a.task_rows * a.chunks;
-    const float alpha = FMT == 0 ? *a.alpha : 0.0f;
+    const NvScaleConst ksc = nv_scale_const(FMT == 0 ? *a.alpha : 0.0f);
+    if (FMT == 0 && blockIdx.x == 0 && threadIdx.x == 0 && !nv_alpha_supported(ksc.alpha))
+        atomicExch(a.err, kErrInvalidArg);
 
     for (int64_t task = warp; task < tasks; task += n_warps_total) {
         const int row = (int)(task / a.chunks);
@@ -96,7 +101,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
 
         uint32_t sfb;
         float xh[8];
-        const uint32_t codes = quant_lane<FMT>(xf, alpha, sfb, xh);
+        const uint32_t codes = quant_lane<FMT>(xf, ksc, sfb, xh);
         const uint32_t sfw = gather_sf_word<FMT>(sfb, lane);
         const int g = chunk * (256 / atom_k(FMT)) + lane / LPA;  // atom index along K
         const bool leader = (lane % LPA) == 0;
@@ -119,7 +124,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
                 residue8(xf, xh, r);
                 uint32_t sfr;
                 float rh[8];
-                const uint32_t rcodes = quant_lane<FMT>(r, alpha, sfr, rh);
+                const uint32_t rcodes = quant_lane<FMT>(r, ksc, sfr, rh);
                 const uint32_t sfrw = gather_sf_word<FMT>(sfr, lane);
                 if (valid)
                     *reinterpret_cast<uint32_t*>(a.out + (size_t)(out_row + 1) * (a.K / 2) + k0 / 2) = rcodes;
@@ -197,6 +202,7 @@ cudaError_t launch_quantize(int fmt, bool paired, int rows, int K, const void* x
     a.rows = rows;
     a.K = K;
     a.alpha = alpha;
+    a.err = device_error_word();
     a.rows_out = paired ? 2 * rows : rows;
     a.rows_pad = (a.rows_out + kAtomRows - 1) / kAtomRows * kAtomRows;
     a.task_rows = rows;
@@ -219,6 +225,7 @@ cudaError_t launch_quantize_weight(int fmt, int N, int K, const void* w, int64_t
     a.rows = N;
     a.K = K;
     a.alpha = alpha;
+    a.err = device_error_word();
     a.task_rows = (N + 127) / 128 * 128;  // padding rows quantize as zeros
     a.n_atoms_k = (K + atom_k(fmt) - 1) / atom_k(fmt);
     a.chunks = (K + 255) / 256;

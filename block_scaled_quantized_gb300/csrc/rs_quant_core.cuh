@@ -25,6 +25,54 @@ __device__ __forceinline__ uint32_t nv_block_scale(float amax, float alpha, floa
     return sf;
 }
 
+// NVFP4 tensor scales the quantizers support: 0, or finite and at least
+// 2^-117, so that every non-zero block scale s~ >= alpha * 2^-9 is a normal
+// float and fl(1/s~) is finite.  (Below that, x * fl(1/s~) can be infinite
+// or NaN and the E2M1 rounding of Eq. 10 is undefined.)
+__device__ __forceinline__ bool nv_alpha_supported(float alpha) {
+    return alpha == 0.0f || (alpha >= 0x1p-117f && alpha <= 3.40282347e38f);
+}
+
+// Per-tensor constants of the fast NVFP4 scale path: c = fl(1/fl(6 alpha)),
+// usable when alpha > 0 and c is a normal float.
+struct NvScaleConst {
+    float alpha, c;
+    bool fast;
+};
+__device__ __forceinline__ NvScaleConst nv_scale_const(float alpha) {
+    NvScaleConst k;
+    k.alpha = alpha;
+    k.c = alpha > 0.0f ? __frcp_rn(__fmul_rn(6.0f, alpha)) : 0.0f;
+    k.fast = alpha > 0.0f && k.c >= 0x1p-126f && k.c < 0x1p126f;
+    return k;
+}
+
+// Same result as nv_block_scale, with the divisions only where they decide.
+// The estimate t~ = fl(amax * c) is within a relative 2^-21 of
+// t = fl(fl(amax/6)/alpha) (five roundings of at most 2^-24 each, which
+// needs fl(6 alpha), c and amax/6 to be normal floats: amax >= 2^-123);
+// E4M3 rounding is monotone, so when both ends of the band t~(1 -+ 2^-20)
+// round to the same byte, t rounds to it too.  t~ >= 448 means t >= 432,
+// which rounds to the largest byte.  Blocks whose t lies within about 2^-20
+// of a rounding boundary (a fraction of about 2^-16 of blocks) take the exact
+// path.  st = fl(alpha * dec(byte)) and mul = fl(1/st) as in nv_block_scale
+// (__frcp_rn is the correctly rounded reciprocal).
+__device__ __forceinline__ uint32_t nv_block_scale_fast(float amax, const NvScaleConst& k, float& st, float& mul) {
+    if (!k.fast || !(amax >= 0x1p-123f)) return nv_block_scale(amax, k.alpha, st, mul);
+    const float t = __fmul_rn(amax, k.c);
+    uint32_t sf;
+    if (!(t < 448.0f)) {
+        sf = 0x7Eu;
+    } else {
+        const uint32_t pr = e4m3x2_encode_hw(__fmul_rn(t, 1.0f - 0x1p-20f), __fmul_rn(t, 1.0f + 0x1p-20f));
+        sf = pr & 0xFFu;
+        if (sf != (pr >> 8)) return nv_block_scale(amax, k.alpha, st, mul);
+    }
+    st = __fmul_rn(k.alpha, e4m3_decode_hw(sf));
+    mul = st == 0.0f ? 0.0f : __frcp_rn(st);
+    return sf;
+}
+
 // MXFP4 block scale: byte = max(E - 2, 0) where E is the biased fp32
 // exponent of amax, i.e. e = floor(log2 amax) - 2 clamped at -127 (amax == 0
 // and fp32-subnormal amax give byte 0).  st = 2^e, mul = 2^-e, both exact.
@@ -48,13 +96,14 @@ __device__ __forceinline__ float block_amax(float a) {
 // bits 4e..4e+3, i.e. element 2j in the low nibble of byte j), the block's
 // scale byte in `sf`, and the reconstruction fl(s~ * dec(q)) in `xh`.
 template <int FMT>
-__device__ __forceinline__ uint32_t quant_lane(const float (&xf)[8], float alpha, uint32_t& sf, float (&xh)[8]) {
+__device__ __forceinline__ uint32_t quant_lane(const float (&xf)[8], const NvScaleConst& k, uint32_t& sf,
+                                               float (&xh)[8]) {
     float am = 0.0f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(xf[e]));
     am = block_amax<FMT>(am);
     float st, mul;
-    sf = FMT == 0 ? nv_block_scale(am, alpha, st, mul) : mx_block_scale(am, st, mul);
+    sf = FMT == 0 ? nv_block_scale_fast(am, k, st, mul) : mx_block_scale(am, st, mul);
     float v[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(xf[e], mul);
@@ -97,8 +146,8 @@ __host__ __device__ constexpr int lanes_per_atom() { return FMT == 0 ? 8 : 16; }
 // word e/8).  Same arithmetic per element as quant_lane; the amax is a max,
 // so its evaluation order does not change it.
 template <int FMT, int E, bool kRecon = true>
-__device__ __forceinline__ void quant_block(const float (&xf)[E], float alpha, uint32_t& sf, uint32_t (&codes)[E / 8],
-                                            float (&xh)[E]) {
+__device__ __forceinline__ void quant_block(const float (&xf)[E], const NvScaleConst& k, uint32_t& sf,
+                                            uint32_t (&codes)[E / 8], float (&xh)[E]) {
     float am0 = 0.0f, am1 = 0.0f;
 #pragma unroll
     for (int e = 0; e < E; e += 2) {
@@ -107,7 +156,7 @@ __device__ __forceinline__ void quant_block(const float (&xf)[E], float alpha, u
     }
     const float am = fmaxf(am0, am1);
     float st, mul;
-    sf = FMT == 0 ? nv_block_scale(am, alpha, st, mul) : mx_block_scale(am, st, mul);
+    sf = FMT == 0 ? nv_block_scale_fast(am, k, st, mul) : mx_block_scale(am, st, mul);
 #pragma unroll
     for (int w = 0; w < E / 8; ++w) {
         float v[8];

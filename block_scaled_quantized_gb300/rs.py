@@ -22,6 +22,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "
 
 STATUS = {0: "RS_OK", 1: "RS_ERR_INVALID_ARG", 2: "RS_ERR_ALIGNMENT", 3: "RS_ERR_SHAPE",
           4: "RS_ERR_UNSUPPORTED", 5: "RS_ERR_WORKSPACE", 6: "RS_ERR_CUDA", 7: "RS_ERR_DEVICE_TIMEOUT"}
+globals().update({name: code for code, name in STATUS.items()})  # RS_OK, RS_ERR_INVALID_ARG, ...
 
 # Every symbol include/rs.h declares.
 EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_offset", "rs_act_bytes",

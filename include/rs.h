@@ -29,7 +29,8 @@
  * Formats (Sec. 2, Fig. 1; App. B.2 Eq. 8-10)
  * -------------------------------------------
  *   RS_NVFP4: E2M1 codes, one E4M3 block scale per 16 elements along K and
- *             one fp32 tensor scale alpha.
+ *             one fp32 tensor scale alpha (0, or finite and >= 2^-117; see
+ *             rs_get_device_error).
  *   RS_MXFP4: E2M1 codes, one E8M0 block scale per 32 elements along K, no
  *             tensor scale (alpha pointers are ignored and may be NULL).
  *
@@ -243,8 +244,11 @@ RS_API rs_status rs_linear_compensated_noalloc(rs_format fmt, int M, int N, int 
 /* Synchronizes `stream`, then returns and clears the device error word of the
  * current device: RS_OK, RS_ERR_DEVICE_TIMEOUT (a kernel's bounded wait ran
  * out; its outputs are invalid and the workspace must be zero-filled again)
- * or RS_ERR_INVALID_ARG (non-finite tensor amax).  Returns RS_ERR_CUDA if the
- * synchronization itself fails. */
+ * or RS_ERR_INVALID_ARG (a non-finite tensor amax, or an NVFP4 tensor scale
+ * that is neither 0 nor a finite value of at least 2^-117, i.e. a tensor amax
+ * below about 4e-32: block scales of such a tensor can be subnormal, their
+ * reciprocals infinite, and the codes of those blocks are unspecified).
+ * Returns RS_ERR_CUDA if the synchronization itself fails. */
 RS_API rs_status rs_get_device_error(rs_stream_t stream);
 
 #ifdef __cplusplus

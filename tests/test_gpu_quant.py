@@ -144,3 +144,44 @@ def test_alpha_zero_gives_zero_operand():
     buf = gpu_quantize(0, x, a, paired=True)
     codes, sf = unpack(buf, 0, 8, 64)
     assert not codes.any() and not sf.any()
+
+
+# The NVFP4 block scale byte E4M3(fl(fl(amax/6)/alpha)) for every positive
+# finite bf16 value as a block amax (ResServe App. B.2 Eq. 8-9): blocks whose
+# scale lies next to an E4M3 rounding boundary (ties included) and blocks far
+# from one, saturation, underflow to zero, subnormal block amaxes, and the
+# ends of the supported tensor-scale range (2^-117 and a scale so large that
+# the quantizer's estimate of 1/(6 alpha) would be subnormal).
+ALPHAS = [1.0, 2.0 ** -10, 0.012345678, 3.7e-5, 1.5e-30, 2.0 ** -110, 2.0 ** -117, 2.0e30, 3.0e37]
+
+
+@pytest.mark.parametrize("alpha", ALPHAS)
+@pytest.mark.parametrize("paired", [False, True])
+def test_nvfp4_scale_every_bf16_amax(alpha, paired):
+    K = 4096
+    amax_bits = torch.arange(1, 0x7F80, dtype=torch.int32)            # 0x0001 .. 0x7F7F
+    nblk = (amax_bits.numel() + K // 16 - 1) // (K // 16) * (K // 16)
+    amax = torch.zeros(nblk, dtype=torch.int32)
+    amax[: amax_bits.numel()] = amax_bits
+    amax = amax.to(torch.int16).view(torch.bfloat16).float()
+    g = torch.Generator().manual_seed(2024)
+    u = torch.rand((nblk, 16), generator=g) * 2.0 - 1.0
+    blocks = amax[:, None] * u
+    blocks[:, 0] = amax                                                # the block amax itself
+    sign = torch.where(torch.rand((nblk, 16), generator=g) < 0.5, -1.0, 1.0)
+    sign[:, 0] = torch.where(torch.arange(nblk) % 2 == 0, 1.0, -1.0)
+    x = (blocks * sign).to(torch.bfloat16).reshape(-1, K)
+    _check(0, x, paired, alpha=np.float32(alpha))
+
+
+@pytest.mark.parametrize("alpha", [1.0e-39, 2.0 ** -118, float("inf"), -1.0])
+def test_unsupported_tensor_scale_flagged(alpha):
+    """An NVFP4 tensor scale outside {0} and [2^-117, max float] sets the
+    device error word (RS_ERR_INVALID_ARG); a supported one does not."""
+    from block_scaled_quantized_gb300 import rs
+    x = workloads.make_x("attn_proj_k4096", 4, K=512)
+    assert rs.rs_get_device_error() == 0
+    gpu_quantize(0, x.to(DEV), torch.tensor([alpha], dtype=torch.float32, device=DEV), False)
+    assert rs.rs_get_device_error() == rs.RS_ERR_INVALID_ARG
+    gpu_quantize(0, x.to(DEV), torch.tensor([2.0 ** -117], dtype=torch.float32, device=DEV), True)
+    assert rs.rs_get_device_error() == 0
