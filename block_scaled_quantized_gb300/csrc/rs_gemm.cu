@@ -163,6 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int outs = g.fold ? BN / 2 : BN;
     const int per_cta = (outs + g.splits - 1) / g.splits;  // split-K: outputs each CTA owns
     const uint32_t slice_bytes = (uint32_t)per_cta * 128u * 4u;
+    // Wide tiles without split-K: eight epilogue warps (warps 8-11 and 0-3,
+    // two per tensor-memory lane quarter) take half of the columns each.
+    const bool epi8 = !FUSED && BN >= 64 && g.splits == 1;
     const uint32_t red_bytes = (uint32_t)g.splits * slice_bytes;
     auto n_tile_of = [&](int j) { return ((int)blockIdx.x + j * (int)gridDim.x) % g.n_tiles; };
     auto b_tile_of = [&](int j) { return ((int)blockIdx.x + j * (int)gridDim.x) / g.n_tiles; };
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(qdone), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accum_full[b]), 1);
-            mbar_init(smem_u32(&accum_empty[b]), 4);          // one arrival per epilogue warp
+            mbar_init(smem_u32(&accum_empty[b]), (uint32_t)(epi8 ? 8 : 4));  // one arrival per epilogue warp
             mbar_init(smem_u32(&red_full[b]), 1);
             mbar_init(smem_u32(&recv_free[b]), (uint32_t)g.splits);  // one arrival per owner
         }
@@ -204,7 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         *consumed = 0;
         *issued = 0;
-        RS_TRACE_MARK(g.trace, 28);
         fence_mbarrier_init();
     }
     if (warp == 4) {
@@ -214,7 +216,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t fb = smem_u32(&full[u]);
                 mbar_arrive_expect_tx(fb, WB + b_tx_of(u));
                 bulk_load(smem_u32(wring + (size_t)u * WB), wsrc_of(u), WB, fb, pol_w);
-                if (u == 0) RS_TRACE_MARK(g.trace, 30);
             }
             RS_TRACE_MARK(g.trace, 2);
         }
@@ -255,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nb_tiles = min(BT, g.b_row_tiles - bt * BT);
             uint8_t* st = bregion + (size_t)s * BSTAGE;
             const uint32_t fb = smem_u32(&full[s]);
-            tma_load_2d(smem_u32(st), &tmap_b, fb, chunk * 128, bt * BN, pol_x);
             const int na = min(APC, g.n_atoms_k - chunk * APC);
+            tma_load_2d(smem_u32(st), &tmap_b, fb, chunk * 128, bt * BN, pol_x);
             for (int t = 0; t < nb_tiles; ++t)
                 bulk_load(smem_u32(st + B_BYTES + (uint32_t)t * APC * 512u),
                           g.sfb + ((size_t)(bt * BT + t) * g.n_atoms_k + (size_t)chunk * APC) * 512,
@@ -273,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* wtile = g.wq + ((size_t)n_tile_of(jj) * g.chunks + c0) * WB;
         for (; u < nu; ++u) {
             if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag, g.err))) break;
+            if (lane == 0 && (u == 8 || u == 16 || u == 24)) RS_TRACE_MARK(g.trace, u == 8 ? 31 : u == 16 ? 29 : 15);
             if (elect_one_sync()) {
                 const uint32_t fb = smem_u32(&full[s]);
                 mbar_arrive_expect_tx(fb, WB + (FUSED ? 0u : b_tx_of(u)));
@@ -324,9 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tm_acc = tmem + (uint32_t)(b * BN);
             const int nb_tiles = min(BT, g.b_row_tiles - b_tile_of(j) * BT);
             for (int i = 0; i < nck; ++i, ++u) {
-                if (u == 0 && lane == 0) RS_TRACE_MARK(g.trace, 15);
                 bool landed = mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err);
-                if (u == 0 && lane == 0) RS_TRACE_MARK(g.trace, 29);
+                if (lane == 0 && (u == 8 || u == 16 || u == 24 || u == 31))
+                    RS_TRACE_MARK(g.trace, u == 8 ? 13 : u == 16 ? 14 : u == 24 ? 28 : 30);
                 // fused plans: the activation slice is quantized (waited for
                 // here, after the loop set-up, which overlaps the quantizer)
                 if (FUSED && u == 0) landed = landed && mbar_wait_bounded(smem_u32(qdone), 0, abort_flag, g.err);
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------ warps 0-3, 6-11
-        const bool epi = warp >= 8;            // epilogue: lane quarter = warp - 8
+        const bool epi = warp >= 8 || (epi8 && warp < 4);  // epilogue: lane quarter = warp % 4
         const int qw = warp < 4 ? warp : warp - 2;  // quantizer warp 0..kQuantWarps-1
         const int qtid = qw * 32 + lane;
         if (FUSED) {
@@ -474,10 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t sfq, codes[E / 8];
                     float xh[E];
                     quant_block<FMT, E>(xs[r], ksc, sfq, codes, xh);
-                    if (qtid == 0 && fw == 0 && r == 0) RS_TRACE_VALUE(g.trace, 13, globaltimer_ns() + (codes[0] & 1u));
                     const uint32_t rb = g.fold ? 2u * (uint32_t)j : (uint32_t)j;
                     put(rb, kk, codes, sfq, live);
-                    if (qtid == 0 && fw == 0 && r == 0) RS_TRACE_MARK(g.trace, 14);
                     if (g.fold) {
                         float rr[E];
 #pragma unroll
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (epi) {
             // ---------------------------------------------- epilogue
-            const int ew = warp - 8;                       // lane quarter
+            const int ew = warp & 3;                       // lane quarter
             const uint32_t quarter = (uint32_t)(ew * 32) << 16;
             const int row = ew * 32 + lane;                // accumulator lane = channel within the tile
             const int ctid = row;                          // 0..127
@@ -537,7 +537,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ctid == 0) bulk_wait_group_read0();
                     named_bar_sync(1, 128);
                 }
-                if (ok) {
+                if (ok && g.splits == 1) {
+                    // this warp's columns; output j of the tile at y + (m0 + j) * N + n
+                    const int ncol = epi8 ? BN / 2 : BN;
+                    const int cbeg = (epi8 && warp < 4) ? ncol : 0;
+                    const int jmax = n < g.N ? min(outs, g.M - m0) : 0;
+                    const size_t ybase = (size_t)m0 * g.N + (size_t)n;
+                    auto put_y = [&](int jj, float z) {
+                        if (jj < jmax) {
+                            const float val = __fmul_rn(gsc, z);
+                            const size_t idx = ybase + (size_t)jj * g.N;
+                            if (g.out_f32) reinterpret_cast<float*>(g.y)[idx] = val;
+                            else reinterpret_cast<__nv_bfloat16*>(g.y)[idx] = __float2bfloat16_rn(val);
+                        }
+                    };
+                    if (ncol % 32 == 0) {
+#pragma unroll 1
+                        for (int c = cbeg; c < cbeg + ncol; c += 32) {
+                            float v[32];
+                            tmem_ld32(tmem + (uint32_t)(b * BN) + quarter + (uint32_t)c, v);
+                            if (g.fold) {
+#pragma unroll
+                                for (int q = 0; q < 16; ++q) put_y(c / 2 + q, __fadd_rn(v[2 * q], v[2 * q + 1]));  // Fold
+                            } else {
+#pragma unroll
+                                for (int q = 0; q < 32; ++q) put_y(c + q, v[q]);
+                            }
+                        }
+                    } else {
+                        float v[16];
+                        tmem_ld16(tmem + (uint32_t)(b * BN) + quarter + (uint32_t)cbeg, v);
+                        if (g.fold) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) put_y(cbeg / 2 + q, __fadd_rn(v[2 * q], v[2 * q + 1]));  // Fold
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) put_y(cbeg + q, v[q]);
+                        }
+                    }
+                } else if (ok) {
 #pragma unroll 1
                     for (int c = 0; c < BN; c += 16) {
                         float v[16];
