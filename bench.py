@@ -39,12 +39,12 @@ WORKLOAD = "nvfp4_compensated_linear_attn_proj_M8_K4096_N4096"
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by
 # the hash of the kernel sources it was taken on (null once they change).
-TRAFFIC = {"sources_sha": "7d4c719fe11e00ad", "bytes_per_launch": 9558784}
+TRAFFIC = {"sources_sha": "baf641178d1c0d1c", "bytes_per_launch": 9580288}
 
 
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
-    for name in ("rs_gemm.cu", "rs_device.cuh"):
+    for name in ("rs_gemm.cu", "rs_device.cuh", "rs_quant_core.cuh"):
         with open(os.path.join(ROOT, "block_scaled_quantized_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -232,6 +232,29 @@ def graph_time_us(torch, fn_step, steps: int, reps: int = 5, warm: int = 3) -> t
         e1.synchronize()
         times.append(e0.elapsed_time(e1) * 1000.0 / steps)
     return statistics.median(times), times
+
+
+PROFILE_CASES = {
+    # name: (format, recipe, M, compensated)
+    "prefill_w4a4": (0, "prefill_k8192", 4096, False),
+    "prefill_comp": (0, "prefill_k8192", 4096, True),
+    "mlp_gate_up": (0, "mlp_gate_up", 8, True),
+    "mlp_down": (0, "mlp_down", 8, True),
+    "mx_m1": (1, "mx_k5120_n27648", 1, True),
+}
+
+
+def run_profile_case(args) -> dict:
+    """One workload's linear calls, graph-replayed (for profiler runs: ncu
+    captures the launches; the printed time is not a bench value)."""
+    import torch
+    from block_scaled_quantized_gb300 import build, rs, workloads
+    build.build()
+    fmt, recipe, M, comp = PROFILE_CASES[args.profile_case]
+    lin = Linear(torch, rs, workloads, fmt, recipe, M, comp, copies_for_l2=M <= 128)
+    us, _ = graph_time_us(torch, lin.call, args.steps, reps=1, warm=args.warmup)
+    assert rs.rs_get_device_error() == 0
+    return {"profile_case": args.profile_case, "us_per_call": round(us, 3), "launches_per_call": lin.launches_per_call()}
 
 
 def run_gpu(args) -> dict:
@@ -479,10 +502,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true",
                     help="time the headline step only (for profiler runs; no sweeps, no baselines)")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
+                    help="run one other workload's calls only (for profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    out = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.profile_case:
+        out = run_profile_case(args)
+    else:
+        out = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if out is not None:
         print(json.dumps(out), flush=True)
 
