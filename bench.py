@@ -379,6 +379,12 @@ def run_gpu(args) -> dict:
             pre[f"{key}_useful_tflops"] = round(useful / (us * 1e-6) / 1e12, 1)
             pre[f"{key}_executed_tflops"] = round(executed / (us * 1e-6) / 1e12, 1)
             del lin
+        # FP4 dense peak: the measured bf16 peak x the nominal FP4/bf16 ratio (13.5 / 2.25)
+        fp4_peak = peaks["bf16_tflops"] * 13.5 / 2.25
+        pre["fp4_peak_tflops"] = round(fp4_peak, 1)
+        pre["fp4_peak_source"] = f"{peaks['source']} bf16 x 6"
+        pre["w4a4_frac"] = round(pre["w4a4_executed_tflops"] / fp4_peak, 4)
+        pre["comp_frac"] = round(pre["comp_executed_tflops"] / fp4_peak, 4)
         extra["prefill_M4096_K8192_N8192"] = pre
         torch.cuda.empty_cache()
 
