@@ -71,7 +71,8 @@ constexpr int kQuantWarps = 10;     // warps 0-3 and 6-11 quantize in fused plan
 constexpr int kQuantThreads = kQuantWarps * 32;
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;   // 227 KB opt-in per block
-constexpr uint32_t kCtrlBytes = 512;
+constexpr uint32_t kCtrlBytes = 1024;
+constexpr int kMaxChunkBars = 32;   // fused plans: one "quantized" mbarrier per resident chunk
 
 __host__ __device__ constexpr int b_atom_tiles(int bn) { return (bn + 127) / 128; }
 // Shared-memory bytes of one activation stage: codes (bn rows x 128 bytes)
@@ -134,12 +135,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t recv_base = smem_u32(recv_region);
     uint64_t* full = reinterpret_cast<uint64_t*>(recv_region + (size_t)g.nacc * g.recv_bytes);
     uint64_t* empty = full + kMaxStages;
-    uint64_t* qdone = empty + kMaxStages;      // fused: activation slice quantized into shared memory
-    uint64_t* accum_full = qdone + 1;              // per accumulator: tile's MMAs done
+    uint64_t* accum_full = empty + kMaxStages;     // per accumulator: tile's MMAs done
     uint64_t* accum_empty = accum_full + 2;        // per accumulator: drained by the epilogue
     uint64_t* red_full = accum_empty + 2;          // split-K: all partials of a tile received
     uint64_t* recv_free = red_full + 2;            // split-K: every owner's receive buffer free again
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_free + 2);
+    uint64_t* cbar = recv_free + 2;                // fused: chunk i of the slice quantized
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + kMaxChunkBars);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     volatile uint32_t* consumed = tmem_slot + 2;
     volatile uint32_t* issued = tmem_slot + 3;
@@ -193,7 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
-        mbar_init(smem_u32(qdone), 1);
+        // every scale block of chunk i (all token rows) arrives once
+        if (FUSED)
+            for (int i = 0; i < nck; ++i) mbar_init(smem_u32(&cbar[i]), (uint32_t)(g.M * (256 / block_elems(FMT))));
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accum_full[b]), 1);
             mbar_init(smem_u32(&accum_empty[b]), (uint32_t)(epi8 ? 8 : 4));  // one arrival per epilogue warp
@@ -329,9 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool landed = mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err);
                 if (lane == 0 && (u == 8 || u == 16 || u == 24 || u == 31))
                     RS_TRACE_MARK(g.trace, u == 8 ? 13 : u == 16 ? 14 : u == 24 ? 28 : 30);
-                // fused plans: the activation slice is quantized (waited for
-                // here, after the loop set-up, which overlaps the quantizer)
-                if (FUSED && u == 0) landed = landed && mbar_wait_bounded(smem_u32(qdone), 0, abort_flag, g.err);
+                // fused plans: chunk i of the activation slice is quantized
+                // (the quantizer finishes chunks in order, so the first MMAs
+                // overlap the quantization of the later chunks)
+                if (FUSED && j == 0) landed = landed && mbar_wait_bounded(smem_u32(&cbar[i]), 0, abort_flag, g.err);
                 if (u == 0 && lane == 0) RS_TRACE_MARK(g.trace, 11);
                 ok = __all_sync(0xFFFFFFFFu, landed);
                 if (!ok) break;
@@ -412,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bbytes = (uint32_t)nck * BSTAGE;
             for (uint32_t off = (uint32_t)qtid * 16u; off < bbytes; off += (uint32_t)kQuantThreads * 16u)
                 *reinterpret_cast<uint4*>(bregion + off) = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();  // the zeros are in every chunk, whoever signals it
             named_bar_sync(2, kQuantThreads);
             pdl_wait_prior_grid();
             if (qtid == 0) RS_TRACE_MARK(g.trace, 16);
@@ -443,12 +448,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint32_t*>(slot + B_BYTES + a * 512 + (rowb % 32) * 16 + (rowb / 32) * 4) = w;
                 }
             };
-            // flat mapping: thread qtid takes scale blocks qtid, qtid + T, ...
-            // (T = quantizer threads); four consecutive lanes hold the four
-            // blocks of one scale-atom word.  All loads of a batch go out
-            // before any arithmetic.
-            const int bpr = nck * 256 / E;  // blocks per token row in this slice
-            const int total = g.M * bpr;
+            // flat chunk-major mapping: thread qtid takes scale blocks qtid,
+            // qtid + T, ... (T = quantizer threads) of the order (chunk, token
+            // row, block), so chunks complete in order; four consecutive lanes
+            // hold the four blocks of one scale-atom word.  All loads of a batch
+            // go out before any arithmetic.
+            constexpr int bpc = 256 / E;    // blocks per token row in one chunk
+            const int cb = g.M * bpc;       // blocks per chunk
+            const int total = nck * cb;
+            auto block_pos = [&](int f, int& j, int& kk) {
+                const int ci = f / cb, rem = f - ci * cb;
+                j = rem / bpc;
+                kk = ci * 256 + (rem - j * bpc) * E;
+            };
             constexpr int kBatch = 32 / E;  // blocks per thread per batch
             // the loop bound is per warp (fw): put() shuffles across all 32 lanes
             for (int fw = qw * 32; fw < total; fw += kBatch * kQuantThreads) {
@@ -457,7 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int r = 0; r < kBatch; ++r) {
                     const int f = f0 + r * kQuantThreads;
-                    const int j = f / bpr, kk = (f % bpr) * E;
+                    int j, kk;
+                    block_pos(f, j, kk);
                     const bool live = f < total && kbeg + kk < kend;
 #pragma unroll
                     for (int q = 0; q < E / 8; ++q) {
@@ -471,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = 0; r < kBatch; ++r) {
                     if (fw + r * kQuantThreads >= total) break;  // whole warp past the end
                     const int f = f0 + r * kQuantThreads;
-                    const int j = f / bpr, kk = (f % bpr) * E;
+                    int j, kk;
+                    block_pos(f, j, kk);
                     const bool live = f < total && kbeg + kk < kend;
                     uint32_t sfq, codes[E / 8];
                     float xh[E];
@@ -487,16 +501,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         quant_block<FMT, E, false>(rr, ksc, sfr, rcodes, rh);
                         put(rb + 1u, kk, rcodes, sfr, live);
                     }
+                    // the block (its scale word is stored by a neighbouring
+                    // lane) is in shared memory: count it for its chunk
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (f < total) mbar_arrive(smem_u32(&cbar[f / cb]));
                 }
             }
             if (qtid == 0) RS_TRACE_MARK(g.trace, 17);
             if (qtid == kQuantThreads - 1) RS_TRACE_MARK(g.trace, 18);
-            fence_proxy_async_smem();
-            named_bar_sync(2, kQuantThreads);
-            if (qtid == 0) {
-                mbar_arrive(smem_u32(qdone));  // the MMA warp may read the activation slice
-                RS_TRACE_MARK(g.trace, 8);
-            }
         } else if (epi) {
             pdl_wait_prior_grid();  // before writing the output
         }
@@ -706,7 +719,7 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
     const int outs = fold ? p.bn / 2 : p.bn;
     const size_t splitbuf = split_buf_bytes(s, outs);
     const int sfc = sf_cols_per_stage(fmt, p.bn);
-    bool fused = allow_fused && p.b_tiles == 1 && p.bn <= 32;
+    bool fused = allow_fused && p.b_tiles == 1 && p.bn <= 32 && max_chunks <= kMaxChunkBars;
     // two accumulators let the epilogue of one tile overlap the next tile's
     // MMAs when a CTA has several tiles
     int nacc = ntl > 1 ? 2 : 1;
