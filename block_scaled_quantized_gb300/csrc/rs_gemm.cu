@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 if (g.splits > 1 && j > 0) {
                     // the previous tile's outgoing copies have read our partial
-                    if (ctid == 0) bulk_wait_group_read0();
+                    if (warp == 8) bulk_wait_group_read0();  // (the issuing lane's copies; no-op on the rest)
                     named_bar_sync(1, 128);
                 }
                 if (ok && g.splits == 1) {
@@ -614,32 +614,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // owner into its receive buffer b at our rank's slot
                     fence_proxy_async_smem();
                     named_bar_sync(1, 128);
-                    if (ctid == 0) {
+                    if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 13);
+                    if (warp == 8) {
                         // every owner has consumed what was sent into buffer b
-                        // for tile j - nacc
-                        const bool free_ok = j < nacc || mbar_wait_bounded(smem_u32(&recv_free[b]),
-                                                                           (uint32_t)(j / nacc - 1) & 1u, abort_flag,
-                                                                           g.err, 1000000000ull, true);
-                        if (free_ok && *abort_flag == 0) {
-                            const uint32_t rbuf = recv_base + (uint32_t)(b * g.recv_bytes);
-                            for (int o = 0; o < g.splits; ++o) {
-                                const uint32_t dst = map_dsmem(rbuf + my_rank * slice_bytes, (uint32_t)o);
-                                const uint32_t bar = map_dsmem(smem_u32(&red_full[b]), (uint32_t)o);
-                                bulk_copy_to_cluster(dst, smem_u32(part) + (uint32_t)o * slice_bytes, slice_bytes,
-                                                     bar);
-                            }
+                        // for tile j - nacc (the whole warp waits; one elected
+                        // lane issues the copies)
+                        bool free_ok = j < nacc || mbar_wait_bounded(smem_u32(&recv_free[b]),
+                                                                     (uint32_t)(j / nacc - 1) & 1u, abort_flag, g.err,
+                                                                     1000000000ull, true);
+                        free_ok = __all_sync(0xFFFFFFFFu, free_ok && *abort_flag == 0);
+                        if (free_ok && elect_one_sync()) {
+                            const uint32_t rbuf = recv_base + (uint32_t)(b * g.recv_bytes) + my_rank * slice_bytes;
+                            const uint32_t rbar = smem_u32(&red_full[b]);
+                            const uint32_t src = smem_u32(part);
+                            for (int o = 0; o < g.splits; ++o)
+                                bulk_copy_to_cluster(map_dsmem(rbuf, (uint32_t)o), src + (uint32_t)o * slice_bytes,
+                                                     slice_bytes, map_dsmem(rbar, (uint32_t)o));
                             bulk_commit_group();
+                            if (j == 0) RS_TRACE_MARK(g.trace, 14);
                         }
+                        __syncwarp();
                     }
                     // own slice: sum the partners' partials in rank order
                     const bool got = mbar_wait_bounded(smem_u32(&red_full[b]), use_ph, abort_flag, g.err);
+                    if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 28);
                     const float* recv = reinterpret_cast<const float*>(recv_region + (size_t)b * g.recv_bytes);
-                    for (int jj = 0; got && jj < per_cta; ++jj) {
+                    const bool live = got && *abort_flag == 0;
+                    for (int jj = 0; live && jj < per_cta; ++jj) {
                         const int jo = split * per_cta + jj;
                         if (jo >= outs) break;
+                        // all partials first, then the sum in rank order
+                        float pv[kMaxSplits];
+#pragma unroll
+                        for (int r = 0; r < kMaxSplits; ++r)
+                            pv[r] = r < g.splits ? recv[(r * per_cta + jj) * 128 + row] : 0.0f;
                         float acc = 0.0f;
-                        for (int r = 0; r < g.splits; ++r) acc = __fadd_rn(acc, recv[(r * per_cta + jj) * 128 + row]);
-                        if (*abort_flag == 0) store_y(m0 + jo, acc);
+#pragma unroll
+                        for (int r = 0; r < kMaxSplits; ++r)
+                            if (r < g.splits) acc = __fadd_rn(acc, pv[r]);
+                        store_y(m0 + jo, acc);
                     }
                     if (j < 3 && ctid == 0) RS_TRACE_MARK(g.trace, 25 + j);
                     if (j + nacc < ntl) {
@@ -654,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (g.splits > 1 && ctid == 0) bulk_wait_group_read0();  // our outgoing copies have read their source
+            if (g.splits > 1 && warp == 8) bulk_wait_group_read0();  // our outgoing copies have read their source
         }
     }
 
