@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    bool tmem_freed = false;  // warp 5: deallocated after the last accumulator was read
     if (threadIdx.x == 0) {
         RS_TRACE_MARK(g.trace, 1);
         uint32_t smid;
@@ -402,6 +403,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
             if (j < 3 && lane == 0) RS_TRACE_MARK(g.trace, 19 + j);
+        }
+        // Free the tensor memory as soon as the epilogue has read the last
+        // accumulator (it reads the tiles in order), while it still exchanges
+        // and stores the outputs.
+        if (ok) {
+            const int jl = ntl - 1;
+            const bool drained = mbar_wait_bounded(smem_u32(&accum_empty[jl & (nacc - 1)]),
+                                                   (uint32_t)(jl / nacc) & 1u, abort_flag, g.err);
+            if (__all_sync(0xFFFFFFFFu, drained)) {
+                tc_fence_after();
+                tmem_dealloc(tmem, (uint32_t)g.tmem_cols);
+                tmem_freed = true;
+                if (lane == 0) RS_TRACE_MARK(g.trace, 10);
+            }
         }
     } else {
         // ------------------------------------------------ warps 0-3, 6-11
@@ -677,16 +692,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag && warp == 4 && lane == 0) {
-        // Let every copy still in flight land before the CTA exits.
-        for (uint32_t u = *consumed; u < *issued; ++u) {
-            const uint32_t s = u % (uint32_t)S;
-            volatile uint32_t no_abort = 0;
-            (void)mbar_wait_bounded(smem_u32(&full[s]), (u / (uint32_t)S) & 1u, &no_abort, nullptr, 100000000ull);
+    if (*abort_flag) {  // CTA-uniform here: every role has finished
+        if (warp == 4 && lane == 0) {
+            // Let every copy still in flight land before the CTA exits.
+            for (uint32_t u = *consumed; u < *issued; ++u) {
+                const uint32_t s = u % (uint32_t)S;
+                volatile uint32_t no_abort = 0;
+                (void)mbar_wait_bounded(smem_u32(&full[s]), (u / (uint32_t)S) & 1u, &no_abort, nullptr,
+                                        100000000ull);
+            }
         }
+        __syncthreads();
     }
-    __syncthreads();
-    if (warp == 5) {
+    if (warp == 5 && !tmem_freed) {
         tc_fence_after();
         tmem_dealloc(tmem, (uint32_t)g.tmem_cols);
         if (lane == 0) RS_TRACE_MARK(g.trace, 10);
