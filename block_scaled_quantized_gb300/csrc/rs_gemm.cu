@@ -638,15 +638,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                      (uint32_t)(j / nacc - 1) & 1u, abort_flag, g.err,
                                                                      1000000000ull, true);
                         free_ok = __all_sync(0xFFFFFFFFu, free_ok && *abort_flag == 0);
-                        if (free_ok && elect_one_sync()) {
+                        if (free_ok && lane < g.splits) {
+                            // lane o sends owner o its slice
                             const uint32_t rbuf = recv_base + (uint32_t)(b * g.recv_bytes) + my_rank * slice_bytes;
-                            const uint32_t rbar = smem_u32(&red_full[b]);
-                            const uint32_t src = smem_u32(part);
-                            for (int o = 0; o < g.splits; ++o)
-                                bulk_copy_to_cluster(map_dsmem(rbuf, (uint32_t)o), src + (uint32_t)o * slice_bytes,
-                                                     slice_bytes, map_dsmem(rbar, (uint32_t)o));
+                            bulk_copy_to_cluster(map_dsmem(rbuf, (uint32_t)lane),
+                                                 smem_u32(part) + (uint32_t)lane * slice_bytes, slice_bytes,
+                                                 map_dsmem(smem_u32(&red_full[b]), (uint32_t)lane));
                             bulk_commit_group();
-                            if (j == 0) RS_TRACE_MARK(g.trace, 14);
+                            if (j == 0 && lane == 0) RS_TRACE_MARK(g.trace, 14);
                         }
                         __syncwarp();
                     }
