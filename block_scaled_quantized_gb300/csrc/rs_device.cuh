@@ -125,6 +125,28 @@ __device__ __forceinline__ uint32_t e4m3_encode_satfinite(float t) {
     return ((uint32_t)(e + 7) << 3) + ni - 8u;             // 16 carries into the exponent
 }
 
+// Two fp32 products / differences in one packed instruction (mul/sub.rn.f32x2,
+// each half rounded to nearest even like __fmul_rn / __fsub_rn).
+__device__ __forceinline__ void fmul2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rc, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rc;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void fsub2_rn(float a0, float a1, float b0, float b1, float& r0, float& r1) {
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rc, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rc;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Hardware E4M3 conversions: cvt.rn.satfinite.e4m3x2.f32 (round to nearest
 // even, finite inputs above 448 saturate to 448) and cvt.rn.f16x2.e4m3x2
 // (exact).  On every non-negative finite float and every finite byte they

@@ -442,32 +442,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // codes of one block (element offset kk of the slice) and, gathered
             // over four consecutive lanes, one scale-atom word
             auto put = [&](uint32_t rowb, int kk, const uint32_t (&codes)[E / 8], uint32_t sfbyte, bool live) {
+                if (!live) return;
                 const int ci = kk / 256;
-                const uint32_t b = (uint32_t)(kk % 256) / 2u;  // byte within the 128-byte row
+                const uint32_t kb = (uint32_t)(kk % 256) / (uint32_t)E;  // block within the chunk
                 uint8_t* slot = bregion + (size_t)ci * BSTAGE;
-                if (live) {
-                    if constexpr (E == 16) {
-                        *reinterpret_cast<uint2*>(slot + sw128_offset(rowb, b)) = make_uint2(codes[0], codes[1]);
-                    } else {
-                        *reinterpret_cast<uint4*>(slot + sw128_offset(rowb, b)) =
-                            make_uint4(codes[0], codes[E / 8 - 3], codes[E / 8 - 2], codes[E / 8 - 1]);
-                    }
+                const uint32_t b = kb * (uint32_t)(E / 2);                // byte within the 128-byte row
+                if constexpr (E == 16) {
+                    *reinterpret_cast<uint2*>(slot + sw128_offset(rowb, b)) = make_uint2(codes[0], codes[1]);
+                } else {
+                    *reinterpret_cast<uint4*>(slot + sw128_offset(rowb, b)) =
+                        make_uint4(codes[0], codes[E / 8 - 3], codes[E / 8 - 2], codes[E / 8 - 1]);
                 }
-                const int base = lane & ~3;
-                const uint32_t w = __shfl_sync(0xFFFFFFFFu, sfbyte, base) |
-                                   (__shfl_sync(0xFFFFFFFFu, sfbyte, base + 1) << 8) |
-                                   (__shfl_sync(0xFFFFFFFFu, sfbyte, base + 2) << 16) |
-                                   (__shfl_sync(0xFFFFFFFFu, sfbyte, base + 3) << 24);
-                if (live && (lane & 3) == 0) {
-                    const int a = (kk % 256) / atom_k(FMT);
-                    *reinterpret_cast<uint32_t*>(slot + B_BYTES + a * 512 + (rowb % 32) * 16 + (rowb / 32) * 4) = w;
-                }
+                // scale byte: atom kb / 4, byte (row % 32) * 16 + (row / 32 % 4) * 4 + kb % 4
+                slot[B_BYTES + (kb / 4) * 512 + (rowb % 32) * 16 + (rowb / 32) * 4 + kb % 4] = (uint8_t)sfbyte;
             };
             // flat chunk-major mapping: thread qtid takes scale blocks qtid,
             // qtid + T, ... (T = quantizer threads) of the order (chunk, token
-            // row, block), so chunks complete in order; four consecutive lanes
-            // hold the four blocks of one scale-atom word.  All loads of a batch
-            // go out before any arithmetic.
+            // row, block), so chunks complete in order.  All loads of a batch go
+            // out before any arithmetic.
             constexpr int bpc = 256 / E;    // blocks per token row in one chunk
             const int cb = g.M * bpc;       // blocks per chunk
             const int total = nck * cb;
@@ -510,16 +502,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (g.fold) {
                         float rr[E];
 #pragma unroll
-                        for (int e = 0; e < E; ++e) rr[e] = __fsub_rn(xs[r][e], xh[e]);  // residue (Alg. 1 line 6)
+                        for (int e = 0; e < E; e += 2)  // residue (Alg. 1 line 6)
+                            fsub2_rn(xs[r][e], xs[r][e + 1], xh[e], xh[e + 1], rr[e], rr[e + 1]);
                         uint32_t sfr, rcodes[E / 8];
                         float rh[E];
                         quant_block<FMT, E, false>(rr, ksc, sfr, rcodes, rh);
                         put(rb + 1u, kk, rcodes, sfr, live);
                     }
-                    // the block (its scale word is stored by a neighbouring
-                    // lane) is in shared memory: count it for its chunk
+                    // the block is in shared memory: count it for its chunk
                     fence_proxy_async_smem();
-                    __syncwarp();
                     if (f < total) mbar_arrive(smem_u32(&cbar[f / cb]));
                 }
             }

@@ -161,13 +161,13 @@ __device__ __forceinline__ void quant_block(const float (&xf)[E], const NvScaleC
     for (int w = 0; w < E / 8; ++w) {
         float v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(xf[8 * w + e], mul);
+        for (int e = 0; e < 8; e += 2) fmul2_rn(xf[8 * w + e], xf[8 * w + e + 1], mul, mul, v[e], v[e + 1]);
         codes[w] = e2m1_encode8(v);
         if constexpr (kRecon) {  // the reconstruction is only needed to form a residue
             float d[8];
             e2m1_decode8(codes[w], d);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xh[8 * w + e] = __fmul_rn(st, d[e]);
+            for (int e = 0; e < 8; e += 2) fmul2_rn(st, st, d[e], d[e + 1], xh[8 * w + e], xh[8 * w + e + 1]);
         }
     }
 }
