@@ -113,7 +113,7 @@ struct GemmArgs {
 };
 
 template <int FMT, int BN, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs g) {
     constexpr int APC = weight_atoms_per_block(FMT);
     constexpr int BT = b_atom_tiles(BN);
@@ -529,6 +529,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float gsc = FMT == 0 ? __fmul_rn(*g.alpha_x, *g.alpha_w) : 1.0f;
             float* part = reinterpret_cast<float*>(part_region);  // split-K: [j][channel]
             const uint32_t my_rank = (uint32_t)split;
+            // split-K: lane o of warp 8 sends to owner o; its destinations in
+            // the cluster (receive buffer b at our rank's slot, owner's red_full[b])
+            uint32_t dst_buf0 = 0, dst_buf1 = 0, dst_bar0 = 0, dst_bar1 = 0;
+            if (g.splits > 1 && warp == 8 && lane < g.splits) {
+                const uint32_t rb = recv_base + my_rank * slice_bytes;
+                dst_buf0 = map_dsmem(rb, (uint32_t)lane);
+                dst_bar0 = map_dsmem(smem_u32(&red_full[0]), (uint32_t)lane);
+                dst_buf1 = map_dsmem(rb + (uint32_t)g.recv_bytes, (uint32_t)lane);
+                dst_bar1 = map_dsmem(smem_u32(&red_full[1]), (uint32_t)lane);
+            }
             for (int j = 0; j < ntl; ++j) {
                 const int b = j % nacc;
                 const uint32_t use_ph = (uint32_t)(j / nacc) & 1u;
@@ -631,10 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         free_ok = __all_sync(0xFFFFFFFFu, free_ok && *abort_flag == 0);
                         if (free_ok && lane < g.splits) {
                             // lane o sends owner o its slice
-                            const uint32_t rbuf = recv_base + (uint32_t)(b * g.recv_bytes) + my_rank * slice_bytes;
-                            bulk_copy_to_cluster(map_dsmem(rbuf, (uint32_t)lane),
+                            bulk_copy_to_cluster(b == 0 ? dst_buf0 : dst_buf1,
                                                  smem_u32(part) + (uint32_t)lane * slice_bytes, slice_bytes,
-                                                 map_dsmem(smem_u32(&red_full[b]), (uint32_t)lane));
+                                                 b == 0 ? dst_bar0 : dst_bar1);
                             bulk_commit_group();
                             if (j == 0 && lane == 0) RS_TRACE_MARK(g.trace, 14);
                         }
