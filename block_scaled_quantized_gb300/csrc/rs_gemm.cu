@@ -113,7 +113,7 @@ struct GemmArgs {
 };
 
 template <int FMT, int BN, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs g) {
     constexpr int APC = weight_atoms_per_block(FMT);
     constexpr int BT = b_atom_tiles(BN);
@@ -566,7 +566,53 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (warp == 8) bulk_wait_group_read0();  // (the issuing lane's copies; no-op on the rest)
                     named_bar_sync(1, 128);
                 }
-                if (ok && g.splits == 1) {
+                bool drained = false;
+                if constexpr (!FUSED && BN >= 128) {
+                    if (ok && g.splits == 1 && !g.out_f32) {
+                        // Wide tile, bf16 output: this warp's BN/2 columns go to
+                        // registers as scaled bf16 first, the accumulator is
+                        // released, and the stores overlap the next tile's MMAs.
+                        constexpr int NC = BN / 2;
+                        const int cbeg = warp < 4 ? NC : 0;
+                        const int jmax = n < g.N ? min(outs, g.M - m0) : 0;
+                        const size_t ybase = (size_t)m0 * g.N + (size_t)n;
+                        uint32_t pk[NC / 2];  // bf16 pairs, output o in half o & 1 of pk[o / 2]
+#pragma unroll
+                        for (int q = 0; q < NC / 2; ++q) pk[q] = 0u;
+                        auto keep = [&](int o, float z) {
+                            const uint32_t hb =
+                                (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(gsc, z)));
+                            pk[o >> 1] |= (o & 1) ? (hb << 16) : hb;
+                        };
+#pragma unroll
+                        for (int c = 0; c < NC; c += 32) {
+                            float v[32];
+                            tmem_ld32(tmem + (uint32_t)(b * BN) + quarter + (uint32_t)(cbeg + c), v);
+                            if (g.fold) {
+#pragma unroll
+                                for (int q = 0; q < 16; ++q) keep(c / 2 + q, __fadd_rn(v[2 * q], v[2 * q + 1]));  // Fold
+                            } else {
+#pragma unroll
+                                for (int q = 0; q < 32; ++q) keep(c + q, v[q]);
+                            }
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&accum_empty[b]));
+                        drained = true;
+                        const int obeg = g.fold ? cbeg / 2 : cbeg;
+                        const int nout = g.fold ? NC / 2 : NC;
+                        __nv_bfloat16* yb = reinterpret_cast<__nv_bfloat16*>(g.y) + ybase;
+#pragma unroll
+                        for (int o = 0; o < NC; ++o)
+                            if (o < nout && obeg + o < jmax)
+                                yb[(size_t)(obeg + o) * g.N] =
+                                    __ushort_as_bfloat16((unsigned short)((o & 1) ? (pk[o >> 1] >> 16) : pk[o >> 1]));
+                    }
+                }
+                if (drained) {
+                    // accumulator already released
+                } else if (ok && g.splits == 1) {
                     // this warp's columns; output j of the tile at y + (m0 + j) * N + n
                     const int ncol = epi8 ? BN / 2 : BN;
                     const int cbeg = (epi8 && warp < 4) ? ncol : 0;
@@ -621,9 +667,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int jj = 0; jj < outs; ++jj) emit(jj, 0.0f);
                 }
                 // accumulator b drained: the MMA warp may start its next tile
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&accum_empty[b]));
+                if (!drained) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&accum_empty[b]));
+                }
                 if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 7);
                 if (g.splits > 1) {
                     // send each owner its slice of outputs: one bulk copy per
