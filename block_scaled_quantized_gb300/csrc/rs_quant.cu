@@ -91,9 +91,18 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
     if (FMT == 0 && blockIdx.x == 0 && threadIdx.x == 0 && !nv_alpha_supported(ksc.alpha))
         atomicExch(a.err, kErrInvalidArg);
 
+    // task = row * chunks + chunk, advanced by n_warps_total without a division
+    const int dstep_row = (int)(n_warps_total / a.chunks), dstep_chunk = (int)(n_warps_total % a.chunks);
+    int row = (int)(warp / a.chunks), chunk = (int)(warp % a.chunks);
     for (int64_t task = warp; task < tasks; task += n_warps_total) {
-        const int row = (int)(task / a.chunks);
-        const int chunk = (int)(task % a.chunks);
+        if (task != warp) {
+            row += dstep_row;
+            chunk += dstep_chunk;
+            if (chunk >= a.chunks) {
+                chunk -= a.chunks;
+                ++row;
+            }
+        }
         const int k0 = chunk * 256 + lane * 8;
         const bool valid = k0 < a.K && row < a.rows;
         float xf[8];
@@ -101,7 +110,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
 
         uint32_t sfb;
         float xh[8];
-        const uint32_t codes = quant_lane<FMT>(xf, ksc, sfb, xh);
+        const uint32_t codes = quant_lane<FMT, MODE == kPaired>(xf, ksc, sfb, xh);
         const uint32_t sfw = gather_sf_word<FMT>(sfb, lane);
         const int g = chunk * (256 / atom_k(FMT)) + lane / LPA;  // atom index along K
         const bool leader = (lane % LPA) == 0;
@@ -124,7 +133,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
                 residue8(xf, xh, r);
                 uint32_t sfr;
                 float rh[8];
-                const uint32_t rcodes = quant_lane<FMT>(r, ksc, sfr, rh);
+                const uint32_t rcodes = quant_lane<FMT, false>(r, ksc, sfr, rh);
                 const uint32_t sfrw = gather_sf_word<FMT>(sfr, lane);
                 if (valid)
                     *reinterpret_cast<uint32_t*>(a.out + (size_t)(out_row + 1) * (a.K / 2) + k0 / 2) = rcodes;

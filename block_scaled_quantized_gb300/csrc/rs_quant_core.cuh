@@ -95,7 +95,7 @@ __device__ __forceinline__ float block_amax(float a) {
 // Quantize this lane's eight values; returns the packed codes (element e in
 // bits 4e..4e+3, i.e. element 2j in the low nibble of byte j), the block's
 // scale byte in `sf`, and the reconstruction fl(s~ * dec(q)) in `xh`.
-template <int FMT>
+template <int FMT, bool kRecon = true>
 __device__ __forceinline__ uint32_t quant_lane(const float (&xf)[8], const NvScaleConst& k, uint32_t& sf,
                                                float (&xh)[8]) {
     float am = 0.0f;
@@ -106,19 +106,21 @@ __device__ __forceinline__ uint32_t quant_lane(const float (&xf)[8], const NvSca
     sf = FMT == 0 ? nv_block_scale_fast(am, k, st, mul) : mx_block_scale(am, st, mul);
     float v[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(xf[e], mul);
+    for (int e = 0; e < 8; e += 2) fmul2_rn(xf[e], xf[e + 1], mul, mul, v[e], v[e + 1]);
     const uint32_t codes = e2m1_encode8(v);
-    float d[8];
-    e2m1_decode8(codes, d);
+    if constexpr (kRecon) {  // the reconstruction is only needed to form a residue
+        float d[8];
+        e2m1_decode8(codes, d);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) xh[e] = __fmul_rn(st, d[e]);
+        for (int e = 0; e < 8; e += 2) fmul2_rn(st, st, d[e], d[e + 1], xh[e], xh[e + 1]);
+    }
     return codes;
 }
 
 // Residue of this lane's eight values, r = fl(x - x^) (Alg. 1 line 6).
 __device__ __forceinline__ void residue8(const float (&xf)[8], const float (&xh)[8], float (&r)[8]) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) r[e] = __fsub_rn(xf[e], xh[e]);
+    for (int e = 0; e < 8; e += 2) fsub2_rn(xf[e], xf[e + 1], xh[e], xh[e + 1], r[e], r[e + 1]);
 }
 
 // Gather the four scale bytes of one atom row (4 consecutive blocks) into the
