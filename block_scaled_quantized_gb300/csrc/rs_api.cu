@@ -90,11 +90,15 @@ rs_status linear_impl(int fmt, bool compensated, int M, int N, int K, const void
     if (M == 0 || N == 0) return RS_OK;
     if ((x == nullptr) == (xq == nullptr)) return RS_ERR_INVALID_ARG;
     if (!wq || !y) return RS_ERR_INVALID_ARG;
-    if (fmt == RS_NVFP4 && (!alpha_x || !alpha_w)) return RS_ERR_INVALID_ARG;
+    // NVFP4: alpha_w is required; alpha_x may be NULL with a bf16 input (the
+    // call then computes the activation tensor scale itself)
+    const bool dyn_alpha = fmt == RS_NVFP4 && alpha_x == nullptr;
+    if (fmt == RS_NVFP4 && !alpha_w) return RS_ERR_INVALID_ARG;
+    if (dyn_alpha && x == nullptr) return RS_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || (xq && !aligned16(xq)) || !aligned16(wq) || !aligned16(y) ||
         (ws && !aligned16(ws)))
         return RS_ERR_ALIGNMENT;
-    if (fmt == RS_NVFP4 && (!aligned4(alpha_x) || !aligned4(alpha_w))) return RS_ERR_ALIGNMENT;
+    if (fmt == RS_NVFP4 && ((alpha_x && !aligned4(alpha_x)) || !aligned4(alpha_w))) return RS_ERR_ALIGNMENT;
     const bool quantize_input = x != nullptr;
     if (quantize_input && (!ws || ws_bytes < workspace_bytes(fmt, compensated, M, K))) return RS_ERR_WORKSPACE;
 
@@ -112,10 +116,20 @@ rs_status linear_impl(int fmt, bool compensated, int M, int N, int K, const void
     c.out_f32 = out_dtype == RS_OUT_F32 ? 1 : 0;
     c.err = dev->err;
     if (quantize_input && plan.fused) {
-        c.x = x;  // the GEMM quantizes its own K slices: one launch
+        c.x = x;  // the GEMM quantizes its own K slices (and finds the tensor scale): one launch
+        c.dyn_alpha = dyn_alpha ? 1 : 0;
     } else if (quantize_input) {
         void* act = ws;
-        cudaError_t e = launch_quantize(fmt, compensated, M, K, x, K, alpha_x, act, stream, dev->num_sms,
+        const float* ax = alpha_x;
+        if (dyn_alpha) {
+            // the tensor scale goes to the workspace slot after the operand
+            float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + alpha_slot_offset(fmt, compensated, M, K));
+            if (launch_tensor_scale(x, (int64_t)M * K, a, dev->err, stream, dev->num_sms) != cudaSuccess)
+                return RS_ERR_CUDA;
+            ax = a;
+            c.alpha_x = a;
+        }
+        cudaError_t e = launch_quantize(fmt, compensated, M, K, x, K, ax, act, stream, dev->num_sms,
                                         /*pdl=*/true);
         if (e != cudaSuccess) return RS_ERR_CUDA;
         c.xq = act;

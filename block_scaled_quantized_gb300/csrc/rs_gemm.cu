@@ -110,6 +110,7 @@ struct GemmArgs {
     int part_bytes;         // split-K: this CTA's partial
     int recv_bytes;         // split-K: one receive buffer (0 without split)
     int tmem_cols;
+    int dyn_alpha;          // fused NVFP4: the tensor scale of X is computed here (alpha_x unused)
 };
 
 template <int FMT, int BN, bool FUSED>
@@ -140,7 +141,10 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     uint64_t* red_full = accum_empty + 2;          // split-K: all partials of a tile received
     uint64_t* recv_free = red_full + 2;            // split-K: every owner's receive buffer free again
     uint64_t* cbar = recv_free + 2;                // fused: chunk i of the slice quantized
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cbar + kMaxChunkBars);
+    uint64_t* abar = cbar + kMaxChunkBars;         // dynamic tensor scale: every split's slice amax in
+    uint32_t* amax_slot = reinterpret_cast<uint32_t*>(abar + 1);  // [kMaxSplits] slice amax (bf16 |x| bits)
+    uint32_t* amax_cta = amax_slot + kMaxSplits;   // this CTA's slice amax
+    uint32_t* tmem_slot = amax_cta + 1;
     volatile uint32_t* abort_flag = tmem_slot + 1;
     volatile uint32_t* consumed = tmem_slot + 2;
     volatile uint32_t* issued = tmem_slot + 3;
@@ -197,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
         // every scale block of chunk i (all token rows) arrives once
         if (FUSED)
             for (int i = 0; i < nck; ++i) mbar_init(smem_u32(&cbar[i]), (uint32_t)(g.M * (256 / block_elems(FMT))));
+        mbar_init(smem_u32(abar), (uint32_t)g.splits);  // one slice amax per CTA of the cluster
+        *amax_cta = 0u;
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accum_full[b]), 1);
             mbar_init(smem_u32(&accum_empty[b]), (uint32_t)(epi8 ? 8 : 4));  // one arrival per epilogue warp
@@ -423,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
         const bool epi = warp >= 8 || (epi8 && warp < 4);  // epilogue: lane quarter = warp % 4
         const int qw = warp < 4 ? warp : warp - 2;  // quantizer warp 0..kQuantWarps-1
         const int qtid = qw * 32 + lane;
+        float ax_val = 0.0f;  // NVFP4 activation tensor scale of this call
         if (FUSED) {
             // Quantizing prologue (Alg. 1), one scale block per thread: this
             // CTA's K slice of every token -> base (row 2j) and residue
@@ -435,10 +442,53 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             named_bar_sync(2, kQuantThreads);
             pdl_wait_prior_grid();
             if (qtid == 0) RS_TRACE_MARK(g.trace, 16);
-            const NvScaleConst ksc = nv_scale_const(FMT == 0 ? *g.alpha_x : 0.0f);
+            const int kbeg = c0 * 256, kend = min(g.K, (c0 + nck) * 256);
+            if (FMT == 0 && g.dyn_alpha) {
+                // This call's tensor scale (App. B.2 Eq. 8): a = fl(amax(X) / 2688),
+                // the same value rs_compute_tensor_scale gives.  Each CTA takes the
+                // max |x| of its K slice; the K splits of the cluster cover K and
+                // trade their maxima (DSMEM store + remote arrival on each CTA).
+                uint32_t m = 0;
+                const int g8 = (kend - kbeg) / 8;  // 8-element groups per token row of the slice
+                for (int t = qtid; t < g.M * g8; t += kQuantThreads) {
+                    const int j = t / g8;
+                    const uint4 v = *reinterpret_cast<const uint4*>(g.x + (size_t)j * g.K + kbeg + (t - j * g8) * 8);
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+                }
+                m = __reduce_max_sync(0xFFFFFFFFu, m);
+                if (lane == 0) atomicMax(amax_cta, m);
+                named_bar_sync(2, kQuantThreads);
+                if (qtid == 0) {
+                    const uint32_t cm = *reinterpret_cast<volatile uint32_t*>(amax_cta);
+                    if (g.splits > 1) {
+                        for (int p = 0; p < g.splits; ++p) {
+                            st_dsmem_u32(map_dsmem(smem_u32(&amax_slot[split]), (uint32_t)p), cm);
+                            mbar_arrive_remote(map_dsmem(smem_u32(abar), (uint32_t)p));
+                        }
+                    } else {
+                        amax_slot[0] = cm;
+                        mbar_arrive(smem_u32(abar));
+                    }
+                }
+                uint32_t gm = 0;
+                if (mbar_wait_bounded(smem_u32(abar), 0, abort_flag, g.err, 1000000000ull, true))
+                    for (int r = 0; r < g.splits; ++r)
+                        gm = max(gm, reinterpret_cast<volatile uint32_t*>(amax_slot)[r]);
+                const uint32_t bits = gm << 16;
+                if (bits >= 0x7F800000u) {  // Inf or NaN in X, as rs_compute_tensor_scale reports it
+                    if (qtid == 0 && blockIdx.x == 0 && split == 0) atomicExch(g.err, kErrInvalidArg);
+                    ax_val = __uint_as_float(0x7FC00000u);
+                } else {
+                    ax_val = __fdiv_rn(__uint_as_float(bits), 2688.0f);
+                }
+            } else if (FMT == 0) {
+                ax_val = *g.alpha_x;
+            }
+            const NvScaleConst ksc = nv_scale_const(ax_val);
             if (FMT == 0 && qtid == 0 && blockIdx.x == 0 && blockIdx.z == 0 && !nv_alpha_supported(ksc.alpha))
                 atomicExch(g.err, kErrInvalidArg);
-            const int kbeg = c0 * 256, kend = min(g.K, (c0 + nck) * 256);
             // codes of one block (element offset kk of the slice) and, gathered
             // over four consecutive lanes, one scale-atom word
             auto put = [&](uint32_t rowb, int kk, const uint32_t (&codes)[E / 8], uint32_t sfbyte, bool live) {
@@ -518,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             if (qtid == kQuantThreads - 1) RS_TRACE_MARK(g.trace, 18);
         } else if (epi) {
             pdl_wait_prior_grid();  // before writing the output
+            if (FMT == 0) ax_val = *g.alpha_x;
         }
 
         if (epi) {
@@ -526,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             const uint32_t quarter = (uint32_t)(ew * 32) << 16;
             const int row = ew * 32 + lane;                // accumulator lane = channel within the tile
             const int ctid = row;                          // 0..127
-            const float gsc = FMT == 0 ? __fmul_rn(*g.alpha_x, *g.alpha_w) : 1.0f;
+            const float gsc = FMT == 0 ? __fmul_rn(ax_val, *g.alpha_w) : 1.0f;
             float* part = reinterpret_cast<float*>(part_region);  // split-K: [j][channel]
             const uint32_t my_rank = (uint32_t)split;
             // split-K: lane o of warp 8 sends to owner o; its destinations in
@@ -878,8 +929,12 @@ GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bo
     return plan_impl(fmt, fold, M, N, K, num_sms, allow_fused);
 }
 
-size_t workspace_bytes(int fmt, bool compensated, int M, int K) {
+size_t alpha_slot_offset(int fmt, bool compensated, int M, int K) {
     return align_up(operand_bytes(fmt, compensated ? 2 * M : M, K), 1024);
+}
+
+size_t workspace_bytes(int fmt, bool compensated, int M, int K) {
+    return alpha_slot_offset(fmt, compensated, M, K) + 256;  // + the activation tensor scale
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -995,6 +1050,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
     a.part_bytes = p.part_bytes;
     a.recv_bytes = p.recv_bytes;
     a.tmem_cols = p.tmem_cols;
+    a.dyn_alpha = c.dyn_alpha;
 #define RS_CASE(F, B, FU)                                                      \
     if (p.fmt == F && p.bn == B && (p.fused != 0) == FU) return launch_typed<F, B, FU>(p, tb, a, stream);
     RS_CASE(0, 16, true) RS_CASE(0, 32, true) RS_CASE(1, 16, true) RS_CASE(1, 32, true)

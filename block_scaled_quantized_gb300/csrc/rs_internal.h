@@ -61,6 +61,9 @@ GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bo
 // operand when the plan quantizes in a separate kernel (sized for the worst
 // case so that it does not depend on the device).
 size_t workspace_bytes(int fmt, bool compensated, int M, int K);
+// Workspace offset of the activation tensor scale a two-kernel plan computes
+// when the caller passes no alpha_x.
+size_t alpha_slot_offset(int fmt, bool compensated, int M, int K);
 
 cudaError_t launch_tensor_scale(const void* x, int64_t n, float* alpha, uint32_t* err,
                                 cudaStream_t stream, int num_sms);
@@ -81,6 +84,7 @@ struct GemmCall {
     void* y;
     int out_f32;
     uint32_t* err;
+    int dyn_alpha;         // fused NVFP4 plans: compute the activation tensor scale in the GEMM
 };
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmCall& call, cudaStream_t stream);

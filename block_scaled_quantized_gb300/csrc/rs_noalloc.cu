@@ -51,10 +51,19 @@ extern "C" rs_status rs_linear_compensated_noalloc(rs_format fmt, int M, int N, 
     if (K <= 0 || K % 32 != 0) return RS_ERR_SHAPE;
     if (M == 0 || N == 0) return RS_OK;
     if (!x_bf16 || !wq || !y) return RS_ERR_INVALID_ARG;
-    // the paired operand of 2*M rows must fit the fixed array
+    // the paired operand of 2*M rows (and, without alpha_x, the tensor scale
+    // after it) must fit the fixed array
     if (rs::operand_bytes(fmt, 2 * M, K) > (size_t)RS_NOALLOC_SCRATCH_BYTES) return RS_ERR_WORKSPACE;
+    const size_t a_off = rs::alpha_slot_offset(fmt, true, M, K);
+    if (fmt == RS_NVFP4 && !alpha_x && a_off + 256 > (size_t)RS_NOALLOC_SCRATCH_BYTES) return RS_ERR_WORKSPACE;
     void* scratch = scratch_on_current_device();
     if (!scratch) return RS_ERR_CUDA;
+    if (fmt == RS_NVFP4 && !alpha_x) {
+        float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + a_off);
+        const rs_status st = rs_compute_tensor_scale(x_bf16, (int64_t)M * K, a, stream);
+        if (st != RS_OK) return st;
+        alpha_x = a;
+    }
     // The quantizer writes every byte of the operand that the GEMM reads
     // (codes, scales and the zero scale padding), so nothing left over from
     // an earlier call needs clearing.

@@ -134,8 +134,9 @@ RS_API size_t rs_act_bytes(rs_format fmt, int rows, int K);
 RS_API size_t rs_weight_bytes(rs_format fmt, int N, int K);
 /* Workspace that rs_linear_w4a4 / rs_linear_compensated need when given a
  * bf16 input: room for the quantized activation operand, which plans with
- * larger M produce in a separate quantizer kernel (small-M plans quantize
- * inside the GEMM and leave the workspace untouched).  No initialisation is
+ * larger M produce in a separate quantizer kernel, and for the activation
+ * tensor scale those plans compute when alpha_x is NULL (small-M plans
+ * quantize inside the GEMM and leave the workspace untouched).  No initialisation is
  * needed; calls that share a workspace must be ordered (same stream). */
 RS_API size_t rs_workspace_bytes(rs_format fmt, int M, int N, int K, int compensated);
 
@@ -176,8 +177,14 @@ RS_API rs_status rs_quantize_residue(rs_format fmt, int M, int K, const void *x_
 /* Uncompensated W4A4 linear (Fig. 1c): Y[M][N] = alpha_x alpha_w * X^ W^T.
  * Exactly one of x_bf16 (device, [M][K] contiguous, quantized inside the
  * call) and xq (device, rs operand with M rows) is non-NULL.  wq: rs weight
- * of W [N][K] from rs_quantize_weight.  alpha_x / alpha_w (device floats) are
- * required for NVFP4.  y (device): [M][N] row-major, bf16 or fp32.
+ * of W [N][K] from rs_quantize_weight.  alpha_w (device float) is required
+ * for NVFP4.  alpha_x (device float) is the activation tensor scale; with
+ * x_bf16 it may be NULL, and the call then uses this input's own scale
+ * fl(amax(X)/2688) (App. B.2 Eq. 8, the value rs_compute_tensor_scale gives):
+ * small-M plans find it inside the GEMM (each K-split CTA takes its slice's
+ * amax and the cluster trades them), others compute it into the workspace
+ * first.  A non-finite amax sets the device error word.  y (device): [M][N]
+ * row-major, bf16 or fp32.
  * workspace (device): at least rs_workspace_bytes(fmt, M, N, K, 0) bytes when
  * x_bf16 is given; may be NULL with xq.
  *

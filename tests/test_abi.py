@@ -84,7 +84,9 @@ def test_linear_argument_checks(librs):
     assert _lin(librs, x=FAKE, xq=FAKE) == 1
     assert _lin(librs, w=None) == 1
     assert _lin(librs, y=None) == 1
-    assert _lin(librs, ax=None) == 1                          # NVFP4 needs alpha
+    assert _lin(librs, aw=None) == 1                          # NVFP4 needs the weight scale
+    assert _lin(librs, ax=None) not in (1, 2, 3, 5)           # bf16 input: alpha_x may be NULL
+    assert _lin(librs, x=None, xq=FAKE, ax=None) == 1         # a quantized input needs its scale
     assert _lin(librs, out=3) == 1
     assert _lin(librs, x=FAKE_ODD) == 2                       # alignment
     assert _lin(librs, y=FAKE_ODD) == 2

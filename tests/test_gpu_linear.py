@@ -167,3 +167,41 @@ def test_config_mxfp4(M, compensated):
 @pytest.mark.parametrize("compensated", [False, True])
 def test_config_prefill(compensated):
     _sampled_parity(0, compensated, "prefill_k8192", 4096, n_rows=128, n_tok=32)
+
+
+# The activation tensor scale found by the call itself (alpha_x omitted):
+# the same a = fl(amax(X)/2688) as rs_compute_tensor_scale (App. B.2 Eq. 8),
+# so Y is bit-identical to the call given that scale, and matches the
+# oracle.  Fused plans (one K split and several, one tile per CTA and
+# several) and two-kernel plans.
+DYN_SHAPES = [(8, 4096, 4096), (1, 2048, 2048), (3, 20416, 512), (8, 1024, 14336), (40, 512, 768),
+              (300, 384, 256)]
+
+
+@pytest.mark.parametrize("compensated", [False, True])
+@pytest.mark.parametrize("M,N,K", DYN_SHAPES)
+def test_tensor_scale_found_in_call(compensated, M, N, K):
+    x = workloads.make_x("attn_proj_k4096", M, K=K, seed=M * 3 + K)
+    w = workloads.make_w("attn_proj_k4096", N=N, K=K, seed=N + K)
+    wp = prepare_weight(0, w)
+    y_given, _ = gpu_linear(0, compensated, x, wp)
+    y = torch.full_like(y_given, float("nan"))
+    ws = rs.empty_workspace(0, M, N, K, compensated)
+    fn = rs.rs_linear_compensated if compensated else rs.rs_linear_w4a4
+    fn(0, M, N, K, x=x.to(DEV), alpha_x=None, wq=wp["wq"], alpha_w=wp["aw"], y=y, workspace=ws)
+    torch.cuda.synchronize()
+    assert rs.rs_get_device_error() == 0
+    assert torch.equal(y, y_given)
+    assert_close_f32(y, oracle_linear(0, compensated, x, wp))
+
+
+def test_tensor_scale_in_call_flags_non_finite_input():
+    M, N, K = 4, 256, 512
+    x = workloads.make_x("attn_proj_k4096", M, K=K, seed=11)
+    x[2, 100] = float("inf")
+    wp = prepare_weight(0, workloads.make_w("attn_proj_k4096", N=N, K=K, seed=12))
+    y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    ws = rs.empty_workspace(0, M, N, K, True)
+    rs.rs_linear_compensated(0, M, N, K, x=x.to(DEV), alpha_x=None, wq=wp["wq"], alpha_w=wp["aw"], y=y,
+                             workspace=ws)
+    assert rs.rs_get_device_error() == rs.RS_ERR_INVALID_ARG

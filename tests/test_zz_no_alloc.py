@@ -54,3 +54,20 @@ def test_noalloc_matches_compensated_twice(fmt):
         torch.cuda.synchronize()
         assert rs.rs_get_device_error() == 0
         assert_close_f32(y, y_ref.cpu().numpy().astype(np.float64))
+
+
+@pytest.mark.gpu
+def test_noalloc_finds_tensor_scale():
+    """Without alpha_x the no-allocation call uses the input's own tensor
+    scale: the same Y as with rs_compute_tensor_scale's value."""
+    M, N, K = 8, 512, 2048
+    x = workloads.make_x("attn_proj_k4096", M, K=K, seed=21).to(DEV)
+    wp = prepare_weight(0, workloads.make_w("attn_proj_k4096", N=N, K=K, seed=22))
+    y1 = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    y2 = torch.empty_like(y1)
+    rs.rs_linear_compensated_noalloc(0, M, N, K, x=x, alpha_x=gpu_tensor_scale(x), wq=wp["wq"], alpha_w=wp["aw"],
+                                     y=y1)
+    rs.rs_linear_compensated_noalloc(0, M, N, K, x=x, alpha_x=None, wq=wp["wq"], alpha_w=wp["aw"], y=y2)
+    torch.cuda.synchronize()
+    assert rs.rs_get_device_error() == 0
+    assert torch.equal(y1, y2)
