@@ -89,6 +89,16 @@ def _load():
         lib.or_e2m1_encode_array.restype = None
         lib.or_e4m3_encode_array.argtypes = [P, i64, P]
         lib.or_e4m3_encode_array.restype = None
+        lib.or_kext_width.argtypes = [i, i]
+        lib.or_kext_width.restype = i
+        lib.or_kext_select.argtypes = [i, i, P, P]
+        lib.or_kext_select.restype = i
+        lib.or_quantize_kext.argtypes = [i, i, i, i, P, f, P, P, P]
+        lib.or_quantize_kext.restype = i
+        lib.or_quantize_weight_kext.argtypes = [i, i, i, i, P, f, P, P, P]
+        lib.or_quantize_weight_kext.restype = i
+        lib.or_linear_kext.argtypes = [i, i, i, i, i, P, f, P, P, P, f, P]
+        lib.or_linear_kext.restype = i
         _lib = lib
         return lib
 
@@ -228,6 +238,71 @@ def linear(fmt: int, compensated: bool, x_u16, alpha_x: float,
                            _ptr(codes_w), _ptr(sf_w), float(alpha_w), _ptr(Y))
     if rc:
         raise ValueError("oracle linear: bad shape")
+    return Y
+
+
+# ---- selective prefill compensation, K-Ext (Sec. 5.3 Eq. 6, App. A Eq. 7) ----
+
+def kext_width(K: int, k: int) -> int:
+    """Extension length K * rho with rho = k / 8 (k channels per group of 8)."""
+    return K // 8 * k
+
+
+def kext_select(score, k: int) -> np.ndarray:
+    """Eq. 7: per group of 8 channels the k channels with the largest
+    calibration score (mean |x|); equal scores keep the lower channel.
+    Returns one uint8 mask per group (bit t = channel 8g + t)."""
+    score = np.ascontiguousarray(score, np.float32)
+    K = score.size
+    mask = np.zeros(K // 8, np.uint8)
+    if _load().or_kext_select(K, int(k), _ptr(score), _ptr(mask)):
+        raise ValueError("oracle kext_select: bad shape")
+    return mask
+
+
+def quantize_kext(fmt: int, x_u16, k: int, mask, alpha: float = 0.0):
+    """Extended activation operand [X^ | R^_S] of bf16 rows [rows][K]:
+    codes [rows][K_eff/2], scales [rows][K_eff/bs]."""
+    x = _as_u16(x_u16)
+    mask = np.ascontiguousarray(mask, np.uint8)
+    rows, K = x.shape
+    Ke = K + kext_width(K, k)
+    bs = block_size(fmt)
+    codes = np.zeros((rows, Ke // 2), np.uint8)
+    sf = np.zeros((rows, Ke // bs), np.uint8)
+    if _load().or_quantize_kext(fmt, rows, K, int(k), _ptr(x), float(alpha), _ptr(mask), _ptr(codes), _ptr(sf)):
+        raise ValueError("oracle quantize_kext: bad shape or mask")
+    return codes, sf
+
+
+def quantize_weight_kext(fmt: int, w_u16, k: int, mask, alpha_w: float = 0.0):
+    """Extended weight [W | W[:, S]] of bf16 [N][K] quantized as one tensor:
+    codes [N][K_eff/2], scales [N][K_eff/bs]."""
+    w = _as_u16(w_u16)
+    mask = np.ascontiguousarray(mask, np.uint8)
+    N, K = w.shape
+    Ke = K + kext_width(K, k)
+    bs = block_size(fmt)
+    codes = np.zeros((N, Ke // 2), np.uint8)
+    sf = np.zeros((N, Ke // bs), np.uint8)
+    if _load().or_quantize_weight_kext(fmt, N, K, int(k), _ptr(w), float(alpha_w), _ptr(mask), _ptr(codes),
+                                       _ptr(sf)):
+        raise ValueError("oracle quantize_weight_kext: bad shape or mask")
+    return codes, sf
+
+
+def linear_kext(fmt: int, x_u16, k: int, mask, alpha_x: float, codes_w, sf_w, alpha_w: float) -> np.ndarray:
+    """Y [M][N] (double) of the K-Ext linear layer, one GEMM over K_eff."""
+    x = _as_u16(x_u16)
+    mask = np.ascontiguousarray(mask, np.uint8)
+    codes_w = np.ascontiguousarray(codes_w, np.uint8)
+    sf_w = np.ascontiguousarray(sf_w, np.uint8)
+    M, K = x.shape
+    N = codes_w.shape[0]
+    Y = np.zeros((M, N), np.float64)
+    if _load().or_linear_kext(fmt, M, N, K, int(k), _ptr(x), float(alpha_x), _ptr(mask), _ptr(codes_w),
+                              _ptr(sf_w), float(alpha_w), _ptr(Y)):
+        raise ValueError("oracle linear_kext: bad shape or mask")
     return Y
 
 

@@ -465,3 +465,166 @@ void or_e4m3_encode_array(const float *v, int64_t n, uint8_t *out)
     for (int64_t i = 0; i < n; ++i)
         out[i] = or_e4m3_encode_satfinite(v[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Selective prefill compensation, K-Ext (Sec. 5.3 and Eq. 6; App. A Eq. 7;  */
+/* App. B.2 Alg. 1 for the partial residues).                                 */
+/*                                                                            */
+/* Readings (also in the design notes):                                       */
+/*   R11 Eq. 7's TopK within a group of 8 channels keeps the channels with    */
+/*       the larger calibration score; equal scores keep the lower channel.   */
+/*   R12 The extension lists, group by group, the selected channels of each   */
+/*       group in increasing channel order (Alg. 1 line 7 SELECT(r, mask)):  */
+/*       extension element e = g*k + j is the j-th selected channel of group  */
+/*       g.  Its residues are quantized as their own blocks of 16 (NVFP4) or  */
+/*       32 (MXFP4) consecutive extension elements with the base operand's    */
+/*       tensor scale (Sec. 5.3: "a separate NVFP4 operand with its own block  */
+/*       scales and share the base operand's tensor scale").                  */
+/*   R13 The weight side of Eq. 6 is [W | W[:, S]] in bf16 (the selected     */
+/*       floating-point weight columns appended in extension order),          */
+/*       quantized as one tensor in the extended block layout with the        */
+/*       weight's tensor scale.                                               */
+/* k = 8 * rho channels per group of 8; K_eff = K + K*k/8 (Eq. after 6).      */
+/* ------------------------------------------------------------------------ */
+
+int or_kext_width(int K, int k) { return K / 8 * k; }
+
+/* Eq. 7: per group of 8 channels, the k channels with the largest score.
+ * mask[g] bit t is set when channel 8g + t is selected. */
+int or_kext_select(int K, int k, const float *score, uint8_t *mask)
+{
+    if (K <= 0 || K % 8 != 0 || k < 0 || k > 8)
+        return 1;
+    for (int g = 0; g < K / 8; ++g) {
+        uint8_t m = 0;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int t = 0; t < 8; ++t) {
+                if (m & (1u << t))
+                    continue;
+                if (best < 0 || score[8 * g + t] > score[8 * g + best])
+                    best = t;
+            }
+            m = (uint8_t)(m | (1u << best));
+        }
+        mask[g] = m;
+    }
+    return 0;
+}
+
+/* Extension element e -> channel (reading R12).  Returns 1 when a group does
+ * not have exactly k selected channels. */
+static int kext_index(int K, int k, const uint8_t *mask, int *ext)
+{
+    for (int g = 0; g < K / 8; ++g) {
+        int j = 0;
+        for (int t = 0; t < 8; ++t)
+            if (mask[g] & (1u << t))
+                ext[g * k + j++] = 8 * g + t;
+        if (j != k)
+            return 1;
+    }
+    return 0;
+}
+
+static int kext_shape_ok(int fmt, int K, int k)
+{
+    int bs = or_block_size(fmt);
+    return K > 0 && K % bs == 0 && k >= 1 && k <= 8 && (K / 8 * k) % bs == 0;
+}
+
+/* Extended activation operand [X^ | R^_S] (Eq. 6), logical layout with K_eff
+ * columns: codes [rows][K_eff/2], scales [rows][K_eff/bs].  The base part is
+ * exactly or_quantize's; R = X - X^ in fp32 (Alg. 1 line 6). */
+int or_quantize_kext(int fmt, int rows, int K, int k, const uint16_t *x, float alpha, const uint8_t *mask,
+                     uint8_t *codes, uint8_t *sf)
+{
+    int bs = or_block_size(fmt), Kx = or_kext_width(K, k), Ke = K + or_kext_width(K, k);
+    int64_t n = (int64_t)rows * K, nx = (int64_t)rows * Kx;
+    int *ext;
+    float *xf, *xh, *rs, *rh;
+    uint8_t *cb, *sb, *ce, *se;
+    if (rows < 0 || !kext_shape_ok(fmt, K, k))
+        return 1;
+    ext = (int *)malloc(sizeof(int) * (size_t)Kx);
+    if (kext_index(K, k, mask, ext)) {
+        free(ext);
+        return 1;
+    }
+    xf = (float *)malloc(sizeof(float) * (size_t)(n + 1));
+    xh = (float *)malloc(sizeof(float) * (size_t)(n + 1));
+    rs = (float *)malloc(sizeof(float) * (size_t)(nx + 1));
+    rh = (float *)malloc(sizeof(float) * (size_t)(nx + 1));
+    cb = (uint8_t *)malloc((size_t)(n / 2 + 1));
+    sb = (uint8_t *)malloc((size_t)(n / bs + 1));
+    ce = (uint8_t *)malloc((size_t)(nx / 2 + 1));
+    se = (uint8_t *)malloc((size_t)(nx / bs + 1));
+    for (int64_t i = 0; i < n; ++i)
+        xf[i] = bf16_to_float(x[i]);
+    quantize_f32_rows(fmt, rows, K, xf, alpha, cb, sb, xh);
+    for (int r = 0; r < rows; ++r)
+        for (int e = 0; e < Kx; ++e) {
+            int64_t i = (int64_t)r * K + ext[e];
+            rs[(int64_t)r * Kx + e] = xf[i] - xh[i];          /* selected residues */
+        }
+    quantize_f32_rows(fmt, rows, Kx, rs, alpha, ce, se, rh);
+    for (int r = 0; r < rows; ++r) {
+        memcpy(codes + (int64_t)r * (Ke / 2), cb + (int64_t)r * (K / 2), (size_t)(K / 2));
+        memcpy(codes + (int64_t)r * (Ke / 2) + K / 2, ce + (int64_t)r * (Kx / 2), (size_t)(Kx / 2));
+        memcpy(sf + (int64_t)r * (Ke / bs), sb + (int64_t)r * (K / bs), (size_t)(K / bs));
+        memcpy(sf + (int64_t)r * (Ke / bs) + K / bs, se + (int64_t)r * (Kx / bs), (size_t)(Kx / bs));
+    }
+    free(se); free(ce); free(sb); free(cb); free(rh); free(rs); free(xh); free(xf); free(ext);
+    return 0;
+}
+
+/* Extended weight (reading R13): [W | W[:, S]] bf16 [N][K_eff], quantized as
+ * one tensor with tensor scale alpha_w. */
+int or_quantize_weight_kext(int fmt, int N, int K, int k, const uint16_t *w, float alpha_w, const uint8_t *mask,
+                            uint8_t *codes, uint8_t *sf)
+{
+    int Kx = or_kext_width(K, k), Ke = K + or_kext_width(K, k), rc;
+    int *ext;
+    uint16_t *we;
+    if (N < 0 || !kext_shape_ok(fmt, K, k))
+        return 1;
+    ext = (int *)malloc(sizeof(int) * (size_t)Kx);
+    if (kext_index(K, k, mask, ext)) {
+        free(ext);
+        return 1;
+    }
+    we = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)((int64_t)N * Ke + 1));
+    for (int nn = 0; nn < N; ++nn) {
+        memcpy(we + (int64_t)nn * Ke, w + (int64_t)nn * K, sizeof(uint16_t) * (size_t)K);
+        for (int e = 0; e < Kx; ++e)
+            we[(int64_t)nn * Ke + K + e] = w[(int64_t)nn * K + ext[e]];
+    }
+    rc = or_quantize(fmt, N, Ke, we, alpha_w, codes, sf, NULL);
+    free(we);
+    free(ext);
+    return rc;
+}
+
+/* The K-Ext linear layer (Eq. 6): one GEMM over K_eff,
+ *   Y = a_x a_w * [X^ | R^_S] [W^ | W^_S]^T   (MXFP4: tensor scales 1). */
+int or_linear_kext(int fmt, int M, int N, int K, int k, const uint16_t *x, float alpha_x, const uint8_t *mask,
+                   const uint8_t *codes_w, const uint8_t *sf_w, float alpha_w, double *Y)
+{
+    int bs = or_block_size(fmt), Ke = K + or_kext_width(K, k), rc;
+    uint8_t *ca, *sa;
+    double g;
+    if (M < 0 || N < 0 || !kext_shape_ok(fmt, K, k))
+        return 1;
+    ca = (uint8_t *)malloc((size_t)((int64_t)M * (Ke / 2) + 1));
+    sa = (uint8_t *)malloc((size_t)((int64_t)M * (Ke / bs) + 1));
+    rc = or_quantize_kext(fmt, M, K, k, x, alpha_x, mask, ca, sa);
+    if (rc == 0)
+        rc = or_block_gemm(fmt, M, N, Ke, ca, sa, codes_w, sf_w, Y);
+    g = (fmt == 0) ? (double)alpha_x * (double)alpha_w : 1.0;
+    if (rc == 0)
+        for (int64_t i = 0; i < (int64_t)M * N; ++i)
+            Y[i] *= g;
+    free(sa);
+    free(ca);
+    return rc;
+}
