@@ -80,12 +80,20 @@ rs_status check_quant(int fmt, int rows, int K, const void* x, int64_t ldx, cons
     return RS_OK;
 }
 
+bool kext_ok(int K, int k) { return (k == 1 || k == 2 || k == 4 || k == 8) && K > 0 && K % 256 == 0; }
+int kext_cols(int K, int k) { return K + K / 8 * k; }
+
+// kext_k > 0: selective compensation (K-Ext): the operand and the weight are
+// the extended ones with K_eff columns and no Fold (compensated == false).
 rs_status linear_impl(int fmt, bool compensated, int M, int N, int K, const void* x, const void* xq,
                       const float* alpha_x, const void* wq, const float* alpha_w, void* y, int out_dtype,
-                      void* ws, size_t ws_bytes, cudaStream_t stream) {
+                      void* ws, size_t ws_bytes, cudaStream_t stream, int kext_k = 0,
+                      const uint8_t* kext_mask = nullptr) {
     if (!fmt_ok(fmt) || M < 0 || N < 0) return RS_ERR_INVALID_ARG;
     if (out_dtype != RS_OUT_BF16 && out_dtype != RS_OUT_F32) return RS_ERR_INVALID_ARG;
     if (!k_ok(K)) return RS_ERR_SHAPE;
+    if (kext_k > 0 && !kext_ok(K, kext_k)) return RS_ERR_SHAPE;
+    const int Kg = kext_k > 0 ? kext_cols(K, kext_k) : K;  // GEMM reduction length
     if ((int64_t)M * 2 > (int64_t)0x7FFFFFFF) return RS_ERR_SHAPE;
     if (M == 0 || N == 0) return RS_OK;
     if ((x == nullptr) == (xq == nullptr)) return RS_ERR_INVALID_ARG;
@@ -100,14 +108,16 @@ rs_status linear_impl(int fmt, bool compensated, int M, int N, int K, const void
         return RS_ERR_ALIGNMENT;
     if (fmt == RS_NVFP4 && ((alpha_x && !aligned4(alpha_x)) || !aligned4(alpha_w))) return RS_ERR_ALIGNMENT;
     const bool quantize_input = x != nullptr;
-    if (quantize_input && (!ws || ws_bytes < workspace_bytes(fmt, compensated, M, K))) return RS_ERR_WORKSPACE;
+    if (kext_k > 0 && quantize_input && !kext_mask) return RS_ERR_INVALID_ARG;
+    if (quantize_input && (!ws || ws_bytes < workspace_bytes(fmt, compensated, M, Kg))) return RS_ERR_WORKSPACE;
 
     cudaError_t why;
     const DeviceInfo* dev = current_device(&why);
     if (!dev) return RS_ERR_CUDA;
     if (!dev->supported) return RS_ERR_UNSUPPORTED;
 
-    const GemmPlan plan = make_gemm_plan(fmt, compensated, M, N, K, dev->num_sms, /*allow_fused=*/quantize_input);
+    const GemmPlan plan =
+        make_gemm_plan(fmt, compensated, M, N, Kg, dev->num_sms, /*allow_fused=*/quantize_input && kext_k == 0);
     GemmCall c{};
     c.wq = wq;
     c.alpha_x = alpha_x;
@@ -123,14 +133,16 @@ rs_status linear_impl(int fmt, bool compensated, int M, int N, int K, const void
         const float* ax = alpha_x;
         if (dyn_alpha) {
             // the tensor scale goes to the workspace slot after the operand
-            float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + alpha_slot_offset(fmt, compensated, M, K));
+            float* a = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + alpha_slot_offset(fmt, compensated, M, Kg));
             if (launch_tensor_scale(x, (int64_t)M * K, a, dev->err, stream, dev->num_sms) != cudaSuccess)
                 return RS_ERR_CUDA;
             ax = a;
             c.alpha_x = a;
         }
-        cudaError_t e = launch_quantize(fmt, compensated, M, K, x, K, ax, act, stream, dev->num_sms,
-                                        /*pdl=*/true);
+        cudaError_t e = kext_k > 0 ? launch_quantize_kext(fmt, kext_k, M, K, x, K, ax, kext_mask, act, stream,
+                                                          dev->num_sms, /*pdl=*/true)
+                                   : launch_quantize(fmt, compensated, M, K, x, K, ax, act, stream, dev->num_sms,
+                                                     /*pdl=*/true);
         if (e != cudaSuccess) return RS_ERR_CUDA;
         c.xq = act;
     } else {
@@ -250,6 +262,86 @@ rs_status rs_linear_compensated(rs_format fmt, int M, int N, int K, const void* 
                                 rs_out_dtype out_dtype, void* workspace, size_t ws_bytes, rs_stream_t stream) {
     return linear_impl(fmt, true, M, N, K, x_bf16, xq_paired, alpha_x, wq, alpha_w, y, out_dtype, workspace,
                        ws_bytes, (cudaStream_t)stream);
+}
+
+int rs_kext_width(int K, int k) { return kext_ok(K, k) ? K / 8 * k : 0; }
+
+rs_status rs_kext_select(int K, int k, const float* score, uint8_t* mask) {
+    // Eq. 7: per group of 8 channels the k largest scores; equal scores keep
+    // the lower channel.
+    if (!score || !mask || K <= 0 || K % 8 != 0 || k < 0 || k > 8) return RS_ERR_INVALID_ARG;
+    for (int g = 0; g < K / 8; ++g) {
+        unsigned chosen = 0;
+        for (int j = 0; j < k; ++j) {
+            int top = -1;
+            for (int t = 0; t < 8; ++t)
+                if (!(chosen >> t & 1u) && (top < 0 || score[8 * g + t] > score[8 * g + top])) top = t;
+            chosen |= 1u << top;
+        }
+        mask[g] = (uint8_t)chosen;
+    }
+    return RS_OK;
+}
+
+rs_status rs_channel_mean_abs(const void* x_bf16, int rows, int K, int64_t ldx, float* score, rs_stream_t stream) {
+    if (rows < 0 || K <= 0 || !x_bf16 || !score || ldx < K) return RS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x_bf16) & 1u) || !aligned4(score)) return RS_ERR_ALIGNMENT;
+    cudaError_t why;
+    const DeviceInfo* dev = current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    return from_cuda(launch_channel_mean_abs(x_bf16, rows, K, ldx, score, (cudaStream_t)stream));
+}
+
+size_t rs_kext_act_bytes(rs_format fmt, int rows, int K, int k) {
+    if (!fmt_ok(fmt) || rows < 0 || !kext_ok(K, k)) return 0;
+    return operand_bytes(fmt, rows, kext_cols(K, k));
+}
+
+size_t rs_kext_weight_bytes(rs_format fmt, int N, int K, int k) {
+    if (!fmt_ok(fmt) || N < 0 || !kext_ok(K, k)) return 0;
+    return weight_bytes(fmt, N, kext_cols(K, k));
+}
+
+size_t rs_kext_workspace_bytes(rs_format fmt, int M, int N, int K, int k) {
+    if (!fmt_ok(fmt) || M <= 0 || N <= 0 || !kext_ok(K, k)) return 0;
+    return workspace_bytes(fmt, false, M, kext_cols(K, k));
+}
+
+rs_status rs_quantize_weight_kext(rs_format fmt, int N, int K, int k, const void* w_bf16, int64_t ldw,
+                                  const float* alpha_w, const uint8_t* mask, void* wq_out, rs_stream_t stream) {
+    rs_status s = check_quant(fmt, N, K, w_bf16, ldw, alpha_w, wq_out);
+    if (s != RS_OK || N == 0) return s;
+    if (!kext_ok(K, k)) return RS_ERR_SHAPE;
+    if (!mask) return RS_ERR_INVALID_ARG;
+    cudaError_t why;
+    const DeviceInfo* dev = current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    return from_cuda(launch_quantize_weight(fmt, N, K, w_bf16, ldw, alpha_w, wq_out, (cudaStream_t)stream,
+                                            dev->num_sms, k, mask));
+}
+
+rs_status rs_quantize_kext(rs_format fmt, int rows, int K, int k, const void* x_bf16, int64_t ldx, const float* alpha,
+                           const uint8_t* mask, void* q_out, rs_stream_t stream) {
+    rs_status s = check_quant(fmt, rows, K, x_bf16, ldx, alpha, q_out);
+    if (s != RS_OK || rows == 0) return s;
+    if (!kext_ok(K, k)) return RS_ERR_SHAPE;
+    if (!mask) return RS_ERR_INVALID_ARG;
+    cudaError_t why;
+    const DeviceInfo* dev = current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    return from_cuda(launch_quantize_kext(fmt, k, rows, K, x_bf16, ldx, alpha, mask, q_out, (cudaStream_t)stream,
+                                          dev->num_sms, /*pdl=*/false));
+}
+
+rs_status rs_linear_kext(rs_format fmt, int M, int N, int K, int k, const void* x_bf16, const void* xq,
+                         const float* alpha_x, const uint8_t* mask, const void* wq_ext, const float* alpha_w,
+                         void* y, rs_out_dtype out_dtype, void* workspace, size_t ws_bytes, rs_stream_t stream) {
+    if (k != 1 && k != 2 && k != 4 && k != 8) return RS_ERR_INVALID_ARG;
+    return linear_impl(fmt, false, M, N, K, x_bf16, xq, alpha_x, wq_ext, alpha_w, y, out_dtype, workspace,
+                       ws_bytes, (cudaStream_t)stream, k, mask);
 }
 
 rs_status rs_get_device_error(rs_stream_t stream) {

@@ -72,8 +72,16 @@ cudaError_t launch_tensor_scale(const void* x, int64_t n, float* alpha, uint32_t
 // previous grid has returned.  Only for activations consumed by our GEMM.
 cudaError_t launch_quantize(int fmt, bool paired, int rows, int K, const void* x, int64_t ldx,
                             const float* alpha, void* q_out, cudaStream_t stream, int num_sms, bool pdl);
+// kext_k > 0: the extended weight [W | W[:, S]] of K-Ext (K_eff = K + K kext_k / 8
+// columns; kext_mask: device bytes, one per group of 8 channels).
 cudaError_t launch_quantize_weight(int fmt, int N, int K, const void* w, int64_t ldw, const float* alpha,
-                                   void* wq_out, cudaStream_t stream, int num_sms);
+                                   void* wq_out, cudaStream_t stream, int num_sms, int kext_k = 0,
+                                   const uint8_t* kext_mask = nullptr);
+// K-Ext activation operand [X^ | R^_S] (rs operand layout, rows x K_eff), K % 256 == 0.
+cudaError_t launch_quantize_kext(int fmt, int k, int rows, int K, const void* x, int64_t ldx, const float* alpha,
+                                 const uint8_t* mask, void* q_out, cudaStream_t stream, int num_sms, bool pdl);
+// Mean |x| of every channel over rows (the calibration score of Eq. 7).
+cudaError_t launch_channel_mean_abs(const void* x, int rows, int K, int64_t ldx, float* score, cudaStream_t stream);
 
 struct GemmCall {
     const void* x;         // fused plans: bf16 activations [M][K]

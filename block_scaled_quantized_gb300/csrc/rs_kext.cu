@@ -1,0 +1,189 @@
+// Selective prefill compensation, K-Ext (ResServe Sec. 5.3 Eq. 6, App. A
+// Eq. 7, App. B.2 Alg. 1 for the partial residues): the quantizer that
+// writes the extended activation operand [X^ | R^_S] of K_eff = K + K k / 8
+// columns in the rs operand layout, so that the block-scaled GEMM over K_eff
+// adds the base and the selected-residue products in one accumulator.
+//
+// One warp takes one token row x 256 channels; lane l holds channels
+// 8l .. 8l+7 of the chunk, which are exactly one 8-channel selection group
+// (Eq. 7), so its byte of the mask says which of its residues are kept.
+// Base: as the plain quantizer (two lanes per 16-element block).  Residues
+// r = fl(x - x^) of the k selected channels, in increasing channel order,
+// are extension elements g k .. g k + k - 1 (g = group index); a block of
+// 16 (NVFP4) / 32 (MXFP4) extension elements spans 16/k (32/k) consecutive
+// lanes, whose block amax is a shuffle reduction; the block scale uses the
+// base operand's tensor scale.
+#include <cuda_bf16.h>
+
+#include "rs_device.cuh"
+#include "rs_internal.h"
+#include "rs_quant_core.cuh"
+
+namespace rs {
+
+struct KextArgs {
+    const uint16_t* x;      // bf16 [rows][ldx]
+    int64_t ldx;
+    int rows, K;            // K: base channels (a multiple of 256)
+    const float* alpha;     // NVFP4 tensor scale (device)
+    const uint8_t* mask;    // [K/8] selection bytes (device), k bits set each
+    uint8_t* out;           // operand base (codes [rows][K_eff/2])
+    uint8_t* sf;            // its scale atoms
+    int rows_pad;           // rows rounded up to 128
+    int n_atoms_k;          // scale atoms per row tile along K_eff
+    int early_trigger;      // release the dependent grid once the prior grid is done
+    uint32_t* err;
+};
+
+template <int FMT, int KS>
+__global__ void __launch_bounds__(256) kext_quantize_kernel(KextArgs a) {
+    pdl_wait_prior_grid();
+    if (a.early_trigger) pdl_launch_dependents();
+    constexpr int BS = block_elems(FMT);
+    constexpr int L = BS / KS;               // lanes per extension block
+    constexpr int LPA = lanes_per_atom<FMT>();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps_total = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int chunks = a.K / 256;
+    const int64_t tasks = (int64_t)a.rows * chunks;
+    const int Ke = a.K + a.K / 8 * KS;
+    const NvScaleConst ksc = nv_scale_const(FMT == 0 ? *a.alpha : 0.0f);
+    if (FMT == 0 && blockIdx.x == 0 && threadIdx.x == 0 && !nv_alpha_supported(ksc.alpha))
+        atomicExch(a.err, kErrInvalidArg);
+
+    for (int64_t task = warp; task < tasks; task += n_warps_total) {
+        const int row = (int)(task / chunks);
+        const int chunk = (int)(task - (int64_t)row * chunks);
+        const int k0 = chunk * 256 + lane * 8;
+        float xf[8];
+        load8_bf16(a.x + (int64_t)row * a.ldx + k0, true, xf);
+        uint8_t* orow = a.out + (size_t)row * (size_t)(Ke / 2);
+
+        // base operand (Eq. 8-10)
+        uint32_t sfb;
+        float xh[8];
+        const uint32_t codes = quant_lane<FMT, true>(xf, ksc, sfb, xh);
+        const uint32_t sfw = gather_sf_word<FMT>(sfb, lane);
+        *reinterpret_cast<uint32_t*>(orow + k0 / 2) = codes;
+        if (lane % LPA == 0)
+            *reinterpret_cast<uint32_t*>(a.sf + sf_offset(row, (chunk * (256 / atom_k(FMT)) + lane / LPA) * kAtomBlocks,
+                                                          a.n_atoms_k)) = sfw;
+
+        // the group's selected residues, in channel order (Alg. 1 lines 6-7)
+        float r[8];
+        residue8(xf, xh, r);
+        const int grp = chunk * 32 + lane;
+        const uint32_t m = a.mask[grp];
+        if (__popc(m) != KS) atomicExch(a.err, kErrInvalidArg);  // a mask must keep k channels per group
+        float sel[KS];
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+            const uint32_t idx = __fns(m, 0, j + 1);  // position of the (j+1)-th set bit
+            float v = 0.0f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) v = idx == (uint32_t)t ? r[t] : v;
+            sel[j] = v;
+        }
+        // block amax over the L lanes of this extension block (lines 8-9)
+        float am = 0.0f;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) am = fmaxf(am, fabsf(sel[j]));
+#pragma unroll
+        for (int o = 1; o < L; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+        float st, mul;
+        const uint32_t sfr = FMT == 0 ? nv_block_scale_fast(am, ksc, st, mul) : mx_block_scale(am, st, mul);
+        float v8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v8[e] = e < KS ? __fmul_rn(sel[e], mul) : 0.0f;
+        const uint32_t rc = e2m1_encode8(v8);  // element j in nibble j
+        const int c = a.K + grp * KS;          // K_eff column of this lane's first extension element
+        if constexpr (KS == 8) {
+            *reinterpret_cast<uint32_t*>(orow + c / 2) = rc;
+        } else if constexpr (KS == 4) {
+            *reinterpret_cast<uint16_t*>(orow + c / 2) = (uint16_t)(rc & 0xFFFFu);
+        } else if constexpr (KS == 2) {
+            orow[c / 2] = (uint8_t)(rc & 0xFFu);
+        } else {
+            const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, rc & 0xFu, 1);
+            if ((lane & 1) == 0) orow[c / 2] = (uint8_t)((rc & 0xFu) | (hi << 4));
+        }
+        if (lane % L == 0) a.sf[sf_offset(row, c / BS, a.n_atoms_k)] = (uint8_t)sfr;
+        // padding blocks of the row's last, partly filled scale atom
+        const int nb = Ke / BS;
+        if (chunk == chunks - 1 && lane < a.n_atoms_k * kAtomBlocks - nb)
+            a.sf[sf_offset(row, nb + lane, a.n_atoms_k)] = 0;
+    }
+
+    // zero scale words of the padding rows [rows, rows_pad)
+    const int64_t pad_words = (int64_t)(a.rows_pad - a.rows) * a.n_atoms_k;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = tid; i < pad_words; i += nthreads) {
+        const int rr = a.rows + (int)(i / a.n_atoms_k);
+        const int gg = (int)(i % a.n_atoms_k);
+        *reinterpret_cast<uint32_t*>(a.sf + sf_offset(rr, gg * kAtomBlocks, a.n_atoms_k)) = 0u;
+    }
+}
+
+// Calibration score of Eq. 7: mean |x| of every channel over `rows` rows,
+// one thread per channel summing in row order (deterministic).
+__global__ void channel_mean_abs_kernel(const uint16_t* __restrict__ x, int rows, int K, int64_t ldx,
+                                        float* __restrict__ score) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= K) return;
+    float s = 0.0f;
+    for (int r = 0; r < rows; ++r) s += fabsf(__uint_as_float((uint32_t)x[(int64_t)r * ldx + c] << 16));
+    score[c] = rows > 0 ? s / (float)rows : 0.0f;
+}
+
+template <int FMT, int KS>
+static cudaError_t launch_kext_typed(const KextArgs& a, int grid, cudaStream_t stream, bool pdl) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kext_quantize_kernel<FMT, KS>, a);
+}
+
+cudaError_t launch_quantize_kext(int fmt, int k, int rows, int K, const void* x, int64_t ldx, const float* alpha,
+                                 const uint8_t* mask, void* q_out, cudaStream_t stream, int num_sms, bool pdl) {
+    const int Ke = K + K / 8 * k;
+    KextArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.ldx = ldx;
+    a.rows = rows;
+    a.K = K;
+    a.alpha = alpha;
+    a.mask = mask;
+    a.out = static_cast<uint8_t*>(q_out);
+    a.sf = static_cast<uint8_t*>(q_out) + operand_sf_offset(fmt, rows, Ke);
+    a.rows_pad = (rows + kAtomRows - 1) / kAtomRows * kAtomRows;
+    a.n_atoms_k = n_atoms_k_host(fmt, Ke);
+    a.early_trigger = pdl ? 1 : 0;
+    a.err = device_error_word();
+    const int64_t warps = (int64_t)rows * (K / 256);
+    int64_t blocks = (warps + 7) / 8;
+    const int64_t pad_blocks = ((int64_t)(a.rows_pad - rows) * a.n_atoms_k + 255) / 256;
+    if (pad_blocks > blocks) blocks = pad_blocks;
+    if (blocks > (int64_t)num_sms * 32) blocks = (int64_t)num_sms * 32;
+    const int grid = (int)(blocks < 1 ? 1 : blocks);
+#define RS_KEXT(F, S) \
+    if (fmt == F && k == S) return launch_kext_typed<F, S>(a, grid, stream, pdl);
+    RS_KEXT(0, 1) RS_KEXT(0, 2) RS_KEXT(0, 4) RS_KEXT(0, 8)
+    RS_KEXT(1, 1) RS_KEXT(1, 2) RS_KEXT(1, 4) RS_KEXT(1, 8)
+#undef RS_KEXT
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_channel_mean_abs(const void* x, int rows, int K, int64_t ldx, float* score, cudaStream_t stream) {
+    channel_mean_abs_kernel<<<(K + 255) / 256, 256, 0, stream>>>(static_cast<const uint16_t*>(x), rows, K, ldx, score);
+    return cudaGetLastError();
+}
+
+}  // namespace rs

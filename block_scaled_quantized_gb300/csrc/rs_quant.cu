@@ -75,6 +75,12 @@ struct QuantArgs {
     int chunks;          // ceil(K / 256)
     int early_trigger;   // release the dependent grid once the prior grid is done
     uint32_t* err;       // device error word
+    // WEIGHT with a K-Ext extension (Eq. 6, reading R13): columns k_base..K-1
+    // are W[:, S] -- column k_base + g*kext_k + j is the j-th selected channel
+    // of group g (kext_mask[g], device)
+    int k_base;
+    int kext_k;
+    const uint8_t* kext_mask;
 };
 
 template <int FMT, int MODE>
@@ -106,7 +112,23 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
         const int k0 = chunk * 256 + lane * 8;
         const bool valid = k0 < a.K && row < a.rows;
         float xf[8];
-        load8_bf16(a.x + (int64_t)row * a.ldx + k0, valid, xf);
+        if (MODE == kWeight && a.kext_k > 0 && k0 >= a.k_base) {
+            // appended columns of the extended weight: gathered
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = k0 - a.k_base + i;
+                float v = 0.0f;
+                if (row < a.rows && e < a.K - a.k_base) {
+                    const int grp = e / a.kext_k;
+                    const uint32_t t = __fns(a.kext_mask[grp], 0, e - grp * a.kext_k + 1);
+                    if (t < 8u) v = __uint_as_float((uint32_t)a.x[(int64_t)row * a.ldx + 8 * grp + (int)t] << 16);
+                    else atomicExch(a.err, kErrInvalidArg);  // fewer than k channels in the group
+                }
+                xf[i] = v;
+            }
+        } else {
+            load8_bf16(a.x + (int64_t)row * a.ldx + k0, valid, xf);
+        }
 
         uint32_t sfb;
         float xh[8];
@@ -227,8 +249,15 @@ cudaError_t launch_quantize(int fmt, bool paired, int rows, int K, const void* x
 }
 
 cudaError_t launch_quantize_weight(int fmt, int N, int K, const void* w, int64_t ldw, const float* alpha,
-                                   void* wq_out, cudaStream_t stream, int num_sms) {
+                                   void* wq_out, cudaStream_t stream, int num_sms, int kext_k,
+                                   const uint8_t* kext_mask) {
     QuantArgs a{};
+    if (kext_k > 0) {  // extended weight [W | W[:, S]] with K_eff columns
+        a.k_base = K;
+        a.kext_k = kext_k;
+        a.kext_mask = kext_mask;
+        K = K + K / 8 * kext_k;
+    }
     a.x = static_cast<const uint16_t*>(w);
     a.ldx = ldw;
     a.rows = N;

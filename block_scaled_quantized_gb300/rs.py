@@ -28,7 +28,9 @@ globals().update({name: code for code, name in STATUS.items()})  # RS_OK, RS_ERR
 EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_offset", "rs_act_bytes",
            "rs_weight_bytes", "rs_workspace_bytes", "rs_compute_tensor_scale", "rs_quantize_fp4",
            "rs_quantize_weight", "rs_quantize_residue", "rs_linear_w4a4", "rs_linear_compensated",
-           "rs_linear_compensated_noalloc", "rs_get_device_error"]
+           "rs_linear_compensated_noalloc", "rs_get_device_error", "rs_kext_width", "rs_kext_select",
+           "rs_channel_mean_abs", "rs_kext_act_bytes", "rs_kext_weight_bytes", "rs_kext_workspace_bytes",
+           "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext"]
 
 
 class RsError(RuntimeError):
@@ -59,6 +61,15 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_linear_compensated": ([I, I, I, I, P, P, P, P, P, P, I, P, SZ, P], I),
         "rs_linear_compensated_noalloc": ([I, I, I, I, P, P, P, P, P, I, P], I),
         "rs_get_device_error": ([P], I),
+        "rs_kext_width": ([I, I], I),
+        "rs_kext_select": ([I, I, P, P], I),
+        "rs_channel_mean_abs": ([P, I, I, I64, P, P], I),
+        "rs_kext_act_bytes": ([I, I, I, I], SZ),
+        "rs_kext_weight_bytes": ([I, I, I, I], SZ),
+        "rs_kext_workspace_bytes": ([I, I, I, I, I], SZ),
+        "rs_quantize_weight_kext": ([I, I, I, I, P, I64, P, P, P, P], I),
+        "rs_quantize_kext": ([I, I, I, I, P, I64, P, P, P, P], I),
+        "rs_linear_kext": ([I, I, I, I, I, P, P, P, P, P, P, P, I, P, SZ, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -200,3 +211,60 @@ def empty_workspace(fmt: int, M: int, N: int, K: int, compensated: bool, device=
     """Workspace for a linear call with bf16 input (no initialisation needed)."""
     n = max(rs_workspace_bytes(fmt, M, N, K, compensated), 16)
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+# ------------------------------------- selective compensation (K-Ext) ----
+
+def rs_kext_width(K: int, k: int) -> int:
+    return lib().rs_kext_width(K, k)
+
+
+def rs_kext_select(score, k: int):
+    """Eq. 7 on the host: numpy float32 scores [K] -> uint8 masks [K/8]."""
+    import numpy as np
+    score = np.ascontiguousarray(score, np.float32)
+    mask = np.zeros(score.size // 8, np.uint8)
+    _check("rs_kext_select", lib().rs_kext_select(score.size, k, score.ctypes.data_as(ctypes.c_void_p),
+                                                  mask.ctypes.data_as(ctypes.c_void_p)))
+    return mask
+
+
+def rs_channel_mean_abs(x: torch.Tensor, score_out: torch.Tensor, stream=None):
+    rows, K = x.shape
+    _check("rs_channel_mean_abs", lib().rs_channel_mean_abs(_ptr(x), rows, K, x.stride(0), _ptr(score_out),
+                                                            _stream(stream)))
+
+
+def rs_kext_act_bytes(fmt: int, rows: int, K: int, k: int) -> int:
+    return lib().rs_kext_act_bytes(fmt, rows, K, k)
+
+
+def rs_kext_weight_bytes(fmt: int, N: int, K: int, k: int) -> int:
+    return lib().rs_kext_weight_bytes(fmt, N, K, k)
+
+
+def rs_kext_workspace_bytes(fmt: int, M: int, N: int, K: int, k: int) -> int:
+    return lib().rs_kext_workspace_bytes(fmt, M, N, K, k)
+
+
+def rs_quantize_weight_kext(fmt: int, w: torch.Tensor, k: int, alpha: torch.Tensor | None, mask: torch.Tensor,
+                            wq_out: torch.Tensor, stream=None):
+    N, K = w.shape
+    _check("rs_quantize_weight_kext", lib().rs_quantize_weight_kext(fmt, N, K, k, _ptr(w), w.stride(0), _ptr(alpha),
+                                                                    _ptr(mask), _ptr(wq_out), _stream(stream)))
+
+
+def rs_quantize_kext(fmt: int, x: torch.Tensor, k: int, alpha: torch.Tensor | None, mask: torch.Tensor,
+                     q_out: torch.Tensor, stream=None):
+    rows, K = x.shape
+    _check("rs_quantize_kext", lib().rs_quantize_kext(fmt, rows, K, k, _ptr(x), x.stride(0), _ptr(alpha),
+                                                      _ptr(mask), _ptr(q_out), _stream(stream)))
+
+
+def rs_linear_kext(fmt: int, M: int, N: int, K: int, k: int, x=None, xq=None, alpha_x=None, mask=None,
+                   wq=None, alpha_w=None, y=None, workspace=None, stream=None):
+    out = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("rs_linear_kext", lib().rs_linear_kext(fmt, M, N, K, k, _ptr(x), _ptr(xq), _ptr(alpha_x), _ptr(mask),
+                                                  _ptr(wq), _ptr(alpha_w), _ptr(y), out, _ptr(workspace), ws_bytes,
+                                                  _stream(stream)))

@@ -214,6 +214,67 @@ RS_API rs_status rs_linear_compensated(rs_format fmt, int M, int N, int K,
                                 void *y, rs_out_dtype out_dtype,
                                 void *workspace, size_t ws_bytes, rs_stream_t stream);
 
+/* ---- selective prefill compensation, K-Ext (Sec. 5.3 Eq. 6, App. A Eq. 7) -- */
+
+/* Selective compensation keeps the residues of k of every 8 consecutive
+ * input channels (ratio rho = k / 8, k in {1, 2, 4, 8}; k = 8 is full
+ * compensation) and appends them to the activation as extra reduction
+ * columns, with the matching weight columns appended offline, so one GEMM
+ * over K_eff = K + K k / 8 sums the base and the correction (Eq. 6):
+ *   Y = alpha_x alpha_w [X^ | R^_S] [W^ | W^_S]^T.
+ * Selection masks: one byte per group of 8 channels, bit t set when channel
+ * 8g + t is compensated, exactly k bits per byte.  Extension element
+ * g k + j holds the j-th selected channel of group g (increasing channel
+ * order); the selected residues r = fl(x - x^) are quantized as their own
+ * blocks of 16 (NVFP4) / 32 (MXFP4) extension elements with the base
+ * operand's tensor scale.  The extended weight is [W | W[:, S]] quantized
+ * as one tensor with alpha_w.  K must be a multiple of 256. */
+
+/* K k / 8 (the number of extension columns), 0 for an unsupported K or k. */
+RS_API int rs_kext_width(int K, int k);
+
+/* Eq. 7 on the host: for each group of 8 channels, the k channels with the
+ * largest calibration score (mean |x|); equal scores keep the lower channel.
+ * score: host float[K]; mask: host uint8[K / 8]. */
+RS_API rs_status rs_kext_select(int K, int k, const float *score, uint8_t *mask);
+
+/* Calibration score of Eq. 7 on the device: score[c] = mean over the rows of
+ * |x[r][c]| (fp32, rows summed in order).  x: bf16 [rows][ldx]. */
+RS_API rs_status rs_channel_mean_abs(const void *x_bf16, int rows, int K, int64_t ldx, float *score,
+                                     rs_stream_t stream);
+
+/* Sizes: the extended activation operand (rs operand layout, rows x K_eff),
+ * the extended weight (rs weight layout, N x K_eff), and the workspace of
+ * rs_linear_kext given a bf16 input.  0 for unsupported arguments. */
+RS_API size_t rs_kext_act_bytes(rs_format fmt, int rows, int K, int k);
+RS_API size_t rs_kext_weight_bytes(rs_format fmt, int N, int K, int k);
+RS_API size_t rs_kext_workspace_bytes(rs_format fmt, int M, int N, int K, int k);
+
+/* Offline: the extended weight [W | W[:, S]] of W bf16 [N][K] (row pitch
+ * ldw), quantized with alpha_w (NVFP4) into wq_out (device,
+ * rs_kext_weight_bytes).  mask: device uint8[K / 8]. */
+RS_API rs_status rs_quantize_weight_kext(rs_format fmt, int N, int K, int k, const void *w_bf16, int64_t ldw,
+                                         const float *alpha_w, const uint8_t *mask, void *wq_out,
+                                         rs_stream_t stream);
+
+/* The extended activation operand [X^ | R^_S] of x bf16 [rows][ldx] (Sec. 5.3,
+ * App. B.2 Alg. 1) into q_out (device, rs_kext_act_bytes).  A mask byte
+ * without exactly k bits set sets the device error word. */
+RS_API rs_status rs_quantize_kext(rs_format fmt, int rows, int K, int k, const void *x_bf16, int64_t ldx,
+                                  const float *alpha, const uint8_t *mask, void *q_out, rs_stream_t stream);
+
+/* Selective-compensation linear (Eq. 6): Y[M][N] = alpha_x alpha_w *
+ * [X^ | R^_S] [W^ | W^_S]^T.  Exactly one of x_bf16 (device [M][K]; then mask
+ * and a workspace of rs_kext_workspace_bytes are needed) and xq (an extended
+ * operand from rs_quantize_kext) is non-NULL; wq_ext from
+ * rs_quantize_weight_kext with the same mask.  alpha_x may be NULL with
+ * x_bf16 (the input's own tensor scale, as for rs_linear_w4a4).  Other
+ * arguments, alignment and errors as for rs_linear_w4a4. */
+RS_API rs_status rs_linear_kext(rs_format fmt, int M, int N, int K, int k, const void *x_bf16, const void *xq,
+                                const float *alpha_x, const uint8_t *mask, const void *wq_ext,
+                                const float *alpha_w, void *y, rs_out_dtype out_dtype, void *workspace,
+                                size_t ws_bytes, rs_stream_t stream);
+
 /* ---- compensated linear without any device allocation -------------------- */
 
 /* Size of the fixed device array that rs_linear_compensated_noalloc uses in

@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from conftest import ROOT
@@ -116,3 +117,32 @@ def test_quantizer_argument_checks(librs):
     assert f(1, 4, 64, FAKE, 64, None, FAKE_ODD, None) == 2
     assert librs.rs_compute_tensor_scale(FAKE, -1, FAKE, None) == 1
     assert librs.rs_compute_tensor_scale(FAKE, 16, None, None) == 1
+
+
+def test_kext_host_selection_matches_oracle(librs, oracle_mod):
+    """rs_kext_select (Eq. 7, host code of librs) against the oracle's."""
+    import ctypes
+    rng = np.random.default_rng(5)
+    for k in (1, 2, 4, 8):
+        score = rng.random(512).astype(np.float32)
+        score[::7] = score[3]  # ties
+        mask = np.zeros(64, np.uint8)
+        assert librs.rs_kext_select(512, k, score.ctypes.data_as(ctypes.c_void_p),
+                                    mask.ctypes.data_as(ctypes.c_void_p)) == 0
+        assert np.array_equal(mask, oracle_mod.kext_select(score, k))
+
+
+def test_kext_argument_checks(librs):
+    assert librs.rs_kext_width(512, 2) == 128
+    assert librs.rs_kext_width(500, 2) == 0 and librs.rs_kext_width(512, 3) == 0
+    assert librs.rs_kext_act_bytes(0, 4, 512, 2) == librs.rs_operand_bytes(0, 4, 640)
+    assert librs.rs_kext_weight_bytes(1, 256, 512, 8) == librs.rs_weight_bytes(1, 256, 1024)
+    f = librs.rs_linear_kext
+    ws = librs.rs_kext_workspace_bytes(0, 8, 256, 512, 2)
+    assert f(0, 8, 256, 512, 3, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, ws, None) == 1   # k
+    assert f(0, 8, 256, 288, 2, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, ws, None) == 3   # K % 256
+    assert f(0, 8, 256, 512, 2, FAKE, None, FAKE, None, FAKE, FAKE, FAKE, 0, FAKE, ws, None) == 1   # mask
+    assert f(0, 8, 256, 512, 2, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 16, None) == 5   # workspace
+    q = librs.rs_quantize_kext
+    assert q(0, 4, 512, 5, FAKE, 512, FAKE, FAKE, FAKE, None) == 3
+    assert q(0, 4, 512, 2, FAKE, 512, FAKE, None, FAKE, None) == 1
