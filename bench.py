@@ -39,7 +39,7 @@ WORKLOAD = "nvfp4_compensated_linear_attn_proj_M8_K4096_N4096"
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by
 # the hash of the kernel sources it was taken on (null once they change).
-TRAFFIC = {"sources_sha": "38610de6fa5324b2", "bytes_per_launch": 9579776}
+TRAFFIC = {"sources_sha": "67d3b9b9b83799ed", "bytes_per_launch": 9587200}
 
 
 def kernel_sources_sha() -> str:
@@ -209,6 +209,55 @@ class Linear:
         return useful, (2 * useful if self.compensated else useful)
 
 
+class KextLinear:
+    """A prefill linear layer with selective compensation (K-Ext): channels
+    chosen per group of 8 from a calibration score (mean |x| over calibration
+    rows of the same recipe), extended weight [W | W[:, S]] quantized once."""
+
+    def __init__(self, torch, rs, workloads, recipe, M, k, seed=None):
+        self.torch, self.rs = torch, rs
+        dev = torch.device("cuda")
+        self.fmt, self.M, self.k = rs.NVFP4, M, k
+        x = workloads.make_x(recipe, M, seed=seed)
+        w = workloads.make_w(recipe, seed=seed)
+        self.N, self.K = w.shape
+        self.x = x.to(dev)
+        calib = workloads.make_x(recipe, 256, seed=(seed or 0) + 7919).to(dev)
+        score = torch.empty(self.K, dtype=torch.float32, device=dev)
+        rs.rs_channel_mean_abs(calib, score)
+        self.mask = torch.from_numpy(rs.rs_kext_select(score.cpu().numpy(), k)).to(dev)
+        wg = w.to(dev)
+        self.ax = torch.empty(1, dtype=torch.float32, device=dev)
+        self.aw = torch.empty(1, dtype=torch.float32, device=dev)
+        rs.rs_compute_tensor_scale(self.x, self.ax)
+        rs.rs_compute_tensor_scale(wg, self.aw)
+        self.wq = torch.empty(rs.rs_kext_weight_bytes(self.fmt, self.N, self.K, k), dtype=torch.uint8, device=dev)
+        rs.rs_quantize_weight_kext(self.fmt, wg, k, self.aw, self.mask, self.wq)
+        del wg
+        self.y = torch.empty((M, self.N), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(rs.rs_kext_workspace_bytes(self.fmt, M, self.N, self.K, k), dtype=torch.uint8,
+                              device=dev)
+        torch.cuda.synchronize()
+
+    def call(self, i: int):
+        self.rs.rs_linear_kext(self.fmt, self.M, self.N, self.K, self.k, x=self.x, alpha_x=self.ax, mask=self.mask,
+                               wq=self.wq, alpha_w=self.aw, y=self.y, workspace=self.ws)
+
+    def launches_per_call(self) -> int:
+        return 2
+
+    def flops(self) -> tuple[int, int]:
+        useful = 2 * self.M * self.N * self.K
+        return useful, useful + useful * self.k // 8
+
+
+def nmse_vs_bf16(torch, x, w, y) -> float:
+    """Normalised squared error of y against the fp32 product of the bf16
+    operands (an accuracy figure beside the timing, not a parity check)."""
+    ref = x.float() @ w.float().t()
+    return float(((y.float() - ref) ** 2).sum() / (ref ** 2).sum())
+
+
 def graph_time_us(torch, fn_step, steps: int, reps: int = 5, warm: int = 3) -> tuple[float, list[float]]:
     """Capture `steps` calls in a CUDA graph; return median us per call."""
     s = torch.cuda.Stream()
@@ -243,6 +292,7 @@ PROFILE_CASES = {
     "mlp_gate_up": (0, "mlp_gate_up", 8, True),
     "mlp_down": (0, "mlp_down", 8, True),
     "mx_m1": (1, "mx_k5120_n27648", 1, True),
+    "prefill_kext1": (0, "prefill_k8192", 4096, "kext1"),
 }
 
 
@@ -253,7 +303,10 @@ def run_profile_case(args) -> dict:
     from block_scaled_quantized_gb300 import build, rs, workloads
     build.build()
     fmt, recipe, M, comp = PROFILE_CASES[args.profile_case]
-    lin = Linear(torch, rs, workloads, fmt, recipe, M, comp, copies_for_l2=M <= 128)
+    if comp == "kext1":
+        lin = KextLinear(torch, rs, workloads, recipe, M, 1)
+    else:
+        lin = Linear(torch, rs, workloads, fmt, recipe, M, comp, copies_for_l2=M <= 128)
     us, _ = graph_time_us(torch, lin.call, args.steps, reps=1, warm=args.warmup)
     assert rs.rs_get_device_error() == 0
     return {"profile_case": args.profile_case, "us_per_call": round(us, 3), "launches_per_call": lin.launches_per_call()}
@@ -376,21 +429,32 @@ def run_gpu(args) -> dict:
         extra["mxfp4_k5120_n27648"] = mx
         # prefill M=4096, K=N=8192
         pre = {}
-        for comp in (False, True):
-            lin = Linear(torch, rs, workloads, rs.NVFP4, "prefill_k8192", 4096, comp, copies_for_l2=False)
+        w_pre = workloads.make_w("prefill_k8192").to(torch.device("cuda"))
+        variants = [("w4a4", False, 0), ("comp", True, 0), ("kext1", None, 1), ("kext2", None, 2)]
+        for key, comp, k in variants:
+            if k:
+                lin = KextLinear(torch, rs, workloads, "prefill_k8192", 4096, k)
+            else:
+                lin = Linear(torch, rs, workloads, rs.NVFP4, "prefill_k8192", 4096, comp, copies_for_l2=False)
             us, _ = graph_time_us(torch, lin.call, 10, reps=3)
             useful, executed = lin.flops()
-            key = "comp" if comp else "w4a4"
             pre[f"{key}_us"] = round(us, 2)
             pre[f"{key}_useful_tflops"] = round(useful / (us * 1e-6) / 1e12, 1)
             pre[f"{key}_executed_tflops"] = round(executed / (us * 1e-6) / 1e12, 1)
+            lin.call(0)
+            torch.cuda.synchronize()
+            pre[f"{key}_nmse_vs_bf16"] = float(f"{nmse_vs_bf16(torch, lin.x, w_pre, lin.y):.4e}")
             del lin
+        del w_pre
+        pre["kext_rho"] = {"kext1": 0.125, "kext2": 0.25}
         # FP4 dense peak: the measured bf16 peak x the nominal FP4/bf16 ratio (13.5 / 2.25)
         fp4_peak = peaks["bf16_tflops"] * 13.5 / 2.25
         pre["fp4_peak_tflops"] = round(fp4_peak, 1)
         pre["fp4_peak_source"] = f"{peaks['source']} bf16 x 6"
         pre["w4a4_frac"] = round(pre["w4a4_executed_tflops"] / fp4_peak, 4)
         pre["comp_frac"] = round(pre["comp_executed_tflops"] / fp4_peak, 4)
+        for key in ("kext1", "kext2"):
+            pre[f"{key}_frac"] = round(pre[f"{key}_executed_tflops"] / fp4_peak, 4)
         extra["prefill_M4096_K8192_N8192"] = pre
         torch.cuda.empty_cache()
 

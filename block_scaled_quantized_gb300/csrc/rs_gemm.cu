@@ -552,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                     if (g.fold) {
                         float rr[E];
 #pragma unroll
-                        for (int e = 0; e < E; e += 2)  // residue (Alg. 1 line 6)
-                            fsub2_rn(xs[r][e], xs[r][e + 1], xh[e], xh[e + 1], rr[e], rr[e + 1]);
+                        for (int e = 0; e < E; ++e)  // residue (Alg. 1 line 6), never fused
+                            rr[e] = __fsub_rn(xs[r][e], xh[e]);
                         uint32_t sfr, rcodes[E / 8];
                         float rh[E];
                         quant_block<FMT, E, false>(rr, ksc, sfr, rcodes, rh);

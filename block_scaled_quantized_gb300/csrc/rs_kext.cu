@@ -35,8 +35,10 @@ struct KextArgs {
     uint32_t* err;
 };
 
-template <int FMT, int KS>
-__global__ void __launch_bounds__(256) kext_quantize_kernel(KextArgs a) {
+// U > 1: a warp takes U consecutive chunks of one row per step and issues
+// their loads before quantizing any of them (large operands).
+template <int FMT, int KS, int U>
+__global__ void __launch_bounds__(256, U > 1 ? 3 : 1) kext_quantize_kernel(KextArgs a) {
     pdl_wait_prior_grid();
     if (a.early_trigger) pdl_launch_dependents();
     constexpr int BS = block_elems(FMT);
@@ -46,73 +48,83 @@ __global__ void __launch_bounds__(256) kext_quantize_kernel(KextArgs a) {
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps_total = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int chunks = a.K / 256;
-    const int64_t tasks = (int64_t)a.rows * chunks;
+    const int n_cg = (chunks + U - 1) / U;
+    const int64_t tasks = (int64_t)a.rows * n_cg;
     const int Ke = a.K + a.K / 8 * KS;
     const NvScaleConst ksc = nv_scale_const(FMT == 0 ? *a.alpha : 0.0f);
     if (FMT == 0 && blockIdx.x == 0 && threadIdx.x == 0 && !nv_alpha_supported(ksc.alpha))
         atomicExch(a.err, kErrInvalidArg);
 
     for (int64_t task = warp; task < tasks; task += n_warps_total) {
-        const int row = (int)(task / chunks);
-        const int chunk = (int)(task - (int64_t)row * chunks);
-        const int k0 = chunk * 256 + lane * 8;
-        float xf[8];
-        load8_bf16(a.x + (int64_t)row * a.ldx + k0, true, xf);
+        const int row = (int)(task / n_cg);
+        const int cg = (int)(task - (int64_t)row * n_cg);
+        uint4 raw[U];  // the U input words, widened when processed
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            raw[u] = load16_or_zero(a.x + (int64_t)row * a.ldx + (cg * U + u) * 256 + lane * 8, cg * U + u < chunks);
         uint8_t* orow = a.out + (size_t)row * (size_t)(Ke / 2);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int chunk = cg * U + u;
+            if (U > 1 && chunk >= chunks) break;  // ragged last group (warp-uniform)
+            const int k0 = chunk * 256 + lane * 8;
+            float xf[8];
+            unpack8_bf16(raw[u], xf);
 
-        // base operand (Eq. 8-10)
-        uint32_t sfb;
-        float xh[8];
-        const uint32_t codes = quant_lane<FMT, true>(xf, ksc, sfb, xh);
-        const uint32_t sfw = gather_sf_word<FMT>(sfb, lane);
-        *reinterpret_cast<uint32_t*>(orow + k0 / 2) = codes;
-        if (lane % LPA == 0)
-            *reinterpret_cast<uint32_t*>(a.sf + sf_offset(row, (chunk * (256 / atom_k(FMT)) + lane / LPA) * kAtomBlocks,
-                                                          a.n_atoms_k)) = sfw;
+            // base operand (Eq. 8-10)
+            uint32_t sfb;
+            float xh[8];
+            const uint32_t codes = quant_lane<FMT, true>(xf, ksc, sfb, xh);
+            const uint32_t sfw = gather_sf_word<FMT>(sfb, lane);
+            *reinterpret_cast<uint32_t*>(orow + k0 / 2) = codes;
+            if (lane % LPA == 0)
+                *reinterpret_cast<uint32_t*>(a.sf + sf_offset(row, (chunk * (256 / atom_k(FMT)) + lane / LPA) * kAtomBlocks,
+                                                              a.n_atoms_k)) = sfw;
 
-        // the group's selected residues, in channel order (Alg. 1 lines 6-7)
-        float r[8];
-        residue8(xf, xh, r);
-        const int grp = chunk * 32 + lane;
-        const uint32_t m = a.mask[grp];
-        if (__popc(m) != KS) atomicExch(a.err, kErrInvalidArg);  // a mask must keep k channels per group
-        float sel[KS];
-#pragma unroll
-        for (int j = 0; j < KS; ++j) {
-            const uint32_t idx = __fns(m, 0, j + 1);  // position of the (j+1)-th set bit
-            float v = 0.0f;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) v = idx == (uint32_t)t ? r[t] : v;
-            sel[j] = v;
+            // the group's selected residues, in channel order (Alg. 1 lines 6-7)
+            float r[8];
+            residue8(xf, xh, r);
+            const int grp = chunk * 32 + lane;
+            const uint32_t m = a.mask[grp];
+            if (__popc(m) != KS) atomicExch(a.err, kErrInvalidArg);  // a mask must keep k channels per group
+            float sel[KS];
+    #pragma unroll
+            for (int j = 0; j < KS; ++j) {
+                const uint32_t idx = __fns(m, 0, j + 1);  // position of the (j+1)-th set bit
+                float v = 0.0f;
+    #pragma unroll
+                for (int t = 0; t < 8; ++t) v = idx == (uint32_t)t ? r[t] : v;
+                sel[j] = v;
+            }
+            // block amax over the L lanes of this extension block (lines 8-9)
+            float am = 0.0f;
+    #pragma unroll
+            for (int j = 0; j < KS; ++j) am = fmaxf(am, fabsf(sel[j]));
+    #pragma unroll
+            for (int o = 1; o < L; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+            float st, mul;
+            const uint32_t sfr = FMT == 0 ? nv_block_scale_fast(am, ksc, st, mul) : mx_block_scale(am, st, mul);
+            float v8[8];
+    #pragma unroll
+            for (int e = 0; e < 8; ++e) v8[e] = e < KS ? __fmul_rn(sel[e], mul) : 0.0f;
+            const uint32_t rc = e2m1_encode8(v8);  // element j in nibble j
+            const int c = a.K + grp * KS;          // K_eff column of this lane's first extension element
+            if constexpr (KS == 8) {
+                *reinterpret_cast<uint32_t*>(orow + c / 2) = rc;
+            } else if constexpr (KS == 4) {
+                *reinterpret_cast<uint16_t*>(orow + c / 2) = (uint16_t)(rc & 0xFFFFu);
+            } else if constexpr (KS == 2) {
+                orow[c / 2] = (uint8_t)(rc & 0xFFu);
+            } else {
+                const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, rc & 0xFu, 1);
+                if ((lane & 1) == 0) orow[c / 2] = (uint8_t)((rc & 0xFu) | (hi << 4));
+            }
+            if (lane % L == 0) a.sf[sf_offset(row, c / BS, a.n_atoms_k)] = (uint8_t)sfr;
+            // padding blocks of the row's last, partly filled scale atom
+            const int nb = Ke / BS;
+            if (chunk == chunks - 1 && lane < a.n_atoms_k * kAtomBlocks - nb)
+                a.sf[sf_offset(row, nb + lane, a.n_atoms_k)] = 0;
         }
-        // block amax over the L lanes of this extension block (lines 8-9)
-        float am = 0.0f;
-#pragma unroll
-        for (int j = 0; j < KS; ++j) am = fmaxf(am, fabsf(sel[j]));
-#pragma unroll
-        for (int o = 1; o < L; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
-        float st, mul;
-        const uint32_t sfr = FMT == 0 ? nv_block_scale_fast(am, ksc, st, mul) : mx_block_scale(am, st, mul);
-        float v8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v8[e] = e < KS ? __fmul_rn(sel[e], mul) : 0.0f;
-        const uint32_t rc = e2m1_encode8(v8);  // element j in nibble j
-        const int c = a.K + grp * KS;          // K_eff column of this lane's first extension element
-        if constexpr (KS == 8) {
-            *reinterpret_cast<uint32_t*>(orow + c / 2) = rc;
-        } else if constexpr (KS == 4) {
-            *reinterpret_cast<uint16_t*>(orow + c / 2) = (uint16_t)(rc & 0xFFFFu);
-        } else if constexpr (KS == 2) {
-            orow[c / 2] = (uint8_t)(rc & 0xFFu);
-        } else {
-            const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, rc & 0xFu, 1);
-            if ((lane & 1) == 0) orow[c / 2] = (uint8_t)((rc & 0xFu) | (hi << 4));
-        }
-        if (lane % L == 0) a.sf[sf_offset(row, c / BS, a.n_atoms_k)] = (uint8_t)sfr;
-        // padding blocks of the row's last, partly filled scale atom
-        const int nb = Ke / BS;
-        if (chunk == chunks - 1 && lane < a.n_atoms_k * kAtomBlocks - nb)
-            a.sf[sf_offset(row, nb + lane, a.n_atoms_k)] = 0;
     }
 
     // zero scale words of the padding rows [rows, rows_pad)
@@ -137,8 +149,18 @@ __global__ void channel_mean_abs_kernel(const uint16_t* __restrict__ x, int rows
     score[c] = rows > 0 ? s / (float)rows : 0.0f;
 }
 
-template <int FMT, int KS>
-static cudaError_t launch_kext_typed(const KextArgs& a, int grid, cudaStream_t stream, bool pdl) {
+template <int FMT, int KS, int U>
+static cudaError_t launch_kext_typed(const KextArgs& a, int grid, cudaStream_t stream, bool pdl, int num_sms) {
+    if (U > 1) {  // large operands: one wave of resident blocks whose warps loop over the tasks
+        static const int occ = [] {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kext_quantize_kernel<FMT, KS, U>, 256, 0) !=
+                    cudaSuccess || n < 1)
+                n = 1;
+            return n;
+        }();
+        if (grid > num_sms * occ) grid = num_sms * occ;
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
@@ -148,7 +170,7 @@ static cudaError_t launch_kext_typed(const KextArgs& a, int grid, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kext_quantize_kernel<FMT, KS>, a);
+    return cudaLaunchKernelEx(&cfg, kext_quantize_kernel<FMT, KS, U>, a);
 }
 
 cudaError_t launch_quantize_kext(int fmt, int k, int rows, int K, const void* x, int64_t ldx, const float* alpha,
@@ -167,14 +189,18 @@ cudaError_t launch_quantize_kext(int fmt, int k, int rows, int K, const void* x,
     a.n_atoms_k = n_atoms_k_host(fmt, Ke);
     a.early_trigger = pdl ? 1 : 0;
     a.err = device_error_word();
-    const int64_t warps = (int64_t)rows * (K / 256);
+    // chunks per warp step: 4 once every SM has 128 single-chunk warp tasks
+    const int U = (int64_t)rows * (K / 256) >= (int64_t)num_sms * 128 ? 4 : 1;
+    const int64_t warps = (int64_t)rows * ((K / 256 + U - 1) / U);
     int64_t blocks = (warps + 7) / 8;
     const int64_t pad_blocks = ((int64_t)(a.rows_pad - rows) * a.n_atoms_k + 255) / 256;
     if (pad_blocks > blocks) blocks = pad_blocks;
     if (blocks > (int64_t)num_sms * 32) blocks = (int64_t)num_sms * 32;
     const int grid = (int)(blocks < 1 ? 1 : blocks);
 #define RS_KEXT(F, S) \
-    if (fmt == F && k == S) return launch_kext_typed<F, S>(a, grid, stream, pdl);
+    if (fmt == F && k == S)   \
+        return U == 4 ? launch_kext_typed<F, S, 4>(a, grid, stream, pdl, num_sms) \
+                      : launch_kext_typed<F, S, 1>(a, grid, stream, pdl, num_sms);
     RS_KEXT(0, 1) RS_KEXT(0, 2) RS_KEXT(0, 4) RS_KEXT(0, 8)
     RS_KEXT(1, 1) RS_KEXT(1, 2) RS_KEXT(1, 4) RS_KEXT(1, 8)
 #undef RS_KEXT

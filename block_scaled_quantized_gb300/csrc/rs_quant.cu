@@ -19,6 +19,8 @@
 //            atoms, so the GEMM streams each block with a single bulk copy.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "rs_device.cuh"
 #include "rs_internal.h"
 #include "rs_quant_core.cuh"
@@ -29,12 +31,34 @@ namespace rs {
 
 __global__ void tensor_amax_kernel(const uint16_t* __restrict__ x, int64_t n,
                                    uint32_t* __restrict__ amax_bits) {
-    uint32_t m = 0;
+    // |x| as bf16 bits (sign cleared) orders like |x|; two halves per word
+    // are compared at once with an unsigned 16-bit SIMD max.
+    uint32_t m2 = 0;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const uint32_t a = x[i] & 0x7FFFu;  // |x| as bf16 bits; order-preserving
-        m = a > m ? a : m;
+    // elements before the first 16-byte boundary take element loads
+    int64_t head = (int64_t)((16 - (reinterpret_cast<uintptr_t>(x) & 15)) & 15) / 2;
+    if (head > n) head = n;
+    const uint4* v = reinterpret_cast<const uint4*>(x + head);
+    const int64_t nv = (n - head) / 8;
+    int64_t i = tid;
+    for (; i + 3 * stride < nv; i += 4 * stride) {  // four independent 16-byte loads in flight
+        uint4 a[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) a[u] = v[i + u * stride];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            m2 = __vmaxu2(__vmaxu2(m2, a[u].x & 0x7FFF7FFFu),
+                          __vmaxu2(__vmaxu2(a[u].y & 0x7FFF7FFFu, a[u].z & 0x7FFF7FFFu), a[u].w & 0x7FFF7FFFu));
     }
+    for (; i < nv; i += stride) {
+        const uint4 a = v[i];
+        m2 = __vmaxu2(__vmaxu2(m2, a.x & 0x7FFF7FFFu),
+                      __vmaxu2(__vmaxu2(a.y & 0x7FFF7FFFu, a.z & 0x7FFF7FFFu), a.w & 0x7FFF7FFFu));
+    }
+    for (int64_t j = head + nv * 8 + tid; j < n; j += stride) m2 = __vmaxu2(m2, x[j] & 0x7FFFu);
+    for (int64_t j = tid; j < head; j += stride) m2 = __vmaxu2(m2, x[j] & 0x7FFFu);
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const uint32_t t = __shfl_xor_sync(0xFFFFFFFFu, m, o);
@@ -83,8 +107,12 @@ struct QuantArgs {
     const uint8_t* kext_mask;
 };
 
-template <int FMT, int MODE>
-__global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
+// U > 1 (large activation operands): a warp takes U consecutive 256-element
+// chunks of one row per step and issues their U loads before quantizing any
+// of them, so that each lane keeps U x 16 bytes in flight.
+template <int FMT, int MODE, int U>
+__global__ void __launch_bounds__(256, U > 1 ? 3 : 1) quantize_kernel(QuantArgs a) {
+    static_assert(U == 1 || MODE != kWeight, "the weight quantizer takes one chunk per step");
     // Inputs may come from the previous kernel in the stream.
     pdl_wait_prior_grid();
     if (a.early_trigger) pdl_launch_dependents();
@@ -92,75 +120,96 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps_total = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t tasks = (int64_t)a.task_rows * a.chunks;
+    const int n_cg = (a.chunks + U - 1) / U;  // chunk groups per row
+    const int64_t tasks = (int64_t)a.task_rows * n_cg;
     const NvScaleConst ksc = nv_scale_const(FMT == 0 ? *a.alpha : 0.0f);
     if (FMT == 0 && blockIdx.x == 0 && threadIdx.x == 0 && !nv_alpha_supported(ksc.alpha))
         atomicExch(a.err, kErrInvalidArg);
 
-    // task = row * chunks + chunk, advanced by n_warps_total without a division
-    const int dstep_row = (int)(n_warps_total / a.chunks), dstep_chunk = (int)(n_warps_total % a.chunks);
-    int row = (int)(warp / a.chunks), chunk = (int)(warp % a.chunks);
+    // task = row * n_cg + cg, advanced by n_warps_total without a division
+    const int dstep_row = (int)(n_warps_total / n_cg), dstep_cg = (int)(n_warps_total % n_cg);
+    int row = (int)(warp / n_cg), cg = (int)(warp % n_cg);
     for (int64_t task = warp; task < tasks; task += n_warps_total) {
         if (task != warp) {
             row += dstep_row;
-            chunk += dstep_chunk;
-            if (chunk >= a.chunks) {
-                chunk -= a.chunks;
+            cg += dstep_cg;
+            if (cg >= n_cg) {
+                cg -= n_cg;
                 ++row;
             }
         }
-        const int k0 = chunk * 256 + lane * 8;
-        const bool valid = k0 < a.K && row < a.rows;
-        float xf[8];
-        if (MODE == kWeight && a.kext_k > 0 && k0 >= a.k_base) {
-            // appended columns of the extended weight: gathered
+        uint4 raw[U];  // the U input words, widened when processed
+        float xw[8];   // the weight path's gathered extension columns
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = k0 - a.k_base + i;
-                float v = 0.0f;
-                if (row < a.rows && e < a.K - a.k_base) {
-                    const int grp = e / a.kext_k;
-                    const uint32_t t = __fns(a.kext_mask[grp], 0, e - grp * a.kext_k + 1);
-                    if (t < 8u) v = __uint_as_float((uint32_t)a.x[(int64_t)row * a.ldx + 8 * grp + (int)t] << 16);
-                    else atomicExch(a.err, kErrInvalidArg);  // fewer than k channels in the group
+        for (int u = 0; u < U; ++u) {
+            const int chunk = cg * U + u;
+            const int k0 = chunk * 256 + lane * 8;
+            if (MODE == kWeight && a.kext_k > 0 && k0 >= a.k_base) {
+                // appended columns of the extended weight: gathered
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = k0 - a.k_base + i;
+                    float v = 0.0f;
+                    if (row < a.rows && e < a.K - a.k_base) {
+                        const int grp = e / a.kext_k;
+                        const uint32_t t = __fns(a.kext_mask[grp], 0, e - grp * a.kext_k + 1);
+                        if (t < 8u) v = __uint_as_float((uint32_t)a.x[(int64_t)row * a.ldx + 8 * grp + (int)t] << 16);
+                        else atomicExch(a.err, kErrInvalidArg);  // fewer than k channels in the group
+                    }
+                    xw[i] = v;
                 }
-                xf[i] = v;
+                raw[u] = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                raw[u] = load16_or_zero(a.x + (int64_t)row * a.ldx + k0, k0 < a.K && row < a.rows);
             }
-        } else {
-            load8_bf16(a.x + (int64_t)row * a.ldx + k0, valid, xf);
         }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int chunk = cg * U + u;
+            if (U > 1 && chunk >= a.chunks) break;  // ragged last group (warp-uniform)
+            const int k0 = chunk * 256 + lane * 8;
+            const bool valid = k0 < a.K && row < a.rows;
+            float xf[8];
+            if (MODE == kWeight && a.kext_k > 0 && k0 >= a.k_base) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) xf[i] = xw[i];
+            } else {
+                unpack8_bf16(raw[u], xf);
+            }
 
-        uint32_t sfb;
-        float xh[8];
-        const uint32_t codes = quant_lane<FMT, MODE == kPaired>(xf, ksc, sfb, xh);
-        const uint32_t sfw = gather_sf_word<FMT>(sfb, lane);
-        const int g = chunk * (256 / atom_k(FMT)) + lane / LPA;  // atom index along K
-        const bool leader = (lane % LPA) == 0;
+            uint32_t sfb;
+            float xh[8];
+            const uint32_t codes = quant_lane<FMT, MODE == kPaired>(xf, ksc, sfb, xh);
+            const uint32_t sfw = gather_sf_word<FMT>(sfb, lane);
+            const int g = chunk * (256 / atom_k(FMT)) + lane / LPA;  // atom index along K
+            const bool leader = (lane % LPA) == 0;
 
-        if (MODE == kWeight) {
-            const int t = row / 128, r = row % 128;
-            uint8_t* blk = a.out + ((size_t)t * a.chunks + chunk) * weight_block_bytes(FMT);
-            *reinterpret_cast<uint32_t*>(blk + sw128_offset((uint32_t)r, (uint32_t)lane * 4u)) = codes;
-            if (leader)
-                *reinterpret_cast<uint32_t*>(blk + kWeightCodeBytes + (lane / LPA) * kAtomBytes + (r % 32) * 16 +
-                                             ((r / 32) % 4) * 4) = sfw;
-        } else {
-            const int out_row = MODE == kPaired ? 2 * row : row;
-            if (valid)
-                *reinterpret_cast<uint32_t*>(a.out + (size_t)out_row * (a.K / 2) + k0 / 2) = codes;
-            if (leader && g < a.n_atoms_k)
-                *reinterpret_cast<uint32_t*>(a.sf + sf_offset(out_row, g * kAtomBlocks, a.n_atoms_k)) = sfw;
-            if (MODE == kPaired) {
-                float r[8];
-                residue8(xf, xh, r);
-                uint32_t sfr;
-                float rh[8];
-                const uint32_t rcodes = quant_lane<FMT, false>(r, ksc, sfr, rh);
-                const uint32_t sfrw = gather_sf_word<FMT>(sfr, lane);
+            if (MODE == kWeight) {
+                const int t = row / 128, r = row % 128;
+                uint8_t* blk = a.out + ((size_t)t * a.chunks + chunk) * weight_block_bytes(FMT);
+                *reinterpret_cast<uint32_t*>(blk + sw128_offset((uint32_t)r, (uint32_t)lane * 4u)) = codes;
+                if (leader)
+                    *reinterpret_cast<uint32_t*>(blk + kWeightCodeBytes + (lane / LPA) * kAtomBytes + (r % 32) * 16 +
+                                                 ((r / 32) % 4) * 4) = sfw;
+            } else {
+                const int out_row = MODE == kPaired ? 2 * row : row;
                 if (valid)
-                    *reinterpret_cast<uint32_t*>(a.out + (size_t)(out_row + 1) * (a.K / 2) + k0 / 2) = rcodes;
+                    *reinterpret_cast<uint32_t*>(a.out + (size_t)out_row * (a.K / 2) + k0 / 2) = codes;
                 if (leader && g < a.n_atoms_k)
-                    *reinterpret_cast<uint32_t*>(a.sf + sf_offset(out_row + 1, g * kAtomBlocks, a.n_atoms_k)) = sfrw;
+                    *reinterpret_cast<uint32_t*>(a.sf + sf_offset(out_row, g * kAtomBlocks, a.n_atoms_k)) = sfw;
+                if (MODE == kPaired) {
+                    float r[8];
+                    residue8(xf, xh, r);
+                    uint32_t sfr;
+                    float rh[8];
+                    const uint32_t rcodes = quant_lane<FMT, false>(r, ksc, sfr, rh);
+                    const uint32_t sfrw = gather_sf_word<FMT>(sfr, lane);
+                    if (valid)
+                        *reinterpret_cast<uint32_t*>(a.out + (size_t)(out_row + 1) * (a.K / 2) + k0 / 2) = rcodes;
+                    if (leader && g < a.n_atoms_k)
+                        *reinterpret_cast<uint32_t*>(a.sf + sf_offset(out_row + 1, g * kAtomBlocks, a.n_atoms_k)) =
+                            sfrw;
+                }
             }
         }
     }
@@ -178,7 +227,125 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
     }
 }
 
+// ------------------------------------------- NVFP4, one block per lane --
+//
+// Large NVFP4 activation operands (ROWS / PAIRED, K a multiple of 512): lane
+// l of a warp quantizes the whole 16-element block 16l..16l+15 of a
+// 512-element chunk, so each block scale is derived once (not on both lanes
+// of a block pair), its amax is taken on the packed bf16 bits, and s~ and
+// fl(1/s~) come from a per-CTA table of the 127 finite E4M3 bytes.  Same
+// arithmetic per element as quant_lane (Eq. 8-10, Alg. 1), identical codes
+// and scale bytes.  U chunks per warp step, loads first.
+template <int MODE, int U>
+__global__ void __launch_bounds__(256, 3) quantize_nv_wide_kernel(QuantArgs a) {
+    __shared__ float tab_st[128], tab_mul[128];
+    pdl_wait_prior_grid();
+    if (a.early_trigger) pdl_launch_dependents();
+    const NvScaleConst ksc = nv_scale_const(*a.alpha);
+    if (threadIdx.x < 128) nv_scale_table_entry(threadIdx.x, ksc.alpha, tab_st[threadIdx.x], tab_mul[threadIdx.x]);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && !nv_alpha_supported(ksc.alpha)) atomicExch(a.err, kErrInvalidArg);
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t n_warps_total = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int chunks = a.K / 512;
+    const int n_cg = (chunks + U - 1) / U;
+    const int64_t tasks = (int64_t)a.rows * n_cg;
+    const int dstep_row = (int)(n_warps_total / n_cg), dstep_cg = (int)(n_warps_total % n_cg);
+    int row = (int)(warp / n_cg), cg = (int)(warp % n_cg);
+    for (int64_t task = warp; task < tasks; task += n_warps_total) {
+        if (task != warp) {
+            row += dstep_row;
+            cg += dstep_cg;
+            if (cg >= n_cg) {
+                cg -= n_cg;
+                ++row;
+            }
+        }
+        const uint16_t* xrow = a.x + (int64_t)row * a.ldx + lane * 16;
+        uint4 raw[U][2];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool ok = cg * U + u < chunks;
+            raw[u][0] = load16_or_zero(xrow + (cg * U + u) * 512, ok);
+            raw[u][1] = load16_or_zero(xrow + (cg * U + u) * 512 + 8, ok);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int chunk = cg * U + u;
+            if (U > 1 && chunk >= chunks) break;  // ragged last group (warp-uniform)
+            const uint32_t w[8] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
+                                   raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
+            const uint32_t sf = nv_block_byte(amax16_bf16(w), ksc);
+            const float st = tab_st[sf], mul = tab_mul[sf];
+            float xf[16];
+            unpack8_bf16(raw[u][0], *reinterpret_cast<float(*)[8]>(&xf[0]));
+            unpack8_bf16(raw[u][1], *reinterpret_cast<float(*)[8]>(&xf[8]));
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) fmul2_rn(xf[e], xf[e + 1], mul, mul, v[e], v[e + 1]);
+            const uint32_t c0 = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[0]));
+            const uint32_t c1 = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[8]));
+            // the atom row word of blocks 4j..4j+3 lands on lane 4j
+            uint32_t t = sf | (__shfl_down_sync(0xFFFFFFFFu, sf, 1) << 8);
+            const uint32_t sfw = t | (__shfl_down_sync(0xFFFFFFFFu, t, 2) << 16);
+            const int out_row = MODE == kPaired ? 2 * row : row;
+            const size_t code_off = (size_t)chunk * 256 + (size_t)lane * 8;
+            *reinterpret_cast<uint2*>(a.out + (size_t)out_row * (a.K / 2) + code_off) = make_uint2(c0, c1);
+            if ((lane & 3) == 0)
+                *reinterpret_cast<uint32_t*>(a.sf + sf_offset(out_row, chunk * 32 + lane, a.n_atoms_k)) = sfw;
+            if (MODE == kPaired) {
+                // residue r = fl(x - fl(s~ dec(q))), quantized with its own block scale
+                float d[16], r[16];
+                e2m1_decode8(c0, *reinterpret_cast<float(*)[8]>(&d[0]));
+                e2m1_decode8(c1, *reinterpret_cast<float(*)[8]>(&d[8]));
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r[e] = __fsub_rn(xf[e], __fmul_rn(st, d[e]));  // never fused
+                float am = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(r[e]));
+                const uint32_t sfr = nv_block_byte(am, ksc);
+                const float mulr = tab_mul[sfr];
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) fmul2_rn(r[e], r[e + 1], mulr, mulr, v[e], v[e + 1]);
+                const uint32_t r0 = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[0]));
+                const uint32_t r1 = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[8]));
+                t = sfr | (__shfl_down_sync(0xFFFFFFFFu, sfr, 1) << 8);
+                const uint32_t sfrw = t | (__shfl_down_sync(0xFFFFFFFFu, t, 2) << 16);
+                *reinterpret_cast<uint2*>(a.out + (size_t)(out_row + 1) * (a.K / 2) + code_off) = make_uint2(r0, r1);
+                if ((lane & 3) == 0)
+                    *reinterpret_cast<uint32_t*>(a.sf + sf_offset(out_row + 1, chunk * 32 + lane, a.n_atoms_k)) =
+                        sfrw;
+            }
+        }
+    }
+
+    // zero scale words of the padding rows [rows_out, rows_pad)
+    const int64_t pad_words = (int64_t)(a.rows_pad - a.rows_out) * a.n_atoms_k;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = tid; i < pad_words; i += nthreads) {
+        const int r = a.rows_out + (int)(i / a.n_atoms_k);
+        const int g = (int)(i % a.n_atoms_k);
+        *reinterpret_cast<uint32_t*>(a.sf + sf_offset(r, g * kAtomBlocks, a.n_atoms_k)) = 0u;
+    }
+}
+
 // ---------------------------------------------------------------- launch --
+
+// Blocks of 256 threads (no dynamic shared memory) of `kernel` that one SM
+// holds at once.
+template <typename Kern>
+static int resident_blocks_per_sm(Kern kernel) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1) n = 1;
+    return n;
+}
+
+// Chunks per warp step: 4 once every SM has at least 128 warp tasks of one
+// chunk to share, else 1 (small operands need every warp they can get).
+static int quant_unroll(int64_t chunk_tasks, int num_sms) { return chunk_tasks >= (int64_t)num_sms * 128 ? 4 : 1; }
 
 static int quant_grid(int64_t warps_needed, int64_t pad_words, int num_sms) {
     int64_t blocks = (warps_needed + 7) / 8;
@@ -194,8 +361,11 @@ cudaError_t launch_tensor_scale(const void* x, int64_t n, float* alpha, uint32_t
     cudaError_t e = cudaMemsetAsync(alpha, 0, sizeof(float), stream);
     if (e != cudaSuccess) return e;
     if (n > 0) {
-        int64_t blocks = (n + 1023) / 1024;
-        if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+        // one wave of resident blocks, each thread looping (no partial last wave)
+        static const int occ = resident_blocks_per_sm(tensor_amax_kernel);
+        int64_t blocks = (n / 8 + 255) / 256;
+        if (blocks > (int64_t)num_sms * occ) blocks = (int64_t)num_sms * occ;
+        if (blocks < 1) blocks = 1;
         tensor_amax_kernel<<<(int)blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), n,
                                                              reinterpret_cast<uint32_t*>(alpha));
         e = cudaGetLastError();
@@ -205,8 +375,12 @@ cudaError_t launch_tensor_scale(const void* x, int64_t n, float* alpha, uint32_t
     return cudaGetLastError();
 }
 
-template <int FMT, int MODE>
-static cudaError_t launch_quant_typed(const QuantArgs& a, int grid, cudaStream_t stream, bool pdl) {
+template <int FMT, int MODE, int U>
+static cudaError_t launch_quant_typed(const QuantArgs& a, int grid, cudaStream_t stream, bool pdl, int num_sms) {
+    if (U > 1) {  // large operands: one wave of resident blocks whose warps loop over the tasks
+        static const int occ = resident_blocks_per_sm(quantize_kernel<FMT, MODE, U>);
+        if (grid > num_sms * occ) grid = num_sms * occ;
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
@@ -217,12 +391,13 @@ static cudaError_t launch_quant_typed(const QuantArgs& a, int grid, cudaStream_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, quantize_kernel<FMT, MODE>, a);
+    return cudaLaunchKernelEx(&cfg, quantize_kernel<FMT, MODE, U>, a);
 }
 
-template <int MODE>
-static cudaError_t launch_mode(int fmt, const QuantArgs& a, int grid, cudaStream_t stream, bool pdl) {
-    return fmt == 0 ? launch_quant_typed<0, MODE>(a, grid, stream, pdl) : launch_quant_typed<1, MODE>(a, grid, stream, pdl);
+template <int MODE, int U = 1>
+static cudaError_t launch_mode(int fmt, const QuantArgs& a, int grid, cudaStream_t stream, bool pdl, int num_sms) {
+    return fmt == 0 ? launch_quant_typed<0, MODE, U>(a, grid, stream, pdl, num_sms)
+                    : launch_quant_typed<1, MODE, U>(a, grid, stream, pdl, num_sms);
 }
 
 cudaError_t launch_quantize(int fmt, bool paired, int rows, int K, const void* x, int64_t ldx, const float* alpha,
@@ -242,10 +417,33 @@ cudaError_t launch_quantize(int fmt, bool paired, int rows, int K, const void* x
     a.out = static_cast<uint8_t*>(q_out);
     a.sf = static_cast<uint8_t*>(q_out) + operand_sf_offset(fmt, a.rows_out, K);
     a.early_trigger = pdl ? 1 : 0;
-    const int64_t warps = (int64_t)rows * a.chunks;
+    if (fmt == 0 && K % 512 == 0 && (int64_t)rows * a.chunks >= (int64_t)num_sms * 128) {
+        // large NVFP4 operand: one scale block per lane, one wave of resident CTAs
+        static const int occ_rows = resident_blocks_per_sm(quantize_nv_wide_kernel<kRows, 2>);
+        static const int occ_paired = resident_blocks_per_sm(quantize_nv_wide_kernel<kPaired, 2>);
+        const int64_t warps = (int64_t)rows * ((K / 512 + 1) / 2);
+        int grid = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)num_sms * (paired ? occ_paired : occ_rows));
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)std::max(grid, 1), 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return paired ? cudaLaunchKernelEx(&cfg, quantize_nv_wide_kernel<kPaired, 2>, a)
+                      : cudaLaunchKernelEx(&cfg, quantize_nv_wide_kernel<kRows, 2>, a);
+    }
+    const int U = quant_unroll((int64_t)rows * a.chunks, num_sms);
+    const int64_t warps = (int64_t)rows * ((a.chunks + U - 1) / U);
     const int64_t pad_words = (int64_t)(a.rows_pad - a.rows_out) * a.n_atoms_k;
     const int grid = quant_grid(warps, pad_words, num_sms);
-    return paired ? launch_mode<kPaired>(fmt, a, grid, stream, pdl) : launch_mode<kRows>(fmt, a, grid, stream, pdl);
+    if (U == 4)
+        return paired ? launch_mode<kPaired, 4>(fmt, a, grid, stream, pdl, num_sms)
+                      : launch_mode<kRows, 4>(fmt, a, grid, stream, pdl, num_sms);
+    return paired ? launch_mode<kPaired>(fmt, a, grid, stream, pdl, num_sms)
+                  : launch_mode<kRows>(fmt, a, grid, stream, pdl, num_sms);
 }
 
 cudaError_t launch_quantize_weight(int fmt, int N, int K, const void* w, int64_t ldw, const float* alpha,
@@ -270,7 +468,7 @@ cudaError_t launch_quantize_weight(int fmt, int N, int K, const void* w, int64_t
     a.out = static_cast<uint8_t*>(wq_out);
     const int64_t warps = (int64_t)a.task_rows * a.chunks;
     const int grid = quant_grid(warps, 0, num_sms);
-    return launch_mode<kWeight>(fmt, a, grid, stream, false);
+    return launch_mode<kWeight>(fmt, a, grid, stream, false, num_sms);
 }
 
 }  // namespace rs

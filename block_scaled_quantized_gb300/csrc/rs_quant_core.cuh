@@ -73,6 +73,36 @@ __device__ __forceinline__ uint32_t nv_block_scale_fast(float amax, const NvScal
     return sf;
 }
 
+// The byte of nv_block_scale_fast alone (the caller looks up s~ and fl(1/s~)
+// for it, e.g. in a table built with nv_scale_table_entry).
+__device__ __forceinline__ uint32_t nv_block_byte(float amax, const NvScaleConst& k) {
+    float st, mul;
+    if (!k.fast || !(amax >= 0x1p-123f)) return nv_block_scale(amax, k.alpha, st, mul);
+    const float t = __fmul_rn(amax, k.c);
+    if (!(t < 448.0f)) return 0x7Eu;
+    const uint32_t pr = e4m3x2_encode_hw(__fmul_rn(t, 1.0f - 0x1p-20f), __fmul_rn(t, 1.0f + 0x1p-20f));
+    const uint32_t sf = pr & 0xFFu;
+    if (sf != (pr >> 8)) return nv_block_scale(amax, k.alpha, st, mul);
+    return sf;
+}
+
+// s~ = fl(alpha * dec(byte)) and mul = fl(1/s~) (0 when s~ == 0) for one of
+// the 127 finite non-negative E4M3 bytes: the values nv_block_scale gives.
+__device__ __forceinline__ void nv_scale_table_entry(uint32_t byte, float alpha, float& st, float& mul) {
+    st = byte < 127u ? __fmul_rn(alpha, e4m3_decode_hw(byte)) : 0.0f;
+    mul = st == 0.0f ? 0.0f : __frcp_rn(st);
+}
+
+// max(|x|) over the sixteen bf16 values of eight words, ignoring NaN like
+// fmaxf and starting from +0 (bf16 -> fp32 is exact, so the order is the
+// fp32 one); two values per max.bf16x2.
+__device__ __forceinline__ float amax16_bf16(const uint32_t (&w)[8]) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) asm("max.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(w[i] & 0x7FFF7FFFu));
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+
 // MXFP4 block scale: byte = max(E - 2, 0) where E is the biased fp32
 // exponent of amax, i.e. e = floor(log2 amax) - 2 clamped at -127 (amax == 0
 // and fp32-subnormal amax give byte 0).  st = 2^e, mul = 2^-e, both exact.
@@ -112,15 +142,18 @@ __device__ __forceinline__ uint32_t quant_lane(const float (&xf)[8], const NvSca
         float d[8];
         e2m1_decode8(codes, d);
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) fmul2_rn(st, st, d[e], d[e + 1], xh[e], xh[e + 1]);
+        for (int e = 0; e < 8; ++e) xh[e] = __fmul_rn(st, d[e]);
     }
     return codes;
 }
 
-// Residue of this lane's eight values, r = fl(x - x^) (Alg. 1 line 6).
+// Residue of this lane's eight values, r = fl(x - x^) (Alg. 1 line 6).  The
+// reconstruction and the residue use the scalar round-to-nearest intrinsics,
+// which are never merged into a multiply-add: a fused x - s~ dec(q) rounds
+// once and can move a residue code across an E2M1 rounding boundary.
 __device__ __forceinline__ void residue8(const float (&xf)[8], const float (&xh)[8], float (&r)[8]) {
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) fsub2_rn(xf[e], xf[e + 1], xh[e], xh[e + 1], r[e], r[e + 1]);
+    for (int e = 0; e < 8; ++e) r[e] = __fsub_rn(xf[e], xh[e]);
 }
 
 // Gather the four scale bytes of one atom row (4 consecutive blocks) into the
@@ -169,9 +202,24 @@ __device__ __forceinline__ void quant_block(const float (&xf)[E], const NvScaleC
             float d[8];
             e2m1_decode8(codes[w], d);
 #pragma unroll
-            for (int e = 0; e < 8; e += 2) fmul2_rn(st, st, d[e], d[e + 1], xh[8 * w + e], xh[8 * w + e + 1]);
+            for (int e = 0; e < 8; ++e) xh[8 * w + e] = __fmul_rn(st, d[e]);
         }
     }
+}
+
+// Eight bf16 values (one 16-byte word) widened to fp32.
+__device__ __forceinline__ void unpack8_bf16(const uint4& v, float (&xf)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        xf[2 * i] = __uint_as_float(w[i] << 16);
+        xf[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// The 16-byte word at p, or zeros when !valid.
+__device__ __forceinline__ uint4 load16_or_zero(const uint16_t* p, bool valid) {
+    return valid ? *reinterpret_cast<const uint4*>(p) : make_uint4(0u, 0u, 0u, 0u);
 }
 
 // Load eight bf16 values (16 bytes) as fp32, or zeros when !valid.

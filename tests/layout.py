@@ -42,14 +42,12 @@ def padding_sf_bytes(buf, fmt, rows, K):
     na = n_atoms_k(fmt, K)
     rows_pad = (rows + 127) // 128 * 128
     nb = K // block_size(fmt)
-    out = []
-    for r in range(rows_pad):
-        for b in range(na * 4):
-            if r < rows and b < nb:
-                continue
-            atom = (r // 128) * na + b // 4
-            out.append(buf[off + atom * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)])
-    return np.array(out, np.uint8)
+    r = np.arange(rows_pad)[:, None]
+    b = np.arange(na * 4)[None, :]
+    pad = (r >= rows) | (b >= nb)
+    atom = (r // 128) * na + b // 4
+    idx = off + atom * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (b % 4)
+    return buf[idx[pad]]
 
 
 def weight_block_bytes(fmt):

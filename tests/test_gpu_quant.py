@@ -185,3 +185,37 @@ def test_unsupported_tensor_scale_flagged(alpha):
     assert rs.rs_get_device_error() == rs.RS_ERR_INVALID_ARG
     gpu_quantize(0, x.to(DEV), torch.tensor([2.0 ** -117], dtype=torch.float32, device=DEV), True)
     assert rs.rs_get_device_error() == 0
+
+
+# Large NVFP4 operands (rows x K/256 >= 128 per SM, K a multiple of 512) take
+# the quantizer that derives each block scale on one lane: the same codes and
+# scale bytes, checked on every row, with ragged row tiles, a chunk group
+# whose second half is past K, sub-normal and huge values, and the full bf16
+# amax sweep.
+@pytest.mark.parametrize("paired", [False, True])
+@pytest.mark.parametrize("rows,K", [(700, 8192), (3300, 1536)])
+def test_quantizer_large_nvfp4_operand(paired, rows, K):
+    x = workloads.make_x("prefill_k8192", rows, K=K, seed=rows + K)
+    x[1, :16] = 0.0
+    x[2, :16] = -0.0
+    x[3, 16] = 1e-40                     # bf16 sub-normal
+    x[3, 17] = 3e30
+    x[4, 32:64] = 1.0
+    _check(0, x, paired)
+
+
+@pytest.mark.parametrize("alpha", [1.0, 0.012345678, 2.0 ** -117, 3.0e37])
+def test_nvfp4_scale_every_bf16_amax_large_operand(alpha):
+    K = 4096
+    amax_bits = torch.arange(1, 0x7F80, dtype=torch.int32)
+    nblk = (amax_bits.numel() + K // 16 - 1) // (K // 16) * (K // 16)
+    amax = torch.zeros(nblk, dtype=torch.int32)
+    amax[: amax_bits.numel()] = amax_bits
+    amax = amax.to(torch.int16).view(torch.bfloat16).float()
+    g = torch.Generator().manual_seed(7)
+    blocks = amax[:, None] * (torch.rand((nblk, 16), generator=g) * 2.0 - 1.0)
+    blocks[:, 0] = amax
+    sign = torch.where(torch.rand((nblk, 16), generator=g) < 0.5, -1.0, 1.0)
+    x = (blocks * sign).to(torch.bfloat16).reshape(-1, K)
+    x = torch.cat([x.roll(i, dims=1) for i in range(10)])    # 1280 rows: the large-operand quantizer
+    _check(0, x, True, alpha=np.float32(alpha))
