@@ -166,3 +166,28 @@ def test_kext_full_prefill_shape_sampled_rows():
     xb = workloads.bf16_bits(x[torch.from_numpy(rows)])
     ref = oracle.linear_kext(0, xb, k, mask, ax.cpu().numpy()[0], wp["cw"], wp["sw"], wp["aw_or"])
     assert_close_f32(y[torch.from_numpy(rows).to(DEV)], ref)
+
+
+# Large NVFP4 operands (rows x K/256 >= 128 per SM, K a multiple of 512)
+# take the quantizer with one 16-element base block (two selection groups)
+# per lane: the extended operand must be the same, bit for bit, on every row.
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
+@pytest.mark.parametrize("rows,K", [(700, 8192), (3300, 1536)])
+def test_extended_operand_bit_exact_large(k, rows, K):
+    import oracle
+    x = workloads.make_x("prefill_k8192", rows, K=K, seed=rows + k)
+    mask = _mask(x[:256], k, rows + k)
+    xb = workloads.bf16_bits(x)
+    a_or = oracle.tensor_scale(xb)
+    Ke = K + rs.rs_kext_width(K, k)
+    buf = torch.full((rs.rs_kext_act_bytes(0, rows, K, k),), 0xAB, dtype=torch.uint8, device=DEV)
+    rs.rs_quantize_kext(0, x.to(DEV), k, torch.tensor([a_or], dtype=torch.float32, device=DEV),
+                        torch.from_numpy(mask).to(DEV), buf)
+    torch.cuda.synchronize()
+    assert rs.rs_get_device_error() == 0
+    host = buf.cpu().numpy()
+    codes, sf = layout.unpack_operand(host, 0, rows, Ke)
+    cx, sx = oracle.quantize_kext(0, xb, k, mask, a_or)
+    np.testing.assert_array_equal(codes, cx)
+    np.testing.assert_array_equal(sf, sx)
+    assert not np.any(layout.padding_sf_bytes(host, 0, rows, Ke))
