@@ -227,6 +227,46 @@ __global__ void __launch_bounds__(256, U > 1 ? 3 : 1) quantize_kernel(QuantArgs 
     }
 }
 
+// NVFP4, one whole 16-element block held as two raw bf16 words: base codes
+// (two words, element e in bits 4(e%8).. of word e/8) and scale byte, and,
+// when `resid`, the residue's codes and scale byte (Eq. 8-10, Alg. 1).
+// s~ and fl(1/s~) come from a table of the 127 finite E4M3 bytes built with
+// nv_scale_table_entry; the block amax is taken on the packed bf16 bits.
+// Same codes and bytes as quant_block; the reconstruction and the residue use
+// the never-fused scalar intrinsics.
+__device__ __forceinline__ void nv_quant16(const uint4 (&raw)[2], const NvScaleConst& k, const float* tab_st,
+                                           const float* tab_mul, bool resid, uint32_t (&cb)[2], uint32_t& sfb,
+                                           uint32_t (&cr)[2], uint32_t& sfr) {
+    const uint32_t w[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
+    sfb = nv_block_byte(amax16_bf16(w), k);
+    const float st = tab_st[sfb], mul = tab_mul[sfb];
+    float xf[16], v[16];
+    unpack8_bf16(raw[0], *reinterpret_cast<float(*)[8]>(&xf[0]));
+    unpack8_bf16(raw[1], *reinterpret_cast<float(*)[8]>(&xf[8]));
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) fmul2_rn(xf[e], xf[e + 1], mul, mul, v[e], v[e + 1]);
+    cb[0] = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[0]));
+    cb[1] = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[8]));
+    if (!resid) return;
+    float d[16];
+    e2m1_decode8(cb[0], *reinterpret_cast<float(*)[8]>(&d[0]));
+    e2m1_decode8(cb[1], *reinterpret_cast<float(*)[8]>(&d[8]));
+#pragma unroll
+    for (int e = 0; e < 16; ++e) xf[e] = __fsub_rn(xf[e], __fmul_rn(st, d[e]));  // r = fl(x - fl(s~ dec(q)))
+    float am0 = 0.0f, am1 = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+        am0 = fmaxf(am0, fabsf(xf[e]));
+        am1 = fmaxf(am1, fabsf(xf[e + 1]));
+    }
+    sfr = nv_block_byte(fmaxf(am0, am1), k);
+    const float mulr = tab_mul[sfr];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) fmul2_rn(xf[e], xf[e + 1], mulr, mulr, v[e], v[e + 1]);
+    cr[0] = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[0]));
+    cr[1] = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[8]));
+}
+
 // ------------------------------------------- NVFP4, one block per lane --
 //
 // Large NVFP4 activation operands (ROWS / PAIRED, K a multiple of 512): lane
@@ -275,45 +315,21 @@ __global__ void __launch_bounds__(256, 3) quantize_nv_wide_kernel(QuantArgs a) {
         for (int u = 0; u < U; ++u) {
             const int chunk = cg * U + u;
             if (U > 1 && chunk >= chunks) break;  // ragged last group (warp-uniform)
-            const uint32_t w[8] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w,
-                                   raw[u][1].x, raw[u][1].y, raw[u][1].z, raw[u][1].w};
-            const uint32_t sf = nv_block_byte(amax16_bf16(w), ksc);
-            const float st = tab_st[sf], mul = tab_mul[sf];
-            float xf[16];
-            unpack8_bf16(raw[u][0], *reinterpret_cast<float(*)[8]>(&xf[0]));
-            unpack8_bf16(raw[u][1], *reinterpret_cast<float(*)[8]>(&xf[8]));
-            float v[16];
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) fmul2_rn(xf[e], xf[e + 1], mul, mul, v[e], v[e + 1]);
-            const uint32_t c0 = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[0]));
-            const uint32_t c1 = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[8]));
+            uint32_t c[2], rc[2], sf, sfr = 0;
+            nv_quant16(raw[u], ksc, tab_st, tab_mul, MODE == kPaired, c, sf, rc, sfr);
             // the atom row word of blocks 4j..4j+3 lands on lane 4j
             uint32_t t = sf | (__shfl_down_sync(0xFFFFFFFFu, sf, 1) << 8);
             const uint32_t sfw = t | (__shfl_down_sync(0xFFFFFFFFu, t, 2) << 16);
             const int out_row = MODE == kPaired ? 2 * row : row;
             const size_t code_off = (size_t)chunk * 256 + (size_t)lane * 8;
-            *reinterpret_cast<uint2*>(a.out + (size_t)out_row * (a.K / 2) + code_off) = make_uint2(c0, c1);
+            *reinterpret_cast<uint2*>(a.out + (size_t)out_row * (a.K / 2) + code_off) = make_uint2(c[0], c[1]);
             if ((lane & 3) == 0)
                 *reinterpret_cast<uint32_t*>(a.sf + sf_offset(out_row, chunk * 32 + lane, a.n_atoms_k)) = sfw;
             if (MODE == kPaired) {
-                // residue r = fl(x - fl(s~ dec(q))), quantized with its own block scale
-                float d[16], r[16];
-                e2m1_decode8(c0, *reinterpret_cast<float(*)[8]>(&d[0]));
-                e2m1_decode8(c1, *reinterpret_cast<float(*)[8]>(&d[8]));
-#pragma unroll
-                for (int e = 0; e < 16; ++e) r[e] = __fsub_rn(xf[e], __fmul_rn(st, d[e]));  // never fused
-                float am = 0.0f;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) am = fmaxf(am, fabsf(r[e]));
-                const uint32_t sfr = nv_block_byte(am, ksc);
-                const float mulr = tab_mul[sfr];
-#pragma unroll
-                for (int e = 0; e < 16; e += 2) fmul2_rn(r[e], r[e + 1], mulr, mulr, v[e], v[e + 1]);
-                const uint32_t r0 = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[0]));
-                const uint32_t r1 = e2m1_encode8(*reinterpret_cast<const float(*)[8]>(&v[8]));
                 t = sfr | (__shfl_down_sync(0xFFFFFFFFu, sfr, 1) << 8);
                 const uint32_t sfrw = t | (__shfl_down_sync(0xFFFFFFFFu, t, 2) << 16);
-                *reinterpret_cast<uint2*>(a.out + (size_t)(out_row + 1) * (a.K / 2) + code_off) = make_uint2(r0, r1);
+                *reinterpret_cast<uint2*>(a.out + (size_t)(out_row + 1) * (a.K / 2) + code_off) =
+                    make_uint2(rc[0], rc[1]);
                 if ((lane & 3) == 0)
                     *reinterpret_cast<uint32_t*>(a.sf + sf_offset(out_row + 1, chunk * 32 + lane, a.n_atoms_k)) =
                         sfrw;
