@@ -125,12 +125,13 @@ class Linear:
     """One prepared linear layer (weights quantized on the GPU, rotated copies)."""
 
     def __init__(self, torch, rs, workloads, fmt, recipe, M, compensated, copies_for_l2=True,
-                 out_dtype=None, seed=None):
+                 out_dtype=None, seed=None, N=None, K=None, w=None):
         self.torch, self.rs = torch, rs
         dev = torch.device("cuda")
         self.fmt, self.M, self.compensated = fmt, M, compensated
-        x = workloads.make_x(recipe, M, seed=seed)
-        w = workloads.make_w(recipe, seed=seed)
+        x = workloads.make_x(recipe, M, K=K, seed=seed)
+        if w is None:
+            w = workloads.make_w(recipe, N=N, K=K, seed=seed)
         self.N, self.K = w.shape
         self.x_host = x
         self.x = x.to(dev)
@@ -256,6 +257,28 @@ def nmse_vs_bf16(torch, x, w, y) -> float:
     operands (an accuracy figure beside the timing, not a parity check)."""
     ref = x.float() @ w.float().t()
     return float(((y.float() - ref) ** 2).sum() / (ref ** 2).sum())
+
+
+def shape_sweep(torch, rs, workloads, hbm, Ms=(8,)) -> list:
+    """Compensated and W4A4 NVFP4 over the 22 projection shapes (N, K) the
+    paper times one by one (Fig. 18 / 19): us per call and HBM fraction."""
+    rows = []
+    for N, K in workloads.PROJECTION_SHAPES:
+        w = workloads.make_w("proj_shapes", N=N, K=K)
+        for M in Ms:
+            row = {"N": N, "K": K, "M": M}
+            for comp in (False, True):
+                lin = Linear(torch, rs, workloads, rs.NVFP4, "proj_shapes", M, comp, N=N, K=K, w=w)
+                us, _ = graph_time_us(torch, lin.call, 30, reps=3)
+                key = "comp" if comp else "w4a4"
+                row[f"{key}_us"] = round(us, 3)
+                row[f"{key}_hbm_frac"] = round(lin.call_bytes() / (us * 1e-6) / 1e9 / hbm, 4)
+                del lin
+            row["comp_over_w4a4"] = round(row["comp_us"] / row["w4a4_us"], 4)
+            rows.append(row)
+        del w
+        torch.cuda.empty_cache()
+    return rows
 
 
 def graph_time_us(torch, fn_step, steps: int, reps: int = 5, warm: int = 3) -> tuple[float, list[float]]:
@@ -427,6 +450,9 @@ def run_gpu(args) -> dict:
             row["comp_over_plain"] = round(row["comp_us"] / row["plain_us"], 4)
             mx.append(row)
         extra["mxfp4_k5120_n27648"] = mx
+        # the paper's 22 projection shapes at M = 8 (M in {1, 8, 64, 512} with --shapes)
+        extra["projection_shapes_nvfp4"] = shape_sweep(torch, rs, workloads, hbm,
+                                                       Ms=(1, 8, 64, 512) if args.shapes else (8,))
         # prefill M=4096, K=N=8192
         pre = {}
         w_pre = workloads.make_w("prefill_k8192").to(torch.device("cuda"))
@@ -574,6 +600,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline and M sweep only")
+    ap.add_argument("--shapes", action="store_true",
+                    help="projection-shape sweep at M in {1, 8, 64, 512} (default: M = 8)")
     ap.add_argument("--soak-s", type=float, default=1.5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

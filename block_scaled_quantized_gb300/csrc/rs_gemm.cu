@@ -873,6 +873,18 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
         fused = false;
         stages = best_stages(false, nacc);
     }
+    // A split plan's CTAs form clusters, and a whole cluster must fit into one
+    // GPC: with one CTA per SM fewer clusters are resident at once than with
+    // two, and the rest wait for a second wave.  A split plan whose CTAs take
+    // one tile each keeps three stages (or all its units) when that lets two
+    // CTAs share an SM; plans that stream several tiles keep the deep ring.
+    if (s > 1 && ntl == 1) {
+        const int floor_st = std::min(3, nu);
+        while (stages > floor_st &&
+               plan_smem(fmt, p.bn, stages, fused, fused ? max_chunks : 0, splitbuf, nacc) > kSmemLimit / 2 &&
+               plan_smem(fmt, p.bn, floor_st, fused, fused ? max_chunks : 0, splitbuf, nacc) <= kSmemLimit / 2)
+            --stages;
+    }
     p.fused = fused ? 1 : 0;
     p.nacc = nacc;
     p.stages = stages;
@@ -898,24 +910,37 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
     return p;
 }
 
-// Split count: minimise the chunks the busiest CTA streams; prefer fewer
-// splits on a tie.  A split plan must keep a pipeline of at least four
-// stages (or all of its units) next to its split-K buffers.
+// Split count: minimise the chunks the busiest CTA streams, plus, for a split
+// plan whose CTAs take several tiles, 1.5 x splits chunks per extra tile (the
+// cross-CTA reduction of every tile holds the whole cluster: measured about
+// 0.75 x splits us per tile against 0.4 us per streamed chunk); prefer fewer
+// splits on a tie.  A split plan must keep a pipeline of at least four stages
+// (three when its CTAs take one tile each and two of them share an SM), or
+// all of its units, next to its split-K buffers.  A plan that could
+// quantize inside the GEMM but does not fit it is charged 7 chunks for the
+// separate quantizer launch and the operand's round trip.
 static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused) {
     const int sms = num_sms > 0 ? num_sms : 148;
     const int chunks = (K + 255) / 256;
     GemmPlan best = plan_for_splits(fmt, fold, M, N, K, sms, 1, allow_fused);
     if (best.stages == 0) best.stages = 1;  // cannot happen for the supported tile shapes
-    auto load_of = [&](const GemmPlan& p) {
+    auto load_of = [&](const GemmPlan& p) {  // in half chunks
         const int tiles = p.n_tiles * p.b_tiles;
-        return (long)((tiles + p.grid_x - 1) / p.grid_x) * (long)((p.chunks + p.splits - 1) / p.splits);
+        const long ntl = (tiles + p.grid_x - 1) / p.grid_x;
+        const long streamed = 2 * ntl * (long)((p.chunks + p.splits - 1) / p.splits);
+        return streamed + (p.splits > 1 ? 3 * (ntl - 1) * p.splits : 0) + (allow_fused && !p.fused ? 14 : 0);
     };
     long best_load = load_of(best);
+    auto ntl_of = [](const GemmPlan& p) {
+        const int tiles = p.n_tiles * p.b_tiles;
+        return (tiles + p.grid_x - 1) / p.grid_x;
+    };
     for (int s = 2; s <= std::min(chunks, kMaxSplits); ++s) {
         const GemmPlan p = plan_for_splits(fmt, fold, M, N, K, sms, s, allow_fused);
         const int tiles = p.n_tiles * p.b_tiles;
         const int nu = ((tiles + p.grid_x - 1) / p.grid_x) * ((chunks + s - 1) / s);
-        if (p.stages < std::min(4, nu)) continue;
+        const bool capped = ntl_of(p) == 1 && p.smem_bytes <= kSmemLimit / 2;  // two CTAs per SM
+        if (p.stages < std::min(capped ? 3 : 4, nu)) continue;
         const long load = load_of(p);
         if (load < best_load) {
             best = p;

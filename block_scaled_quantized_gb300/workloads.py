@@ -23,6 +23,11 @@ Recipes (name -> shapes and distributions):
   X ~ N(0,1) with 1% of channels (51) scaled by 30; W ~ N(0, 0.02^2).
 * ``prefill_k8192``: M=4096, K=N=8192.  X as ``attn_proj_k4096``;
   W ~ N(0, 0.01^2).
+* ``proj_shapes``: the 22 projection shapes (N, K) of the paper's per-shape
+  M-Ext latency figures (ResServe Fig. 18 NVFP4, Fig. 19 MXFP4; QKV, output,
+  gate/up and down projections of several models at TP1 / TP8), listed in
+  ``PROJECTION_SHAPES``, M in {1, 8, 64, 512}.  X as ``attn_proj_k4096``;
+  W ~ N(0, 0.02^2); N and K given per call.
 """
 from __future__ import annotations
 
@@ -53,7 +58,19 @@ RECIPES = {
     "mx_k5120_n27648": Recipe("mx_k5120_n27648", 5120, 27648,
                               "gauss_outlier", (51, 30.0), 0.02, 0),
     "prefill_k8192": Recipe("prefill_k8192", 8192, 8192, "t_lognormal", (4.0,), 0.01, 0),
+    "proj_shapes": Recipe("proj_shapes", 4096, 4096, "t_lognormal", (4.0,), 0.02, 5),
 }
+
+# (N, K) of the 22 projection shapes timed per shape in ResServe Fig. 18 / 19,
+# in increasing N * K.
+PROJECTION_SHAPES = tuple(sorted([
+    (6144, 2560), (2560, 4096), (19456, 2560), (2560, 9728),
+    (6144, 4096), (4096, 4096), (24576, 4096), (4096, 12288),
+    (10240, 5120), (5120, 8192), (51200, 5120), (5120, 25600),
+    (14336, 5120), (34816, 5120), (5120, 17408), (16384, 5120),
+    (5120, 6144), (4608, 8192), (8192, 2048), (8192, 1024),
+    (2304, 8192), (2560, 8192),
+], key=lambda nk: (nk[0] * nk[1], nk)))
 
 
 def _rng(seed: int, tag: int) -> np.random.Generator:
