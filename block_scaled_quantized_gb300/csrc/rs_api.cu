@@ -204,6 +204,19 @@ size_t rs_workspace_bytes(rs_format fmt, int M, int N, int K, int compensated) {
     return workspace_bytes(fmt, compensated != 0, M, K);
 }
 
+int rs_plan_linear(rs_format fmt, int compensated, int M, int N, int K, int num_sms, int x_in_call, int* out,
+                   int n_out) {
+    if (!fmt_ok(fmt) || M < 1 || N < 1 || num_sms < 1 || n_out < 0 || (n_out > 0 && !out))
+        return -(int)RS_ERR_INVALID_ARG;
+    if (!k_ok(K) || (int64_t)M * 2 > (int64_t)0x7FFFFFFF) return -(int)RS_ERR_SHAPE;
+    const GemmPlan p = make_gemm_plan(fmt, compensated != 0, M, N, K, num_sms, x_in_call != 0);
+    const int v[] = {p.bn,     p.n_tiles, p.b_tiles, p.chunks, p.splits,    p.grid_x,
+                     p.stages, p.fused,   p.slots,   p.nacc,   p.tmem_cols, (int)p.smem_bytes};
+    const int n = n_out < (int)(sizeof(v) / sizeof(v[0])) ? n_out : (int)(sizeof(v) / sizeof(v[0]));
+    for (int i = 0; i < n; ++i) out[i] = v[i];
+    return n;
+}
+
 rs_status rs_compute_tensor_scale(const void* x_bf16, int64_t n, float* alpha_out, rs_stream_t stream) {
     if (n < 0 || !alpha_out || (n > 0 && !x_bf16)) return RS_ERR_INVALID_ARG;
     if ((x_bf16 && (reinterpret_cast<uintptr_t>(x_bf16) & 1u)) || !aligned4(alpha_out)) return RS_ERR_ALIGNMENT;

@@ -30,7 +30,7 @@ EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_
            "rs_quantize_weight", "rs_quantize_residue", "rs_linear_w4a4", "rs_linear_compensated",
            "rs_linear_compensated_noalloc", "rs_get_device_error", "rs_kext_width", "rs_kext_select",
            "rs_channel_mean_abs", "rs_kext_act_bytes", "rs_kext_weight_bytes", "rs_kext_workspace_bytes",
-           "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext"]
+           "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext", "rs_plan_linear"]
 
 
 class RsError(RuntimeError):
@@ -70,6 +70,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_quantize_weight_kext": ([I, I, I, I, P, I64, P, P, P, P], I),
         "rs_quantize_kext": ([I, I, I, I, P, I64, P, P, P, P], I),
         "rs_linear_kext": ([I, I, I, I, I, P, P, P, P, P, P, P, I, P, SZ, P], I),
+        "rs_plan_linear": ([I, I, I, I, I, I, I, P, I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -127,6 +128,19 @@ def rs_weight_bytes(fmt: int, N: int, K: int) -> int:
 
 def rs_workspace_bytes(fmt: int, M: int, N: int, K: int, compensated: bool) -> int:
     return lib().rs_workspace_bytes(fmt, M, N, K, int(bool(compensated)))
+
+
+PLAN_FIELDS = ("bn", "n_tiles", "b_tiles", "chunks", "splits", "grid_x", "stages", "fused", "slots", "nacc",
+               "tmem_cols", "smem_bytes")
+
+
+def rs_plan_linear(fmt: int, compensated: bool, M: int, N: int, K: int, num_sms: int, x_in_call: bool = True) -> dict:
+    """The launch plan of a linear call of this shape (host only)."""
+    out = (ctypes.c_int * len(PLAN_FIELDS))()
+    n = lib().rs_plan_linear(fmt, int(bool(compensated)), M, N, K, num_sms, int(bool(x_in_call)), out, len(out))
+    if n < 0:
+        raise RsError("rs_plan_linear", -n)
+    return dict(zip(PLAN_FIELDS, out[:n]))
 
 
 def rs_version() -> int:

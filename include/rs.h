@@ -140,6 +140,18 @@ RS_API size_t rs_weight_bytes(rs_format fmt, int N, int K);
  * needed; calls that share a workspace must be ordered (same stream). */
 RS_API size_t rs_workspace_bytes(rs_format fmt, int M, int N, int K, int compensated);
 
+/* Diagnostic, host only (no GPU needed): the launch plan that rs_linear_* of
+ * this shape would use on a GPU with num_sms SMs.  x_in_call != 0: the call
+ * passes bf16 X (small operands are then quantized inside the GEMM).  Writes
+ * up to n_out ints to out (host), in this order: bn (MMA N: 16..256), n_tiles
+ * (ceil(N/128)), b_tiles, chunks (ceil(K/256)), splits (K splits = cluster
+ * size), grid_x (persistent CTAs per split), stages (weight ring depth),
+ * fused (1: quantized inside the GEMM), slots, nacc (accumulator buffers),
+ * tmem_cols, smem_bytes (dynamic shared memory per CTA).  Returns the number
+ * written, or minus an rs_status code on bad arguments. */
+RS_API int rs_plan_linear(rs_format fmt, int compensated, int M, int N, int K, int num_sms, int x_in_call,
+                          int *out, int n_out);
+
 /* ---- tensor scale (App. B.2 Eq. 8) -------------------------------------- */
 
 /* alpha = fl(amax / 2688) over n bf16 values (device); writes one float to
