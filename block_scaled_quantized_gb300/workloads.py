@@ -23,6 +23,8 @@ Recipes (name -> shapes and distributions):
   X ~ N(0,1) with 1% of channels (51) scaled by 30; W ~ N(0, 0.02^2).
 * ``prefill_k8192``: M=4096, K=N=8192.  X as ``attn_proj_k4096``;
   W ~ N(0, 0.01^2).
+* ``attn_decode`` (``make_attention``): decode-attention query, keys and
+  values; see that function.
 * ``proj_shapes``: the 22 projection shapes (N, K) of the paper's per-shape
   M-Ext latency figures (ResServe Fig. 18 NVFP4, Fig. 19 MXFP4; QKV, output,
   gate/up and down projections of several models at TP1 / TP8), listed in
@@ -130,6 +132,23 @@ def make_w(recipe: str | Recipe, N: int | None = None, K: int | None = None,
     s = r.seed if seed is None else seed
     w = _rng(s, 3).standard_normal((N, K), dtype=np.float32) * np.float32(r.w_sigma)
     return to_bf16(w)
+
+
+def make_attention(B: int, Hq: int, Hkv: int, D: int, L: int, seed: int = 0):
+    """bf16 decode-attention inputs (``attn_decode`` recipe): query
+    [B][Hq][D] = Student-t(nu=4) times one LogNormal(0, 0.5) factor per head
+    dimension; keys [B][L][Hkv][D] = N(0,1) times one LogNormal(0, 1) factor
+    per (KV head, dimension), so a few dimensions carry outliers as cached
+    keys do; values [B][L][Hkv][D] = N(0,1).  The paper evaluates head sizes
+    128 and 256 with 4, 6 or 8 query heads per KV head and 8K to 500K cached
+    tokens (decode-attention evaluation, Fig. 10)."""
+    rng, ch = _rng(seed, 11), _rng(seed, 12)
+    q = rng.standard_t(4.0, size=(B, Hq, D)).astype(np.float32)
+    q *= ch.lognormal(0.0, 0.5, size=D).astype(np.float32)[None, None, :]
+    k = rng.standard_normal((B, L, Hkv, D), dtype=np.float32)
+    k *= ch.lognormal(0.0, 1.0, size=(Hkv, D)).astype(np.float32)[None, None, :, :]
+    v = rng.standard_normal((B, L, Hkv, D), dtype=np.float32)
+    return to_bf16(q), to_bf16(k), to_bf16(v)
 
 
 def random_bf16(shape, seed: int, scale: float = 1.0) -> torch.Tensor:

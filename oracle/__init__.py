@@ -15,6 +15,9 @@ on the logical layouts:
 
 Formats: ``NVFP4 = 0`` (block 16, E4M3 scale, fp32 tensor scale) and
 ``MXFP4 = 1`` (block 32, E8M0 scale), ResServe Sec. 2 and Fig. 1.
+
+``oracle.resattn`` holds the decode-attention oracle (ResAttn, Sec. 4.3 and
+5.2) in numpy on top of these quantizers.
 """
 from __future__ import annotations
 
