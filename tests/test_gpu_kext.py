@@ -191,3 +191,26 @@ def test_extended_operand_bit_exact_large(k, rows, K):
     np.testing.assert_array_equal(codes, cx)
     np.testing.assert_array_equal(sf, sx)
     assert not np.any(layout.padding_sf_bytes(host, 0, rows, Ke))
+
+
+# Large K-Ext operands outside the one-block-per-lane kernel (MXFP4, or NVFP4
+# with K not a multiple of 512): four chunks per warp step, ragged last group.
+@pytest.mark.parametrize("fmt,k,rows,K", [(1, 1, 700, 8192), (1, 4, 600, 8448), (0, 2, 600, 8448)])
+def test_extended_operand_bit_exact_large_four_chunk_steps(fmt, k, rows, K):
+    import oracle
+    x = workloads.make_x("prefill_k8192", rows, K=K, seed=rows + k + fmt)
+    mask = _mask(x[:256], k, rows + k)
+    xb = workloads.bf16_bits(x)
+    a_or = oracle.tensor_scale(xb) if fmt == 0 else np.float32(0)
+    a_gpu = torch.tensor([a_or], dtype=torch.float32, device=DEV) if fmt == 0 else None
+    Ke = K + rs.rs_kext_width(K, k)
+    buf = torch.full((rs.rs_kext_act_bytes(fmt, rows, K, k),), 0xAB, dtype=torch.uint8, device=DEV)
+    rs.rs_quantize_kext(fmt, x.to(DEV), k, a_gpu, torch.from_numpy(mask).to(DEV), buf)
+    torch.cuda.synchronize()
+    assert rs.rs_get_device_error() == 0
+    host = buf.cpu().numpy()
+    codes, sf = layout.unpack_operand(host, fmt, rows, Ke)
+    cx, sx = oracle.quantize_kext(fmt, xb, k, mask, a_or)
+    np.testing.assert_array_equal(codes, cx)
+    np.testing.assert_array_equal(sf, sx)
+    assert not np.any(layout.padding_sf_bytes(host, fmt, rows, Ke))

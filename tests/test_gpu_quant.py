@@ -219,3 +219,13 @@ def test_nvfp4_scale_every_bf16_amax_large_operand(alpha):
     x = (blocks * sign).to(torch.bfloat16).reshape(-1, K)
     x = torch.cat([x.roll(i, dims=1) for i in range(10)])    # 1280 rows: the large-operand quantizer
     _check(0, x, True, alpha=np.float32(alpha))
+
+
+# Large operands that the one-block-per-lane kernel does not take (MXFP4, or
+# NVFP4 with K not a multiple of 512) use the two-lanes-per-block kernel with
+# four chunks per warp step: K = 8448 leaves a last group of one chunk.
+@pytest.mark.parametrize("fmt,rows,K", [(1, 700, 8192), (0, 600, 8448), (1, 600, 8448)])
+@pytest.mark.parametrize("paired", [False, True])
+def test_quantizer_large_operand_four_chunk_steps(fmt, rows, K, paired):
+    x = workloads.make_x("prefill_k8192", rows, K=K, seed=rows + K + fmt)
+    _check(fmt, x, paired)
