@@ -101,6 +101,8 @@ def _load():
         lib.or_quantize_weight_kext.argtypes = [i, i, i, i, P, f, P, P, P]
         lib.or_quantize_weight_kext.restype = i
         lib.or_linear_kext.argtypes = [i, i, i, i, i, P, f, P, P, P, f, P]
+        lib.or_quantize_nvfp4_div.argtypes = [i, i, P, f, P, P]
+        lib.or_quantize_nvfp4_div.restype = i
         lib.or_linear_kext.restype = i
         _lib = lib
         return lib
@@ -180,6 +182,19 @@ def quantize(fmt: int, x_u16, alpha: float = 0.0):
     if rc:
         raise ValueError("oracle quantize: bad shape")
     return codes, sf, xhat
+
+
+def quantize_nvfp4_div(x_u16, alpha: float):
+    """NVFP4 codes and scale bytes with Eq. 10's division v = fl(x / s~)
+    instead of Alg. 1's multiplier (the alternative reading; parity uses the
+    multiplier)."""
+    x = _as_u16(x_u16)
+    rows, K = x.shape
+    codes = np.zeros((rows, K // 2), np.uint8)
+    sf = np.zeros((rows, K // 16), np.uint8)
+    if _load().or_quantize_nvfp4_div(rows, K, _ptr(x), float(alpha), _ptr(codes), _ptr(sf)):
+        raise ValueError("oracle quantize_nvfp4_div: bad shape")
+    return codes, sf
 
 
 def quantize_residue(fmt: int, x_u16, alpha: float = 0.0):

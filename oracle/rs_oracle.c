@@ -231,6 +231,25 @@ static void nvfp4_block(const float *xf, int n, float alpha,
     *sf_out = sf;
 }
 
+/* The same block with Eq. 10's true division v = fl(x / s~) in place of
+ * Alg. 1's multiplier (the alternative to reading R3; parity is defined on
+ * the multiplier).  Codes and scale byte only. */
+static void nvfp4_block_div(const float *xf, int n, float alpha, uint8_t *sf_out, uint8_t *codes)
+{
+    float amax = 0.0f, s, t, st;
+    uint8_t sf;
+    for (int i = 0; i < n; ++i)
+        if (fabsf(xf[i]) > amax)
+            amax = fabsf(xf[i]);
+    s = amax / 6.0f;
+    t = (alpha > 0.0f) ? s / alpha : 0.0f;
+    sf = or_e4m3_encode_satfinite(t);
+    st = alpha * (float)or_e4m3_decode(sf);
+    for (int i = 0; i < n; ++i)
+        codes[i] = or_e2m1_encode(st == 0.0f ? 0.0f * xf[i] : xf[i] / st);   /* Eq. 10: x / s~_i */
+    *sf_out = sf;
+}
+
 /* ------------------------------------------------------------------------ */
 /* One MXFP4 block (Sec. 2: E8M0 power-of-two scale per 32 elements;         */
 /* reading R6 for the exponent).                                              */
@@ -320,6 +339,26 @@ int or_quantize(int fmt, int rows, int K, const uint16_t *x, float alpha,
     if (!xhat)
         free(h);
     free(xf);
+    return 0;
+}
+
+/* NVFP4 base quantization of bf16 rows with Eq. 10's division (see
+ * nvfp4_block_div).  Returns 0 on success. */
+int or_quantize_nvfp4_div(int rows, int K, const uint16_t *x, float alpha, uint8_t *codes, uint8_t *sf)
+{
+    uint8_t q[16];
+    float xf[16];
+    if (rows < 0 || K <= 0 || K % 16 != 0)
+        return 1;
+    for (int r = 0; r < rows; ++r) {
+        for (int b = 0; b < K / 16; ++b) {
+            for (int i = 0; i < 16; ++i)
+                xf[i] = bf16_to_float(x[(int64_t)r * K + b * 16 + i]);
+            nvfp4_block_div(xf, 16, alpha, &sf[(int64_t)r * (K / 16) + b], q);
+            for (int i = 0; i < 16; ++i)
+                put_nibble(codes + (int64_t)r * (K / 2), b * 16 + i, q[i]);
+        }
+    }
     return 0;
 }
 

@@ -233,3 +233,45 @@ def test_zero_and_tiny_blocks(oracle_mod):
     # alpha = 0 (all-zero tensor) quantizes to zero scales and +-0 codes
     z = o.quantize_residue(o.NVFP4, _bits(np.zeros((1, 16), np.float32)), 0.0)
     assert not np.any(z["sf_x"]) and not np.any(z["codes_x"])
+
+
+def test_division_reading_differs_rarely_by_one_step(oracle_mod):
+    """Eq. 10 divides, x / s~; Alg. 1 multiplies by the fp32 reciprocal (the
+    reading the quantizers take, R3).  Both give the same scale bytes; codes
+    differ only where the two fp32 values straddle an E2M1 rounding boundary,
+    by one step and with the same sign, and rarely.  The first difference is
+    recomputed by hand in numpy fp32."""
+    o = oracle_mod
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    total = changed = 0
+    example = None
+    for rec in ["gauss_outlier_k2048", "attn_proj_k4096", "mlp_down", "prefill_k8192"]:
+        x = workloads.make_x(rec, 64, seed=3)
+        xb = workloads.bf16_bits(x)
+        a = o.tensor_scale(xb)
+        cm, sm, _ = o.quantize(0, xb, a)
+        cd, sd = o.quantize_nvfp4_div(xb, a)
+        assert np.array_equal(sm, sd)
+        qm = np.stack([cm & 15, cm >> 4], axis=-1).reshape(cm.shape[0], -1)
+        qd = np.stack([cd & 15, cd >> 4], axis=-1).reshape(cd.shape[0], -1)
+        diff = np.argwhere(qm != qd)
+        for r, k in diff:
+            assert (qm[r, k] & 8) == (qd[r, k] & 8) and abs(int(qm[r, k] & 7) - int(qd[r, k] & 7)) == 1
+        if len(diff) and example is None:
+            r, k = diff[0]
+            example = (x[r, k].item(), float(a), int(sm[r, k // 16]), int(qm[r, k]), int(qd[r, k]))
+        total += qm.size
+        changed += len(diff)
+    assert changed / total < 1e-3 and example is not None
+    xv, alpha, sfb, code_mul, code_div = example
+    st = np.float32(np.float32(alpha) * np.float32(o.e4m3_decode(sfb)))
+    v_mul = np.float32(np.float32(xv) * np.float32(np.float32(1.0) / st))
+    v_div = np.float32(np.float32(xv) / st)
+    assert v_mul != v_div
+    for v, code in ((v_mul, code_mul), (v_div, code_div)):
+        mag = abs(float(v))
+        i = int(np.argmin(np.abs(grid - mag)))
+        d = np.abs(grid - mag)
+        if np.sum(d == d[i]) > 1:  # a tie: the even code
+            i = [j for j in np.flatnonzero(d == d[i]) if j % 2 == 0][0]
+        assert (code & 7) == i
