@@ -335,6 +335,18 @@ def run_profile_case(args) -> dict:
     return {"profile_case": args.profile_case, "us_per_call": round(us, 3), "launches_per_call": lin.launches_per_call()}
 
 
+def max_over_ranks(value: float, world: int, device: str) -> float:
+    """The slowest rank's value (the job's time), via an all-reduce over the
+    initialised process group; the value itself with one rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_gpu(args) -> dict:
     import torch
     import torch.distributed as dist
@@ -389,10 +401,7 @@ def run_gpu(args) -> dict:
         out = {"metric": METRIC, "value": round(t_ms * 1000.0 / K_steps, 3), "unit": "us", "n_gpus": world,
                "steps": K_steps, "warmup": W, "headline_only": True, "clocks": clocks}
         return out if rank == 0 else None
-    if world > 1:
-        t = torch.tensor([t_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_ms = float(t.item())
+    t_ms = max_over_ranks(t_ms, world, "cuda")
     us_per_step = t_ms * 1000.0 / K_steps
     hbm = peaks["hbm_gbs"]
 
