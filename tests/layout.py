@@ -87,3 +87,65 @@ def unpack_weight(buf, fmt, N, K):
     pad_ok = (not codes_full[N:].any() and not codes_full[:, K // 2:].any()
               and not sf_full[N:].any() and not sf_full[:, K // bs:].any())
     return codes, sf, pad_ok
+
+
+# ---- paged NVFP4 KV cache (decode attention) ----
+# Page p of KV head h: codes [32 tokens][D/2] then E4M3 scales [32][D/16];
+# pages stored [page][Hkv]; a block table [B][max_pages] maps each sequence's
+# logical pages (token t -> page block_table[b][t // 32], row t % 32).
+
+PAGE = 32
+
+
+def page_bytes(D):
+    return PAGE * (D // 2 + D // 16)
+
+
+def pack_paged_cache(codes, sf, seq_lens, rng=None):
+    """Logical codes [B][L][Hkv][D/2] and scales [B][L][Hkv][D/16] -> (cache
+    bytes [n_pages][Hkv][page_bytes], block table int32 [B][max_pages]).
+    Pages are handed out in a shuffled order so the table is not trivial;
+    rows past a sequence's length stay zero."""
+    codes = np.asarray(codes, np.uint8)
+    sf = np.asarray(sf, np.uint8)
+    B, L, H, CB = codes.shape
+    SB = sf.shape[3]
+    D = 2 * CB
+    max_pages = (L + PAGE - 1) // PAGE
+    need = [(int(n) + PAGE - 1) // PAGE for n in seq_lens]
+    order = np.arange(sum(need))
+    if rng is not None:
+        rng.shuffle(order)
+    cache = np.zeros((max(len(order), 1), H, page_bytes(D)), np.uint8)
+    table = np.zeros((B, max_pages), np.int32)
+    k = 0
+    for b in range(B):
+        for lp in range(need[b]):
+            page = int(order[k])
+            k += 1
+            table[b, lp] = page
+            t0, t1 = lp * PAGE, min(int(seq_lens[b]), (lp + 1) * PAGE)
+            for h in range(H):
+                blk = cache[page, h]
+                rows = t1 - t0
+                blk[:rows * CB] = codes[b, t0:t1, h].reshape(-1)
+                blk[PAGE * CB:PAGE * CB + rows * SB] = sf[b, t0:t1, h].reshape(-1)
+    return cache, table
+
+
+def unpack_paged_cache(cache, table, seq_lens, D):
+    """Inverse of pack_paged_cache on the first seq_lens[b] tokens."""
+    cache = np.asarray(cache, np.uint8)
+    B = table.shape[0]
+    H = cache.shape[1]
+    CB, SB = D // 2, D // 16
+    L = table.shape[1] * PAGE
+    codes = np.zeros((B, L, H, CB), np.uint8)
+    sf = np.zeros((B, L, H, SB), np.uint8)
+    for b in range(B):
+        for t in range(int(seq_lens[b])):
+            blk = cache[table[b, t // PAGE]]
+            r = t % PAGE
+            codes[b, t] = blk[:, r * CB:(r + 1) * CB]
+            sf[b, t] = blk[:, PAGE * CB + r * SB:PAGE * CB + (r + 1) * SB]
+    return codes, sf
