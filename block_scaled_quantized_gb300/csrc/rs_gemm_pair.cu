@@ -151,7 +151,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         uint32_t ph = 0;
         for (int u = 0; u < nu; ++u) {
             const int j = u / g.chunks, i = u - j * g.chunks;
-            if (u >= S && !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag, g.err)))
+            // released by the leader's multicast commit: cluster-scope acquire
+            if (u >= S && !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag, g.err,
+                                                                     1000000000ull, true)))
                 break;
             if (elect_one_sync()) {
                 uint8_t* st = smem + (size_t)s * STAGE;
@@ -252,7 +254,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const int outs = g.fold ? BN / 2 : BN;
         const uint32_t leader_empty = map_dsmem(smem_u32(accum_empty), 0);
         for (int j = 0; j < ntl; ++j) {
-            bool ok = mbar_wait_bounded(smem_u32(accum_full), (uint32_t)j & 1u, abort_flag, g.err);
+            bool ok = mbar_wait_bounded(smem_u32(accum_full), (uint32_t)j & 1u, abort_flag, g.err, 1000000000ull, true);
             ok = __all_sync(0xFFFFFFFFu, ok && *abort_flag == 0);
             if (!ok) break;
             tc_fence_after();
