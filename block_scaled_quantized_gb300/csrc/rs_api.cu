@@ -357,6 +357,34 @@ rs_status rs_linear_kext(rs_format fmt, int M, int N, int K, int k, const void* 
                        ws_bytes, (cudaStream_t)stream, k, mask);
 }
 
+namespace rs {
+// Failure detection without a fault: one CTA waits on an mbarrier that
+// nothing arrives on, with the bounded wait every kernel uses; the wait runs
+// out after limit_ns, sets the device error word (RS_ERR_DEVICE_TIMEOUT) and
+// returns, and the kernel exits normally.
+__global__ void wait_probe_kernel(uint64_t limit_ns, uint32_t* err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0u;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) (void)mbar_wait_bounded(smem_u32(&bar), 0u, &abort_flag, err, limit_ns);
+}
+}  // namespace rs
+
+rs_status rs_debug_wait_probe(uint64_t limit_ns, rs_stream_t stream) {
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return RS_ERR_INVALID_ARG;
+    cudaError_t why;
+    const rs::DeviceInfo* dev = rs::current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    rs::wait_probe_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(limit_ns, dev->err);
+    return cudaGetLastError() == cudaSuccess ? RS_OK : RS_ERR_CUDA;
+}
+
 rs_status rs_get_device_error(rs_stream_t stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return RS_ERR_CUDA;
     uint32_t* p = device_error_word();

@@ -30,7 +30,7 @@ EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_
            "rs_quantize_weight", "rs_quantize_residue", "rs_linear_w4a4", "rs_linear_compensated",
            "rs_linear_compensated_noalloc", "rs_get_device_error", "rs_kext_width", "rs_kext_select",
            "rs_channel_mean_abs", "rs_kext_act_bytes", "rs_kext_weight_bytes", "rs_kext_workspace_bytes",
-           "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext", "rs_plan_linear"]
+           "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext", "rs_plan_linear", "rs_debug_wait_probe"]
 
 
 class RsError(RuntimeError):
@@ -71,6 +71,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_quantize_kext": ([I, I, I, I, P, I64, P, P, P, P], I),
         "rs_linear_kext": ([I, I, I, I, I, P, P, P, P, P, P, P, I, P, SZ, P], I),
         "rs_plan_linear": ([I, I, I, I, I, I, I, P, I], I),
+        "rs_debug_wait_probe": ([ctypes.c_uint64, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -128,6 +129,11 @@ def rs_weight_bytes(fmt: int, N: int, K: int) -> int:
 
 def rs_workspace_bytes(fmt: int, M: int, N: int, K: int, compensated: bool) -> int:
     return lib().rs_workspace_bytes(fmt, M, N, K, int(bool(compensated)))
+
+
+def rs_debug_wait_probe(limit_ns: int, stream=None):
+    """One bounded wait that runs out after limit_ns on the device (see rs.h)."""
+    _check("rs_debug_wait_probe", lib().rs_debug_wait_probe(int(limit_ns), _stream(stream)))
 
 
 PLAN_FIELDS = ("bn", "n_tiles", "b_tiles", "chunks", "splits", "grid_x", "stages", "fused", "slots", "nacc",

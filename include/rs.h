@@ -321,6 +321,14 @@ RS_API rs_status rs_linear_compensated_noalloc(rs_format fmt, int M, int N, int 
 
 /* ---- device error word --------------------------------------------------- */
 
+/* Diagnostic of failure detection (no GPU fault): launches one CTA that
+ * waits on an mbarrier nothing arrives on, with the bounded wait the kernels
+ * use and a limit of limit_ns (1 .. 1e9 ns); the wait runs out, sets the
+ * device error word to RS_ERR_DEVICE_TIMEOUT (read and cleared by
+ * rs_get_device_error) and the kernel exits normally, leaving the context
+ * usable.  RS_ERR_INVALID_ARG for a limit outside that range. */
+RS_API rs_status rs_debug_wait_probe(uint64_t limit_ns, rs_stream_t stream);
+
 /* Synchronizes `stream`, then returns and clears the device error word of the
  * current device: RS_OK, RS_ERR_DEVICE_TIMEOUT (a kernel's bounded wait ran
  * out; its outputs are invalid and the workspace must be zero-filled again)

@@ -146,3 +146,11 @@ def test_kext_argument_checks(librs):
     q = librs.rs_quantize_kext
     assert q(0, 4, 512, 5, FAKE, 512, FAKE, FAKE, FAKE, None) == 3
     assert q(0, 4, 512, 2, FAKE, 512, FAKE, None, FAKE, None) == 1
+
+
+def test_wait_probe_rejects_out_of_range_limits():
+    from block_scaled_quantized_gb300 import rs
+    for bad in (0, 2_000_000_000):
+        with pytest.raises(rs.RsError) as e:
+            rs.rs_debug_wait_probe(bad, stream=0)  # argument checks come before any CUDA call
+        assert e.value.status == rs.RS_ERR_INVALID_ARG
