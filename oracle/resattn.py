@@ -14,7 +14,7 @@ softmax; V is converted from NVFP4 to FP8 on chip and PV runs with FP8
 operands, FP32 accumulation and normalization; the sequence is split into
 parts whose partial outputs and softmax statistics are combined).
 
-Readings taken where the pages leave a step open (also listed in the design
+Readings taken where the paper leaves a step open (also listed in the design
 notes):
 
   R14  K and V are NVFP4 (16-element blocks along the head dimension, E4M3
@@ -147,9 +147,9 @@ def resattn_decode(q_u16, alpha_q: float, k_codes, k_sf, v_codes, v_sf, seq_lens
 
 def attention_reference(q_values, k_values, v_values, seq_lens, groups: int) -> np.ndarray:
     """Plain softmax attention in double on given (already dequantized or
-    bf16) values: q [B][Hq][D], k, v [B][L][Hkv][D].  The pages measure
+    bf16) values: q [B][Hq][D], k, v [B][L][Hkv][D].  ResServe measures
     ResAttn's error against an FP32 attention on the same dequantized KV
-    (Sec. 6, decode-attention evaluation); this is that reference in double."""
+    (decode-attention evaluation, Fig. 10d); this is that reference in double."""
     q = np.asarray(q_values, np.float64)
     B, Hq, D = q.shape
     O = np.zeros((B, Hq, D))

@@ -24,7 +24,7 @@
  *     compensation), computed as a stacked GEMM followed by the Fold
  *     Y_j = Z_j + Z_{M+j}.
  *
- * Readings taken where the pages leave a step open (each one is also listed
+ * Readings taken where the paper leaves a step open (each one is also listed
  * in the design notes):
  *   R1  The tensor scale is an input (Alg. 1 "receives a precomputed tensor
  *       scale").  When it is computed here it is fl(amax / 2688.0f), i.e. the
@@ -39,7 +39,7 @@
  *       rounds to zero gives code 0x8).
  *   R5  Reconstruction uses Eq. 10's product x^ = fl(s~ * dec(q)); the
  *       residue is r = fl(x - x^) in fp32.
- *   R6  MXFP4 scale (the pages only cite the OCP MX format): the shared
+ *   R6  MXFP4 scale (the paper only cites the OCP MX format): the shared
  *       exponent is e = floor(log2(Max)) - 2 (2 = emax of E2M1), clamped to
  *       [-127, 127]; Max == 0 gives e = -127.  Stored byte = e + 127.
  *       v = fl(x * 2^-e); x^ = dec(q) * 2^e.  The residue gets its own scale.
