@@ -54,3 +54,23 @@ def test_reference_arm_only_on_rank_0(monkeypatch):
         steps, warmup, cpu_seconds = 2, 3, 5.0
 
     assert bench.run_reference(A()) is None
+
+
+def test_reference_arm_json_line_keys(monkeypatch):
+    """The reference arm's line carries the keys the bench contract names
+    (the oracle timed on the host, here on a short budget)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+
+    class A:
+        steps, warmup, cpu_seconds = 2, 3, 1.0
+
+    line = bench.run_reference(A())
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"] is False
+    assert line["config"]["workload"] and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
