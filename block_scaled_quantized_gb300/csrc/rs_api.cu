@@ -88,7 +88,7 @@ int kext_cols(int K, int k) { return K + K / 8 * k; }
 rs_status linear_impl(int fmt, bool compensated, int M, int N, int K, const void* x, const void* xq,
                       const float* alpha_x, const void* wq, const float* alpha_w, void* y, int out_dtype,
                       void* ws, size_t ws_bytes, cudaStream_t stream, int kext_k = 0,
-                      const uint8_t* kext_mask = nullptr) {
+                      const uint8_t* kext_mask = nullptr, void* qdump = nullptr) {
     if (!fmt_ok(fmt) || M < 0 || N < 0) return RS_ERR_INVALID_ARG;
     if (out_dtype != RS_OUT_BF16 && out_dtype != RS_OUT_F32) return RS_ERR_INVALID_ARG;
     if (!k_ok(K)) return RS_ERR_SHAPE;
@@ -128,6 +128,7 @@ rs_status linear_impl(int fmt, bool compensated, int M, int N, int K, const void
     if (quantize_input && plan.fused) {
         c.x = x;  // the GEMM quantizes its own K slices (and finds the tensor scale): one launch
         c.dyn_alpha = dyn_alpha ? 1 : 0;
+        c.qdump = qdump;
     } else if (quantize_input) {
         void* act = ws;
         const float* ax = alpha_x;
@@ -383,6 +384,45 @@ rs_status rs_debug_wait_probe(uint64_t limit_ns, rs_stream_t stream) {
     if (!dev->supported) return RS_ERR_UNSUPPORTED;
     rs::wait_probe_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(limit_ns, dev->err);
     return cudaGetLastError() == cudaSuccess ? RS_OK : RS_ERR_CUDA;
+}
+
+namespace rs {
+// One thread: hand the error word to the caller's buffer and clear it.
+__global__ void read_error_kernel(uint32_t* err, uint32_t* out) { *out = atomicExch(err, 0u); }
+}  // namespace rs
+
+rs_status rs_get_device_error_async(uint32_t* out, rs_stream_t stream) {
+    if (!out) return RS_ERR_INVALID_ARG;
+    if (!aligned4(out)) return RS_ERR_ALIGNMENT;
+    cudaError_t why;
+    const rs::DeviceInfo* dev = rs::current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    rs::read_error_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(dev->err, out);
+    return cudaGetLastError() == cudaSuccess ? RS_OK : RS_ERR_CUDA;
+}
+
+rs_status rs_debug_linear_dump(rs_format fmt, int compensated, int M, int N, int K, const void* x_bf16,
+                               const float* alpha_x, const void* wq, const float* alpha_w, void* y,
+                               rs_out_dtype out_dtype, void* workspace, size_t ws_bytes, void* dump,
+                               size_t dump_bytes, int* layout, rs_stream_t stream) {
+    if (!layout || !fmt_ok(fmt) || M < 1 || N < 1) return RS_ERR_INVALID_ARG;
+    if (!k_ok(K) || (int64_t)M * 2 > (int64_t)0x7FFFFFFF) return RS_ERR_SHAPE;
+    cudaError_t why;
+    const rs::DeviceInfo* dev = rs::current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    const GemmPlan p = make_gemm_plan(fmt, compensated != 0, M, N, K, dev->num_sms, /*allow_fused=*/true);
+    const size_t stage = plan_b_stage_bytes(p);
+    const int v[7] = {p.fused, p.bn, p.grid_x, p.splits, p.slots, (int)stage, p.chunks};
+    for (int i = 0; i < 7; ++i) layout[i] = v[i];
+    if (!dump) return RS_OK;  // layout query only
+    if (!p.fused) return RS_ERR_UNSUPPORTED;
+    if (!aligned16(dump)) return RS_ERR_ALIGNMENT;
+    if (dump_bytes < (size_t)p.grid_x * (size_t)p.splits * (size_t)p.slots * stage) return RS_ERR_WORKSPACE;
+    if (!x_bf16) return RS_ERR_INVALID_ARG;
+    return linear_impl(fmt, compensated != 0, M, N, K, x_bf16, nullptr, alpha_x, wq, alpha_w, y, out_dtype,
+                       workspace, ws_bytes, (cudaStream_t)stream, 0, nullptr, dump);
 }
 
 rs_status rs_get_device_error(rs_stream_t stream) {

@@ -75,6 +75,10 @@ constexpr uint32_t kCtrlBytes = 1024;
 constexpr int kMaxChunkBars = 32;   // fused plans: one "quantized" mbarrier per resident chunk
 
 __host__ __device__ constexpr int b_atom_tiles(int bn) { return (bn + 127) / 128; }
+// Split-K: outputs of a tile each owner CTA sums, a multiple of four.
+__host__ __device__ constexpr int split_slice(int outs, int splits) {
+    return ((outs + splits - 1) / splits + 3) / 4 * 4;
+}
 // Shared-memory bytes of one activation stage: codes (bn rows x 128 bytes)
 // plus its scale atoms, rounded to the 1024-byte swizzle period.
 __host__ __device__ constexpr uint32_t b_stage_bytes(int fmt, int bn) {
@@ -95,6 +99,7 @@ struct GemmArgs {
     const float* alpha_w;
     uint32_t* err;
     uint64_t* trace;        // trace builds only: 32 timer stamps per CTA
+    uint8_t* qdump;         // fused plans, test hook: each CTA's quantized slice (null: off)
     int N, K, M, Rb;
     int n_atoms_k;          // activation operand atoms per row tile along K
     int b_row_tiles;        // scale-atom row tiles of the activation operand
@@ -107,7 +112,6 @@ struct GemmArgs {
     int stages;
     int slots;              // fused: resident activation chunks
     int nacc;               // accumulator buffers in tensor memory (1 or 2)
-    int part_bytes;         // split-K: this CTA's partial
     int recv_bytes;         // split-K: one receive buffer (0 without split)
     int tmem_cols;
     int dyn_alpha;          // fused NVFP4: the tensor scale of X is computed here (alpha_x unused)
@@ -131,8 +135,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     uint8_t* wring = smem;                                   // S x WB
     uint8_t* bregion = smem + (size_t)S * WB;                // S (or slots) x BSTAGE
     const int nbslots = FUSED ? g.slots : S;
-    uint8_t* part_region = bregion + (size_t)nbslots * BSTAGE;    // split-K: our partial
-    uint8_t* recv_region = part_region + g.part_bytes;            // split-K: nacc receive buffers
+    uint8_t* recv_region = bregion + (size_t)nbslots * BSTAGE;    // split-K: nacc receive buffers
     const uint32_t recv_base = smem_u32(recv_region);
     uint64_t* full = reinterpret_cast<uint64_t*>(recv_region + (size_t)g.nacc * g.recv_bytes);
     uint64_t* empty = full + kMaxStages;
@@ -166,7 +169,12 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     const int pre = nu < S ? nu : S;
     const int nacc = g.nacc;
     const int outs = g.fold ? BN / 2 : BN;
-    const int per_cta = (outs + g.splits - 1) / g.splits;  // split-K: outputs each CTA owns
+    // split-K: the outputs are dealt to the first `owners` CTAs of the cluster
+    // in slices of per_cta (a multiple of four, so that a sender moves four
+    // at a time); each owner sums its slice over the K splits
+    const int per_cta = split_slice(outs, g.splits);
+    const int owners = (outs + per_cta - 1) / per_cta;
+    const bool owner = g.splits > 1 && split < owners;
     const uint32_t slice_bytes = (uint32_t)per_cta * 128u * 4u;
     // Wide tiles without split-K: eight epilogue warps (warps 8-11 and 0-3,
     // two per tensor-memory lane quarter) take half of the columns each.
@@ -207,11 +215,11 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             mbar_init(smem_u32(&accum_full[b]), 1);
             mbar_init(smem_u32(&accum_empty[b]), (uint32_t)(epi8 ? 8 : 4));  // one arrival per epilogue warp
             mbar_init(smem_u32(&red_full[b]), 1);
-            mbar_init(smem_u32(&recv_free[b]), (uint32_t)g.splits);  // one arrival per owner
+            mbar_init(smem_u32(&recv_free[b]), (uint32_t)owners);  // one arrival per owner
         }
         // the first use of each receive buffer is armed before any partner
         // can send (they send only after the cluster barrier below)
-        if (g.splits > 1)
+        if (owner)
             for (int b = 0; b < nacc && b < ntl; ++b) mbar_arrive_expect_tx(smem_u32(&red_full[b]), red_bytes);
         *abort_flag = 0;
         *consumed = 0;
@@ -274,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                           (uint32_t)na * 512u, fb, pol_x);
         };
         pdl_wait_prior_grid();
+        if (!FUSED && lane == 0) RS_TRACE_MARK(g.trace, 16);
         if (elect_one_sync())
             for (int u = 0; u < pre; ++u) load_b(u);
         __syncwarp();
@@ -321,9 +330,26 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
         const uint64_t sfadesc0 = sf_atom_desc(smem_u32(wring) + kWeightCodeBytes);
         const uint64_t sfbdesc0 = sf_atom_desc(smem_u32(bregion) + B_BYTES);
         constexpr uint32_t kIdesc = mxf4_idesc(BN, FMT == 1, 0);
+        // Fused plans: the weight scale atoms of the stages prefetched ahead of
+        // the previous kernel's completion go to tensor memory as soon as they
+        // land, so that after the quantizer only the activation scales and the
+        // MMAs remain.  (A weight block always holds all of its atoms.)
+        const int npre = FUSED ? (nu < S ? nu : S) : 0;
+        bool ok = true;
+        for (int u0 = 0; ok && u0 < npre; ++u0) {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&full[u0]), 0u, abort_flag, g.err));
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one_sync()) {
+#pragma unroll
+                for (int a = 0; a < APC; ++a)
+                    tc_cp_sf_atom(tm_sf + (uint32_t)(u0 * SF_COLS + a * 4), sfadesc0 + (uint32_t)u0 * (WB >> 4) +
+                                                                                 (uint32_t)a * 32u);
+            }
+            __syncwarp();
+        }
         int u = 0, s = 0;
         uint32_t ph = 0;
-        bool ok = true;
         for (int j = 0; ok && j < ntl; ++j) {
             const int b = j & (nacc - 1);
             if (j >= nacc) {
@@ -357,11 +383,12 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 const uint32_t tsfa = tm_sf + (uint32_t)(s * SF_COLS);
                 const uint32_t tsfb = tsfa + SFA_COLS;
                 const bool whole = c0 + i < g.chunks - 1 || (g.K & 255) == 0;  // all four k-steps
+                const bool a_sf = u >= npre;  // weight scales not yet in tensor memory
                 if (elect_one_sync()) {
                     if (whole) {
 #pragma unroll
                         for (int a = 0; a < APC; ++a) {
-                            tc_cp_sf_atom(tsfa + a * 4, sad + (uint32_t)a * 32u);
+                            if (a_sf) tc_cp_sf_atom(tsfa + a * 4, sad + (uint32_t)a * 32u);
                             for (int t = 0; t < nb_tiles; ++t)
                                 tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sbd + (uint32_t)(t * APC + a) * 32u);
                         }
@@ -381,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                         const int nks = (g.K - (c0 + i) * 256 + 63) / 64;
                         const int na = FMT == 0 ? nks : (nks + 1) / 2;
                         for (int a = 0; a < na; ++a) {
-                            tc_cp_sf_atom(tsfa + a * 4, sad + (uint32_t)a * 32u);
+                            if (a_sf) tc_cp_sf_atom(tsfa + a * 4, sad + (uint32_t)a * 32u);
                             for (int t = 0; t < nb_tiles; ++t)
                                 tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sbd + (uint32_t)(t * APC + a) * 32u);
                         }
@@ -409,6 +436,15 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 __syncwarp();
             }
             if (j < 3 && lane == 0) RS_TRACE_MARK(g.trace, 19 + j);
+        }
+        // Test hook (null on every production call): copy this CTA's quantized
+        // activation slice, codes and scale atoms exactly as the MMAs read
+        // them, to the dump buffer; every chunk's barrier was waited above.
+        if (FUSED && g.qdump != nullptr && ok) {
+            uint8_t* dst = g.qdump + ((size_t)split * gridDim.x + blockIdx.x) * (size_t)g.slots * BSTAGE;
+            const uint32_t bytes = (uint32_t)nck * BSTAGE;
+            for (uint32_t off = (uint32_t)lane * 16u; off < bytes; off += 512u)
+                *reinterpret_cast<uint4*>(dst + off) = *reinterpret_cast<const uint4*>(bregion + off);
         }
         // Free the tensor memory as soon as the epilogue has read the last
         // accumulator (it reads the tiles in order), while it still exchanges
@@ -443,6 +479,37 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             pdl_wait_prior_grid();
             if (qtid == 0) RS_TRACE_MARK(g.trace, 16);
             const int kbeg = c0 * 256, kend = min(g.K, (c0 + nck) * 256);
+            // flat chunk-major mapping: thread qtid takes scale blocks qtid,
+            // qtid + T, ... (T = quantizer threads) of the order (chunk, token
+            // row, block), so chunks complete in order.
+            constexpr int bpc = 256 / E;    // blocks per token row in one chunk
+            constexpr int kWords = E / 8;   // 16-byte words of X per block
+            constexpr int kBatch = 32 / E;  // blocks per thread per batch
+            const int cb = g.M * bpc;       // blocks per chunk
+            const int total = nck * cb;
+            auto block_pos = [&](int f, int& j, int& kk) {
+                const int ci = f / cb, rem = f - ci * cb;
+                j = rem / bpc;
+                kk = ci * 256 + (rem - j * bpc) * E;
+            };
+            // raw bf16 words of this thread's blocks in one batch; the first
+            // batch is requested before the tensor scale is read, so that both
+            // come back in one round trip
+            uint4 raw[kBatch][kWords];
+            auto load_batch = [&](int fw) {
+#pragma unroll
+                for (int r = 0; r < kBatch; ++r) {
+                    const int f = fw + lane + r * kQuantThreads;
+                    int j, kk;
+                    block_pos(f, j, kk);
+                    const bool live = f < total && kbeg + kk < kend;
+#pragma unroll
+                    for (int q = 0; q < kWords; ++q)
+                        raw[r][q] = load16_or_zero(g.x + (size_t)j * g.K + kbeg + kk + 8 * q, live);
+                }
+            };
+            const int fw0 = qw * 32;
+            if (fw0 < total) load_batch(fw0);
             if (FMT == 0 && g.dyn_alpha) {
                 // This call's tensor scale (App. B.2 Eq. 8): a = fl(amax(X) / 2688),
                 // the same value rs_compute_tensor_scale gives.  Each CTA takes the
@@ -487,10 +554,15 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 ax_val = *g.alpha_x;
             }
             const NvScaleConst ksc = nv_scale_const(ax_val);
+#ifdef RS_TRACE
+            if (qtid == 0 && fw0 < total) {
+                asm volatile("" ::"r"(raw[0][0].x));  // the first block's X words have arrived
+                RS_TRACE_MARK(g.trace, 20);
+            }
+#endif
             if (FMT == 0 && qtid == 0 && blockIdx.x == 0 && blockIdx.z == 0 && !nv_alpha_supported(ksc.alpha))
                 atomicExch(g.err, kErrInvalidArg);
-            // codes of one block (element offset kk of the slice) and, gathered
-            // over four consecutive lanes, one scale-atom word
+            // codes of one block (element offset kk of the slice) and its scale byte
             auto put = [&](uint32_t rowb, int kk, const uint32_t (&codes)[E / 8], uint32_t sfbyte, bool live) {
                 if (!live) return;
                 const int ci = kk / 256;
@@ -506,62 +578,40 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 // scale byte: atom kb / 4, byte (row % 32) * 16 + (row / 32 % 4) * 4 + kb % 4
                 slot[B_BYTES + (kb / 4) * 512 + (rowb % 32) * 16 + (rowb / 32) * 4 + kb % 4] = (uint8_t)sfbyte;
             };
-            // flat chunk-major mapping: thread qtid takes scale blocks qtid,
-            // qtid + T, ... (T = quantizer threads) of the order (chunk, token
-            // row, block), so chunks complete in order.  All loads of a batch go
-            // out before any arithmetic.
-            constexpr int bpc = 256 / E;    // blocks per token row in one chunk
-            const int cb = g.M * bpc;       // blocks per chunk
-            const int total = nck * cb;
-            auto block_pos = [&](int f, int& j, int& kk) {
-                const int ci = f / cb, rem = f - ci * cb;
-                j = rem / bpc;
-                kk = ci * 256 + (rem - j * bpc) * E;
-            };
-            constexpr int kBatch = 32 / E;  // blocks per thread per batch
-            // the loop bound is per warp (fw): put() shuffles across all 32 lanes
-            for (int fw = qw * 32; fw < total; fw += kBatch * kQuantThreads) {
-                const int f0 = fw + lane;
-                float xs[kBatch][E];
-#pragma unroll
-                for (int r = 0; r < kBatch; ++r) {
-                    const int f = f0 + r * kQuantThreads;
-                    int j, kk;
-                    block_pos(f, j, kk);
-                    const bool live = f < total && kbeg + kk < kend;
-#pragma unroll
-                    for (int q = 0; q < E / 8; ++q) {
-                        float v8[8];
-                        load8_bf16(g.x + (size_t)j * g.K + kbeg + kk + 8 * q, live, v8);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) xs[r][8 * q + e] = v8[e];
-                    }
-                }
+            // the loop bound is per warp (fw): the warp-wide arrival below
+            for (int fw = fw0; fw < total; fw += kBatch * kQuantThreads) {
+                if (fw != fw0) load_batch(fw);
 #pragma unroll
                 for (int r = 0; r < kBatch; ++r) {
                     if (fw + r * kQuantThreads >= total) break;  // whole warp past the end
-                    const int f = f0 + r * kQuantThreads;
+                    const int f = fw + lane + r * kQuantThreads;
                     int j, kk;
                     block_pos(f, j, kk);
                     const bool live = f < total && kbeg + kk < kend;
-                    uint32_t sfq, codes[E / 8];
-                    float xh[E];
-                    quant_block<FMT, E>(xs[r], ksc, sfq, codes, xh);
+                    uint32_t sfq, codes[E / 8], sfr = 0u, rcodes[E / 8];
                     const uint32_t rb = g.fold ? 2u * (uint32_t)j : (uint32_t)j;
-                    put(rb, kk, codes, sfq, live);
                     if (g.fold) {
-                        float rr[E];
-#pragma unroll
-                        for (int e = 0; e < E; ++e)  // residue (Alg. 1 line 6), never fused
-                            rr[e] = __fsub_rn(xs[r][e], xh[e]);
-                        uint32_t sfr, rcodes[E / 8];
-                        float rh[E];
-                        quant_block<FMT, E, false>(rr, ksc, sfr, rcodes, rh);
+                        quant_block_raw<FMT, E, true>(raw[r], ksc, sfq, codes, sfr, rcodes);
+                        put(rb, kk, codes, sfq, live);
                         put(rb + 1u, kk, rcodes, sfr, live);
+                    } else {
+                        quant_block_raw<FMT, E, false>(raw[r], ksc, sfq, codes, sfr, rcodes);
+                        put(rb, kk, codes, sfq, live);
                     }
-                    // the block is in shared memory: count it for its chunk
+#ifdef RS_TRACE
+                    if (qtid == 0 && r == 0 && fw == fw0) RS_TRACE_MARK(g.trace, 21);
+#endif
+                    // these blocks are in shared memory: make them visible to the
+                    // tensor pipe, then one arrival per warp and chunk counts them
                     fence_proxy_async_smem();
-                    if (f < total) mbar_arrive(smem_u32(&cbar[f / cb]));
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int lo = fw + r * kQuantThreads, hi = min(lo + 32, total);
+                        for (int c = lo / cb; c * cb < hi; ++c) {
+                            const int n = min(hi, (c + 1) * cb) - max(lo, c * cb);
+                            mbar_arrive_cnt(smem_u32(&cbar[c]), (uint32_t)n);
+                        }
+                    }
                 }
             }
             if (qtid == 0) RS_TRACE_MARK(g.trace, 17);
@@ -578,18 +628,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             const int row = ew * 32 + lane;                // accumulator lane = channel within the tile
             const int ctid = row;                          // 0..127
             const float gsc = FMT == 0 ? __fmul_rn(ax_val, *g.alpha_w) : 1.0f;
-            float* part = reinterpret_cast<float*>(part_region);  // split-K: [j][channel]
             const uint32_t my_rank = (uint32_t)split;
-            // split-K: lane o of warp 8 sends to owner o; its destinations in
-            // the cluster (receive buffer b at our rank's slot, owner's red_full[b])
-            uint32_t dst_buf0 = 0, dst_buf1 = 0, dst_bar0 = 0, dst_bar1 = 0;
-            if (g.splits > 1 && warp == 8 && lane < g.splits) {
-                const uint32_t rb = recv_base + my_rank * slice_bytes;
-                dst_buf0 = map_dsmem(rb, (uint32_t)lane);
-                dst_bar0 = map_dsmem(smem_u32(&red_full[0]), (uint32_t)lane);
-                dst_buf1 = map_dsmem(rb + (uint32_t)g.recv_bytes, (uint32_t)lane);
-                dst_bar1 = map_dsmem(smem_u32(&red_full[1]), (uint32_t)lane);
-            }
             for (int j = 0; j < ntl; ++j) {
                 const int b = j % nacc;
                 const uint32_t use_ph = (uint32_t)(j / nacc) & 1u;
@@ -603,19 +642,31 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                         else reinterpret_cast<__nv_bfloat16*>(g.y)[idx] = __float2bfloat16_rn(val);
                     }
                 };
-                auto emit = [&](int jj, float z) {
-                    if (g.splits > 1) part[jj * 128 + row] = z;
-                    else store_y(m0 + jj, z);
+                // split-K: outputs o0 .. o0 + 3 go to owner o0 / per_cta, into its
+                // receive buffer b at (our rank, channel row), as one 16-byte
+                // st.async completing on the owner's red_full[b]
+                bool send_ok = true;
+                const uint32_t rbuf = recv_base + (uint32_t)b * (uint32_t)g.recv_bytes +
+                                      (my_rank * 128u + (uint32_t)row) * (uint32_t)per_cta * 4u;
+                const uint32_t rbar = smem_u32(&red_full[b]);
+                auto emit4 = [&](int o0, float z0, float z1, float z2, float z3) {
+                    if (!send_ok) return;
+                    const int o = o0 / per_cta;
+                    st_async_v4(map_dsmem(rbuf + (uint32_t)(o0 - o * per_cta) * 4u, (uint32_t)o),
+                                make_uint4(__float_as_uint(z0), __float_as_uint(z1), __float_as_uint(z2),
+                                           __float_as_uint(z3)),
+                                map_dsmem(rbar, (uint32_t)o));
                 };
                 bool ok = mbar_wait_bounded(smem_u32(&accum_full[b]), use_ph, abort_flag, g.err);
                 if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 6);
                 if (j < 3 && ctid == 0) RS_TRACE_MARK(g.trace, 22 + j);
                 ok = __all_sync(0xFFFFFFFFu, ok && *abort_flag == 0);  // warp-uniform for tcgen05.ld
                 tc_fence_after();
-                if (g.splits > 1 && j > 0) {
-                    // the previous tile's outgoing copies have read our partial
-                    if (warp == 8) bulk_wait_group_read0();  // (the issuing lane's copies; no-op on the rest)
-                    named_bar_sync(1, 128);
+                if (g.splits > 1 && j >= nacc) {
+                    // every owner has summed what was sent into buffer b for tile
+                    // j - nacc (a failed wait sends nothing: the error is recorded)
+                    send_ok = mbar_wait_bounded(smem_u32(&recv_free[b]), (uint32_t)(j / nacc - 1) & 1u, abort_flag,
+                                                g.err, 1000000000ull, true);
                 }
                 bool drained = false;
                 if constexpr (!FUSED && BN >= 128) {
@@ -707,16 +758,22 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                         float v[16];
                         tmem_ld16(tmem + (uint32_t)(b * BN) + quarter + (uint32_t)c, v);
                         if (g.fold) {
+                            float f[8];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q) emit(c / 2 + q, __fadd_rn(v[2 * q], v[2 * q + 1]));  // Fold
+                            for (int q = 0; q < 8; ++q) f[q] = __fadd_rn(v[2 * q], v[2 * q + 1]);  // Fold
+                            emit4(c / 2, f[0], f[1], f[2], f[3]);
+                            emit4(c / 2 + 4, f[4], f[5], f[6], f[7]);
                         } else {
 #pragma unroll
-                            for (int q = 0; q < 16; ++q) emit(c + q, v[q]);
+                            for (int q = 0; q < 16; q += 4) emit4(c + q, v[q], v[q + 1], v[q + 2], v[q + 3]);
                         }
                     }
                 } else if (g.splits > 1) {
-                    for (int jj = 0; jj < outs; ++jj) emit(jj, 0.0f);
+                    for (int o0 = 0; o0 < outs; o0 += 4) emit4(o0, 0.0f, 0.0f, 0.0f, 0.0f);
                 }
+                // every owner expects a full slice: pad the last one
+                if (g.splits > 1)
+                    for (int o0 = outs; o0 < owners * per_cta; o0 += 4) emit4(o0, 0.0f, 0.0f, 0.0f, 0.0f);
                 // accumulator b drained: the MMA warp may start its next tile
                 if (!drained) {
                     tc_fence_before();
@@ -725,47 +782,38 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 }
                 if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 7);
                 if (g.splits > 1) {
-                    // send each owner its slice of outputs: one bulk copy per
-                    // owner into its receive buffer b at our rank's slot
-                    fence_proxy_async_smem();
-                    named_bar_sync(1, 128);
                     if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 13);
-                    if (warp == 8) {
-                        // every owner has consumed what was sent into buffer b
-                        // for tile j - nacc (the whole warp waits; one elected
-                        // lane issues the copies)
-                        bool free_ok = j < nacc || mbar_wait_bounded(smem_u32(&recv_free[b]),
-                                                                     (uint32_t)(j / nacc - 1) & 1u, abort_flag, g.err,
-                                                                     1000000000ull, true);
-                        free_ok = __all_sync(0xFFFFFFFFu, free_ok && *abort_flag == 0);
-                        if (free_ok && lane < g.splits) {
-                            // lane o sends owner o its slice
-                            bulk_copy_to_cluster(b == 0 ? dst_buf0 : dst_buf1,
-                                                 smem_u32(part) + (uint32_t)lane * slice_bytes, slice_bytes,
-                                                 b == 0 ? dst_bar0 : dst_bar1);
-                            bulk_commit_group();
-                            if (j == 0 && lane == 0) RS_TRACE_MARK(g.trace, 14);
-                        }
-                        __syncwarp();
-                    }
+                }
+                if (owner) {
                     // own slice: sum the partners' partials in rank order
-                    const bool got = mbar_wait_bounded(smem_u32(&red_full[b]), use_ph, abort_flag, g.err);
+                    const bool got = mbar_wait_bounded(smem_u32(&red_full[b]), use_ph, abort_flag, g.err,
+                                                       1000000000ull, true);
                     if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 28);
                     const float* recv = reinterpret_cast<const float*>(recv_region + (size_t)b * g.recv_bytes);
                     const bool live = got && *abort_flag == 0;
-                    for (int jj = 0; live && jj < per_cta; ++jj) {
-                        const int jo = split * per_cta + jj;
+                    for (int j4 = 0; live && j4 < per_cta; j4 += 4) {
+                        const int jo = split * per_cta + j4;
                         if (jo >= outs) break;
-                        // all partials first, then the sum in rank order
-                        float pv[kMaxSplits];
+                        // all partials first, then the sums in rank order
+                        float4 pv[kMaxSplits];
 #pragma unroll
                         for (int r = 0; r < kMaxSplits; ++r)
-                            pv[r] = r < g.splits ? recv[(r * per_cta + jj) * 128 + row] : 0.0f;
-                        float acc = 0.0f;
+                            pv[r] = r < g.splits
+                                        ? *reinterpret_cast<const float4*>(recv + ((size_t)r * 128 + row) * per_cta + j4)
+                                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
                         for (int r = 0; r < kMaxSplits; ++r)
-                            if (r < g.splits) acc = __fadd_rn(acc, pv[r]);
-                        store_y(m0 + jo, acc);
+                            if (r < g.splits) {
+                                acc.x = __fadd_rn(acc.x, pv[r].x);
+                                acc.y = __fadd_rn(acc.y, pv[r].y);
+                                acc.z = __fadd_rn(acc.z, pv[r].z);
+                                acc.w = __fadd_rn(acc.w, pv[r].w);
+                            }
+                        store_y(m0 + jo, acc.x);
+                        store_y(m0 + jo + 1, acc.y);
+                        store_y(m0 + jo + 2, acc.z);
+                        store_y(m0 + jo + 3, acc.w);
                     }
                     if (j < 3 && ctid == 0) RS_TRACE_MARK(g.trace, 25 + j);
                     if (j + nacc < ntl) {
@@ -780,7 +828,6 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                     }
                 }
             }
-            if (g.splits > 1 && warp == 8) bulk_wait_group_read0();  // our outgoing copies have read their source
         }
     }
 
@@ -811,17 +858,16 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
 
 // ------------------------------------------------------------------- host --
 
-// Split-K buffers: this CTA's partial and each receive buffer hold `splits`
-// slices of ceil(outs / splits) outputs x 128 channels (fp32).
+// Split-K receive buffer: `splits` slices (one per sending CTA) of
+// ceil(outs / splits) outputs x 128 channels (fp32).
 static size_t split_buf_bytes(int splits, int outs) {
     if (splits <= 1) return 0;
-    const int per_cta = (outs + splits - 1) / splits;
-    return align_up((size_t)splits * per_cta * 128 * sizeof(float), 1024);
+    return align_up((size_t)splits * split_slice(outs, splits) * 128 * sizeof(float), 1024);
 }
 
 static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots, size_t splitbuf, int nacc) {
     const size_t b = fused ? (size_t)slots * b_stage_bytes(fmt, bn) : (size_t)stages * b_stage_bytes(fmt, bn);
-    return 1024 + (size_t)stages * weight_block_bytes(fmt) + b + splitbuf * (size_t)(1 + nacc) + kCtrlBytes;
+    return 1024 + (size_t)stages * weight_block_bytes(fmt) + b + splitbuf * (size_t)nacc + kCtrlBytes;
 }
 
 // Complete plan for a given split count s; stages == 0 when it does not fit.
@@ -889,7 +935,6 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
     p.nacc = nacc;
     p.stages = stages;
     p.slots = p.fused ? max_chunks : 0;
-    p.part_bytes = (int)splitbuf;
     p.recv_bytes = (int)splitbuf;
     if (stages == 0) return p;
     // Two CTAs can share an SM when the shared memory allows it (a dependent
@@ -953,6 +998,8 @@ static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, 
 GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused) {
     return plan_impl(fmt, fold, M, N, K, num_sms, allow_fused);
 }
+
+size_t plan_b_stage_bytes(const GemmPlan& p) { return b_stage_bytes(p.fmt, p.bn); }
 
 size_t alpha_slot_offset(int fmt, bool compensated, int M, int K) {
     return align_up(operand_bytes(fmt, compensated ? 2 * M : M, K), 1024);
@@ -1072,10 +1119,10 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
     a.n_tiles = p.n_tiles;
     a.b_tiles = p.b_tiles;
     a.nacc = p.nacc;
-    a.part_bytes = p.part_bytes;
     a.recv_bytes = p.recv_bytes;
     a.tmem_cols = p.tmem_cols;
     a.dyn_alpha = c.dyn_alpha;
+    a.qdump = p.fused ? static_cast<uint8_t*>(c.qdump) : nullptr;
 #define RS_CASE(F, B, FU)                                                      \
     if (p.fmt == F && p.bn == B && (p.fused != 0) == FU) return launch_typed<F, B, FU>(p, tb, a, stream);
     RS_CASE(0, 16, true) RS_CASE(0, 32, true) RS_CASE(1, 16, true) RS_CASE(1, 32, true)

@@ -42,7 +42,6 @@ struct GemmPlan {
     int splits;      // K splits per output tile (= cluster size when > 1)
     int grid_x;      // persistent CTAs per K split; CTA x takes tiles x, x + grid_x, ...
     int nacc;        // accumulator buffers in tensor memory (2: epilogue overlaps the next tile)
-    int part_bytes;  // split-K: partial buffer in shared memory
     int stages;      // pipeline depth
     int fused;       // quantize the activations inside the GEMM
     int slots;       // fused: activation chunks resident in shared memory
@@ -93,7 +92,10 @@ struct GemmCall {
     int out_f32;
     uint32_t* err;
     int dyn_alpha;         // fused NVFP4 plans: compute the activation tensor scale in the GEMM
+    void* qdump;           // fused plans, test hook: quantized slices out (null: off)
 };
+// Shared-memory bytes of one activation stage (codes + scale atoms) of a plan.
+size_t plan_b_stage_bytes(const GemmPlan& p);
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmCall& call, cudaStream_t stream);
 

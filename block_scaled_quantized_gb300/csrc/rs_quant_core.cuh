@@ -207,6 +207,66 @@ __device__ __forceinline__ void quant_block(const float (&xf)[E], const NvScaleC
     }
 }
 
+// max(|x|) over the bf16 values of W 32-bit words (two per word), as
+// amax16_bf16 does for eight words.
+template <int W>
+__device__ __forceinline__ float amax_bf16_words(const uint32_t* w) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < W; ++i) asm("max.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(w[i] & 0x7FFF7FFFu));
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+}
+
+// One whole block (E = 16 NVFP4 / 32 MXFP4 elements) straight from its raw
+// bf16 words: base codes and scale byte, and with kResidue the residue
+// r = fl(x - fl(s~ dec(q))) quantized with its own scale (Alg. 1: base, then
+// residue).  Same arithmetic per element as quant_block; the elements are
+// widened one 16-byte word at a time, so only the residues are held whole.
+template <int FMT, int E, bool kResidue>
+__device__ __forceinline__ void quant_block_raw(const uint4 (&raw)[E / 8], const NvScaleConst& k, uint32_t& sf,
+                                                uint32_t (&codes)[E / 8], uint32_t& sfr, uint32_t (&rcodes)[E / 8]) {
+    const float am = amax_bf16_words<E / 2>(reinterpret_cast<const uint32_t*>(&raw[0]));
+    float st, mul;
+    sf = FMT == 0 ? nv_block_scale_fast(am, k, st, mul) : mx_block_scale(am, st, mul);
+    float r[kResidue ? E : 1];
+#pragma unroll
+    for (int w = 0; w < E / 8; ++w) {
+        const uint32_t h[4] = {raw[w].x, raw[w].y, raw[w].z, raw[w].w};
+        float x[8], v[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(h[i] << 16);
+            x[2 * i + 1] = __uint_as_float(h[i] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) fmul2_rn(x[e], x[e + 1], mul, mul, v[e], v[e + 1]);
+        codes[w] = e2m1_encode8(v);
+        if constexpr (kResidue) {
+            float d[8];
+            e2m1_decode8(codes[w], d);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) r[8 * w + e] = __fsub_rn(x[e], __fmul_rn(st, d[e]));  // never fused
+        }
+    }
+    if constexpr (kResidue) {
+        float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+            a0 = fmaxf(a0, fabsf(r[e]));
+            a1 = fmaxf(a1, fabsf(r[e + 1]));
+        }
+        float rst, rmul;
+        sfr = FMT == 0 ? nv_block_scale_fast(fmaxf(a0, a1), k, rst, rmul) : mx_block_scale(fmaxf(a0, a1), rst, rmul);
+#pragma unroll
+        for (int w = 0; w < E / 8; ++w) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) fmul2_rn(r[8 * w + e], r[8 * w + e + 1], rmul, rmul, v[e], v[e + 1]);
+            rcodes[w] = e2m1_encode8(v);
+        }
+    }
+}
+
 // Eight bf16 values (one 16-byte word) widened to fp32.
 __device__ __forceinline__ void unpack8_bf16(const uint4& v, float (&xf)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};

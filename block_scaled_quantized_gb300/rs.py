@@ -30,7 +30,8 @@ EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_
            "rs_quantize_weight", "rs_quantize_residue", "rs_linear_w4a4", "rs_linear_compensated",
            "rs_linear_compensated_noalloc", "rs_get_device_error", "rs_kext_width", "rs_kext_select",
            "rs_channel_mean_abs", "rs_kext_act_bytes", "rs_kext_weight_bytes", "rs_kext_workspace_bytes",
-           "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext", "rs_plan_linear", "rs_debug_wait_probe"]
+           "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext", "rs_plan_linear", "rs_debug_wait_probe",
+           "rs_get_device_error_async", "rs_debug_linear_dump"]
 
 
 class RsError(RuntimeError):
@@ -72,6 +73,8 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_linear_kext": ([I, I, I, I, I, P, P, P, P, P, P, P, I, P, SZ, P], I),
         "rs_plan_linear": ([I, I, I, I, I, I, I, P, I], I),
         "rs_debug_wait_probe": ([ctypes.c_uint64, P], I),
+        "rs_get_device_error_async": ([P, P], I),
+        "rs_debug_linear_dump": ([I, I, I, I, I, P, P, P, P, P, I, P, SZ, P, SZ, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -213,6 +216,31 @@ def rs_linear_compensated_noalloc(fmt: int, M: int, N: int, K: int, x=None, alph
 
 def rs_get_device_error(stream=None) -> int:
     return lib().rs_get_device_error(_stream(stream))
+
+
+def rs_get_device_error_async(out: torch.Tensor, stream=None):
+    """Enqueue the read-and-clear of the device error word into out (one
+    int32/uint32 element, device or pinned host memory); no synchronization."""
+    ptr = out.data_ptr()
+    _check("rs_get_device_error_async", lib().rs_get_device_error_async(ptr, _stream(stream)))
+
+
+DUMP_FIELDS = ("fused", "bn", "grid_x", "splits", "slots", "stage_bytes", "chunks")
+
+
+def rs_debug_linear_dump(fmt: int, compensated: bool, M: int, N: int, K: int, x=None, alpha_x=None, wq=None,
+                         alpha_w=None, y=None, workspace=None, dump=None, stream=None) -> dict:
+    """The linear call with its quantizing prologue's slices copied to dump
+    (see rs.h); with dump None, only the layout is returned."""
+    layout = (ctypes.c_int * len(DUMP_FIELDS))()
+    out = OUT_F32 if (y is not None and y.dtype == torch.float32) else OUT_BF16
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    dump_bytes = dump.numel() * dump.element_size() if dump is not None else 0
+    _check("rs_debug_linear_dump",
+           lib().rs_debug_linear_dump(fmt, int(bool(compensated)), M, N, K, _ptr(x), _ptr(alpha_x), _ptr(wq),
+                                      _ptr(alpha_w), _ptr(y), out, _ptr(workspace), ws_bytes, _ptr(dump),
+                                      dump_bytes, layout, _stream(stream)))
+    return dict(zip(DUMP_FIELDS, layout[:]))
 
 
 # -------------------------------------------------- buffer conveniences ----

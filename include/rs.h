@@ -339,6 +339,42 @@ RS_API rs_status rs_debug_wait_probe(uint64_t limit_ns, rs_stream_t stream);
  * Returns RS_ERR_CUDA if the synchronization itself fails. */
 RS_API rs_status rs_get_device_error(rs_stream_t stream);
 
+/* Sync-free form of rs_get_device_error, for a serving loop that polls the
+ * error word without stalling its stream (no operation of the paper: the
+ * device error word is this library's failure reporting).  Enqueues on
+ * `stream`, behind the work already there, one single-thread kernel that
+ * writes the device error word of the current device to *out and clears it.
+ * `out` (4-byte aligned) is device memory, or pinned host memory the device
+ * can reach; its value is one of the codes rs_get_device_error returns and
+ * is valid once the stream has passed this point (an event, a later
+ * synchronization).  Nothing is synchronized inside the call.
+ * RS_ERR_INVALID_ARG for NULL, RS_ERR_ALIGNMENT for a misaligned pointer. */
+RS_API rs_status rs_get_device_error_async(uint32_t *out, rs_stream_t stream);
+
+/* Test hook of the quantizing GEMM prologue (Sec. 4.4: Algorithm 1 of
+ * App. B.2 fused into the GEMM for small M).  Runs exactly the call
+ * rs_linear_compensated (compensated != 0) or rs_linear_w4a4 makes with a
+ * bf16 input and, when its plan quantizes inside the GEMM, also copies every
+ * CTA's quantized activation slice to `dump` (device), as the MMAs read it.
+ * layout (host, 7 ints) receives: fused (0/1), bn (rows of the activation
+ * tile), grid_x (CTAs per K split), splits, slots (chunk stages per CTA),
+ * stage_bytes, chunks (256-element K chunks of the call).  The slice of the
+ * CTA (x, split z) starts at byte (z * grid_x + x) * slots * stage_bytes;
+ * its K chunks are the consecutive chunks c0 .. c0 + n - 1 of split z, where
+ * the chunks are dealt out as evenly as possible, the first
+ * (chunks % splits) splits taking one more.  Chunk i of the slice occupies
+ * stage_bytes at offset i * stage_bytes: codes of bn rows x 128 bytes in the
+ * 128-byte-swizzled image (row r, byte b at r * 128 + ((b / 16) ^ (r % 8))
+ * * 16 + b % 16; paired rows 2j = base, 2j + 1 = residue of token j), then
+ * one 512-byte scale atom per 4 blocks in the rs operand's atom layout.
+ * With dump == NULL only layout is written.  RS_ERR_UNSUPPORTED when the plan
+ * quantizes in a separate kernel; RS_ERR_WORKSPACE when dump_bytes is below
+ * grid_x * splits * slots * stage_bytes. */
+RS_API rs_status rs_debug_linear_dump(rs_format fmt, int compensated, int M, int N, int K, const void *x_bf16,
+                                      const float *alpha_x, const void *wq, const float *alpha_w, void *y,
+                                      rs_out_dtype out_dtype, void *workspace, size_t ws_bytes, void *dump,
+                                      size_t dump_bytes, int *layout, rs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

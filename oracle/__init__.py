@@ -103,6 +103,8 @@ def _load():
         lib.or_linear_kext.argtypes = [i, i, i, i, i, P, f, P, P, P, f, P]
         lib.or_quantize_nvfp4_div.argtypes = [i, i, P, f, P, P]
         lib.or_quantize_nvfp4_div.restype = i
+        lib.or_quantize_residue_nvfp4_recon_div.argtypes = [i, i, P, f, P, P, P, P]
+        lib.or_quantize_residue_nvfp4_recon_div.restype = i
         lib.or_linear_kext.restype = i
         _lib = lib
         return lib
@@ -195,6 +197,21 @@ def quantize_nvfp4_div(x_u16, alpha: float):
     if _load().or_quantize_nvfp4_div(rows, K, _ptr(x), float(alpha), _ptr(codes), _ptr(sf)):
         raise ValueError("oracle quantize_nvfp4_div: bad shape")
     return codes, sf
+
+
+def quantize_residue_nvfp4_recon_div(x_u16, alpha: float):
+    """NVFP4 base and residue operands with Alg. 1's reconstruction
+    x^ = fl(dec(q) / fl(1/s~)) in place of Eq. 10's fl(s~ dec(q)) (the
+    alternative reading; parity uses Eq. 10).  Returns dict with codes_x,
+    sf_x, codes_r, sf_r."""
+    x = _as_u16(x_u16)
+    rows, K = x.shape
+    out = dict(codes_x=np.zeros((rows, K // 2), np.uint8), sf_x=np.zeros((rows, K // 16), np.uint8),
+               codes_r=np.zeros((rows, K // 2), np.uint8), sf_r=np.zeros((rows, K // 16), np.uint8))
+    if _load().or_quantize_residue_nvfp4_recon_div(rows, K, _ptr(x), float(alpha), _ptr(out["codes_x"]),
+                                                   _ptr(out["sf_x"]), _ptr(out["codes_r"]), _ptr(out["sf_r"])):
+        raise ValueError("oracle quantize_residue_nvfp4_recon_div: bad shape")
+    return out
 
 
 def quantize_residue(fmt: int, x_u16, alpha: float = 0.0):

@@ -362,6 +362,51 @@ int or_quantize_nvfp4_div(int rows, int K, const uint16_t *x, float alpha, uint8
     return 0;
 }
 
+/* NVFP4 base plus residue with Alg. 1's form of the reconstruction in place
+ * of Eq. 10's (the alternative to reading R5; parity is defined on Eq. 10).
+ * Alg. 1 line 5 forms x_q = QDQ(scale * x), i.e. dec(q) in the scaled
+ * domain, with `scale` the fp32 multiplier fl(1/s~); line 6 writes the
+ * residue as x - x_q / scale.  So x^ = fl(dec(q) / fl(1/s~)) (0 when the
+ * multiplier is 0), r = fl(x - x^), and r is quantized by the same rule as
+ * the base (its own block scale, the same alpha).  Codes and scale bytes of
+ * both operands, logical layout. */
+int or_quantize_residue_nvfp4_recon_div(int rows, int K, const uint16_t *x, float alpha,
+                                        uint8_t *codes_x, uint8_t *sf_x, uint8_t *codes_r, uint8_t *sf_r)
+{
+    float xf[16], r[16], xh_unused[16];
+    uint8_t q[16];
+    if (rows < 0 || K <= 0 || K % 16 != 0)
+        return 1;
+    for (int row = 0; row < rows; ++row) {
+        for (int b = 0; b < K / 16; ++b) {
+            float amax = 0.0f, s, t, st, mul;
+            uint8_t sf;
+            for (int i = 0; i < 16; ++i) {
+                xf[i] = bf16_to_float(x[(int64_t)row * K + b * 16 + i]);
+                if (fabsf(xf[i]) > amax)
+                    amax = fabsf(xf[i]);
+            }
+            s = amax / 6.0f;
+            t = (alpha > 0.0f) ? s / alpha : 0.0f;
+            sf = or_e4m3_encode_satfinite(t);
+            st = alpha * (float)or_e4m3_decode(sf);
+            mul = (st == 0.0f) ? 0.0f : 1.0f / st;           /* Alg. 1 line 3: multiplier */
+            for (int i = 0; i < 16; ++i) {
+                float xq;
+                q[i] = or_e2m1_encode(xf[i] * mul);           /* line 5: q of scale * x    */
+                xq = (float)or_e2m1_decode(q[i]);             /* line 5: x_q = dec(q)      */
+                r[i] = xf[i] - (mul == 0.0f ? 0.0f : xq / mul); /* line 6: x - x_q / scale */
+                put_nibble(codes_x + (int64_t)row * (K / 2), b * 16 + i, q[i]);
+            }
+            sf_x[(int64_t)row * (K / 16) + b] = sf;
+            nvfp4_block(r, 16, alpha, &sf_r[(int64_t)row * (K / 16) + b], q, xh_unused);
+            for (int i = 0; i < 16; ++i)
+                put_nibble(codes_r + (int64_t)row * (K / 2), b * 16 + i, q[i]);
+        }
+    }
+    return 0;
+}
+
 /* Base plus residue (Sec. 2 "r = x - x^"; Sec. 4.2 R = X - X^; App. B.2: the
  * residue is a separate operand with its own block scales and the same tensor
  * scale).  Outputs the two operands separately in logical layout.
