@@ -5,14 +5,18 @@ residue quantization, block-scaled tcgen05 GEMM with on-chip Fold, bf16
 output) for the attention-projection workload: M=8 tokens, K=N=4096,
 X = Student-t(nu=4) x per-channel LogNormal(0,1), W ~ N(0, 0.02^2), seed 0.
 The weight operand is rotated over enough copies that every step reads it
-from HBM (working set > 2x L2).  K steps are captured in one CUDA graph and
-timed with CUDA events; `value` is microseconds per step.
+from HBM (working set > 2x L2).  K steps are captured in one CUDA graph; the
+graph is replayed several times, each replay timed with CUDA events between
+synchronizations, and `value` is the median microseconds per step.
 
-Extra keys: the M in {1,2,4,8} sweep of compensated vs W4A4 latency and HBM
-roofline fraction, the MLP pair, the MXFP4 sweep and the prefill TFLOP/s,
-the roofline of the dominant kernel (the GEMM, timed alone), the CPU oracle
-baseline, an end-to-end number through host buffers, and the SM clocks
-sampled during the timed region.
+Extra keys: the paper's protocol (a 200-call graph, median of five replays)
+and the latency of one call on its own; config 1 (M=1, K=N=2048); the M in
+{1,2,4,8} sweep of compensated vs W4A4 latency and HBM roofline fraction;
+the MLP pair, the MXFP4 sweep, the prefill TFLOP/s, the 22 projection shapes
+and the on-chip Fold ablation; the roofline of the dominant kernel; the CPU
+oracle on all host cores and on one (and on a sample of the prefill rows);
+an end-to-end number through host buffers; the SM clocks sampled during the
+timed region.
 
 --impl reference times the CPU oracle (the plain C reference) on the same
 workload on the host cores.
@@ -281,6 +285,92 @@ def shape_sweep(torch, rs, workloads, hbm, Ms=(8,)) -> list:
     return rows
 
 
+def capture(torch, fn_step, steps: int):
+    """A CUDA graph of `steps` calls (after three eager warm-up calls)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(3):
+            fn_step(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(steps):
+                fn_step(i)
+    torch.cuda.synchronize()
+    return g
+
+
+def replay_us(torch, g, steps: int, reps: int, world: int = 1) -> list[float]:
+    """us per call of each of `reps` replays of a graph of `steps` calls, each
+    replay bracketed by a barrier (several ranks) and a synchronize."""
+    times = []
+    for _ in range(reps):
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1000.0 / steps)
+    return times
+
+
+def isolated_call_us(torch, lin, reps: int = 60) -> dict:
+    """Latency of one call with no kernel of ours in flight before it: one
+    call per CUDA graph (one graph per weight copy, so each call reads its
+    weights from HBM), launched behind a sleep kernel so that the host launch
+    is hidden, CUDA events right around it."""
+    graphs = [capture(torch, lambda i, c=c: lin.call(c), 1) for c in range(len(lin.wqs))]
+    times = []
+    for r in range(reps):
+        g = graphs[r % len(graphs)]
+        torch.cuda._sleep(40000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1000.0)
+    return {"us": round(statistics.median(times), 3), "min_us": round(min(times), 3), "calls": reps}
+
+
+def fold_ablation(torch, rs, workloads, hbm, Ms=(1, 2, 4, 8, 16, 32, 64)) -> list:
+    """On-chip Fold against writing the expanded Z and folding in a separate
+    kernel (Sec. 5.1, Fig. 6b), compensated NVFP4, K = N = 4096: both start
+    from the standalone paired quantizer; the unfused path runs the plain
+    GEMM over the 2M paired rows with fp32 output, then rs_fold_pairs."""
+    rows = []
+    for M in Ms:
+        lin = Linear(torch, rs, workloads, rs.NVFP4, "attn_proj_k4096", M, True)
+        z = torch.empty((2 * M, lin.N), dtype=torch.float32, device="cuda")
+
+        def quant(i):
+            rs.rs_quantize_residue(rs.NVFP4, lin.x, lin.ax, lin.xq)
+
+        def onchip(i):
+            quant(i)
+            rs.rs_linear_compensated(rs.NVFP4, M, lin.N, lin.K, xq_paired=lin.xq, alpha_x=lin.ax,
+                                     wq=lin.wqs[i % len(lin.wqs)], alpha_w=lin.aw, y=lin.y, workspace=lin.ws)
+
+        def separate(i):
+            quant(i)
+            rs.rs_linear_w4a4(rs.NVFP4, 2 * M, lin.N, lin.K, xq=lin.xq, alpha_x=lin.ax,
+                              wq=lin.wqs[i % len(lin.wqs)], alpha_w=lin.aw, y=z, workspace=lin.ws)
+            rs.rs_fold_pairs(M, lin.N, z, lin.y)
+
+        a, _ = graph_time_us(torch, onchip, 100)
+        b, _ = graph_time_us(torch, separate, 100)
+        c, _ = graph_time_us(torch, lin.call, 100)
+        rows.append({"M": M, "onchip_fold_us": round(a, 3), "separate_fold_us": round(b, 3),
+                     "separate_over_onchip": round(b / a, 4), "one_launch_us": round(c, 3)})
+        del lin, z
+    return rows
+
+
 def graph_time_us(torch, fn_step, steps: int, reps: int = 5, warm: int = 3) -> tuple[float, list[float]]:
     """Capture `steps` calls in a CUDA graph; return median us per call."""
     s = torch.cuda.Stream()
@@ -365,17 +455,7 @@ def run_gpu(args) -> dict:
     # ---------------- headline: compensated, M=8, K=N=4096, NVFP4
     main = Linear(torch, rs, workloads, rs.NVFP4, "attn_proj_k4096", 8, True)
     K_steps, W = args.steps, args.warmup
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        for i in range(3):
-            main.call(i)
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            for i in range(K_steps):
-                main.call(i)
-    torch.cuda.synchronize()
+    g = capture(torch, main.call, K_steps)
     for _ in range(W):
         g.replay()
     torch.cuda.synchronize()
@@ -386,24 +466,26 @@ def run_gpu(args) -> dict:
     while time.time() < t_end:
         g.replay()
         torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    g.replay()
-    e1.record()
-    e1.synchronize()
-    torch.cuda.synchronize()
+    # the timed region: `replays` replays of the K-step graph, each bracketed
+    # by a barrier and a synchronize; the step time is their median
+    reps = replay_us(torch, g, K_steps, max(5, args.replays), world)
     clocks = sampler.stop()
-    t_ms = e0.elapsed_time(e1)
+    us_local = statistics.median(reps)
     if args.headline_only:
-        out = {"metric": METRIC, "value": round(t_ms * 1000.0 / K_steps, 3), "unit": "us", "n_gpus": world,
+        out = {"metric": METRIC, "value": round(us_local, 3), "unit": "us", "n_gpus": world,
                "steps": K_steps, "warmup": W, "headline_only": True, "clocks": clocks}
         return out if rank == 0 else None
-    t_ms = max_over_ranks(t_ms, world, "cuda")
-    us_per_step = t_ms * 1000.0 / K_steps
+    us_per_step = max_over_ranks(us_local, world, "cuda")
     hbm = peaks["hbm_gbs"]
+    # the paper's protocol (App. C.1): CUDA-graph replay of >= 200 calls,
+    # median of five replays; and one call on its own
+    g200 = capture(torch, main.call, 200)
+    protocol = {"graph_calls": 200, "replays": 5, "us": round(statistics.median(replay_us(torch, g200, 200, 5)), 3)}
+    del g200
+    sampler2 = ClockSampler(local)
+    sampler2.start()
+    isolated = isolated_call_us(torch, main)
+    isolated["clocks"] = sampler2.stop()
 
     # ---------------- dominant kernel alone: the GEMM on a pre-quantized operand
     # The headline step is one launch of the fused quantize+GEMM+Fold kernel,
@@ -418,6 +500,17 @@ def run_gpu(args) -> dict:
     # the headline call finding its own activation tensor scale (no alpha_x)
     own_us, _ = graph_time_us(torch, lambda i: main.call(i, own_scale=True), K_steps)
     extra_own = {"us": round(own_us, 3), "over_given_scale": round(own_us / us_per_step, 4)}
+
+    # ---------------- config 1: NVFP4, M = 1, K = N = 2048 (compensated and W4A4)
+    cfg1 = {}
+    for comp in (False, True):
+        lin = Linear(torch, rs, workloads, rs.NVFP4, "gauss_outlier_k2048", 1, comp)
+        us, _ = graph_time_us(torch, lin.call, 200)
+        key = "comp" if comp else "w4a4"
+        cfg1[f"{key}_us"] = round(us, 3)
+        cfg1[f"{key}_hbm_frac"] = round(lin.call_bytes() / (us * 1e-6) / 1e9 / hbm, 4)
+        del lin
+    cfg1["comp_over_w4a4"] = round(cfg1["comp_us"] / cfg1["w4a4_us"], 4)
 
     # ---------------- sweep M = 1, 2, 4, 8 compensated vs W4A4
     sweep = []
@@ -492,6 +585,7 @@ def run_gpu(args) -> dict:
             pre[f"{key}_frac"] = round(pre[f"{key}_executed_tflops"] / fp4_peak, 4)
         extra["prefill_M4096_K8192_N8192"] = pre
         torch.cuda.empty_cache()
+        extra["fold_ablation_k4096_n4096"] = fold_ablation(torch, rs, workloads, hbm)
 
     # ---------------- end to end through host buffers (pinned), public API
     xh = main.x_host.pin_memory()
@@ -521,7 +615,12 @@ def run_gpu(args) -> dict:
         "config": {"workload": WORKLOAD, "M": 8, "K": 4096, "N": 4096, "format": "nvfp4",
                    "compensated": True, "global_batch": 8, "weight_copies": len(main.wqs),
                    "l2_policy": "weights rotated over copies > 2x L2 (inputs larger than L2)",
-                   "parallelism": f"replicas{world}", "timing": "cuda-graph of K calls, cuda events"},
+                   "parallelism": f"replicas{world}",
+                   "timing": f"cuda-graph of K calls, median of {max(5, args.replays)} replays, cuda events"},
+        "replays_us": [round(t, 3) for t in reps],
+        "protocol_graph200": protocol,
+        "isolated_call": isolated,
+        "config1_nvfp4_m1_k2048_n2048": cfg1,
         "sweep_attn_proj_k4096": sweep,
         "headline_own_tensor_scale": extra_own,
         **extra,
@@ -542,6 +641,8 @@ def run_gpu(args) -> dict:
     }
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        if not args.quick:
+            out["cpu_oracle_prefill_sample"] = cpu_prefill_sample()
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -550,10 +651,7 @@ def run_gpu(args) -> dict:
 
 # --------------------------------------------------------------- CPU oracle --
 
-def cpu_baseline(budget_s: float) -> dict:
-    """The oracle (single-threaded plain C, double GEMM) on the same workload:
-    one compensated linear call, M=8, K=N=4096, repeated for ~budget_s."""
-    import numpy as np
+def _oracle_headline_inputs():
     import oracle
     from block_scaled_quantized_gb300 import workloads
     oracle.build()
@@ -563,17 +661,64 @@ def cpu_baseline(budget_s: float) -> dict:
     aw = oracle.tensor_scale(wb)
     cw, sw, _ = oracle.quantize(0, wb, aw)          # offline weight quantization: untimed
     ax = oracle.tensor_scale(xb)                    # calibrated activation scale: untimed
+    return xb, ax, cw, sw, aw
+
+
+def _time_oracle_calls(args, budget_s: float, max_calls: int) -> list:
+    import oracle
     times = []
     t_end = time.time() + budget_s
     while True:
         t0 = time.perf_counter()
-        oracle.linear(0, True, xb, ax, cw, sw, aw)
+        oracle.linear(0, True, *args)
         times.append(time.perf_counter() - t0)
-        if time.time() > t_end or len(times) >= 50:
+        if time.time() > t_end or len(times) >= max_calls:
             break
-    us = statistics.median(times) * 1e6
-    return {"value": round(us, 1), "unit": "us", "cores": 1, "kind": "oracle",
-            "sample": f"full workload step (M=8, K=N=4096 compensated NVFP4), {len(times)} calls, median"}
+    return times
+
+
+def cpu_baseline(budget_s: float) -> dict:
+    """The oracle (plain C, double GEMM) on the same workload, one compensated
+    linear call at M=8, K=N=4096: on all host cores (OpenMP over the output
+    elements; `value`, `cores`) and single-threaded, ~budget_s in total."""
+    import oracle
+    inputs = _oracle_headline_inputs()
+    cores = os.cpu_count() or 1
+    oracle.set_threads(1)
+    single = _time_oracle_calls(inputs, budget_s / 2, 30)
+    oracle.set_threads(cores)
+    multi = _time_oracle_calls(inputs, budget_s / 2, 200)
+    oracle.set_threads(1)
+    return {"value": round(statistics.median(multi) * 1e6, 1), "unit": "us", "cores": cores, "kind": "oracle",
+            "single_thread_us": round(statistics.median(single) * 1e6, 1),
+            "sample": f"full workload step (M=8, K=N=4096 compensated NVFP4): median of {len(multi)} calls "
+                      f"on {cores} threads, {len(single)} calls on one thread"}
+
+
+def cpu_prefill_sample(rows: int = 256) -> dict:
+    """The oracle on a seeded sample of the prefill workload (M = 4096,
+    K = N = 8192, compensated): `rows` token rows x all N, on all cores; the
+    time of the whole call is that x 4096 / rows (labelled as extrapolated)."""
+    import numpy as np
+    import oracle
+    from block_scaled_quantized_gb300 import workloads
+    oracle.build()
+    cores = os.cpu_count() or 1
+    x = workloads.make_x("prefill_k8192", 4096)
+    pick = np.sort(np.random.default_rng(5).choice(4096, rows, replace=False))
+    xb = workloads.bf16_bits(x)[pick]
+    wb = workloads.bf16_bits(workloads.make_w("prefill_k8192"))
+    oracle.set_threads(cores)
+    aw = oracle.tensor_scale(wb)
+    cw, sw, _ = oracle.quantize(0, wb, aw)
+    ax = oracle.tensor_scale(workloads.bf16_bits(x))
+    t0 = time.perf_counter()
+    oracle.linear(0, True, xb, ax, cw, sw, aw)
+    dt = time.perf_counter() - t0
+    oracle.set_threads(1)
+    return {"rows": rows, "N": 8192, "K": 8192, "seconds": round(dt, 3), "cores": cores,
+            "extrapolated_full_call_s": round(dt * 4096 / rows, 2), "kind": "oracle",
+            "sample": f"{rows} seeded token rows of 4096 x all 8192 channels, compensated NVFP4"}
 
 
 def run_reference(args) -> dict | None:
@@ -612,6 +757,7 @@ def main():
     ap.add_argument("--shapes", action="store_true",
                     help="projection-shape sweep at M in {1, 8, 64, 512} (default: M = 8)")
     ap.add_argument("--soak-s", type=float, default=1.5)
+    ap.add_argument("--replays", type=int, default=7, help="timed replays of the K-step graph (median; at least 5)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true",

@@ -391,6 +391,19 @@ namespace rs {
 __global__ void read_error_kernel(uint32_t* err, uint32_t* out) { *out = atomicExch(err, 0u); }
 }  // namespace rs
 
+rs_status rs_fold_pairs(int M, int N, const float* z, void* y, rs_out_dtype out_dtype, rs_stream_t stream) {
+    if (M < 0 || N < 0 || (out_dtype != RS_OUT_BF16 && out_dtype != RS_OUT_F32)) return RS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return RS_OK;
+    if (!z || !y) return RS_ERR_INVALID_ARG;
+    if (!aligned16(z) || !aligned16(y)) return RS_ERR_ALIGNMENT;
+    cudaError_t why;
+    const rs::DeviceInfo* dev = rs::current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    return from_cuda(launch_fold_pairs(z, y, M, N, out_dtype == RS_OUT_F32 ? 1 : 0, (cudaStream_t)stream,
+                                       dev->num_sms));
+}
+
 rs_status rs_get_device_error_async(uint32_t* out, rs_stream_t stream) {
     if (!out) return RS_ERR_INVALID_ARG;
     if (!aligned4(out)) return RS_ERR_ALIGNMENT;

@@ -856,7 +856,43 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     }
 }
 
+// Separate Fold (Sec. 4.3 Eq. 2) for the on-chip Fold ablation (Sec. 5.1,
+// Fig. 6b): y[j][n] = z[2j][n] + z[2j+1][n] from an expanded fp32 output of
+// the paired rows; four outputs per thread when N % 4 == 0.
+__global__ void __launch_bounds__(256) fold_pairs_kernel(const float* __restrict__ z, void* __restrict__ y, int M,
+                                                         int N, int out_f32) {
+    const bool vec = (N & 3) == 0;
+    const int64_t per_row = vec ? N / 4 : N;
+    const int64_t total = (int64_t)M * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t j = i / per_row, c = i - j * per_row;
+        if (vec) {
+            const float4 a = reinterpret_cast<const float4*>(z + (2 * j) * N)[c];
+            const float4 b = reinterpret_cast<const float4*>(z + (2 * j + 1) * N)[c];
+            const float4 v = make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+            if (out_f32) {
+                reinterpret_cast<float4*>(static_cast<float*>(y) + j * N)[c] = v;
+            } else {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+                reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + j * N)[c] = pk;
+            }
+        } else {
+            const float v = __fadd_rn(z[(2 * j) * N + c], z[(2 * j + 1) * N + c]);
+            if (out_f32) static_cast<float*>(y)[j * N + c] = v;
+            else static_cast<__nv_bfloat16*>(y)[j * N + c] = __float2bfloat16_rn(v);
+        }
+    }
+}
+
 // ------------------------------------------------------------------- host --
+
+cudaError_t launch_fold_pairs(const float* z, void* y, int M, int N, int out_f32, cudaStream_t stream, int num_sms) {
+    const int64_t work = (int64_t)M * (((N & 3) == 0) ? N / 4 : N);
+    const int64_t blocks = std::min<int64_t>((work + 255) / 256, (int64_t)num_sms * 8);
+    fold_pairs_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, stream>>>(z, y, M, N, out_f32);
+    return cudaGetLastError();
+}
 
 // Split-K receive buffer: `splits` slices (one per sending CTA) of
 // ceil(outs / splits) outputs x 128 channels (fp32).

@@ -99,6 +99,9 @@ size_t plan_b_stage_bytes(const GemmPlan& p);
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmCall& call, cudaStream_t stream);
 
+// Separate Fold of an expanded fp32 output of paired rows (z [2M][N] -> y [M][N]).
+cudaError_t launch_fold_pairs(const float* z, void* y, int M, int N, int out_f32, cudaStream_t stream, int num_sms);
+
 // Device error word of the current device.
 uint32_t* device_error_word();
 

@@ -31,7 +31,7 @@ EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_
            "rs_linear_compensated_noalloc", "rs_get_device_error", "rs_kext_width", "rs_kext_select",
            "rs_channel_mean_abs", "rs_kext_act_bytes", "rs_kext_weight_bytes", "rs_kext_workspace_bytes",
            "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext", "rs_plan_linear", "rs_debug_wait_probe",
-           "rs_get_device_error_async", "rs_debug_linear_dump"]
+           "rs_get_device_error_async", "rs_debug_linear_dump", "rs_fold_pairs"]
 
 
 class RsError(RuntimeError):
@@ -74,6 +74,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_plan_linear": ([I, I, I, I, I, I, I, P, I], I),
         "rs_debug_wait_probe": ([ctypes.c_uint64, P], I),
         "rs_get_device_error_async": ([P, P], I),
+        "rs_fold_pairs": ([I, I, P, P, I, P], I),
         "rs_debug_linear_dump": ([I, I, I, I, I, P, P, P, P, P, I, P, SZ, P, SZ, P, P], I),
     }
     for name, (args, res) in sig.items():
@@ -212,6 +213,12 @@ def rs_linear_compensated_noalloc(fmt: int, M: int, N: int, K: int, x=None, alph
     _check("rs_linear_compensated_noalloc",
            lib().rs_linear_compensated_noalloc(fmt, M, N, K, _ptr(x), _ptr(alpha_x), _ptr(wq), _ptr(alpha_w),
                                                _ptr(y), out, _stream(stream)))
+
+
+def rs_fold_pairs(M: int, N: int, z: torch.Tensor, y: torch.Tensor, stream=None):
+    """y[j] = z[2j] + z[2j+1] (separate Fold kernel, for the ablation)."""
+    out = OUT_F32 if y.dtype == torch.float32 else OUT_BF16
+    _check("rs_fold_pairs", lib().rs_fold_pairs(M, N, _ptr(z), _ptr(y), out, _stream(stream)))
 
 
 def rs_get_device_error(stream=None) -> int:

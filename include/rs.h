@@ -287,6 +287,18 @@ RS_API rs_status rs_linear_kext(rs_format fmt, int M, int N, int K, int k, const
                                 const float *alpha_w, void *y, rs_out_dtype out_dtype, void *workspace,
                                 size_t ws_bytes, rs_stream_t stream);
 
+/* ---- separate Fold (ablation of the on-chip Fold) ------------------------ */
+
+/* y[j][n] = z[2j][n] + z[2j+1][n] for j < M, n < N (Sec. 4.3 Eq. 2, Fold):
+ * the Fold as its own kernel over an expanded fp32 output z [2M][N]
+ * (device, row-major) of paired activation rows, e.g. rs_linear_w4a4 run on a
+ * paired operand of 2M rows with fp32 output.  y [M][N] (device) is bf16 or
+ * fp32 per out_dtype; the sums are fp32, rounded once.  It exists to measure
+ * what folding on chip saves (Sec. 5.1, Fig. 6b); the linear calls never use
+ * it.  RS_ERR_INVALID_ARG for negative sizes, a NULL pointer or a bad dtype;
+ * RS_ERR_ALIGNMENT unless z and y are 16-byte aligned. */
+RS_API rs_status rs_fold_pairs(int M, int N, const float *z, void *y, rs_out_dtype out_dtype, rs_stream_t stream);
+
 /* ---- compensated linear without any device allocation -------------------- */
 
 /* Size of the fixed device array that rs_linear_compensated_noalloc uses in

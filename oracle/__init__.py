@@ -47,7 +47,7 @@ def build(force: bool = False) -> str:
              or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
     if force or stale:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
                "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB_PATH)
@@ -103,6 +103,8 @@ def _load():
         lib.or_linear_kext.argtypes = [i, i, i, i, i, P, f, P, P, P, f, P]
         lib.or_quantize_nvfp4_div.argtypes = [i, i, P, f, P, P]
         lib.or_quantize_nvfp4_div.restype = i
+        lib.or_set_threads.argtypes = [i]
+        lib.or_set_threads.restype = None
         lib.or_quantize_residue_nvfp4_recon_div.argtypes = [i, i, P, f, P, P, P, P]
         lib.or_quantize_residue_nvfp4_recon_div.restype = i
         lib.or_linear_kext.restype = i
@@ -164,6 +166,12 @@ def e8m0_decode(b: int) -> float:
 
 
 # ------------------------------------------------------------- quantizer ---
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's dequantization and GEMM loops (default 1);
+    results do not depend on it (each output is the same ordered sum)."""
+    _load().or_set_threads(int(n))
+
 
 def tensor_scale(x_u16) -> np.float32:
     """alpha = fl(amax / 2688) over the whole tensor (App. B.2 Eq. 8)."""

@@ -452,10 +452,17 @@ static double decode_sf(int fmt, uint8_t b)
 
 /* Values represented by the codes and block scales, without the tensor scale:
  * out[r][k] = dec(code[r][k]) * dec(sf[r][k / bs]). */
+/* Threads for the dequantization and the GEMM loops (1 unless the caller
+ * asks for more: the all-core timing of the CPU baseline). */
+static int or_threads = 1;
+
+void or_set_threads(int n) { or_threads = n > 0 ? n : 1; }
+
 void or_dequantize(int fmt, int rows, int K, const uint8_t *codes, const uint8_t *sf,
                    double *out)
 {
     int bs = or_block_size(fmt);
+#pragma omp parallel for schedule(static) num_threads(or_threads)
     for (int r = 0; r < rows; ++r) {
         for (int k = 0; k < K; ++k) {
             uint8_t byte = codes[(int64_t)r * (K / 2) + k / 2];
@@ -479,9 +486,11 @@ int or_block_gemm(int fmt, int M, int N, int K,
     B = (double *)malloc(sizeof(double) * (size_t)((int64_t)N * K + 1));
     or_dequantize(fmt, M, K, codes_a, sf_a, A);
     or_dequantize(fmt, N, K, codes_b, sf_b, B);
+    /* each output is the same k-ordered double sum whatever the thread count */
+#pragma omp parallel for collapse(2) schedule(static) num_threads(or_threads)
     for (int m = 0; m < M; ++m) {
-        const double *a = A + (int64_t)m * K;
         for (int n = 0; n < N; ++n) {
+            const double *a = A + (int64_t)m * K;
             const double *b = B + (int64_t)n * K;
             double acc = 0.0;
             for (int k = 0; k < K; ++k)

@@ -205,3 +205,32 @@ def test_tensor_scale_in_call_flags_non_finite_input():
     rs.rs_linear_compensated(0, M, N, K, x=x.to(DEV), alpha_x=None, wq=wp["wq"], alpha_w=wp["aw"], y=y,
                              workspace=ws)
     assert rs.rs_get_device_error() == rs.RS_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("M,N", [(1, 4096), (8, 4096), (5, 387), (64, 1024)])
+def test_separate_fold_pipeline(M, N):
+    """The unfused alternative the on-chip Fold is measured against (Sec. 5.1,
+    Fig. 6b): the paired operand through the plain GEMM as 2M rows with fp32
+    output (the expanded Z), then the Fold kernel.  The Fold is the fp32 sum
+    of row pairs (bit-exact against torch), and the pipeline matches the
+    oracle's compensated layer within the output tolerance."""
+    K = 1024
+    x = workloads.make_x("attn_proj_k4096", M, K=K, seed=M + 1)
+    w = workloads.make_w("attn_proj_k4096", N=N, K=K, seed=N)
+    wp = prepare_weight(0, w)
+    x_gpu = x.to(DEV)
+    ax = gpu_tensor_scale(x_gpu)
+    xq = torch.empty(rs.rs_operand_bytes(0, 2 * M, K), dtype=torch.uint8, device=DEV)
+    rs.rs_quantize_residue(0, x_gpu, ax, xq)
+    z = torch.full((2 * M, N), float("nan"), dtype=torch.float32, device=DEV)
+    rs.rs_linear_w4a4(0, 2 * M, N, K, xq=xq, alpha_x=ax, wq=wp["wq"], alpha_w=wp["aw"], y=z)
+    y32 = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    y16 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    rs.rs_fold_pairs(M, N, z, y32)
+    rs.rs_fold_pairs(M, N, z, y16)
+    torch.cuda.synchronize()
+    assert rs.rs_get_device_error() == 0
+    want = z[0::2] + z[1::2]
+    assert torch.equal(y32, want)
+    assert torch.equal(y16, want.to(torch.bfloat16))
+    assert_close_f32(y32, oracle_linear(0, True, x, wp))

@@ -113,3 +113,22 @@ def test_compensation_lowers_nmse(oracle_mod, fmt, recipe):
     # With the weight error removed the activation error shrinks sharply.
     ref_w = x.double().numpy() @ wq.astype(np.float64).T
     assert o.nmse(comp, ref_w) < 0.1 * o.nmse(plain, ref_w)
+
+
+def test_thread_count_does_not_change_results():
+    """The all-core baseline runs the same k-ordered double sums: outputs are
+    bit-identical for any number of oracle threads."""
+    import oracle
+    from block_scaled_quantized_gb300 import workloads
+    x = workloads.make_x("attn_proj_k4096", 5, K=512, seed=9)
+    w = workloads.make_w("attn_proj_k4096", N=300, K=512, seed=9)
+    xb, wb = workloads.bf16_bits(x), workloads.bf16_bits(w)
+    aw = oracle.tensor_scale(wb)
+    cw, sw, _ = oracle.quantize(0, wb, aw)
+    ax = oracle.tensor_scale(xb)
+    ys = []
+    for t in (1, 3, 8):
+        oracle.set_threads(t)
+        ys.append(oracle.linear(0, True, xb, ax, cw, sw, aw))
+    oracle.set_threads(1)
+    assert np.array_equal(ys[0], ys[1]) and np.array_equal(ys[0], ys[2])
