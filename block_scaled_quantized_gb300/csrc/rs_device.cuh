@@ -498,22 +498,9 @@ __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-// Asynchronous 32-bit store into another CTA's shared memory (cluster
-// addresses from map_dsmem); completes 4 bytes of transaction count on that
-// CTA's mbarrier, whose waiters then see the value.
-__device__ __forceinline__ void st_async_b32(uint32_t dst_cluster, uint32_t v, uint32_t bar_cluster) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst_cluster),
-                 "r"(v), "r"(bar_cluster)
-                 : "memory");
-}
-
-// Two / four consecutive 32-bit values (8- / 16-byte aligned destination).
-__device__ __forceinline__ void st_async_v2(uint32_t dst_cluster, uint32_t a, uint32_t b, uint32_t bar_cluster) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(dst_cluster),
-                 "r"(a), "r"(b), "r"(bar_cluster)
-                 : "memory");
-}
-
+// Asynchronous 16-byte store into another CTA's shared memory (cluster
+// addresses from map_dsmem, 16-byte aligned); completes 16 bytes of
+// transaction count on that CTA's mbarrier, whose waiters then see the data.
 __device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, uint4 v, uint32_t bar_cluster) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                      dst_cluster),

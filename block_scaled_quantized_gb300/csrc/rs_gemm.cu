@@ -75,9 +75,15 @@ constexpr uint32_t kCtrlBytes = 1024;
 constexpr int kMaxChunkBars = 32;   // fused plans: one "quantized" mbarrier per resident chunk
 
 __host__ __device__ constexpr int b_atom_tiles(int bn) { return (bn + 127) / 128; }
-// Split-K: outputs of a tile each owner CTA sums, a multiple of four.
+// Split-K exchange of a tile with `outs` outputs per channel.  Narrow tiles
+// (at most 16 outputs: every one-launch decode plan) send their outputs from
+// registers with 16-byte st.async stores, dealt to the first CTAs of the
+// cluster in slices of a multiple of four; wider tiles stage a partial in
+// shared memory and send each CTA its slice of ceil(outs / splits) outputs
+// with one bulk copy (many small remote stores would be slower there).
+__host__ __device__ constexpr bool split_async(int outs) { return outs <= 16; }
 __host__ __device__ constexpr int split_slice(int outs, int splits) {
-    return ((outs + splits - 1) / splits + 3) / 4 * 4;
+    return split_async(outs) ? ((outs + splits - 1) / splits + 3) / 4 * 4 : (outs + splits - 1) / splits;
 }
 // Shared-memory bytes of one activation stage: codes (bn rows x 128 bytes)
 // plus its scale atoms, rounded to the 1024-byte swizzle period.
@@ -112,6 +118,7 @@ struct GemmArgs {
     int stages;
     int slots;              // fused: resident activation chunks
     int nacc;               // accumulator buffers in tensor memory (1 or 2)
+    int part_bytes;         // split-K: this CTA's partial
     int recv_bytes;         // split-K: one receive buffer (0 without split)
     int tmem_cols;
     int dyn_alpha;          // fused NVFP4: the tensor scale of X is computed here (alpha_x unused)
@@ -135,7 +142,8 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     uint8_t* wring = smem;                                   // S x WB
     uint8_t* bregion = smem + (size_t)S * WB;                // S (or slots) x BSTAGE
     const int nbslots = FUSED ? g.slots : S;
-    uint8_t* recv_region = bregion + (size_t)nbslots * BSTAGE;    // split-K: nacc receive buffers
+    uint8_t* part_region = bregion + (size_t)nbslots * BSTAGE;    // split-K: our partial
+    uint8_t* recv_region = part_region + g.part_bytes;            // split-K: nacc receive buffers
     const uint32_t recv_base = smem_u32(recv_region);
     uint64_t* full = reinterpret_cast<uint64_t*>(recv_region + (size_t)g.nacc * g.recv_bytes);
     uint64_t* empty = full + kMaxStages;
@@ -169,11 +177,10 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     const int pre = nu < S ? nu : S;
     const int nacc = g.nacc;
     const int outs = g.fold ? BN / 2 : BN;
-    // split-K: the outputs are dealt to the first `owners` CTAs of the cluster
-    // in slices of per_cta (a multiple of four, so that a sender moves four
-    // at a time); each owner sums its slice over the K splits
+    // split-K: outputs each owner sums, owners, and how the partials travel
+    const bool xasync = g.splits > 1 && split_async(outs);
     const int per_cta = split_slice(outs, g.splits);
-    const int owners = (outs + per_cta - 1) / per_cta;
+    const int owners = xasync ? (outs + per_cta - 1) / per_cta : g.splits;
     const bool owner = g.splits > 1 && split < owners;
     const uint32_t slice_bytes = (uint32_t)per_cta * 128u * 4u;
     // Wide tiles without split-K: eight epilogue warps (warps 8-11 and 0-3,
@@ -628,7 +635,18 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             const int row = ew * 32 + lane;                // accumulator lane = channel within the tile
             const int ctid = row;                          // 0..127
             const float gsc = FMT == 0 ? __fmul_rn(ax_val, *g.alpha_w) : 1.0f;
+            float* part = reinterpret_cast<float*>(part_region);  // split-K: [j][channel]
             const uint32_t my_rank = (uint32_t)split;
+            // split-K: lane o of warp 8 sends to owner o; its destinations in
+            // the cluster (receive buffer b at our rank's slot, owner's red_full[b])
+            uint32_t dst_buf0 = 0, dst_buf1 = 0, dst_bar0 = 0, dst_bar1 = 0;
+            if (g.splits > 1 && warp == 8 && lane < g.splits) {
+                const uint32_t rb = recv_base + my_rank * slice_bytes;
+                dst_buf0 = map_dsmem(rb, (uint32_t)lane);
+                dst_bar0 = map_dsmem(smem_u32(&red_full[0]), (uint32_t)lane);
+                dst_buf1 = map_dsmem(rb + (uint32_t)g.recv_bytes, (uint32_t)lane);
+                dst_bar1 = map_dsmem(smem_u32(&red_full[1]), (uint32_t)lane);
+            }
             for (int j = 0; j < ntl; ++j) {
                 const int b = j % nacc;
                 const uint32_t use_ph = (uint32_t)(j / nacc) & 1u;
@@ -642,9 +660,12 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                         else reinterpret_cast<__nv_bfloat16*>(g.y)[idx] = __float2bfloat16_rn(val);
                     }
                 };
-                // split-K: outputs o0 .. o0 + 3 go to owner o0 / per_cta, into its
-                // receive buffer b at (our rank, channel row), as one 16-byte
-                // st.async completing on the owner's red_full[b]
+                auto emit = [&](int jj, float z) {
+                    if (g.splits > 1) part[jj * 128 + row] = z;
+                    else store_y(m0 + jj, z);
+                };
+                // narrow tiles: outputs o0 .. o0 + 3 go to owner o0 / per_cta, into
+                // its receive buffer b at (our rank, channel row), one st.async
                 bool send_ok = true;
                 const uint32_t rbuf = recv_base + (uint32_t)b * (uint32_t)g.recv_bytes +
                                       (my_rank * 128u + (uint32_t)row) * (uint32_t)per_cta * 4u;
@@ -662,11 +683,15 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 if (j < 3 && ctid == 0) RS_TRACE_MARK(g.trace, 22 + j);
                 ok = __all_sync(0xFFFFFFFFu, ok && *abort_flag == 0);  // warp-uniform for tcgen05.ld
                 tc_fence_after();
-                if (g.splits > 1 && j >= nacc) {
+                if (xasync && j >= nacc) {
                     // every owner has summed what was sent into buffer b for tile
-                    // j - nacc (a failed wait sends nothing: the error is recorded)
+                    // j - nacc (after a failed wait nothing is sent: the error is recorded)
                     send_ok = mbar_wait_bounded(smem_u32(&recv_free[b]), (uint32_t)(j / nacc - 1) & 1u, abort_flag,
                                                 g.err, 1000000000ull, true);
+                } else if (g.splits > 1 && j > 0) {
+                    // the previous tile's outgoing copies have read our partial
+                    if (warp == 8) bulk_wait_group_read0();  // (the issuing lane's copies; no-op on the rest)
+                    named_bar_sync(1, 128);
                 }
                 bool drained = false;
                 if constexpr (!FUSED && BN >= 128) {
@@ -752,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                             for (int q = 0; q < 16; ++q) put_y(cbeg + q, v[q]);
                         }
                     }
-                } else if (ok) {
+                } else if (ok && xasync) {
 #pragma unroll 1
                     for (int c = 0; c < BN; c += 16) {
                         float v[16];
@@ -768,11 +793,26 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                             for (int q = 0; q < 16; q += 4) emit4(c + q, v[q], v[q + 1], v[q + 2], v[q + 3]);
                         }
                     }
-                } else if (g.splits > 1) {
+                } else if (ok) {
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 16) {
+                        float v[16];
+                        tmem_ld16(tmem + (uint32_t)(b * BN) + quarter + (uint32_t)c, v);
+                        if (g.fold) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) emit(c / 2 + q, __fadd_rn(v[2 * q], v[2 * q + 1]));  // Fold
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) emit(c + q, v[q]);
+                        }
+                    }
+                } else if (xasync) {
                     for (int o0 = 0; o0 < outs; o0 += 4) emit4(o0, 0.0f, 0.0f, 0.0f, 0.0f);
+                } else if (g.splits > 1) {
+                    for (int jj = 0; jj < outs; ++jj) emit(jj, 0.0f);
                 }
                 // every owner expects a full slice: pad the last one
-                if (g.splits > 1)
+                if (xasync)
                     for (int o0 = outs; o0 < owners * per_cta; o0 += 4) emit4(o0, 0.0f, 0.0f, 0.0f, 0.0f);
                 // accumulator b drained: the MMA warp may start its next tile
                 if (!drained) {
@@ -781,8 +821,30 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                     if (lane == 0) mbar_arrive(smem_u32(&accum_empty[b]));
                 }
                 if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 7);
-                if (g.splits > 1) {
+                if (g.splits > 1 && !xasync) {
+                    // send each owner its slice of outputs: one bulk copy per
+                    // owner into its receive buffer b at our rank's slot
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, 128);
                     if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 13);
+                    if (warp == 8) {
+                        // every owner has consumed what was sent into buffer b
+                        // for tile j - nacc (the whole warp waits; one elected
+                        // lane issues the copies)
+                        bool free_ok = j < nacc || mbar_wait_bounded(smem_u32(&recv_free[b]),
+                                                                     (uint32_t)(j / nacc - 1) & 1u, abort_flag, g.err,
+                                                                     1000000000ull, true);
+                        free_ok = __all_sync(0xFFFFFFFFu, free_ok && *abort_flag == 0);
+                        if (free_ok && lane < g.splits) {
+                            // lane o sends owner o its slice
+                            bulk_copy_to_cluster(b == 0 ? dst_buf0 : dst_buf1,
+                                                 smem_u32(part) + (uint32_t)lane * slice_bytes, slice_bytes,
+                                                 b == 0 ? dst_bar0 : dst_bar1);
+                            bulk_commit_group();
+                            if (j == 0 && lane == 0) RS_TRACE_MARK(g.trace, 14);
+                        }
+                        __syncwarp();
+                    }
                 }
                 if (owner) {
                     // own slice: sum the partners' partials in rank order
@@ -791,29 +853,47 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                     if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 28);
                     const float* recv = reinterpret_cast<const float*>(recv_region + (size_t)b * g.recv_bytes);
                     const bool live = got && *abort_flag == 0;
-                    for (int j4 = 0; live && j4 < per_cta; j4 += 4) {
-                        const int jo = split * per_cta + j4;
-                        if (jo >= outs) break;
-                        // all partials first, then the sums in rank order
-                        float4 pv[kMaxSplits];
+                    if (xasync) {
+                        // receive layout [rank][channel][per_cta], four outputs at a time
+                        for (int j4 = 0; live && j4 < per_cta; j4 += 4) {
+                            const int jo = split * per_cta + j4;
+                            if (jo >= outs) break;
+                            float4 pv[kMaxSplits];
 #pragma unroll
-                        for (int r = 0; r < kMaxSplits; ++r)
-                            pv[r] = r < g.splits
-                                        ? *reinterpret_cast<const float4*>(recv + ((size_t)r * 128 + row) * per_cta + j4)
-                                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            for (int r = 0; r < kMaxSplits; ++r)
+                                pv[r] = r < g.splits ? *reinterpret_cast<const float4*>(
+                                                           recv + ((size_t)r * 128 + row) * per_cta + j4)
+                                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-                        for (int r = 0; r < kMaxSplits; ++r)
-                            if (r < g.splits) {
-                                acc.x = __fadd_rn(acc.x, pv[r].x);
-                                acc.y = __fadd_rn(acc.y, pv[r].y);
-                                acc.z = __fadd_rn(acc.z, pv[r].z);
-                                acc.w = __fadd_rn(acc.w, pv[r].w);
-                            }
-                        store_y(m0 + jo, acc.x);
-                        store_y(m0 + jo + 1, acc.y);
-                        store_y(m0 + jo + 2, acc.z);
-                        store_y(m0 + jo + 3, acc.w);
+                            for (int r = 0; r < kMaxSplits; ++r)
+                                if (r < g.splits) {
+                                    acc.x = __fadd_rn(acc.x, pv[r].x);
+                                    acc.y = __fadd_rn(acc.y, pv[r].y);
+                                    acc.z = __fadd_rn(acc.z, pv[r].z);
+                                    acc.w = __fadd_rn(acc.w, pv[r].w);
+                                }
+                            store_y(m0 + jo, acc.x);
+                            store_y(m0 + jo + 1, acc.y);
+                            store_y(m0 + jo + 2, acc.z);
+                            store_y(m0 + jo + 3, acc.w);
+                        }
+                    } else {
+                        // receive layout [rank][output][channel]
+                        for (int jj = 0; live && jj < per_cta; ++jj) {
+                            const int jo = split * per_cta + jj;
+                            if (jo >= outs) break;
+                            // all partials first, then the sum in rank order
+                            float pv[kMaxSplits];
+#pragma unroll
+                            for (int r = 0; r < kMaxSplits; ++r)
+                                pv[r] = r < g.splits ? recv[(r * per_cta + jj) * 128 + row] : 0.0f;
+                            float acc = 0.0f;
+#pragma unroll
+                            for (int r = 0; r < kMaxSplits; ++r)
+                                if (r < g.splits) acc = __fadd_rn(acc, pv[r]);
+                            store_y(m0 + jo, acc);
+                        }
                     }
                     if (j < 3 && ctid == 0) RS_TRACE_MARK(g.trace, 25 + j);
                     if (j + nacc < ntl) {
@@ -828,6 +908,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                     }
                 }
             }
+            if (g.splits > 1 && !xasync && warp == 8) bulk_wait_group_read0();  // outgoing copies have read their source
         }
     }
 
@@ -894,16 +975,18 @@ cudaError_t launch_fold_pairs(const float* z, void* y, int M, int N, int out_f32
     return cudaGetLastError();
 }
 
-// Split-K receive buffer: `splits` slices (one per sending CTA) of
-// ceil(outs / splits) outputs x 128 channels (fp32).
+// Split-K buffers: each receive buffer holds `splits` slices of
+// split_slice(outs, splits) outputs x 128 channels (fp32); tiles sent by bulk
+// copy also stage their partial (the same size) in shared memory.
 static size_t split_buf_bytes(int splits, int outs) {
     if (splits <= 1) return 0;
     return align_up((size_t)splits * split_slice(outs, splits) * 128 * sizeof(float), 1024);
 }
 
-static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots, size_t splitbuf, int nacc) {
+static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots, size_t splitbuf, int nacc,
+                        size_t partbuf) {
     const size_t b = fused ? (size_t)slots * b_stage_bytes(fmt, bn) : (size_t)stages * b_stage_bytes(fmt, bn);
-    return 1024 + (size_t)stages * weight_block_bytes(fmt) + b + splitbuf * (size_t)nacc + kCtrlBytes;
+    return 1024 + (size_t)stages * weight_block_bytes(fmt) + b + partbuf + splitbuf * (size_t)nacc + kCtrlBytes;
 }
 
 // Complete plan for a given split count s; stages == 0 when it does not fit.
@@ -929,13 +1012,14 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
     const int nu = ntl * max_chunks;
     const int outs = fold ? p.bn / 2 : p.bn;
     const size_t splitbuf = split_buf_bytes(s, outs);
+    const size_t partbuf = split_async(outs) ? 0 : splitbuf;
     const int sfc = sf_cols_per_stage(fmt, p.bn);
     bool fused = allow_fused && p.b_tiles == 1 && p.bn <= 32 && max_chunks <= kMaxChunkBars;
     // two accumulators let the epilogue of one tile overlap the next tile's
     // MMAs when a CTA has several tiles
     int nacc = ntl > 1 ? 2 : 1;
     auto fits = [&](int st, bool fu, int na) {
-        return plan_smem(fmt, p.bn, st, fu, fu ? max_chunks : 0, splitbuf, na) <= kSmemLimit &&
+        return plan_smem(fmt, p.bn, st, fu, fu ? max_chunks : 0, splitbuf, na, partbuf) <= kSmemLimit &&
                na * p.bn + st * sfc <= 512;
     };
     auto best_stages = [&](bool fu, int na) {
@@ -963,27 +1047,28 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
     if (s > 1 && ntl == 1) {
         const int floor_st = std::min(3, nu);
         while (stages > floor_st &&
-               plan_smem(fmt, p.bn, stages, fused, fused ? max_chunks : 0, splitbuf, nacc) > kSmemLimit / 2 &&
-               plan_smem(fmt, p.bn, floor_st, fused, fused ? max_chunks : 0, splitbuf, nacc) <= kSmemLimit / 2)
+               plan_smem(fmt, p.bn, stages, fused, fused ? max_chunks : 0, splitbuf, nacc, partbuf) > kSmemLimit / 2 &&
+               plan_smem(fmt, p.bn, floor_st, fused, fused ? max_chunks : 0, splitbuf, nacc, partbuf) <= kSmemLimit / 2)
             --stages;
     }
     p.fused = fused ? 1 : 0;
     p.nacc = nacc;
     p.stages = stages;
     p.slots = p.fused ? max_chunks : 0;
+    p.part_bytes = (int)partbuf;
     p.recv_bytes = (int)splitbuf;
     if (stages == 0) return p;
     // Two CTAs can share an SM when the shared memory allows it (a dependent
     // launch starting early); keep the tensor-memory allocation within half
     // of the SM's 512 columns then.
-    p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots, splitbuf, p.nacc);
+    p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots, splitbuf, p.nacc, partbuf);
     int cols = p.nacc * p.bn + p.stages * sfc;
     if (p.smem_bytes <= kSmemLimit / 2) {
         while (cols > 256 && p.stages > 1) {
             --p.stages;
             cols = p.nacc * p.bn + p.stages * sfc;
         }
-        p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots, splitbuf, p.nacc);
+        p.smem_bytes = plan_smem(fmt, p.bn, p.stages, p.fused, p.slots, splitbuf, p.nacc, partbuf);
     }
     int alloc = 32;
     while (alloc < cols) alloc *= 2;
@@ -1157,6 +1242,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
     a.nacc = p.nacc;
     a.recv_bytes = p.recv_bytes;
     a.tmem_cols = p.tmem_cols;
+    a.part_bytes = p.part_bytes;
     a.dyn_alpha = c.dyn_alpha;
     a.qdump = p.fused ? static_cast<uint8_t*>(c.qdump) : nullptr;
 #define RS_CASE(F, B, FU)                                                      \

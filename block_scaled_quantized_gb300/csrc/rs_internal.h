@@ -42,6 +42,7 @@ struct GemmPlan {
     int splits;      // K splits per output tile (= cluster size when > 1)
     int grid_x;      // persistent CTAs per K split; CTA x takes tiles x, x + grid_x, ...
     int nacc;        // accumulator buffers in tensor memory (2: epilogue overlaps the next tile)
+    int part_bytes;  // split-K: partial buffer in shared memory
     int stages;      // pipeline depth
     int fused;       // quantize the activations inside the GEMM
     int slots;       // fused: activation chunks resident in shared memory
