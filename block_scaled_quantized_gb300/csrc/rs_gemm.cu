@@ -71,7 +71,7 @@ constexpr int kQuantWarps = 10;     // warps 0-3 and 6-11 quantize in fused plan
 constexpr int kQuantThreads = kQuantWarps * 32;
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;   // 227 KB opt-in per block
-constexpr uint32_t kCtrlBytes = 1024;
+constexpr uint32_t kCtrlBytes = 2048;  // barriers and flags, then the fused NVFP4 scale table (1 KB)
 constexpr int kMaxChunkBars = 32;   // fused plans: one "quantized" mbarrier per resident chunk
 
 __host__ __device__ constexpr int b_atom_tiles(int bn) { return (bn + 127) / 128; }
@@ -159,6 +159,8 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     volatile uint32_t* abort_flag = tmem_slot + 1;
     volatile uint32_t* consumed = tmem_slot + 2;
     volatile uint32_t* issued = tmem_slot + 3;
+    float* alpha_spec = reinterpret_cast<float*>(tmem_slot + 4);                       // fused: alpha_x before the wait
+    float2* sc_tab = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(full) + 1024);  // fused NVFP4: s~, 1/s~ per byte
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -479,10 +481,27 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             // (row 2j+1) codes in the swizzled B tiles, scales in the B atoms.
             constexpr int E = block_elems(FMT);  // 16 (NVFP4) or 32 (MXFP4)
             const uint32_t bbytes = (uint32_t)nck * BSTAGE;
+            // NVFP4 scale table (s~ and fl(1/s~) of every scale byte): built here
+            // from the tensor scale as it reads before the dependency wait (one
+            // thread reads it, so that every thread uses the same value), and
+            // rebuilt after the wait only if the scale turns out to differ
+            const bool spec_tab = FMT == 0 && !g.dyn_alpha;
+            if (spec_tab && qtid == 0) *alpha_spec = *g.alpha_x;
             for (uint32_t off = (uint32_t)qtid * 16u; off < bbytes; off += (uint32_t)kQuantThreads * 16u)
                 *reinterpret_cast<uint4*>(bregion + off) = make_uint4(0u, 0u, 0u, 0u);
             fence_proxy_async_smem();  // the zeros are in every chunk, whoever signals it
             named_bar_sync(2, kQuantThreads);
+            auto build_table = [&](float a) {
+                for (int i = qtid; i < 128; i += kQuantThreads) {
+                    float st, mul;
+                    nv_scale_table_entry((uint32_t)i, a, st, mul);
+                    sc_tab[i] = make_float2(st, mul);
+                }
+            };
+            if (spec_tab) {
+                build_table(*alpha_spec);
+                named_bar_sync(2, kQuantThreads);
+            }
             pdl_wait_prior_grid();
             if (qtid == 0) RS_TRACE_MARK(g.trace, 16);
             const int kbeg = c0 * 256, kend = min(g.K, (c0 + nck) * 256);
@@ -561,6 +580,12 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 ax_val = *g.alpha_x;
             }
             const NvScaleConst ksc = nv_scale_const(ax_val);
+            if (FMT == 0 && (g.dyn_alpha || __float_as_uint(ax_val) != __float_as_uint(*alpha_spec))) {
+                // (the same value on every thread: read after the wait, or found by the cluster)
+                named_bar_sync(2, kQuantThreads);
+                build_table(ax_val);
+                named_bar_sync(2, kQuantThreads);
+            }
 #ifdef RS_TRACE
             if (qtid == 0 && fw0 < total) {
                 asm volatile("" ::"r"(raw[0][0].x));  // the first block's X words have arrived
@@ -597,12 +622,13 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                     const bool live = f < total && kbeg + kk < kend;
                     uint32_t sfq, codes[E / 8], sfr = 0u, rcodes[E / 8];
                     const uint32_t rb = g.fold ? 2u * (uint32_t)j : (uint32_t)j;
+                    const float2* tab = FMT == 0 ? sc_tab : nullptr;
                     if (g.fold) {
-                        quant_block_raw<FMT, E, true>(raw[r], ksc, sfq, codes, sfr, rcodes);
+                        quant_block_raw<FMT, E, true>(raw[r], ksc, sfq, codes, sfr, rcodes, tab);
                         put(rb, kk, codes, sfq, live);
                         put(rb + 1u, kk, rcodes, sfr, live);
                     } else {
-                        quant_block_raw<FMT, E, false>(raw[r], ksc, sfq, codes, sfr, rcodes);
+                        quant_block_raw<FMT, E, false>(raw[r], ksc, sfq, codes, sfr, rcodes, tab);
                         put(rb, kk, codes, sfq, live);
                     }
 #ifdef RS_TRACE

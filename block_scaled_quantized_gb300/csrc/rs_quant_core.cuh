@@ -222,12 +222,25 @@ __device__ __forceinline__ float amax_bf16_words(const uint32_t* w) {
 // r = fl(x - fl(s~ dec(q))) quantized with its own scale (Alg. 1: base, then
 // residue).  Same arithmetic per element as quant_block; the elements are
 // widened one 16-byte word at a time, so only the residues are held whole.
+// With an NVFP4 table (s~, fl(1/s~) of each scale byte, nv_scale_table_entry)
+// the scale byte comes from nv_block_byte and s~ and the multiplier from the
+// table: the same values, with a shorter dependency chain.
 template <int FMT, int E, bool kResidue>
 __device__ __forceinline__ void quant_block_raw(const uint4 (&raw)[E / 8], const NvScaleConst& k, uint32_t& sf,
-                                                uint32_t (&codes)[E / 8], uint32_t& sfr, uint32_t (&rcodes)[E / 8]) {
+                                                uint32_t (&codes)[E / 8], uint32_t& sfr, uint32_t (&rcodes)[E / 8],
+                                                const float2* tab = nullptr) {
+    auto scale = [&](float amax, float& st, float& mul) -> uint32_t {
+        if (FMT == 1) return mx_block_scale(amax, st, mul);
+        if (tab == nullptr) return nv_block_scale_fast(amax, k, st, mul);
+        const uint32_t byte = nv_block_byte(amax, k);
+        const float2 e = tab[byte];
+        st = e.x;
+        mul = e.y;
+        return byte;
+    };
     const float am = amax_bf16_words<E / 2>(reinterpret_cast<const uint32_t*>(&raw[0]));
     float st, mul;
-    sf = FMT == 0 ? nv_block_scale_fast(am, k, st, mul) : mx_block_scale(am, st, mul);
+    sf = scale(am, st, mul);
     float r[kResidue ? E : 1];
 #pragma unroll
     for (int w = 0; w < E / 8; ++w) {
@@ -256,7 +269,7 @@ __device__ __forceinline__ void quant_block_raw(const uint4 (&raw)[E / 8], const
             a1 = fmaxf(a1, fabsf(r[e + 1]));
         }
         float rst, rmul;
-        sfr = FMT == 0 ? nv_block_scale_fast(fmaxf(a0, a1), k, rst, rmul) : mx_block_scale(fmaxf(a0, a1), rst, rmul);
+        sfr = scale(fmaxf(a0, a1), rst, rmul);
 #pragma unroll
         for (int w = 0; w < E / 8; ++w) {
             float v[8];
