@@ -391,6 +391,71 @@ namespace rs {
 __global__ void read_error_kernel(uint32_t* err, uint32_t* out) { *out = atomicExch(err, 0u); }
 }  // namespace rs
 
+namespace {
+bool attn_shape_ok(int B, int Hq, int Hkv, int D, int max_pages, int max_len) {
+    return B >= 1 && Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0 && Hq / Hkv <= 8 && (D == 128 || D == 256) &&
+           max_pages >= 1 && max_len >= 0 && (int64_t)max_len <= (int64_t)max_pages * 32 &&
+           (int64_t)B * Hq * 2 <= 0x7FFFFFFF;
+}
+size_t attn_q_bytes(int B, int Hq, int D) { return rs::align_up(rs::operand_bytes(RS_NVFP4, 2 * B * Hq, D), 1024); }
+}  // namespace
+
+size_t rs_resattn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len) {
+    if (!attn_shape_ok(B, Hq, Hkv, D, (max_len + 31) / 32 + 1, max_len)) return 0;
+    const int max_splits = max_len > 0 ? (max_len + 127) / 128 : 1;
+    return attn_q_bytes(B, Hq, D) + (size_t)B * Hkv * max_splits * (Hq / Hkv) * (D + 2) * sizeof(float);
+}
+
+int rs_resattn_split_tokens(int B, int Hkv, int max_len, int num_sms) {
+    if (B < 1 || Hkv < 1 || max_len < 0 || num_sms < 1) return 0;
+    return rs::resattn_split_tokens(B, Hkv, max_len, num_sms);
+}
+
+rs_status rs_resattn_decode(int B, int Hq, int Hkv, int D, int max_pages, int max_len, const void* q_bf16,
+                            const float* alpha_q, const void* k_cache, const void* v_cache, const int* block_table,
+                            const int* seq_lens, void* out, rs_out_dtype out_dtype, void* workspace, size_t ws_bytes,
+                            rs_stream_t stream) {
+    if (!attn_shape_ok(B, Hq, Hkv, D, max_pages, max_len)) return RS_ERR_SHAPE;
+    if (out_dtype != RS_OUT_BF16 && out_dtype != RS_OUT_F32) return RS_ERR_INVALID_ARG;
+    if (!q_bf16 || !alpha_q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace)
+        return RS_ERR_INVALID_ARG;
+    if (!aligned16(q_bf16) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace) ||
+        !aligned4(alpha_q) || !aligned4(block_table) || !aligned4(seq_lens))
+        return RS_ERR_ALIGNMENT;
+    if (ws_bytes < rs_resattn_workspace_bytes(B, Hq, Hkv, D, max_len)) return RS_ERR_WORKSPACE;
+    cudaError_t why;
+    const rs::DeviceInfo* dev = rs::current_device(&why);
+    if (!dev) return RS_ERR_CUDA;
+    if (!dev->supported) return RS_ERR_UNSUPPORTED;
+    // the query-quantization step (Sec. 5.2): base and residue rows of Q
+    const int rows = B * Hq;
+    uint8_t* qop = static_cast<uint8_t*>(workspace);
+    if (launch_quantize(RS_NVFP4, true, rows, D, q_bf16, D, alpha_q, qop, (cudaStream_t)stream, dev->num_sms,
+                        /*pdl=*/false) != cudaSuccess)
+        return RS_ERR_CUDA;
+    rs::AttnArgs a{};
+    a.q_op = qop;
+    a.q_sf = qop + operand_sf_offset(RS_NVFP4, 2 * rows, D);
+    a.alpha_q = alpha_q;
+    a.k_cache = static_cast<const uint8_t*>(k_cache);
+    a.v_cache = static_cast<const uint8_t*>(v_cache);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.part = reinterpret_cast<float*>(qop + attn_q_bytes(B, Hq, D));
+    a.err = dev->err;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.max_pages = max_pages;
+    a.max_len = max_len;
+    a.split_tokens = rs::resattn_split_tokens(B, Hkv, max_len, dev->num_sms);
+    a.splits = max_len > 0 ? (max_len + a.split_tokens - 1) / a.split_tokens : 1;
+    a.q_rows_pad = (2 * rows + 127) / 128 * 128;
+    a.q_atoms_k = n_atoms_k_host(RS_NVFP4, D);
+    return from_cuda(rs::launch_resattn(D, a, out, out_dtype == RS_OUT_F32 ? 1 : 0, (cudaStream_t)stream));
+}
+
 rs_status rs_fold_pairs(int M, int N, const float* z, void* y, rs_out_dtype out_dtype, rs_stream_t stream) {
     if (M < 0 || N < 0 || (out_dtype != RS_OUT_BF16 && out_dtype != RS_OUT_F32)) return RS_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return RS_OK;

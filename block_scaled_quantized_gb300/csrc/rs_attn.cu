@@ -31,22 +31,17 @@ constexpr int kAttnThreads = 256;
 constexpr int kAttnTile = 128;
 constexpr int kPage = 32;
 
-struct AttnArgs {
-    const uint8_t* q_op;      // paired query operand of [B*Hq] rows (rows 2j base, 2j+1 residue), K = D
-    const uint8_t* q_sf;      // its scale atoms
-    const float* alpha_q;     // query tensor scale (device)
-    const uint8_t* k_cache;   // [pages][Hkv] page blocks
-    const uint8_t* v_cache;
-    const int* block_table;   // [B][max_pages]
-    const int* seq_lens;      // [B]
-    float* part;              // [B][Hkv][splits][G][D + 2]: o, then m, l per head
-    uint32_t* err;
-    int B, Hq, Hkv, D, max_pages, split_tokens, splits;
-    int q_rows_pad;           // paired operand rows rounded to 128 (scale atoms)
-    int q_atoms_k;            // scale atoms per 128-row tile of the query operand
-};
 
 __host__ __device__ constexpr int page_bytes(int D) { return kPage * (D / 2 + D / 16); }
+
+// Tokens of sequence b the kernels attend to: its length, clamped to
+// [0, max_len] (a longer one is reported in the device error word, so that
+// no block-table entry beyond max_len is ever read).
+__device__ __forceinline__ int attn_len(const AttnArgs& g, int b) {
+    const int L = g.seq_lens[b];
+    if (L > g.max_len && threadIdx.x == 0 && blockIdx.x == 0) atomicExch(g.err, kErrInvalidArg);
+    return L < 0 ? 0 : (L > g.max_len ? g.max_len : L);
+}
 
 // E4M3 value of an fp32 value (nearest-even, saturating, sign kept) as float.
 __device__ __forceinline__ float e4m3_round(float p) { return e4m3_decode_hw(e4m3x2_encode_hw(0.0f, p) & 0xFFu); }
@@ -83,7 +78,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) resattn_split_kernel(const At
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = g.Hq / g.Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = g.seq_lens[b];
+    const int L = attn_len(g, b);
     const int t0 = split * g.split_tokens, t1 = min(L, t0 + g.split_tokens);
     float* part = g.part + (((size_t)b * g.Hkv + h) * g.splits + split) * (size_t)G * (D + 2);
 
@@ -115,13 +110,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) resattn_split_kernel(const At
                 qsf_src[sf_offset(row, blk, g.q_atoms_k)];
         }
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TCOLS);
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TCOLS);
+        tmem_relinquish();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;                 // accumulator: columns 0-15
     const uint32_t tsfa = tmem + 16, tsfb = tmem + 16 + 4 * NA;
-    const float c = __fmul_rn(*g.alpha_q, rsqrtf((float)D));  // alpha_k = 1
+    const float c = __fmul_rn(*g.alpha_q, __frsqrt_rn((float)D));  // alpha_q / sqrt(D), alpha_k = 1
     float o[HPT];                                      // thread: d = tid % D, heads og0 .. og0 + HPT - 1
 #pragma unroll
     for (int q = 0; q < HPT; ++q) o[q] = 0.0f;
@@ -269,13 +267,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) resattn_split_kernel(const At
 }
 
 // O = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s (R19); empty sequences give 0.
-__global__ void resattn_combine_kernel(const float* part, int B, int Hq, int Hkv, int D, int splits, int split_tokens,
-                                       const int* seq_lens, void* out, int out_f32) {
+__global__ void resattn_combine_kernel(const AttnArgs g, void* out, int out_f32) {
+    const int B = g.B, Hq = g.Hq, Hkv = g.Hkv, D = g.D, splits = g.splits, split_tokens = g.split_tokens;
+    const float* part = g.part;
+    (void)B;
     const int G = Hq / Hkv;
     const int b = blockIdx.y, hq = blockIdx.x, d = threadIdx.x;
     if (d >= D) return;
     const int h = hq / G, gg = hq % G;
-    const int L = seq_lens[b];
+    const int L = attn_len(g, b);
     const int ns = min(splits, (L + split_tokens - 1) / split_tokens);
     float M = -INFINITY;
     for (int s = 0; s < ns; ++s)
@@ -323,8 +323,7 @@ cudaError_t launch_resattn(int D, const AttnArgs& a, void* out, int out_f32, cud
     if (e != cudaSuccess) return e;
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    resattn_combine_kernel<<<dim3((unsigned)a.Hq, (unsigned)a.B), D, 0, stream>>>(
-        a.part, a.B, a.Hq, a.Hkv, D, a.splits, a.split_tokens, a.seq_lens, out, out_f32);
+    resattn_combine_kernel<<<dim3((unsigned)a.Hq, (unsigned)a.B), D, 0, stream>>>(a, out, out_f32);
     return cudaGetLastError();
 }
 

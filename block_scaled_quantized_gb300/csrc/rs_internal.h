@@ -103,6 +103,26 @@ cudaError_t launch_gemm(const GemmPlan& plan, const GemmCall& call, cudaStream_t
 // Separate Fold of an expanded fp32 output of paired rows (z [2M][N] -> y [M][N]).
 cudaError_t launch_fold_pairs(const float* z, void* y, int M, int N, int out_f32, cudaStream_t stream, int num_sms);
 
+// Residue-compensated decode attention (rs_attn.cu).
+struct AttnArgs {
+    const uint8_t* q_op;      // paired query operand of [B*Hq] rows (rows 2j base, 2j+1 residue), K = D
+    const uint8_t* q_sf;      // its scale atoms
+    const float* alpha_q;     // query tensor scale (device)
+    const uint8_t* k_cache;   // [pages][Hkv] page blocks
+    const uint8_t* v_cache;
+    const int* block_table;   // [B][max_pages]
+    const int* seq_lens;      // [B]
+    float* part;              // [B][Hkv][splits][G][D + 2]: o, then m, l per head
+    uint32_t* err;
+    int B, Hq, Hkv, D, max_pages, max_len, split_tokens, splits;
+    int q_rows_pad;           // paired operand rows rounded to 128 (scale atoms)
+    int q_atoms_k;            // scale atoms per 128-row tile of the query operand
+};
+
+// Tokens per split of a ResAttn call, a multiple of the 128-token tile.
+int resattn_split_tokens(int B, int Hkv, int max_len, int num_sms);
+cudaError_t launch_resattn(int D, const AttnArgs& a, void* out, int out_f32, cudaStream_t stream);
+
 // Device error word of the current device.
 uint32_t* device_error_word();
 

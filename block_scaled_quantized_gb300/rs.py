@@ -31,7 +31,8 @@ EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_
            "rs_linear_compensated_noalloc", "rs_get_device_error", "rs_kext_width", "rs_kext_select",
            "rs_channel_mean_abs", "rs_kext_act_bytes", "rs_kext_weight_bytes", "rs_kext_workspace_bytes",
            "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext", "rs_plan_linear", "rs_debug_wait_probe",
-           "rs_get_device_error_async", "rs_debug_linear_dump", "rs_fold_pairs"]
+           "rs_get_device_error_async", "rs_debug_linear_dump", "rs_fold_pairs", "rs_resattn_workspace_bytes",
+           "rs_resattn_split_tokens", "rs_resattn_decode"]
 
 
 class RsError(RuntimeError):
@@ -75,6 +76,9 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_debug_wait_probe": ([ctypes.c_uint64, P], I),
         "rs_get_device_error_async": ([P, P], I),
         "rs_fold_pairs": ([I, I, P, P, I, P], I),
+        "rs_resattn_workspace_bytes": ([I, I, I, I, I], SZ),
+        "rs_resattn_split_tokens": ([I, I, I, I], I),
+        "rs_resattn_decode": ([I, I, I, I, I, I, P, P, P, P, P, P, P, I, P, SZ, P], I),
         "rs_debug_linear_dump": ([I, I, I, I, I, P, P, P, P, P, I, P, SZ, P, SZ, P, P], I),
     }
     for name, (args, res) in sig.items():
@@ -213,6 +217,28 @@ def rs_linear_compensated_noalloc(fmt: int, M: int, N: int, K: int, x=None, alph
     _check("rs_linear_compensated_noalloc",
            lib().rs_linear_compensated_noalloc(fmt, M, N, K, _ptr(x), _ptr(alpha_x), _ptr(wq), _ptr(alpha_w),
                                                _ptr(y), out, _stream(stream)))
+
+
+def rs_resattn_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, max_len: int) -> int:
+    return lib().rs_resattn_workspace_bytes(B, Hq, Hkv, D, max_len)
+
+
+def rs_resattn_split_tokens(B: int, Hkv: int, max_len: int, num_sms: int) -> int:
+    return lib().rs_resattn_split_tokens(B, Hkv, max_len, num_sms)
+
+
+def rs_resattn_decode(q: torch.Tensor, alpha_q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_table: torch.Tensor, seq_lens: torch.Tensor, max_len: int, out: torch.Tensor,
+                      workspace: torch.Tensor, Hkv: int, stream=None):
+    """One ResAttn decode step (see rs.h): q [B][Hq][D] bf16, paged NVFP4
+    caches, block_table [B][max_pages] int32, seq_lens [B] int32."""
+    B, Hq, D = q.shape
+    dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check("rs_resattn_decode",
+           lib().rs_resattn_decode(B, Hq, Hkv, D, block_table.shape[1], max_len, _ptr(q), _ptr(alpha_q),
+                                   _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(out),
+                                   dtype, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream)))
 
 
 def rs_fold_pairs(M: int, N: int, z: torch.Tensor, y: torch.Tensor, stream=None):

@@ -287,6 +287,49 @@ RS_API rs_status rs_linear_kext(rs_format fmt, int M, int N, int K, int k, const
                                 const float *alpha_w, void *y, rs_out_dtype out_dtype, void *workspace,
                                 size_t ws_bytes, rs_stream_t stream);
 
+/* ---- residue-compensated decode attention (ResAttn, Sec. 4.3, Sec. 5.2) -- */
+
+/* Paged NVFP4 KV cache ("rs page"): the cache holds pages of 32 tokens; page
+ * p of KV head h is the block of 32 * (D/2 + D/16) bytes at byte
+ * (p * Hkv + h) * 32 * (D/2 + D/16): the E2M1 codes of its 32 tokens
+ * [32][D/2] (token-major, element 2j of a token in the low nibble of byte
+ * j), then their E4M3 block scales [32][D/16] (16-element blocks along the
+ * head dimension, tensor scale 1.0).  block_table [B][max_pages] (int32)
+ * lists the pages of each sequence in token order; token t of sequence b
+ * lives in page block_table[b][t / 32] at row t % 32.  Unused entries of a
+ * page are never read. */
+
+/* Workspace of rs_resattn_decode: the quantized query and the partial
+ * outputs of the sequence splits (an upper bound for any device).  0 for a
+ * shape rs_resattn_decode refuses. */
+RS_API size_t rs_resattn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len);
+
+/* Tokens per sequence split that rs_resattn_decode uses on a device with
+ * num_sms SMs (a multiple of 128; host only): enough (split, KV head,
+ * sequence) CTAs to cover the SMs, at least one 128-token tile each. */
+RS_API int rs_resattn_split_tokens(int B, int Hkv, int max_len, int num_sms);
+
+/* One decode step of ResAttn (Sec. 4.3 Eq. 3, Fig. 3; Sec. 5.2 "ResAttn
+ * execution").  q_bf16 [B][Hq][D] (device, bf16) is quantized with Alg. 1
+ * into base and residue rows with the tensor scale *alpha_q (device; e.g.
+ * rs_compute_tensor_scale over Q); query head g reads KV head g / (Hq/Hkv).
+ * Scores s = (<Q^, K^> + <R^, K^>) alpha_q / sqrt(D) are folded in fp32
+ * before an online softmax over 128-token tiles; V goes from NVFP4 to E4M3
+ * on chip; the softmax weights are rounded to E4M3 for PV with fp32
+ * accumulation, and the normalizer sums the rounded weights; the sequence
+ * splits are combined as O = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s.
+ * out [B][Hq][D] (device) is bf16 or fp32; a sequence of length 0 gives 0.
+ * seq_lens [B] (device, int32) must not exceed max_len <= 32 * max_pages: a
+ * longer one is clamped to max_len and reported as RS_ERR_INVALID_ARG by
+ * rs_get_device_error.  D is 128 or 256, Hq a multiple of Hkv with at most
+ * 8 query heads per KV head.  Errors: RS_ERR_SHAPE (sizes), RS_ERR_INVALID_ARG
+ * (NULL pointer, dtype), RS_ERR_ALIGNMENT (16 bytes for q, caches, out and
+ * workspace; 4 for alpha_q, block_table, seq_lens), RS_ERR_WORKSPACE. */
+RS_API rs_status rs_resattn_decode(int B, int Hq, int Hkv, int D, int max_pages, int max_len, const void *q_bf16,
+                                   const float *alpha_q, const void *k_cache, const void *v_cache,
+                                   const int *block_table, const int *seq_lens, void *out, rs_out_dtype out_dtype,
+                                   void *workspace, size_t ws_bytes, rs_stream_t stream);
+
 /* ---- separate Fold (ablation of the on-chip Fold) ------------------------ */
 
 /* y[j][n] = z[2j][n] + z[2j+1][n] for j < M, n < N (Sec. 4.3 Eq. 2, Fold):

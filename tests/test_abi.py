@@ -154,3 +154,33 @@ def test_wait_probe_rejects_out_of_range_limits():
         with pytest.raises(rs.RsError) as e:
             rs.rs_debug_wait_probe(bad, stream=0)  # argument checks come before any CUDA call
         assert e.value.status == rs.RS_ERR_INVALID_ARG
+
+
+def test_resattn_sizes_and_argument_checks(librs):
+    from block_scaled_quantized_gb300 import rs
+    f = librs.rs_resattn_decode
+    P = ctypes.c_void_p
+    f.argtypes = [ctypes.c_int] * 6 + [P] * 7 + [ctypes.c_int, P, ctypes.c_size_t, P]
+    dummy = P(1 << 20)  # aligned, never dereferenced: every call fails validation first
+    ok = (2, 8, 2, 128, 4, 128)
+    # workspace: quantized query (2*B*Hq rows of D) + partials of up to ceil(max_len/128) splits
+    B, Hq, Hkv, D, L = 2, 8, 2, 128, 1000
+    q_bytes = (layout.operand_bytes(0, 2 * B * Hq, D) + 1023) // 1024 * 1024
+    assert librs.rs_resattn_workspace_bytes(B, Hq, Hkv, D, L) == q_bytes + B * Hkv * 8 * (Hq // Hkv) * (D + 2) * 4
+    assert librs.rs_resattn_workspace_bytes(B, Hq, Hkv, 64, L) == 0      # head size
+    assert librs.rs_resattn_workspace_bytes(B, 18, 2, D, L) == 0         # 9 query heads per KV head
+    assert librs.rs_resattn_split_tokens(1, 8, 4096, 152) % 128 == 0
+    assert librs.rs_resattn_split_tokens(1, 1, 4096, 152) == 128        # one tile per split covers the SMs
+
+    def call(shape, ptrs=None, dtype=0, ws=1 << 30):
+        pp = ptrs or [dummy] * 7
+        return f(*shape, *pp, dtype, dummy, ws, None)
+
+    assert call((2, 8, 2, 96, 4, 128)) == rs.RS_ERR_SHAPE             # D
+    assert call((2, 8, 3, 128, 4, 128)) == rs.RS_ERR_SHAPE            # Hq % Hkv
+    assert call((2, 8, 2, 128, 4, 129)) == rs.RS_ERR_SHAPE            # max_len > 32 * max_pages
+    assert call((0, 8, 2, 128, 4, 128)) == rs.RS_ERR_SHAPE            # B
+    assert call(ok, dtype=7) == rs.RS_ERR_INVALID_ARG
+    assert call(ok, ptrs=[None] + [dummy] * 6) == rs.RS_ERR_INVALID_ARG
+    assert call(ok, ptrs=[P((1 << 20) + 8)] + [dummy] * 6) == rs.RS_ERR_ALIGNMENT
+    assert call(ok, ws=16) == rs.RS_ERR_WORKSPACE
