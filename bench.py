@@ -371,6 +371,62 @@ def fold_ablation(torch, rs, workloads, hbm, Ms=(1, 2, 4, 8, 16, 32, 64)) -> lis
     return rows
 
 
+RESATTN_CASES = [
+    # (B, Hq, Hkv, D, tokens per sequence): head sizes 128 / 256, 4 to 8 query heads per KV head
+    (1, 32, 8, 128, 32768), (8, 32, 8, 128, 8192), (32, 32, 8, 128, 2048), (1, 32, 4, 128, 131072),
+    (4, 48, 8, 256, 16384), (16, 64, 8, 128, 4096),
+]
+
+
+def resattn_leg(torch, rs, hbm) -> list:
+    """ResAttn decode steps over synthetic paged NVFP4 caches (random codes,
+    E4M3 scales in [2^-2, 2^2], every sequence full length, a shuffled block
+    table), rotated over enough copies that each step reads its cache from
+    HBM.  Algorithmic bytes: K and V of every cached token and KV head,
+    2 (D/2 + D/16) bytes (144 B at D = 128), plus Q and O."""
+    rows = []
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    for B, Hq, Hkv, D, L in RESATTN_CASES:
+        pages = (L + 31) // 32
+        page_bytes = 32 * (D // 2 + D // 16)
+        cache_bytes = B * pages * Hkv * page_bytes
+        copies = max(2, math.ceil(2 * l2 / (2 * cache_bytes)) + 1)
+        caches = []
+        for _ in range(copies):
+            kv = []
+            for _ in range(2):
+                c = torch.randint(0, 256, (B * pages, Hkv, page_bytes), dtype=torch.uint8, device="cuda",
+                                  generator=gen)
+                sc = torch.randint(0x28, 0x49, (B * pages, Hkv, 32 * (D // 16)), dtype=torch.uint8, device="cuda",
+                                   generator=gen)
+                c[:, :, 32 * (D // 2):] = sc
+                kv.append(c)
+            caches.append(kv)
+        table = torch.randperm(B * pages, device="cuda", generator=gen).to(torch.int32).reshape(B, pages)
+        lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
+        q = (torch.randn((B, Hq, D), device="cuda", generator=gen)).to(torch.bfloat16)
+        aq = torch.empty(1, dtype=torch.float32, device="cuda")
+        rs.rs_compute_tensor_scale(q, aq)
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(rs.rs_resattn_workspace_bytes(B, Hq, Hkv, D, L), dtype=torch.uint8, device="cuda")
+
+        def step(i):
+            k, v = caches[i % copies]
+            rs.rs_resattn_decode(q, aq, k, v, table, lens, L, out, ws, Hkv)
+
+        us, _ = graph_time_us(torch, step, 30)
+        algo = 2 * B * L * Hkv * (D // 2 + D // 16) + 2 * B * Hq * D * 2
+        rows.append({"B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "tokens": L, "us": round(us, 2),
+                     "achieved_gbs": round(algo / (us * 1e-6) / 1e9, 1),
+                     "hbm_frac": round(algo / (us * 1e-6) / 1e9 / hbm, 4), "kv_bytes_per_token_head": 2 * (D // 2 + D // 16)})
+        del caches, table, q, out, ws
+        torch.cuda.empty_cache()
+    assert rs.rs_get_device_error() == 0
+    return rows
+
+
 def graph_time_us(torch, fn_step, steps: int, reps: int = 5, warm: int = 3) -> tuple[float, list[float]]:
     """Capture `steps` calls in a CUDA graph; return median us per call."""
     s = torch.cuda.Stream()
@@ -586,6 +642,7 @@ def run_gpu(args) -> dict:
         extra["prefill_M4096_K8192_N8192"] = pre
         torch.cuda.empty_cache()
         extra["fold_ablation_k4096_n4096"] = fold_ablation(torch, rs, workloads, hbm)
+        extra["resattn_decode"] = resattn_leg(torch, rs, hbm)
 
     # ---------------- end to end through host buffers (pinned), public API
     xh = main.x_host.pin_memory()

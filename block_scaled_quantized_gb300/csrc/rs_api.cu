@@ -154,6 +154,16 @@ rs_status linear_impl(int fmt, bool compensated, int M, int N, int K, const void
 
 }  // namespace
 
+rs_status current_device_status(int* num_sms, uint32_t** err) {
+    cudaError_t why;
+    const DeviceInfo* d = current_device(&why);
+    if (!d) return RS_ERR_CUDA;
+    if (!d->supported) return RS_ERR_UNSUPPORTED;
+    *num_sms = d->num_sms;
+    *err = d->err;
+    return RS_OK;
+}
+
 uint32_t* device_error_word() {
     cudaError_t why;
     const DeviceInfo* d = current_device(&why);

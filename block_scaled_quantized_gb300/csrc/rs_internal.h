@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "rs.h"
 #include "rs_device.cuh"
 
 namespace rs {
@@ -125,5 +126,8 @@ cudaError_t launch_resattn(int D, const AttnArgs& a, void* out, int out_f32, cud
 
 // Device error word of the current device.
 uint32_t* device_error_word();
+// RS_OK with the SM count and error word of the current device, or the
+// status a call on it returns (RS_ERR_CUDA, RS_ERR_UNSUPPORTED).
+rs_status current_device_status(int* num_sms, uint32_t** err);
 
 }  // namespace rs

@@ -344,8 +344,9 @@ RS_API rs_status rs_fold_pairs(int M, int N, const float *z, void *y, rs_out_dty
 
 /* ---- compensated linear without any device allocation -------------------- */
 
-/* Size of the fixed device array that rs_linear_compensated_noalloc uses in
- * place of a workspace (4 MiB).  Every GPU that loads librs holds it until the
+/* Largest quantized operand rs_linear_compensated_noalloc accepts (4 MiB);
+ * its fixed device array holds that plus 1280 bytes (alignment and the
+ * tensor-scale slot).  Every GPU that loads librs holds the array until the
  * process exits. */
 #define RS_NOALLOC_SCRATCH_BYTES (4u << 20)
 
@@ -354,14 +355,19 @@ RS_API rs_status rs_fold_pairs(int M, int N, const float *z, void *y, rs_out_dty
  * framework hands only its input and output buffers, or a process whose
  * device footprint must stay fixed after start-up.
  *
- * Same result as rs_linear_compensated with a bf16 input x_bf16 ([M][K],
- * device, contiguous), but the quantized activations (the paired base and
- * residue operand, rs_act_bytes(fmt, 2*M, K) bytes) go to a fixed device
- * array of RS_NOALLOC_SCRATCH_BYTES inside librs instead of a caller
- * workspace.  Nothing is allocated: no cudaMalloc, no cudaFree.
- *   - Sizes whose operand does not fit the array are rejected with
- *     RS_ERR_WORKSPACE before anything is enqueued (NVFP4, K = 4096: up to
- *     M = 904 fits; rs_act_bytes(fmt, 2*M, K) gives the exact size).
+ * The compensated layer of rs_linear_compensated for a bf16 input x_bf16
+ * ([M][K], device, contiguous), with the quantized activations (the paired
+ * base and residue operand, rs_act_bytes(fmt, 2*M, K) bytes) in a fixed
+ * device array inside librs instead of a caller workspace.  It always runs
+ * the two-kernel form (the paired quantizer, then the GEMM on its operand),
+ * where rs_linear_compensated may quantize inside the GEMM; the outputs agree
+ * within the output tolerance (max|dY| <= 1e-3 max|Y|), not bit for bit.
+ * Nothing is allocated: no cudaMalloc, no cudaFree.
+ *   - Operands larger than RS_NOALLOC_SCRATCH_BYTES are rejected with
+ *     RS_ERR_WORKSPACE before anything is enqueued, with or without alpha_x
+ *     (NVFP4, K = 4096: up to M = 904; rs_act_bytes(fmt, 2*M, K) gives the
+ *     exact size).  The array also holds the tensor-scale slot that a call
+ *     without alpha_x fills.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
  *     stream capture.

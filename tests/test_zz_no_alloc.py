@@ -29,6 +29,11 @@ def test_noalloc_refuses_sizes_beyond_the_array():
     assert layout.operand_bytes(0, 2 * M_fit, K) <= SCRATCH_BYTES < layout.operand_bytes(0, 2 * (M_fit + 1), K)
     f = lib.rs_linear_compensated_noalloc
     assert f(0, M_fit + 1, 128, K, fake, fake, fake, fake, fake, 0, None) == 5  # RS_ERR_WORKSPACE
+    assert f(0, M_fit + 1, 128, K, fake, None, fake, fake, fake, 0, None) == 5  # also without alpha_x
+    # the largest size fits with and without alpha_x: validation goes on to the
+    # alignment check (a misaligned output stops the call before any launch)
+    assert f(0, M_fit, 128, K, fake, fake, fake, fake, fake + 2, 0, None) == 2  # RS_ERR_ALIGNMENT
+    assert f(0, M_fit, 128, K, fake, None, fake, fake, fake + 2, 0, None) == 2
     assert f(0, 4, 128, 48, fake, fake, fake, fake, fake, 0, None) == 3         # K % 32
     assert f(0, 4, 128, K, None, fake, fake, fake, fake, 0, None) == 1          # no input
     assert f(0, 0, 128, K, None, None, None, None, None, 0, None) == 0          # nothing to do
