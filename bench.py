@@ -623,6 +623,18 @@ def run_gpu(args) -> dict:
             us, _ = graph_time_us(torch, lin.call, 10, reps=3)
             useful, executed = lin.flops()
             pre[f"{key}_us"] = round(us, 2)
+            if not k:
+                # the GEMM alone on the quantized operand: the default kernel, and the
+                # paired-CTA kernel (cta_group::2, 256 x 256 per pair) for comparison
+                g1, _ = graph_time_us(torch, lambda i: lin.call(i, prequantized=True), 10, reps=3)
+                rs.rs_debug_pair_gemm(True)
+                try:
+                    g2, _ = graph_time_us(torch, lambda i: lin.call(i, prequantized=True), 10, reps=3)
+                finally:
+                    rs.rs_debug_pair_gemm(False)
+                pre[f"{key}_gemm_only_us"] = round(g1, 2)
+                pre[f"{key}_gemm_only_frac"] = round(executed / (g1 * 1e-6) / 1e12 / (peaks["bf16_tflops"] * 6), 4)
+                pre[f"{key}_pair_cta_gemm_only_us"] = round(g2, 2)
             pre[f"{key}_useful_tflops"] = round(useful / (us * 1e-6) / 1e12, 1)
             pre[f"{key}_executed_tflops"] = round(executed / (us * 1e-6) / 1e12, 1)
             lin.call(0)

@@ -466,6 +466,8 @@ rs_status rs_resattn_decode(int B, int Hq, int Hkv, int D, int max_pages, int ma
     return from_cuda(rs::launch_resattn(D, a, out, out_dtype == RS_OUT_F32 ? 1 : 0, (cudaStream_t)stream));
 }
 
+void rs_debug_pair_gemm(int enable) { rs::set_pair_gemm(enable); }
+
 rs_status rs_fold_pairs(int M, int N, const float* z, void* y, rs_out_dtype out_dtype, rs_stream_t stream) {
     if (M < 0 || N < 0 || (out_dtype != RS_OUT_BF16 && out_dtype != RS_OUT_F32)) return RS_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return RS_OK;

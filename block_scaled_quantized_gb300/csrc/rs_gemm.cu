@@ -1142,9 +1142,22 @@ static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, 
     return best;
 }
 
+// The paired-CTA kernel (rs_gemm_pair.cu) is chosen only on request: on
+// this GPU the single-CTA kernel is faster for every shape measured (the
+// pair's stages land at about 52 GB/s per SM from L2 against about 81 GB/s
+// for the single-CTA kernel's larger stages).
+static int g_pair_gemm = 0;
+
 GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused) {
-    return plan_impl(fmt, fold, M, N, K, num_sms, allow_fused);
+    GemmPlan p = plan_impl(fmt, fold, M, N, K, num_sms, allow_fused);
+    // Operands of at least two 256-row activation tiles with an even number
+    // of channel tiles can run on the pair kernel, whose two SMs share one
+    // 256 x 256 MMA and each stage half the activation bytes.
+    p.pair = (g_pair_gemm && !p.fused && p.Rb >= 512 && p.n_tiles % 2 == 0) ? 1 : 0;
+    return p;
 }
+
+void set_pair_gemm(int enable) { g_pair_gemm = enable ? 1 : 0; }
 
 size_t plan_b_stage_bytes(const GemmPlan& p) { return b_stage_bytes(p.fmt, p.bn); }
 
@@ -1235,6 +1248,19 @@ static uint64_t* g_trace = nullptr;
 #endif
 
 cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t stream) {
+    if (p.pair) {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+#ifdef RS_TRACE
+        uint64_t* trace = g_trace;
+#else
+        uint64_t* trace = nullptr;
+#endif
+        return launch_gemm_pair(p.fmt, p.M, p.Rb, p.N, p.K, p.fold, c.xq, c.wq, c.alpha_x, c.alpha_w, c.y, c.out_f32,
+                                c.err, trace, sms, stream);
+    }
     alignas(64) CUtensorMap tb;
     std::memset(&tb, 0, sizeof tb);
     if (!p.fused && !encode_codes_map(&tb, c.xq, p.Rb, p.K, p.bn)) return cudaErrorInvalidValue;

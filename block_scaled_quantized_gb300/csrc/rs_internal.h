@@ -50,6 +50,7 @@ struct GemmPlan {
     int recv_bytes;  // split-K: one receive buffer in shared memory
     int tmem_cols;   // tensor-memory columns to allocate
     size_t smem_bytes;
+    int pair;        // large operands: the paired-CTA kernel (rs_gemm_pair.cu) runs the call
 };
 
 constexpr int kMaxSplits = 8;   // portable thread-block cluster size
@@ -100,6 +101,13 @@ struct GemmCall {
 size_t plan_b_stage_bytes(const GemmPlan& p);
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmCall& call, cudaStream_t stream);
+// Route eligible large calls to the paired-CTA GEMM (off by default).
+void set_pair_gemm(int enable);
+// Paired-CTA GEMM on a quantized activation operand of Rb rows (Rb >= 256,
+// an even number of 128-channel tiles).
+cudaError_t launch_gemm_pair(int fmt, int M, int Rb, int N, int K, int fold, const void* xq, const void* wq,
+                             const float* alpha_x, const float* alpha_w, void* y, int out_f32, uint32_t* err,
+                             uint64_t* trace, int num_sms, cudaStream_t stream);
 
 // Separate Fold of an expanded fp32 output of paired rows (z [2M][N] -> y [M][N]).
 cudaError_t launch_fold_pairs(const float* z, void* y, int M, int N, int out_f32, cudaStream_t stream, int num_sms);

@@ -32,7 +32,7 @@ EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_
            "rs_channel_mean_abs", "rs_kext_act_bytes", "rs_kext_weight_bytes", "rs_kext_workspace_bytes",
            "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext", "rs_plan_linear", "rs_debug_wait_probe",
            "rs_get_device_error_async", "rs_debug_linear_dump", "rs_fold_pairs", "rs_resattn_workspace_bytes",
-           "rs_resattn_split_tokens", "rs_resattn_decode"]
+           "rs_resattn_split_tokens", "rs_resattn_decode", "rs_debug_pair_gemm"]
 
 
 class RsError(RuntimeError):
@@ -78,6 +78,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_fold_pairs": ([I, I, P, P, I, P], I),
         "rs_resattn_workspace_bytes": ([I, I, I, I, I], SZ),
         "rs_resattn_split_tokens": ([I, I, I, I], I),
+        "rs_debug_pair_gemm": ([I], None),
         "rs_resattn_decode": ([I, I, I, I, I, I, P, P, P, P, P, P, P, I, P, SZ, P], I),
         "rs_debug_linear_dump": ([I, I, I, I, I, P, P, P, P, P, I, P, SZ, P, SZ, P, P], I),
     }
@@ -239,6 +240,11 @@ def rs_resattn_decode(q: torch.Tensor, alpha_q: torch.Tensor, k_cache: torch.Ten
                                    _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(out),
                                    dtype, _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)))
+
+
+def rs_debug_pair_gemm(enable: bool):
+    """Route eligible large calls to the paired-CTA GEMM (see rs.h)."""
+    lib().rs_debug_pair_gemm(int(bool(enable)))
 
 
 def rs_fold_pairs(M: int, N: int, z: torch.Tensor, y: torch.Tensor, stream=None):

@@ -330,6 +330,19 @@ RS_API rs_status rs_resattn_decode(int B, int Hq, int Hkv, int D, int max_pages,
                                    const int *block_table, const int *seq_lens, void *out, rs_out_dtype out_dtype,
                                    void *workspace, size_t ws_bytes, rs_stream_t stream);
 
+/* ---- alternative prefill GEMM (comparison) ------------------------------- */
+
+/* enable != 0: linear calls whose activation operand has at least 512 rows
+ * (after pairing) and an even number of 128-channel tiles, and that do not
+ * quantize inside the GEMM, run on the paired-CTA kernel instead: two CTAs
+ * of a cluster share one tcgen05.mma.cta_group::2 of 256 output channels x
+ * 256 activation rows (the larger tile of ResServe Sec. 5.1), each staging
+ * its own 128 weight channels and 128 activation rows.  Results are those
+ * of the default kernel within the output tolerance.  It is off by default
+ * because it is slower on GB300 (see the benchmark's prefill figures); the
+ * switch is process-wide and not thread-safe, for tests and benchmarks. */
+RS_API void rs_debug_pair_gemm(int enable);
+
 /* ---- separate Fold (ablation of the on-chip Fold) ------------------------ */
 
 /* y[j][n] = z[2j][n] + z[2j+1][n] for j < M, n < N (Sec. 4.3 Eq. 2, Fold):

@@ -234,3 +234,27 @@ def test_separate_fold_pipeline(M, N):
     assert torch.equal(y32, want)
     assert torch.equal(y16, want.to(torch.bfloat16))
     assert_close_f32(y32, oracle_linear(0, True, x, wp))
+
+
+PAIR_SHAPES = [(0, False, 512, 256, 256), (0, False, 700, 512, 800), (0, True, 256, 256, 512),
+               (0, True, 300, 1024, 2048), (1, False, 512, 512, 512), (1, True, 600, 768, 1024),
+               (0, False, 1100, 20480, 512)]
+
+
+@pytest.mark.parametrize("fmt,compensated,M,N,K", PAIR_SHAPES)
+def test_paired_cta_gemm_parity(fmt, compensated, M, N, K):
+    """The paired-CTA kernel (tcgen05.mma.cta_group::2, 256 x 256 per pair)
+    against the oracle: one and several pair tiles per pair, ragged M, N and
+    K, both formats, fp32 and bf16 output."""
+    x = workloads.make_x("gauss_outlier_k2048", M, K=K, seed=M + N + K)
+    w = workloads.make_w("gauss_outlier_k2048", N=N, K=K, seed=N * 7 + K)
+    wp = prepare_weight(fmt, w)
+    rs.rs_debug_pair_gemm(True)
+    try:
+        y, _ = gpu_linear(fmt, compensated, x, wp)
+        yb, _ = gpu_linear(fmt, compensated, x, wp, out_dtype=torch.bfloat16)
+    finally:
+        rs.rs_debug_pair_gemm(False)
+    ref = oracle_linear(fmt, compensated, x, wp)
+    assert_close_f32(y, ref)
+    assert_close_bf16(yb, ref)
