@@ -16,10 +16,11 @@
 //    activation operand, or, for small M, from a quantizing prologue that
 //    converts the CTA's slice of the bf16 input straight into shared memory
 //    (Alg. 1 fused into the GEMM: one launch per linear layer);
-//  * scale atoms go shared memory -> tensor memory through the four epilogue
-//    warps (each writes its lane quarter with tcgen05.st, the image a
-//    32x128b.warpx4 copy would make), where the kind::mxf4nvf4 block-scaled
-//    MMA reads them; the tensor pipe then only runs MMAs.
+//  * scale atoms go shared memory -> tensor memory with tcgen05.cp
+//    (32x128b.warpx4, issued by the MMA warp ahead of the MMAs that read
+//    them), where the kind::mxf4nvf4 block-scaled MMA reads them; in fused
+//    plans the weight atoms of the prefetched stages are copied before the
+//    dependency wait.
 //
 // Fold (Sec. 4.3 Eq. 2): with paired rows, the base and residue products of
 // token j are accumulator columns 2j and 2j+1; a 32x32b tensor-memory load
@@ -34,24 +35,24 @@
 //
 // Split-K: when the output tiles alone cannot keep every SM streaming
 // weights, the K range of each tile is split across the CTAs of a thread-
-// block cluster (up to 8); each CTA owns a slice of the outputs, every CTA
-// writes its folded fp32 partial to its own shared memory and bulk-copies
-// each owner's slice into that owner's receive buffer (DSMEM), completing on
-// the owner's mbarrier; each owner sums its slice in a fixed partner order
-// and writes Y.  With several tiles per CTA the receive buffers alternate
-// with the accumulators, and an owner that has summed a buffer re-arms it
-// and signals every partner (remote mbarrier arrive) before they send into
-// it again.
+// block cluster (up to 8); each owner CTA sums a slice of the outputs over
+// the splits in a fixed partner order and writes Y.  Narrow tiles (at most
+// 16 outputs per channel) send their folded fp32 partials straight from
+// registers with 16-byte st.async stores into the owner's receive buffer;
+// wider tiles stage the partial in shared memory and bulk-copy each owner's
+// slice (DSMEM); both complete on the owner's mbarrier.  With several tiles
+// per CTA the receive buffers alternate with the accumulators, and an owner
+// that has summed a buffer re-arms it and signals every partner (remote
+// mbarrier arrive) before they send into it again.
 //
 // Programmatic dependent launch: the kernel releases its dependents at once
 // and starts streaming weights before waiting for the previous grid; only
 // the activation / output accesses come after that wait.
 //
-// Warp roles (384 threads): warp 4 bulk/TMA producer; warp 5 TMEM allocator
-// and MMA issuer; warps 0-3 (tensor-memory lane quarters 0-3) write each
-// stage's scale atoms into tensor memory; warps 8-11 (lane quarters 0-3)
-// run the epilogue; in fused plans warps 0-3 and 6-11 first run the
-// quantizing prologue.  Every wait is
+// Warp roles (384 threads): warp 4 bulk/TMA producer; warp 5 TMEM allocator,
+// scale copies and MMA issuer; warps 8-11 (lane quarters 0-3) run the
+// epilogue, with warps 0-3 for wide tiles without split-K; in fused plans
+// warps 0-3 and 6-11 first run the quantizing prologue.  Every wait is
 // bounded (about one second); a wait that runs out sets the device error
 // word and an abort flag, and the CTA drains its copies and exits.
 #include <cuda.h>
