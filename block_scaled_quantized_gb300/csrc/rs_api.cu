@@ -453,6 +453,7 @@ rs_status rs_resattn_decode(int B, int Hq, int Hkv, int D, int max_pages, int ma
     a.seq_lens = seq_lens;
     a.part = reinterpret_cast<float*>(qop + attn_q_bytes(B, Hq, D));
     a.err = dev->err;
+    a.trace = rs::trace_buffer();
     a.B = B;
     a.Hq = Hq;
     a.Hkv = Hkv;

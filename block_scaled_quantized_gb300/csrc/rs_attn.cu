@@ -5,19 +5,29 @@
 // E4M3 scales [32][D/16], tensor scale 1.0; page bytes = 32 (D/2 + D/16).
 // A block table [B][max_pages] (int32) maps a sequence's logical pages.
 //
-// One CTA per (split, KV head, sequence); tiles of 128 tokens (4 pages):
+// One CTA per (split, KV head, sequence); tiles of 128 tokens (four pages):
+//   * warp 0 streams the tile's K and V pages with bulk copies into a ring
+//     of stages, ahead of the compute (pages taken from the block table);
+//   * warps 1-7 rearrange a landed stage in shared memory: K codes into the
+//     128-byte-swizzled rows of the MMA operand, K scales into atoms, and V
+//     from NVFP4 to E4M3 (R17) in its own token-major order (128 head
+//     dimensions per 128-byte-swizzled row);
 //   * QK on the tensor cores: kind::mxf4nvf4, A = the key tile (M = 128
-//     tokens, K-major 128-byte-swizzled rows; D = 128 uses two 64-element
-//     k-steps), B = the group's 2G <= 16 query rows (base 2g, residue 2g+1,
+//     tokens), B = the group's 2G <= 16 query rows (base 2g, residue 2g+1,
 //     from the paired quantizer), accumulator 128 x 16 fp32;
-//   * fold, online softmax: thread t of warps 0-3 reads token t's 2G scores,
-//     s_g = fl(fl(z_2g + z_2g+1) c), the tile maximum per head through warp
-//     shuffles and shared memory, p = exp(s - m), rounded to E4M3;
-//   * V: NVFP4 -> E4M3 (R17) into shared memory as fp16 (exact), then
-//     O[g][d] = O[g][d] a_g + sum_t p8[g][t] v8[t][d] in fp32 (the products
-//     are exact); the normalizer sums the rounded weights (R18);
+//   * fold and online softmax (warps 4-7, one token per thread):
+//     s_g = fl(fl(z_2g + z_2g+1) c), the tile maximum per head, p = exp(s - m)
+//     rounded to E4M3 (R18) and written as the PV operand P [head][token];
+//   * PV on the tensor cores: kind::f8f6f4 (E4M3 x E4M3, fp32 accumulation),
+//     A = V^T read as an MN-major operand (M = 128 head dimensions per MMA,
+//     contiguous in each token row), B = P (N = 16), K = 128 tokens in four
+//     steps of 32 rows; warps 4-7 add the tile's accumulator into their
+//     running outputs after rescaling them by exp(m_old - m_new), and the
+//     normalizer sums the rounded weights (R18);
 //   * the split's o, m, l go to a workspace; a second kernel combines the
 //     splits (R19) and writes bf16 or fp32.
+// Several CTAs share an SM (head size 128), so one CTA's rearranging and
+// softmax overlap another's MMAs and copies.  Every wait is bounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -27,12 +37,54 @@
 
 namespace rs {
 
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 256;     // warp 0 copies, warp 1 MMAs, warps 1-7 rearrange, warps 4-7 softmax/PV
+constexpr int kAttnCompute = 224;     // warps 1-7
 constexpr int kAttnTile = 128;
 constexpr int kPage = 32;
 
-
 __host__ __device__ constexpr int page_bytes(int D) { return kPage * (D / 2 + D / 16); }
+
+// Shared-memory layout of one CTA (offsets from a 1024-byte aligned base).
+template <int D>
+struct AttnLayout {
+    static constexpr int CB = D / 2, SB = D / 16;      // code / scale bytes per token
+    static constexpr int NA = D / 64;                  // scale atoms (4 blocks) per token row; = QK k-steps
+    static constexpr int PB = page_bytes(D);
+    static constexpr int STAGES = D == 128 ? 3 : 2;
+    static constexpr uint32_t STG = 8u * (uint32_t)PB;         // four K pages, then four V pages
+    static constexpr uint32_t OFF_K = (uint32_t)STAGES * STG;  // key tile: 128 SW128 rows
+    static constexpr uint32_t OFF_V = OFF_K + 16384u;          // V (E4M3): per 128 dims, 128 SW128 token rows
+    static constexpr uint32_t OFF_Q = OFF_V + (uint32_t)D * 128u;  // query rows: 16 SW128 rows
+    static constexpr uint32_t OFF_P = OFF_Q + 2048u;           // P: 16 SW128 rows of 128 tokens
+    static constexpr uint32_t OFF_KSF = OFF_P + 2048u;         // key scale atoms
+    static constexpr uint32_t OFF_QSF = OFF_KSF + (uint32_t)NA * 512u;
+    static constexpr uint32_t OFF_CTRL = OFF_QSF + (uint32_t)NA * 512u;
+    static constexpr size_t SMEM = 1024 + OFF_CTRL + 512;
+    // tensor memory: QK accumulator (16 columns), PV accumulators (16 per
+    // 128 head dimensions), then the key and query scale atoms
+    static constexpr uint32_t T_PV = 16u, T_SFK = T_PV + 16u * (D / 128), T_SFQ = T_SFK + 4u * NA;
+    static constexpr uint32_t TCOLS = D == 128 ? 64u : 128u;
+    static_assert(STG % 1024 == 0 && OFF_K % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+    static_assert(T_SFQ + 4u * NA <= TCOLS, "tensor-memory columns");
+};
+
+// Instruction descriptor of kind::f8f6f4: A and B E4M3 (format 0), fp32
+// accumulator (bit 4), A MN-major (bit 15: M contiguous), B K-major,
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t f8_idesc_amn(int n, int m) {
+    return (1u << 4) | (1u << 15) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// D[128 x N] (+)= A[128 x 32] * B[N x 32]^T, E4M3 operands, fp32 accumulation.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 
 // Tokens of sequence b the kernels attend to: its length, clamped to
 // [0, max_len] (a longer one is reported in the device error word, so that
@@ -43,234 +95,353 @@ __device__ __forceinline__ int attn_len(const AttnArgs& g, int b) {
     return L < 0 ? 0 : (L > g.max_len ? g.max_len : L);
 }
 
-// E4M3 value of an fp32 value (nearest-even, saturating, sign kept) as float.
-__device__ __forceinline__ float e4m3_round(float p) { return e4m3_decode_hw(e4m3x2_encode_hw(0.0f, p) & 0xFFu); }
+// E4M3 bytes (round to nearest even, saturating; R17) of the sixteen values
+// of one V block: scale byte times the E2M1 codes.  The product of an E4M3
+// and an E2M1 value has at most five significant bits and lies within
+// [2^-10, 2688], so it is exact in fp16, and its E4M3 rounding is that of the
+// exact product.  Byte e of the block is byte e % 4 of w[e / 4].
+__device__ __forceinline__ void v_block_e4m3(uint2 codes, uint32_t sbyte, uint32_t (&w)[4]) {
+    uint32_t s2;  // (s, s) as f16x2
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"((uint16_t)(sbyte | (sbyte << 8))));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t word = k < 4 ? codes.x : codes.y;
+        const uint16_t byte2 = (uint16_t)((word >> (8 * (k & 3))) & 0xFFu);
+        uint32_t h2, p2;
+        uint16_t e2;
+        asm("{\n\t.reg .b8 cb;\n\tcvt.u8.u16 cb, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, cb;\n\t}" : "=r"(h2) : "h"(byte2));
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p2) : "r"(h2), "r"(s2));
+        asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e2) : "r"(p2));
+        // element 2k (low nibble -> low half -> low byte), then element 2k + 1
+        w[k >> 1] |= (uint32_t)e2 << (16 * (k & 1));
+    }
+}
 
-// Dynamic shared memory of one CTA.
-__host__ __device__ constexpr size_t attn_smem_bytes(int D) {
-    return 1024 + kAttnTile * 128 + 16 * 128 + 2 * (D / 64) * 512 + (size_t)kAttnTile * D * 2 + 8 * kAttnTile * 4 +
-           4 * 8 * 4 + 3 * 8 * 4 + 64;
+// Warp maximum of a float (NaN-free inputs; -inf allowed) with one redux.sync
+// on an order-preserving integer image of its bits.
+__device__ __forceinline__ float warp_max_f32(float x) {
+    const int i = __float_as_int(x);
+    int key = i >= 0 ? i : (i ^ 0x7FFFFFFF);
+    key = __reduce_max_sync(0xFFFFFFFFu, key);
+    return __int_as_float(key >= 0 ? key : (key ^ 0x7FFFFFFF));
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1) resattn_split_kernel(const AttnArgs g) {
-    constexpr int CB = D / 2, SB = D / 16;          // code / scale bytes per token row
-    constexpr int NKS = D / 64;                     // 64-element k-steps
-    constexpr int NA = D / 64;                      // scale atoms (4 blocks each) per row
-    constexpr int HPT = 8 * D / kAttnThreads;       // heads per PV thread (4 at D = 128, 8 at D = 256)
-    constexpr uint32_t TCOLS = D == 128 ? 32 : 64;  // accumulator 16 + scale atoms 2 x 4 NA
+__global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_kernel(const AttnArgs g) {
+    using Ly = AttnLayout<D>;
+    constexpr int CB = Ly::CB, SB = Ly::SB, NA = Ly::NA, PB = Ly::PB, S = Ly::STAGES;
+    constexpr int MB = D / 128;  // PV MMAs of 128 head dimensions
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* ktile = sm;                                         // 128 SW128 rows, D/2 bytes used
-    uint8_t* qtile = ktile + kAttnTile * 128;                    // 16 SW128 rows
-    uint8_t* ksf = qtile + 16 * 128;                             // NA key scale atoms
-    uint8_t* qsf = ksf + NA * 512;                               // NA query scale atoms
-    __half* vt = reinterpret_cast<__half*>(qsf + NA * 512);      // V8 values [token][d]
-    float (*pw)[kAttnTile] = reinterpret_cast<float (*)[kAttnTile]>(vt + kAttnTile * D);  // p8 [head][token]
-    float (*red)[8] = reinterpret_cast<float (*)[8]>(&pw[8][0]);
-    float* m_run = &red[4][0];
-    float* l_run = m_run + 8;
-    float* a_fac = l_run + 8;
-    uint64_t* mma_done = reinterpret_cast<uint64_t*>(a_fac + 8);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint8_t* stg = sm;
+    uint8_t* ktile = sm + Ly::OFF_K;
+    uint8_t* vt = sm + Ly::OFF_V;
+    uint8_t* qtile = sm + Ly::OFF_Q;
+    uint8_t* ptile = sm + Ly::OFF_P;
+    uint8_t* ksf = sm + Ly::OFF_KSF;
+    uint8_t* qsf = sm + Ly::OFF_QSF;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly::OFF_CTRL);  // [S]: a stage's pages landed
+    uint64_t* empty = full + 3;                                       // [S]: a stage was read
+    uint64_t* qk_done = empty + 3;                                    // the tile's QK MMAs are done
+    uint64_t* pv_done = qk_done + 1;                                  // the tile's PV MMAs are done
+    float* red = reinterpret_cast<float*>(pv_done + 1);               // [4][8] tile maxima per warp
+    int* red2 = reinterpret_cast<int*>(red + 32);                      // [4][8] weight sums per warp (2^-9 units)
+    float* m_run = red + 64;                                          // [8] running maxima
+    float* l_run = m_run + 8;                                         // [8] running normalizers
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(l_run + 8);
     volatile uint32_t* abort_flag = tmem_slot + 1;
+    volatile uint32_t* issued = tmem_slot + 2;    // tiles whose copies were issued
+    volatile uint32_t* consumed = tmem_slot + 3;  // tiles whose stage was released
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = g.Hq / g.Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int L = attn_len(g, b);
     const int t0 = split * g.split_tokens, t1 = min(L, t0 + g.split_tokens);
+    const int ntiles = t1 > t0 ? (t1 - t0 + kAttnTile - 1) / kAttnTile : 0;
     float* part = g.part + (((size_t)b * g.Hkv + h) * g.splits + split) * (size_t)G * (D + 2);
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(mma_done), 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(qk_done), 1);
+        mbar_init(smem_u32(pv_done), 1);
         *abort_flag = 0u;
+        *issued = 0u;
+        *consumed = 0u;
         fence_mbarrier_init();
     }
     if (threadIdx.x < 8) {
         m_run[threadIdx.x] = -INFINITY;
         l_run[threadIdx.x] = 0.0f;
     }
-    // the group's 2G query rows (zero rows up to 16) and their scale bytes
-    for (int i = threadIdx.x; i < 16 * 8; i += kAttnThreads) {  // 16 rows x 8 chunks of 16 bytes
+    // the group's 2G query rows (zero rows up to 16), P all zero (rows >= G
+    // stay zero), the query scales in atoms
+    for (int i = threadIdx.x; i < 16 * 8; i += kAttnThreads) {
         const int r = i / 8, c = i % 8;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         const int row = 2 * (b * g.Hq + h * G) + r;
         if (r < 2 * G && c * 16 < CB) v = *reinterpret_cast<const uint4*>(g.q_op + (size_t)row * CB + c * 16);
         *reinterpret_cast<uint4*>(qtile + sw128_offset((uint32_t)r, (uint32_t)c * 16u)) = v;
+        *reinterpret_cast<uint4*>(ptile + (size_t)i * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
-    for (int i = threadIdx.x; i < NA * 512; i += kAttnThreads) qsf[i] = 0;
+    for (int i = threadIdx.x; i < NA * 128; i += kAttnThreads) reinterpret_cast<uint32_t*>(qsf)[i] = 0u;
     __syncthreads();
-    {
-        const uint8_t* qsf_src = g.q_sf;
-        for (int i = threadIdx.x; i < 2 * G * SB; i += kAttnThreads) {
-            const int r = i / SB, blk = i % SB;
-            const int row = 2 * (b * g.Hq + h * G) + r;
-            qsf[(blk / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + blk % 4] =
-                qsf_src[sf_offset(row, blk, g.q_atoms_k)];
-        }
+    for (int i = threadIdx.x; i < 2 * G * SB; i += kAttnThreads) {
+        const int r = i / SB, blk = i % SB;
+        const int row = 2 * (b * g.Hq + h * G) + r;
+        qsf[(blk / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + blk % 4] = g.q_sf[sf_offset(row, blk, g.q_atoms_k)];
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TCOLS);
+        tmem_alloc(smem_u32(tmem_slot), Ly::TCOLS);
         tmem_relinquish();
     }
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;                 // accumulator: columns 0-15
-    const uint32_t tsfa = tmem + 16, tsfb = tmem + 16 + 4 * NA;
-    const float c = __fmul_rn(*g.alpha_q, __frsqrt_rn((float)D));  // alpha_q / sqrt(D), alpha_k = 1
-    float o[HPT];                                      // thread: d = tid % D, heads og0 .. og0 + HPT - 1
-#pragma unroll
-    for (int q = 0; q < HPT; ++q) o[q] = 0.0f;
-    const int od = threadIdx.x % D, og0 = (threadIdx.x / D) * HPT;
-    uint32_t ph = 0;
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t t_qk = tmem, t_pv = tmem + Ly::T_PV, t_sfk = tmem + Ly::T_SFK, t_sfq = tmem + Ly::T_SFQ;
 
-    for (int u0 = t0; *abort_flag == 0u && u0 < t1; u0 += kAttnTile) {
-        const int nt = min(kAttnTile, t1 - u0);
-        // K tile: codes into the swizzled rows, scales into the atoms
-        for (int i = threadIdx.x; i < kAttnTile * (CB / 16); i += kAttnThreads) {
-            const int r = i / (CB / 16), cc = i % (CB / 16);
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < nt) {
-                const int t = u0 + r;
-                const int page = g.block_table[(size_t)b * g.max_pages + t / kPage];
-                const uint8_t* pg = g.k_cache + ((size_t)page * g.Hkv + h) * page_bytes(D);
-                v = *reinterpret_cast<const uint4*>(pg + (size_t)(t % kPage) * CB + cc * 16);
-            }
-            *reinterpret_cast<uint4*>(ktile + sw128_offset((uint32_t)r, (uint32_t)cc * 16u)) = v;
-        }
-        for (int i = threadIdx.x; i < kAttnTile * NA; i += kAttnThreads) {
-            const int r = i / NA, a = i % NA;
-            uint32_t w = 0u;
-            if (r < nt) {
-                const int t = u0 + r;
-                const int page = g.block_table[(size_t)b * g.max_pages + t / kPage];
-                const uint8_t* pg = g.k_cache + ((size_t)page * g.Hkv + h) * page_bytes(D) + kPage * CB;
-                w = *reinterpret_cast<const uint32_t*>(pg + (size_t)(t % kPage) * SB + a * 4);
-            }
-            *reinterpret_cast<uint32_t*>(ksf + a * 512 + (r % 32) * 16 + (r / 32) * 4) = w;
-        }
-        // V tile -> E4M3 values (as fp16, exact) in [token][d]
-        for (int i = threadIdx.x; i < kAttnTile * SB; i += kAttnThreads) {
-            const int r = i / SB, blk = i % SB;
-            __half hv[16];
-            if (r < nt) {
-                const int t = u0 + r;
-                const int page = g.block_table[(size_t)b * g.max_pages + t / kPage];
-                const uint8_t* pg = g.v_cache + ((size_t)page * g.Hkv + h) * page_bytes(D);
-                const uint2 cw = *reinterpret_cast<const uint2*>(pg + (size_t)(t % kPage) * CB + blk * 8);
-                const float s = e4m3_decode_hw(pg[kPage * CB + (t % kPage) * SB + blk]);
-                float d8[8];
-                e2m1_decode8(cw.x, d8);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) hv[e] = __float2half_rn(e4m3_round(__fmul_rn(s, d8[e])));
-                e2m1_decode8(cw.y, d8);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) hv[8 + e] = __float2half_rn(e4m3_round(__fmul_rn(s, d8[e])));
-            } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) hv[e] = __float2half_rn(0.0f);
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) vt[r * D + blk * 16 + e] = hv[e];
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // QK: base and residue scores of the group against the tile
-        if (warp == 1) {
-            tc_fence_after();
+    if (warp == 0) {
+        // ------------------------------------------------ page copies
+        const uint64_t pol = l2_policy_evict_first();  // the cache is read once
+        int s = 0;
+        uint32_t ph = 0;
+        for (int it = 0; it < ntiles; ++it) {
+            if (it >= S &&
+                !__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort_flag, g.err)))
+                break;
             if (elect_one_sync()) {
-                const uint64_t ad = kmajor_sw128_desc(smem_u32(ktile)), bd = kmajor_sw128_desc(smem_u32(qtile));
-                for (int a = 0; a < NA; ++a) {
-                    tc_cp_sf_atom(tsfa + a * 4, sf_atom_desc(smem_u32(ksf + a * 512)));
-                    tc_cp_sf_atom(tsfb + a * 4, sf_atom_desc(smem_u32(qsf + a * 512)));
+                const int u0 = t0 + it * kAttnTile, nt = min(kAttnTile, t1 - u0), np = (nt + kPage - 1) / kPage;
+                uint8_t* st = stg + (size_t)s * Ly::STG;
+                const uint32_t fb = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(fb, 2u * (uint32_t)np * (uint32_t)PB);
+                for (int p = 0; p < np; ++p) {
+                    const int page = g.block_table[(size_t)b * g.max_pages + u0 / kPage + p];
+                    const size_t off = ((size_t)page * g.Hkv + h) * (size_t)PB;
+                    bulk_load(smem_u32(st + p * PB), g.k_cache + off, (uint32_t)PB, fb, pol);
+                    bulk_load(smem_u32(st + (4 + p) * PB), g.v_cache + off, (uint32_t)PB, fb, pol);
                 }
-                for (int ks = 0; ks < NKS; ++ks)
-                    mma_nvfp4(tmem, ad + (uint32_t)ks * 2u, bd + (uint32_t)ks * 2u, mxf4_idesc(16, false, 0),
-                              tsfa + ks * 4, tsfb + ks * 4, ks > 0 ? 1u : 0u);
-                tc_commit(smem_u32(mma_done));
+                *issued = (uint32_t)(it + 1);
             }
             __syncwarp();
-        }
-        // fold, tile maximum, weights (warps 0-3: token = thread)
-        float sc[8];
-        if (warp < 4) {
-            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(mma_done), ph, abort_flag, g.err));
-            tc_fence_after();
-            float z[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) z[e] = 0.0f;
-            if (ok) tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), z);
-            const int r = threadIdx.x;
-#pragma unroll
-            for (int gg = 0; gg < 8; ++gg) {
-                sc[gg] = (gg < G && r < nt) ? __fmul_rn(__fadd_rn(z[2 * gg], z[2 * gg + 1]), c) : -INFINITY;
-                float mx = sc[gg];
-#pragma unroll
-                for (int o2 = 16; o2 > 0; o2 >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o2));
-                if (lane == 0) red[warp][gg] = mx;
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
             }
         }
-        ph ^= 1u;
-        __syncthreads();
-        if (threadIdx.x < 8) {
-            const int gg = threadIdx.x;
-            const float tm = fmaxf(fmaxf(red[0][gg], red[1][gg]), fmaxf(red[2][gg], red[3][gg]));
-            const float mn = fmaxf(m_run[gg], tm);
-            a_fac[gg] = m_run[gg] == -INFINITY ? 0.0f : __expf(m_run[gg] - mn);
-            m_run[gg] = mn;
+    } else {
+        // ------------------------------------------------ warps 1-7
+        const int ct = threadIdx.x - 32;               // 0..223: rearranging thread
+        const bool smw = warp >= 4;                    // softmax / PV warps
+        const int r = (warp & 3) * 32 + lane;          // token (softmax), head dimension (PV)
+        const uint32_t quarter = (uint32_t)((warp & 3) * 32) << 16;
+        const float c = __fmul_rn(*g.alpha_q, __frsqrt_rn((float)D));  // alpha_q / sqrt(D), alpha_k = 1
+        const uint64_t kdesc = kmajor_sw128_desc(smem_u32(ktile)), qdesc = kmajor_sw128_desc(smem_u32(qtile));
+        const uint64_t vdesc = kmajor_sw128_desc(smem_u32(vt)), pdesc = kmajor_sw128_desc(smem_u32(ptile));
+        float o[MB][8];
+#pragma unroll
+        for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o[mb][q] = 0.0f;
+        float a_t[8];  // this tile's rescale factors exp(m_old - m_new)
+        if (warp == 1) {
+            if (elect_one_sync())
+                for (int a = 0; a < NA; ++a) tc_cp_sf_atom(t_sfq + a * 4, sf_atom_desc(smem_u32(qsf + a * 512)));
+            __syncwarp();
         }
-        __syncthreads();
-        if (warp < 4) {
-            const int r = threadIdx.x;
+        int s = 0;
+        uint32_t ph = 0;
+        for (int it = 0; it < ntiles; ++it) {
+            const int u0 = t0 + it * kAttnTile, nt = min(kAttnTile, t1 - u0);
+            // the previous tile's MMAs have read the key tile, V^T and P
+            if (it > 0) (void)mbar_wait_bounded(smem_u32(pv_done), (uint32_t)(it - 1) & 1u, abort_flag, g.err);
+            const bool landed = mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err);
+            if (ct == 0 && it < 6) RS_TRACE_MARK(g.trace, 5 * it);  // stage landed
+            const uint8_t* st = stg + (size_t)s * Ly::STG;
+            if (landed) {
+                // key codes -> 128-byte-swizzled rows (tokens past the end: zero)
+                for (int i = ct; i < kAttnTile * (CB / 16); i += kAttnCompute) {
+                    const int rr = i / (CB / 16), cc = i % (CB / 16);
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (rr < nt)
+                        v = *reinterpret_cast<const uint4*>(st + (rr / kPage) * PB + (rr % kPage) * CB + cc * 16);
+                    *reinterpret_cast<uint4*>(ktile + sw128_offset((uint32_t)rr, (uint32_t)cc * 16u)) = v;
+                }
+                // key scales -> atoms (the four blocks of an atom are one word per token)
+                for (int i = ct; i < kAttnTile * NA; i += kAttnCompute) {
+                    const int rr = i / NA, a = i % NA;
+                    uint32_t w = 0u;
+                    if (rr < nt)
+                        w = *reinterpret_cast<const uint32_t*>(st + (rr / kPage) * PB + kPage * CB + (rr % kPage) * SB +
+                                                               a * 4);
+                    *reinterpret_cast<uint32_t*>(ksf + a * 512 + (rr % 32) * 16 + (rr / 32) * 4) = w;
+                }
+                // V -> E4M3 (R17): token row t holds its head dimensions, 128 per tile
+                for (int i = ct; i < kAttnTile * SB; i += kAttnCompute) {
+                    const int t = i / SB, bb = i % SB;
+                    uint32_t w[4] = {0u, 0u, 0u, 0u};
+                    if (t < nt) {
+                        const uint8_t* pg = st + (4 + t / kPage) * PB;
+                        v_block_e4m3(*reinterpret_cast<const uint2*>(pg + (t % kPage) * CB + bb * 8),
+                                     pg[kPage * CB + (t % kPage) * SB + bb], w);
+                    }
+                    *reinterpret_cast<uint4*>(vt + (bb / 8) * 16384 +
+                                              sw128_offset((uint32_t)t, (uint32_t)(bb % 8) * 16u)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, kAttnCompute);
+            if (ct == 0 && it < 6) RS_TRACE_MARK(g.trace, 5 * it + 1);  // rearranged
+            if (warp == 1) {
+                // stage free again; QK of the group's base and residue rows
+                tc_fence_after();
+                if (elect_one_sync()) {
+                    mbar_arrive(smem_u32(&empty[s]));
+                    *consumed = (uint32_t)(it + 1);
+                    if (*abort_flag == 0u) {
+                        for (int a = 0; a < NA; ++a)
+                            tc_cp_sf_atom(t_sfk + a * 4, sf_atom_desc(smem_u32(ksf + a * 512)));
+                        for (int ks = 0; ks < NA; ++ks)
+                            mma_nvfp4(t_qk, kdesc + (uint32_t)ks * 2u, qdesc + (uint32_t)ks * 2u, mxf4_idesc(16, false, 0),
+                                      t_sfk + ks * 4, t_sfq + ks * 4, ks > 0 ? 1u : 0u);
+                        tc_commit(smem_u32(qk_done));
+                    }
+                }
+                __syncwarp();
+            }
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (smw) {
+                // fold, tile maximum, E4M3 weights, normalizer (token r per thread)
+                const bool ok =
+                    __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(qk_done), (uint32_t)it & 1u, abort_flag, g.err));
+                tc_fence_after();
+                float z[16];
 #pragma unroll
-            for (int gg = 0; gg < 8; ++gg) {
-                const float p8 = (gg < G && r < nt) ? e4m3_round(__expf(sc[gg] - m_run[gg])) : 0.0f;
-                pw[gg][r] = p8;
-                float sm = p8;
+                for (int e = 0; e < 16; ++e) z[e] = 0.0f;
+                if (ok) tmem_ld16(t_qk + quarter, z);
+                if (r == 0 && it < 6) RS_TRACE_MARK(g.trace, 5 * it + 2);  // QK done
+                float sc[8];
 #pragma unroll
-                for (int o2 = 16; o2 > 0; o2 >>= 1) sm += __shfl_xor_sync(0xFFFFFFFFu, sm, o2);
-                if (lane == 0) red[warp][gg] = sm;
+                for (int q = 0; q < 8; ++q) {
+                    sc[q] = -INFINITY;
+                    if (q < G) {
+                        if (r < nt) sc[q] = __fmul_rn(__fadd_rn(z[2 * q], z[2 * q + 1]), c);
+                        const float mx = warp_max_f32(sc[q]);
+                        if (lane == 0) red[(warp - 4) * 8 + q] = mx;
+                    }
+                }
+                named_bar_sync(2, 128);
+                float m_new[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    m_new[q] = -INFINITY;
+                    a_t[q] = 0.0f;
+                    if (q < G) {
+                        const float tm = fmaxf(fmaxf(red[q], red[8 + q]), fmaxf(red[16 + q], red[24 + q]));
+                        const float mo = m_run[q];
+                        m_new[q] = fmaxf(mo, tm);
+                        a_t[q] = mo == -INFINITY ? 0.0f : __expf(mo - m_new[q]);
+                        uint32_t pb = 0u;
+                        if (r < nt) pb = e4m3x2_encode_hw(0.0f, __expf(sc[q] - m_new[q])) & 0xFFu;
+                        ptile[sw128_offset((uint32_t)q, (uint32_t)r)] = (uint8_t)pb;
+                        // E4M3 weights in [0, 1] are multiples of 2^-9: their sum is exact in integers
+                        const int units = __float2int_rn(__fmul_rn(e4m3_decode_hw(pb), 512.0f));
+                        const int sum = __reduce_add_sync(0xFFFFFFFFu, units);
+                        if (lane == 0) red2[(warp - 4) * 8 + q] = sum;
+                    }
+                }
+                named_bar_sync(2, 128);
+                if (r == 0)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if (q < G) {
+                            const int tile_sum = (red2[q] + red2[8 + q]) + (red2[16 + q] + red2[24 + q]);
+                            l_run[q] = l_run[q] * a_t[q] + __fmul_rn((float)tile_sum, 0x1p-9f);
+                            m_run[q] = m_new[q];
+                        }
+                    }
+                fence_proxy_async_smem();  // P for the tensor pipe
+            }
+            if (warp == 1 || smw) named_bar_sync(3, 160);  // warps 1 and 4-7: P is in shared memory
+            if (r == 0 && smw && it < 6) RS_TRACE_MARK(g.trace, 5 * it + 3);  // softmax done
+            if (warp == 1) {
+                // PV: V^T (128 head dimensions per MMA) x P^T over the tile's tokens
+                tc_fence_after();
+                if (elect_one_sync() && *abort_flag == 0u) {
+#pragma unroll
+                    for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+                        for (int kt = 0; kt < kAttnTile / 32; ++kt)
+                            mma_e4m3(t_pv + (uint32_t)(mb * 16),
+                                     vdesc + (uint32_t)(mb * (16384 >> 4)) + (uint32_t)kt * (4096u >> 4),
+                                     pdesc + (uint32_t)kt * 2u, f8_idesc_amn(16, 128), kt > 0 ? 1u : 0u);
+                    tc_commit(smem_u32(pv_done));
+                }
+                __syncwarp();
+            }
+            if (smw) {
+                // running outputs: o = o exp(m_old - m_new) + the tile's P V (head dimension r)
+                const bool ok =
+                    __all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(pv_done), (uint32_t)it & 1u, abort_flag, g.err));
+                tc_fence_after();
+#pragma unroll
+                for (int mb = 0; mb < MB; ++mb) {
+                    float pv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pv[e] = 0.0f;
+                    if (ok) tmem_ld16(t_pv + (uint32_t)(mb * 16) + quarter, pv);
+                    if (r == 0 && mb == 0 && it < 6) RS_TRACE_MARK(g.trace, 5 * it + 4);  // PV done
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) o[mb][q] = fmaf(o[mb][q], a_t[q], pv[q]);
+                }
             }
         }
-        __syncthreads();
-        if (threadIdx.x < 8) {
-            const int gg = threadIdx.x;
-            l_run[gg] = l_run[gg] * a_fac[gg] + ((red[0][gg] + red[1][gg]) + (red[2][gg] + red[3][gg]));
-        }
-        // PV: thread (d, 4 heads), exact fp32 products of E4M3 values
-        __syncthreads();  // l_run and a_fac are final for this tile
+        // this split's o, m, l
+        if (smw) {
 #pragma unroll
-        for (int q = 0; q < HPT; ++q) o[q] *= a_fac[og0 + q];
-        for (int t = 0; t < nt; ++t) {
-            const float v = __half2float(vt[t * D + od]);
+            for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
-            for (int q = 0; q < HPT; ++q) o[q] = fmaf(pw[og0 + q][t], v, o[q]);
+                for (int q = 0; q < 8; ++q)
+                    if (q < G) part[(size_t)q * (D + 2) + mb * 128 + r] = o[mb][q];
+            if (r < G) {
+                part[(size_t)r * (D + 2) + D] = m_run[r];
+                part[(size_t)r * (D + 2) + D + 1] = l_run[r];
+            }
         }
-        __syncthreads();
     }
 
-    // this split's o, m, l
-#pragma unroll
-    for (int q = 0; q < HPT; ++q)
-        if (og0 + q < G) part[(size_t)(og0 + q) * (D + 2) + od] = o[q];
-    if (threadIdx.x < G) {
-        part[(size_t)threadIdx.x * (D + 2) + D] = m_run[threadIdx.x];
-        part[(size_t)threadIdx.x * (D + 2) + D + 1] = l_run[threadIdx.x];
-    }
+    // teardown: after an abort, let the page copies still in flight land
+    // before the shared memory goes away
     tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, TCOLS);
+    if (*abort_flag) {
+        if (warp == 0 && lane == 0) {
+            for (uint32_t u = *consumed; u < *issued; ++u) {
+                volatile uint32_t no_abort = 0;
+                (void)mbar_wait_bounded(smem_u32(&full[u % (uint32_t)S]), (u / (uint32_t)S) & 1u, &no_abort, nullptr,
+                                        100000000ull);
+            }
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Ly::TCOLS);
+    }
 }
 
 // O = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s (R19); empty sequences give 0.
 __global__ void resattn_combine_kernel(const AttnArgs g, void* out, int out_f32) {
-    const int B = g.B, Hq = g.Hq, Hkv = g.Hkv, D = g.D, splits = g.splits, split_tokens = g.split_tokens;
+    const int Hq = g.Hq, Hkv = g.Hkv, D = g.D, splits = g.splits, split_tokens = g.split_tokens;
     const float* part = g.part;
-    (void)B;
     const int G = Hq / Hkv;
     const int b = blockIdx.y, hq = blockIdx.x, d = threadIdx.x;
     if (d >= D) return;
@@ -295,33 +466,40 @@ __global__ void resattn_combine_kernel(const AttnArgs g, void* out, int out_f32)
 
 // ---------------------------------------------------------------- launch --
 
-// Splits: enough (split, KV head, sequence) CTAs for every SM, in multiples
-// of the tile, at least one tile per split (the preset rule of Sec. 5.2 from
-// batch, KV heads, sequence length and SM count).
+// Splits: enough (split, KV head, sequence) CTAs to fill every SM with the
+// CTAs that fit on it (two at head size 128), in multiples of the tile and
+// at least one tile per split (the preset rule of Sec. 5.2 from batch, KV
+// heads, sequence length and SM count).
 int resattn_split_tokens(int B, int Hkv, int max_len, int num_sms) {
     const int tiles = (max_len + kAttnTile - 1) / kAttnTile;
-    int splits = (num_sms + B * Hkv - 1) / (B * Hkv);
+    const int slots = 2 * num_sms;
+    int splits = (slots + B * Hkv - 1) / (B * Hkv);
     if (splits > tiles) splits = tiles;
     if (splits < 1) splits = 1;
     const int tiles_per_split = (tiles + splits - 1) / splits;
     return (tiles_per_split < 1 ? 1 : tiles_per_split) * kAttnTile;
 }
 
-cudaError_t launch_resattn(int D, const AttnArgs& a, void* out, int out_f32, cudaStream_t stream) {
-    const size_t smem = attn_smem_bytes(D);
-    dim3 grid((unsigned)a.splits, (unsigned)a.Hkv, (unsigned)a.B);
-    cudaError_t e;
-    if (D == 128) {
-        e = cudaFuncSetAttribute(resattn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) resattn_split_kernel<128><<<grid, kAttnThreads, smem, stream>>>(a);
-    } else if (D == 256) {
-        e = cudaFuncSetAttribute(resattn_split_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) resattn_split_kernel<256><<<grid, kAttnThreads, smem, stream>>>(a);
-    } else {
-        return cudaErrorInvalidValue;
-    }
+template <int D>
+static cudaError_t launch_split(const AttnArgs& a, cudaStream_t stream) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = cudaGetLastError();
+    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(resattn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)AttnLayout<D>::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) attr_done[dev] = true;
+    }
+    dim3 grid((unsigned)a.splits, (unsigned)a.Hkv, (unsigned)a.B);
+    resattn_split_kernel<D><<<grid, kAttnThreads, AttnLayout<D>::SMEM, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_resattn(int D, const AttnArgs& a, void* out, int out_f32, cudaStream_t stream) {
+    cudaError_t e = D == 128 ? launch_split<128>(a, stream) : D == 256 ? launch_split<256>(a, stream)
+                                                                      : cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     resattn_combine_kernel<<<dim3((unsigned)a.Hq, (unsigned)a.B), D, 0, stream>>>(a, out, out_f32);
     return cudaGetLastError();

@@ -1248,6 +1248,14 @@ static cudaError_t launch_typed(const GemmPlan& p, const CUtensorMap& tb, const 
 static uint64_t* g_trace = nullptr;
 #endif
 
+uint64_t* trace_buffer() {
+#ifdef RS_TRACE
+    return g_trace;
+#else
+    return nullptr;
+#endif
+}
+
 cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t stream) {
     if (p.pair) {
         int dev = 0, sms = 0;

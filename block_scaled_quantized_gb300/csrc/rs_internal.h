@@ -101,6 +101,8 @@ struct GemmCall {
 size_t plan_b_stage_bytes(const GemmPlan& p);
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_gemm(const GemmPlan& plan, const GemmCall& call, cudaStream_t stream);
+// Trace builds: the buffer the kernels stamp (null otherwise).
+uint64_t* trace_buffer();
 // Route eligible large calls to the paired-CTA GEMM (off by default).
 void set_pair_gemm(int enable);
 // Paired-CTA GEMM on a quantized activation operand of Rb rows (Rb >= 256,
@@ -123,6 +125,7 @@ struct AttnArgs {
     const int* seq_lens;      // [B]
     float* part;              // [B][Hkv][splits][G][D + 2]: o, then m, l per head
     uint32_t* err;
+    uint64_t* trace;          // trace builds only: 32 timer stamps per CTA
     int B, Hq, Hkv, D, max_pages, max_len, split_tokens, splits;
     int q_rows_pad;           // paired operand rows rounded to 128 (scale atoms)
     int q_atoms_k;            // scale atoms per 128-row tile of the query operand
