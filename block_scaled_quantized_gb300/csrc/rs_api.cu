@@ -441,7 +441,7 @@ rs_status rs_resattn_decode(int B, int Hq, int Hkv, int D, int max_pages, int ma
     const int rows = B * Hq;
     uint8_t* qop = static_cast<uint8_t*>(workspace);
     if (launch_quantize(RS_NVFP4, true, rows, D, q_bf16, D, alpha_q, qop, (cudaStream_t)stream, dev->num_sms,
-                        /*pdl=*/false) != cudaSuccess)
+                        /*pdl=*/true) != cudaSuccess)
         return RS_ERR_CUDA;
     rs::AttnArgs a{};
     a.q_op = qop;

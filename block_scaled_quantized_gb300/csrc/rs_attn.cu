@@ -58,7 +58,8 @@ struct AttnLayout {
     static constexpr uint32_t OFF_P = OFF_Q + 2048u;           // P: 16 SW128 rows of 128 tokens
     static constexpr uint32_t OFF_KSF = OFF_P + 2048u;         // key scale atoms
     static constexpr uint32_t OFF_QSF = OFF_KSF + (uint32_t)NA * 512u;
-    static constexpr uint32_t OFF_CTRL = OFF_QSF + (uint32_t)NA * 512u;
+    static constexpr uint32_t OFF_LUT = OFF_QSF + (uint32_t)NA * 512u;  // V: E4M3 of s~ x |E2M1| per scale byte
+    static constexpr uint32_t OFF_CTRL = OFF_LUT + 1024u;
     static constexpr size_t SMEM = 1024 + OFF_CTRL + 512;
     // tensor memory: QK accumulator (16 columns), PV accumulators (16 per
     // 128 head dimensions), then the key and query scale atoms
@@ -95,25 +96,37 @@ __device__ __forceinline__ int attn_len(const AttnArgs& g, int b) {
     return L < 0 ? 0 : (L > g.max_len ? g.max_len : L);
 }
 
-// E4M3 bytes (round to nearest even, saturating; R17) of the sixteen values
-// of one V block: scale byte times the E2M1 codes.  The product of an E4M3
-// and an E2M1 value has at most five significant bits and lies within
-// [2^-10, 2688], so it is exact in fp16, and its E4M3 rounding is that of the
-// exact product.  Byte e of the block is byte e % 4 of w[e / 4].
-__device__ __forceinline__ void v_block_e4m3(uint2 codes, uint32_t sbyte, uint32_t (&w)[4]) {
-    uint32_t s2;  // (s, s) as f16x2
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"((uint16_t)(sbyte | (sbyte << 8))));
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint32_t word = k < 4 ? codes.x : codes.y;
-        const uint16_t byte2 = (uint16_t)((word >> (8 * (k & 3))) & 0xFFu);
-        uint32_t h2, p2;
+// V from NVFP4 to E4M3 (R17).  The E4M3 value of s~ x dec(q) depends only
+// on the block's scale byte and the code's magnitude, so each CTA first
+// builds lut[byte][m] = E4M3(s~(byte) x |dec(m)|), m = 0..7: the product of an
+// E4M3 and an E2M1 value has at most five significant bits and lies within
+// [2^-10, 2688], so it is exact in fp16 and its E4M3 rounding (nearest even,
+// saturating) is that of the exact product.  A block's sixteen bytes are then
+// byte permutations of its table row selected by the code nibbles, with the
+// code's sign bit as the E4M3 sign.
+__device__ __forceinline__ void build_v_lut(uint8_t* lut, int tid, int nthreads) {
+    for (int i = tid; i < 128 * 4; i += nthreads) {
+        const uint32_t byte = (uint32_t)(i >> 2), pair = (uint32_t)(i & 3);
+        uint32_t s2, p2;
         uint16_t e2;
-        asm("{\n\t.reg .b8 cb;\n\tcvt.u8.u16 cb, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, cb;\n\t}" : "=r"(h2) : "h"(byte2));
-        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p2) : "r"(h2), "r"(s2));
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"((uint16_t)(byte | (byte << 8))));
+        // |dec(m)| for m = 2 pair, 2 pair + 1 as f16x2 (low half first): {0, .5}, {1, 1.5}, {2, 3}, {4, 6}
+        const uint32_t d2 = pair == 0 ? 0x38000000u : pair == 1 ? 0x3E003C00u : pair == 2 ? 0x42004000u : 0x46004400u;
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(p2) : "r"(d2), "r"(s2));
         asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e2) : "r"(p2));
-        // element 2k (low nibble -> low half -> low byte), then element 2k + 1
-        w[k >> 1] |= (uint32_t)e2 << (16 * (k & 1));
+        *reinterpret_cast<uint16_t*>(lut + byte * 8 + pair * 2) = e2;
+    }
+}
+
+// The sixteen E4M3 bytes of one V block (codes: element e in nibble e;
+// row: its scale byte's table row), byte e of the block in byte e % 4 of w[e / 4].
+__device__ __forceinline__ void v_block_e4m3(uint2 codes, uint2 row, uint32_t (&w)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t c = ((k < 2 ? codes.x : codes.y) >> (16 * (k & 1))) & 0xFFFFu;
+        const uint32_t mag = __byte_perm(row.x, row.y, c & 0x7777u);          // magnitude bytes
+        const uint32_t sgn = __byte_perm(0x8000u, 0u, (c >> 3) & 0x1111u);    // 0x00 or 0x80 per byte
+        w[k] = mag | sgn;
     }
 }
 
@@ -140,6 +153,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
     uint8_t* ptile = sm + Ly::OFF_P;
     uint8_t* ksf = sm + Ly::OFF_KSF;
     uint8_t* qsf = sm + Ly::OFF_QSF;
+    uint8_t* vlut = sm + Ly::OFF_LUT;
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly::OFF_CTRL);  // [S]: a stage's pages landed
     uint64_t* empty = full + 3;                                       // [S]: a stage was read
     uint64_t* qk_done = empty + 3;                                    // the tile's QK MMAs are done
@@ -156,9 +170,6 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int G = g.Hq / g.Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = attn_len(g, b);
-    const int t0 = split * g.split_tokens, t1 = min(L, t0 + g.split_tokens);
-    const int ntiles = t1 > t0 ? (t1 - t0 + kAttnTile - 1) / kAttnTile : 0;
     float* part = g.part + (((size_t)b * g.Hkv + h) * g.splits + split) * (size_t)G * (D + 2);
 
     if (threadIdx.x == 0) {
@@ -177,6 +188,18 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
         m_run[threadIdx.x] = -INFINITY;
         l_run[threadIdx.x] = 0.0f;
     }
+    build_v_lut(vlut, threadIdx.x, kAttnThreads);
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), Ly::TCOLS);
+        tmem_relinquish();
+    }
+    // Set-up above overlaps the previous kernel (programmatic launch); the
+    // query operand, sequence lengths, block table and cache come after it.
+    pdl_wait_prior_grid();
+    pdl_launch_dependents();
+    const int L = attn_len(g, b);
+    const int t0 = split * g.split_tokens, t1 = min(L, t0 + g.split_tokens);
+    const int ntiles = t1 > t0 ? (t1 - t0 + kAttnTile - 1) / kAttnTile : 0;
     // the group's 2G query rows (zero rows up to 16), P all zero (rows >= G
     // stay zero), the query scales in atoms
     for (int i = threadIdx.x; i < 16 * 8; i += kAttnThreads) {
@@ -193,10 +216,6 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
         const int r = i / SB, blk = i % SB;
         const int row = 2 * (b * g.Hq + h * G) + r;
         qsf[(blk / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + blk % 4] = g.q_sf[sf_offset(row, blk, g.q_atoms_k)];
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), Ly::TCOLS);
-        tmem_relinquish();
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -263,35 +282,67 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
             if (ct == 0 && it < 6) RS_TRACE_MARK(g.trace, 5 * it);  // stage landed
             const uint8_t* st = stg + (size_t)s * Ly::STG;
             if (landed) {
+                // every load of this thread's share first, then the stores
+                constexpr int NKC = (kAttnTile * (CB / 16) + kAttnCompute - 1) / kAttnCompute;  // key code chunks
+                constexpr int NKS = (kAttnTile * NA + kAttnCompute - 1) / kAttnCompute;        // key scale words
+                constexpr int NV = (kAttnTile * SB + kAttnCompute - 1) / kAttnCompute;         // V blocks
+                uint4 kc[NKC];
+                uint32_t ks[NKS];
+                uint2 vc[NV];
+                uint32_t vs[NV];
+#pragma unroll
+                for (int j = 0; j < NKC; ++j) {
+                    const int i = ct + j * kAttnCompute, rr = i / (CB / 16), cc = i % (CB / 16);
+                    kc[j] = make_uint4(0u, 0u, 0u, 0u);
+                    if (i < kAttnTile * (CB / 16) && rr < nt)
+                        kc[j] = *reinterpret_cast<const uint4*>(st + (rr / kPage) * PB + (rr % kPage) * CB + cc * 16);
+                }
+#pragma unroll
+                for (int j = 0; j < NKS; ++j) {
+                    const int i = ct + j * kAttnCompute, rr = i / NA, a = i % NA;
+                    ks[j] = 0u;
+                    if (i < kAttnTile * NA && rr < nt)
+                        ks[j] = *reinterpret_cast<const uint32_t*>(st + (rr / kPage) * PB + kPage * CB +
+                                                                   (rr % kPage) * SB + a * 4);
+                }
+#pragma unroll
+                for (int j = 0; j < NV; ++j) {
+                    const int i = ct + j * kAttnCompute, t = i / SB, bb = i % SB;
+                    vc[j] = make_uint2(0u, 0u);
+                    vs[j] = 0u;
+                    if (i < kAttnTile * SB && t < nt) {
+                        const uint8_t* pg = st + (4 + t / kPage) * PB;
+                        vc[j] = *reinterpret_cast<const uint2*>(pg + (t % kPage) * CB + bb * 8);
+                        vs[j] = pg[kPage * CB + (t % kPage) * SB + bb];
+                    }
+                }
+                uint2 vrow[NV];  // each V block's table row (its scale byte's E4M3 magnitudes)
+#pragma unroll
+                for (int j = 0; j < NV; ++j) vrow[j] = *reinterpret_cast<const uint2*>(vlut + vs[j] * 8);
                 // key codes -> 128-byte-swizzled rows (tokens past the end: zero)
-                for (int i = ct; i < kAttnTile * (CB / 16); i += kAttnCompute) {
-                    const int rr = i / (CB / 16), cc = i % (CB / 16);
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (rr < nt)
-                        v = *reinterpret_cast<const uint4*>(st + (rr / kPage) * PB + (rr % kPage) * CB + cc * 16);
-                    *reinterpret_cast<uint4*>(ktile + sw128_offset((uint32_t)rr, (uint32_t)cc * 16u)) = v;
+#pragma unroll
+                for (int j = 0; j < NKC; ++j) {
+                    const int i = ct + j * kAttnCompute, rr = i / (CB / 16), cc = i % (CB / 16);
+                    if (i < kAttnTile * (CB / 16))
+                        *reinterpret_cast<uint4*>(ktile + sw128_offset((uint32_t)rr, (uint32_t)cc * 16u)) = kc[j];
                 }
                 // key scales -> atoms (the four blocks of an atom are one word per token)
-                for (int i = ct; i < kAttnTile * NA; i += kAttnCompute) {
-                    const int rr = i / NA, a = i % NA;
-                    uint32_t w = 0u;
-                    if (rr < nt)
-                        w = *reinterpret_cast<const uint32_t*>(st + (rr / kPage) * PB + kPage * CB + (rr % kPage) * SB +
-                                                               a * 4);
-                    *reinterpret_cast<uint32_t*>(ksf + a * 512 + (rr % 32) * 16 + (rr / 32) * 4) = w;
+#pragma unroll
+                for (int j = 0; j < NKS; ++j) {
+                    const int i = ct + j * kAttnCompute, rr = i / NA, a = i % NA;
+                    if (i < kAttnTile * NA)
+                        *reinterpret_cast<uint32_t*>(ksf + a * 512 + (rr % 32) * 16 + (rr / 32) * 4) = ks[j];
                 }
                 // V -> E4M3 (R17): token row t holds its head dimensions, 128 per tile
-                for (int i = ct; i < kAttnTile * SB; i += kAttnCompute) {
-                    const int t = i / SB, bb = i % SB;
-                    uint32_t w[4] = {0u, 0u, 0u, 0u};
-                    if (t < nt) {
-                        const uint8_t* pg = st + (4 + t / kPage) * PB;
-                        v_block_e4m3(*reinterpret_cast<const uint2*>(pg + (t % kPage) * CB + bb * 8),
-                                     pg[kPage * CB + (t % kPage) * SB + bb], w);
-                    }
-                    *reinterpret_cast<uint4*>(vt + (bb / 8) * 16384 +
-                                              sw128_offset((uint32_t)t, (uint32_t)(bb % 8) * 16u)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+                for (int j = 0; j < NV; ++j) {
+                    const int i = ct + j * kAttnCompute, t = i / SB, bb = i % SB;
+                    uint32_t w[4];
+                    v_block_e4m3(vc[j], vrow[j], w);
+                    if (i < kAttnTile * SB)
+                        *reinterpret_cast<uint4*>(vt + (bb / 8) * 16384 +
+                                                  sw128_offset((uint32_t)t, (uint32_t)(bb % 8) * 16u)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             fence_proxy_async_smem();
@@ -331,42 +382,34 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
                 float sc[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    sc[q] = -INFINITY;
-                    if (q < G) {
-                        if (r < nt) sc[q] = __fmul_rn(__fadd_rn(z[2 * q], z[2 * q + 1]), c);
-                        const float mx = warp_max_f32(sc[q]);
-                        if (lane == 0) red[(warp - 4) * 8 + q] = mx;
-                    }
+                    sc[q] = (q < G && r < nt) ? __fmul_rn(__fadd_rn(z[2 * q], z[2 * q + 1]), c) : -INFINITY;
+                    const float mx = warp_max_f32(sc[q]);
+                    if (lane == 0) red[(warp - 4) * 8 + q] = mx;
                 }
                 named_bar_sync(2, 128);
                 float m_new[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    m_new[q] = -INFINITY;
-                    a_t[q] = 0.0f;
-                    if (q < G) {
-                        const float tm = fmaxf(fmaxf(red[q], red[8 + q]), fmaxf(red[16 + q], red[24 + q]));
-                        const float mo = m_run[q];
-                        m_new[q] = fmaxf(mo, tm);
-                        a_t[q] = mo == -INFINITY ? 0.0f : __expf(mo - m_new[q]);
-                        uint32_t pb = 0u;
-                        if (r < nt) pb = e4m3x2_encode_hw(0.0f, __expf(sc[q] - m_new[q])) & 0xFFu;
-                        ptile[sw128_offset((uint32_t)q, (uint32_t)r)] = (uint8_t)pb;
-                        // E4M3 weights in [0, 1] are multiples of 2^-9: their sum is exact in integers
-                        const int units = __float2int_rn(__fmul_rn(e4m3_decode_hw(pb), 512.0f));
-                        const int sum = __reduce_add_sync(0xFFFFFFFFu, units);
-                        if (lane == 0) red2[(warp - 4) * 8 + q] = sum;
-                    }
+                    const float tm = fmaxf(fmaxf(red[q], red[8 + q]), fmaxf(red[16 + q], red[24 + q]));
+                    const float mo = m_run[q];
+                    m_new[q] = fmaxf(mo, tm);
+                    a_t[q] = mo == -INFINITY ? 0.0f : __expf(mo - m_new[q]);
+                    // exp(-inf - m) = 0 for padded tokens; heads beyond G have m = -inf: weight 0
+                    const float e = m_new[q] == -INFINITY ? 0.0f : __expf(sc[q] - m_new[q]);
+                    const uint32_t pb = e4m3x2_encode_hw(0.0f, e) & 0xFFu;
+                    if (q < G) ptile[sw128_offset((uint32_t)q, (uint32_t)r)] = (uint8_t)pb;
+                    // E4M3 weights in [0, 1] are multiples of 2^-9: their sum is exact in integers
+                    const int units = __float2int_rn(__fmul_rn(e4m3_decode_hw(pb), 512.0f));
+                    const int sum = __reduce_add_sync(0xFFFFFFFFu, units);
+                    if (lane == 0) red2[(warp - 4) * 8 + q] = sum;
                 }
                 named_bar_sync(2, 128);
                 if (r == 0)
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        if (q < G) {
-                            const int tile_sum = (red2[q] + red2[8 + q]) + (red2[16 + q] + red2[24 + q]);
-                            l_run[q] = l_run[q] * a_t[q] + __fmul_rn((float)tile_sum, 0x1p-9f);
-                            m_run[q] = m_new[q];
-                        }
+                        const int tile_sum = (red2[q] + red2[8 + q]) + (red2[16 + q] + red2[24 + q]);
+                        l_run[q] = l_run[q] * a_t[q] + __fmul_rn((float)tile_sum, 0x1p-9f);
+                        m_run[q] = m_new[q];
                     }
                 fence_proxy_async_smem();  // P for the tensor pipe
             }
@@ -440,6 +483,8 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
 
 // O = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s (R19); empty sequences give 0.
 __global__ void resattn_combine_kernel(const AttnArgs g, void* out, int out_f32) {
+    pdl_wait_prior_grid();  // the splits' partial results
+    pdl_launch_dependents();
     const int Hq = g.Hq, Hkv = g.Hkv, D = g.D, splits = g.splits, split_tokens = g.split_tokens;
     const float* part = g.part;
     const int G = Hq / Hkv;
@@ -492,17 +537,33 @@ static cudaError_t launch_split(const AttnArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
     }
-    dim3 grid((unsigned)a.splits, (unsigned)a.Hkv, (unsigned)a.B);
-    resattn_split_kernel<D><<<grid, kAttnThreads, AttnLayout<D>::SMEM, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)a.splits, (unsigned)a.Hkv, (unsigned)a.B);
+    cfg.blockDim = dim3(kAttnThreads, 1, 1);
+    cfg.dynamicSmemBytes = AttnLayout<D>::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, resattn_split_kernel<D>, a);
 }
 
 cudaError_t launch_resattn(int D, const AttnArgs& a, void* out, int out_f32, cudaStream_t stream) {
     cudaError_t e = D == 128 ? launch_split<128>(a, stream) : D == 256 ? launch_split<256>(a, stream)
                                                                       : cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
-    resattn_combine_kernel<<<dim3((unsigned)a.Hq, (unsigned)a.B), D, 0, stream>>>(a, out, out_f32);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)a.Hq, (unsigned)a.B, 1);
+    cfg.blockDim = dim3((unsigned)D, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, resattn_combine_kernel, a, out, out_f32);
 }
 
 }  // namespace rs
