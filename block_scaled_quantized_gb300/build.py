@@ -19,8 +19,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "librs.so")
-SOURCES = ["rs_api.cu", "rs_quant.cu", "rs_gemm.cu", "rs_noalloc.cu", "rs_kext.cu", "rs_attn.cu", "rs_gemm_pair.cu"]
-HEADERS = ["rs_device.cuh", "rs_internal.h", "rs_quant_core.cuh"]
+SOURCES = ["rs_api.cu", "rs_quant.cu", "rs_gemm.cu", "rs_noalloc.cu", "rs_kext.cu", "rs_attn.cu", "rs_gemm_pair.cu",
+           "rs_tactics.cu"]
+HEADERS = ["rs_device.cuh", "rs_internal.h", "rs_quant_core.cuh", "rs_tactics_gb300.inc"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -221,12 +221,27 @@ int rs_plan_linear(rs_format fmt, int compensated, int M, int N, int K, int num_
         return -(int)RS_ERR_INVALID_ARG;
     if (!k_ok(K) || (int64_t)M * 2 > (int64_t)0x7FFFFFFF) return -(int)RS_ERR_SHAPE;
     const GemmPlan p = make_gemm_plan(fmt, compensated != 0, M, N, K, num_sms, x_in_call != 0);
-    const int v[] = {p.bn,     p.n_tiles, p.b_tiles, p.chunks, p.splits,    p.grid_x,
-                     p.stages, p.fused,   p.slots,   p.nacc,   p.tmem_cols, (int)p.smem_bytes};
+    const int v[] = {p.bn,     p.n_tiles, p.b_tiles, p.chunks,    p.splits,          p.grid_x, p.stages,
+                     p.fused,  p.slots,   p.nacc,    p.tmem_cols, (int)p.smem_bytes, p.tuned};
     const int n = n_out < (int)(sizeof(v) / sizeof(v[0])) ? n_out : (int)(sizeof(v) / sizeof(v[0]));
     for (int i = 0; i < n; ++i) out[i] = v[i];
     return n;
 }
+
+rs_status rs_set_tactic(rs_format fmt, int compensated, int M, int N, int K, int num_sms, int splits, int fused,
+                        int bn) {
+    if (!fmt_ok(fmt) || M < 1 || N < 1 || num_sms < 1) return RS_ERR_INVALID_ARG;
+    if (!k_ok(K)) return RS_ERR_SHAPE;
+    return set_tactic(fmt, compensated != 0, M, N, K, num_sms, Tactic{splits, fused, bn}) ? RS_OK
+                                                                                         : RS_ERR_INVALID_ARG;
+}
+
+rs_status rs_reset_tactics(int builtin) {
+    reset_tactics(builtin != 0);
+    return RS_OK;
+}
+
+int rs_tactic_count(void) { return tactic_count(); }
 
 rs_status rs_compute_tensor_scale(const void* x_bf16, int64_t n, float* alpha_out, rs_stream_t stream) {
     if (n < 0 || !alpha_out || (n > 0 && !x_bf16)) return RS_ERR_INVALID_ARG;

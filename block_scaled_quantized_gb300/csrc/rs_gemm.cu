@@ -180,10 +180,14 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     const int pre = nu < S ? nu : S;
     const int nacc = g.nacc;
     const int outs = g.fold ? BN / 2 : BN;
-    // split-K: outputs each owner sums, owners, and how the partials travel
+    // split-K: outputs each owner sums, owners, and how the partials travel.
+    // Narrow tiles exchange only the outputs of real tokens (rounded up to
+    // four) when the operand is one activation tile: the padding columns of
+    // a wide MMA are never sent.
     const bool xasync = g.splits > 1 && split_async(outs);
-    const int per_cta = split_slice(outs, g.splits);
-    const int owners = xasync ? (outs + per_cta - 1) / per_cta : g.splits;
+    const int xouts = (xasync && g.b_tiles == 1) ? min(outs, (g.M + 3) / 4 * 4) : outs;
+    const int per_cta = split_slice(xouts, g.splits);
+    const int owners = xasync ? (xouts + per_cta - 1) / per_cta : g.splits;
     const bool owner = g.splits > 1 && split < owners;
     const uint32_t slice_bytes = (uint32_t)per_cta * 128u * 4u;
     // Wide tiles without split-K: eight epilogue warps (warps 8-11 and 0-3,
@@ -698,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                                       (my_rank * 128u + (uint32_t)row) * (uint32_t)per_cta * 4u;
                 const uint32_t rbar = smem_u32(&red_full[b]);
                 auto emit4 = [&](int o0, float z0, float z1, float z2, float z3) {
-                    if (!send_ok) return;
+                    if (!send_ok || o0 >= owners * per_cta) return;
                     const int o = o0 / per_cta;
                     st_async_v4(map_dsmem(rbuf + (uint32_t)(o0 - o * per_cta) * 4u, (uint32_t)o),
                                 make_uint4(__float_as_uint(z0), __float_as_uint(z1), __float_as_uint(z2),
@@ -838,7 +842,8 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 } else if (g.splits > 1) {
                     for (int jj = 0; jj < outs; ++jj) emit(jj, 0.0f);
                 }
-                // every owner expects a full slice: pad the last one
+                // every owner expects a full slice: pad the last one (emit4 drops
+                // the outputs past the owners' slices, so each is sent once)
                 if (xasync)
                     for (int o0 = outs; o0 < owners * per_cta; o0 += 4) emit4(o0, 0.0f, 0.0f, 0.0f, 0.0f);
                 // accumulator b drained: the MMA warp may start its next tile
@@ -884,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                         // receive layout [rank][channel][per_cta], four outputs at a time
                         for (int j4 = 0; live && j4 < per_cta; j4 += 4) {
                             const int jo = split * per_cta + j4;
-                            if (jo >= outs) break;
+                            if (jo >= xouts) break;
                             float4 pv[kMaxSplits];
 #pragma unroll
                             for (int r = 0; r < kMaxSplits; ++r)
@@ -1017,7 +1022,10 @@ static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots, size
 }
 
 // Complete plan for a given split count s; stages == 0 when it does not fit.
-static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms, int s, bool allow_fused) {
+// bn_min: the MMA width, at least the one the activation rows need (a measured
+// tactic may ask for a wider one; the extra operand rows are zero).
+static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms, int s, bool allow_fused,
+                                int bn_min = 16) {
     GemmPlan p{};
     p.fmt = fmt;
     p.fold = fold ? 1 : 0;
@@ -1026,6 +1034,7 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
     p.K = K;
     p.Rb = fold ? 2 * M : M;
     p.bn = p.Rb <= 16 ? 16 : p.Rb <= 32 ? 32 : p.Rb <= 64 ? 64 : p.Rb <= 128 ? 128 : 256;
+    p.bn = std::max(p.bn, std::min(bn_min, 256));
     p.n_tiles = (N + 127) / 128;
     p.b_tiles = (p.Rb + p.bn - 1) / p.bn;
     p.chunks = (K + 255) / 256;
@@ -1100,6 +1109,9 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
     int alloc = 32;
     while (alloc < cols) alloc *= 2;
     p.tmem_cols = alloc;
+    // more than half of the tensor memory: never two such CTAs on one SM
+    // (the second one's allocation would wait for the first to finish)
+    if (alloc > 256 && p.smem_bytes <= kSmemLimit / 2) p.smem_bytes = kSmemLimit / 2 + 1024;
     return p;
 }
 
@@ -1149,8 +1161,20 @@ static GemmPlan plan_impl(int fmt, bool fold, int M, int N, int K, int num_sms, 
 // for the single-CTA kernel's larger stages).
 static int g_pair_gemm = 0;
 
+GemmPlan make_gemm_plan_analytic(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused) {
+    return plan_impl(fmt, fold, M, N, K, num_sms, allow_fused);
+}
+
 GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused) {
     GemmPlan p = plan_impl(fmt, fold, M, N, K, num_sms, allow_fused);
+    Tactic t;
+    if (num_sms > 0 && find_tactic(fmt, fold, M, N, K, num_sms, &t) && t.splits <= (K + 255) / 256) {
+        const GemmPlan q = plan_for_splits(fmt, fold, M, N, K, num_sms, t.splits, allow_fused && t.fused, t.bn);
+        if (q.stages > 0) {
+            p = q;
+            p.tuned = 1;
+        }
+    }
     // Operands of at least two 256-row activation tiles with an even number
     // of channel tiles can run on the pair kernel, whose two SMs share one
     // 256 x 256 MMA and each stage half the activation bytes.

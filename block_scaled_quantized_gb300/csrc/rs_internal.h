@@ -51,13 +51,37 @@ struct GemmPlan {
     int tmem_cols;   // tensor-memory columns to allocate
     size_t smem_bytes;
     int pair;        // large operands: the paired-CTA kernel (rs_gemm_pair.cu) runs the call
+    int tuned;       // 1: a measured tactic chose splits, fused and bn
 };
 
 constexpr int kMaxSplits = 8;   // portable thread-block cluster size
 
 // Plan for a given SM count.  allow_fused: the caller passes bf16 input, so
-// small-M plans may quantize inside the GEMM.
+// small-M plans may quantize inside the GEMM.  A measured tactic for the
+// shape (below) takes precedence over the analytic choice when its plan fits.
 GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused);
+// The analytic plan alone (what make_gemm_plan gives without a tactic).
+GemmPlan make_gemm_plan_analytic(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused);
+
+// Layout autotuning (ResServe Sec. 5.1, Fig. 3): a launch tactic measured for
+// one linear shape on a GPU with num_sms SMs -- the K-split count, whether a
+// bf16 input is quantized inside the GEMM, and the MMA width bn (at least
+// the width the activation rows need; wider pads the operand with zero rows).
+struct Tactic {
+    int splits;  // 1..kMaxSplits
+    int fused;   // 0 or 1
+    int bn;      // 16, 32, 64, 128 or 256
+};
+// Install (replace) the tactic of (fmt, fold, M, N, K, num_sms); false on an
+// out-of-range field.  Thread-safe.
+bool set_tactic(int fmt, bool fold, int M, int N, int K, int num_sms, const Tactic& t);
+// Remove every installed tactic, built-in ones included (builtin = false), or
+// restore the built-in table (builtin = true).
+void reset_tactics(bool builtin);
+int tactic_count();
+// The tactic for a call of M rows: the entry of the same format, fold, N, K
+// and SM count with the smallest tuned row count >= M.
+bool find_tactic(int fmt, bool fold, int M, int N, int K, int num_sms, Tactic* t);
 
 // Workspace of a linear call given a bf16 input: the quantized activation
 // operand when the plan quantizes in a separate kernel (sized for the worst

@@ -32,7 +32,8 @@ EXPORTS = ["rs_status_string", "rs_version", "rs_operand_bytes", "rs_operand_sf_
            "rs_channel_mean_abs", "rs_kext_act_bytes", "rs_kext_weight_bytes", "rs_kext_workspace_bytes",
            "rs_quantize_weight_kext", "rs_quantize_kext", "rs_linear_kext", "rs_plan_linear", "rs_debug_wait_probe",
            "rs_get_device_error_async", "rs_debug_linear_dump", "rs_fold_pairs", "rs_resattn_workspace_bytes",
-           "rs_resattn_split_tokens", "rs_resattn_decode", "rs_debug_pair_gemm"]
+           "rs_resattn_split_tokens", "rs_resattn_decode", "rs_debug_pair_gemm", "rs_set_tactic",
+           "rs_reset_tactics", "rs_tactic_count"]
 
 
 class RsError(RuntimeError):
@@ -79,6 +80,9 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_resattn_workspace_bytes": ([I, I, I, I, I], SZ),
         "rs_resattn_split_tokens": ([I, I, I, I], I),
         "rs_debug_pair_gemm": ([I], None),
+        "rs_set_tactic": ([I, I, I, I, I, I, I, I, I], I),
+        "rs_reset_tactics": ([I], I),
+        "rs_tactic_count": ([], I),
         "rs_resattn_decode": ([I, I, I, I, I, I, P, P, P, P, P, P, P, I, P, SZ, P], I),
         "rs_debug_linear_dump": ([I, I, I, I, I, P, P, P, P, P, I, P, SZ, P, SZ, P, P], I),
     }
@@ -146,7 +150,7 @@ def rs_debug_wait_probe(limit_ns: int, stream=None):
 
 
 PLAN_FIELDS = ("bn", "n_tiles", "b_tiles", "chunks", "splits", "grid_x", "stages", "fused", "slots", "nacc",
-               "tmem_cols", "smem_bytes")
+               "tmem_cols", "smem_bytes", "tuned")
 
 
 def rs_plan_linear(fmt: int, compensated: bool, M: int, N: int, K: int, num_sms: int, x_in_call: bool = True) -> dict:
@@ -245,6 +249,21 @@ def rs_resattn_decode(q: torch.Tensor, alpha_q: torch.Tensor, k_cache: torch.Ten
 def rs_debug_pair_gemm(enable: bool):
     """Route eligible large calls to the paired-CTA GEMM (see rs.h)."""
     lib().rs_debug_pair_gemm(int(bool(enable)))
+
+
+def rs_set_tactic(fmt: int, compensated: bool, M: int, N: int, K: int, num_sms: int, splits: int, fused: bool,
+                  bn: int):
+    """Install a measured launch tactic for one shape (see rs.h)."""
+    _check("rs_set_tactic", lib().rs_set_tactic(fmt, int(bool(compensated)), M, N, K, num_sms, splits,
+                                                int(bool(fused)), bn))
+
+
+def rs_reset_tactics(builtin: bool = True):
+    _check("rs_reset_tactics", lib().rs_reset_tactics(int(bool(builtin))))
+
+
+def rs_tactic_count() -> int:
+    return lib().rs_tactic_count()
 
 
 def rs_fold_pairs(M: int, N: int, z: torch.Tensor, y: torch.Tensor, stream=None):

@@ -147,10 +147,37 @@ RS_API size_t rs_workspace_bytes(rs_format fmt, int M, int N, int K, int compens
  * (ceil(N/128)), b_tiles, chunks (ceil(K/256)), splits (K splits = cluster
  * size), grid_x (persistent CTAs per split), stages (weight ring depth),
  * fused (1: quantized inside the GEMM), slots, nacc (accumulator buffers),
- * tmem_cols, smem_bytes (dynamic shared memory per CTA).  Returns the number
+ * tmem_cols, smem_bytes (dynamic shared memory per CTA), tuned (1: a
+ * measured tactic below chose splits, fused and bn).  Returns the number
  * written, or minus an rs_status code on bad arguments. */
 RS_API int rs_plan_linear(rs_format fmt, int compensated, int M, int N, int K, int num_sms, int x_in_call,
                           int *out, int n_out);
+
+/* ---- layout autotuning (Sec. 5.1 "Layout Autotuning", Fig. 3) ------------ */
+
+/* The paper picks a kernel layout per (M, N, K) by measurement.  Here a
+ * tactic fixes, for one (fmt, compensated, M, N, K) on a GPU with num_sms
+ * SMs: the K-split count (1..8, the cluster size), whether a bf16 input may
+ * be quantized inside the GEMM (fused, 0/1; only plans whose activation
+ * tile is at most 32 rows can), and the MMA width bn (16, 32, 64, 128 or
+ * 256; a width below what the activation rows need is raised to it, a wider
+ * one pads the operand with zero rows).  A linear call of M rows takes the
+ * tactic of the same fmt, compensated, N, K and SM count with the smallest
+ * tuned M' >= M; its plan replaces the analytic one when it fits the SM's
+ * shared and tensor memory and splits <= ceil(K/256), else the analytic plan
+ * stays.  Results agree with any other plan within the output tolerance
+ * (the K-split order of the fp32 sums differs).  librs ships a table
+ * measured on GB300 (152 SMs) by block_scaled_quantized_gb300/tune.py.
+ * Host only, thread-safe; a change affects calls planned after it (not CUDA
+ * graphs already captured).  RS_ERR_INVALID_ARG for a field out of range,
+ * RS_ERR_SHAPE unless K % 32 == 0. */
+RS_API rs_status rs_set_tactic(rs_format fmt, int compensated, int M, int N, int K, int num_sms, int splits,
+                               int fused, int bn);
+/* builtin != 0: restore the shipped table (dropping rs_set_tactic entries);
+ * builtin == 0: remove every tactic, so that every call uses the analytic plan. */
+RS_API rs_status rs_reset_tactics(int builtin);
+/* Number of tactics installed (shipped ones included). */
+RS_API int rs_tactic_count(void);
 
 /* ---- tensor scale (App. B.2 Eq. 8) -------------------------------------- */
 
