@@ -221,8 +221,9 @@ int rs_plan_linear(rs_format fmt, int compensated, int M, int N, int K, int num_
         return -(int)RS_ERR_INVALID_ARG;
     if (!k_ok(K) || (int64_t)M * 2 > (int64_t)0x7FFFFFFF) return -(int)RS_ERR_SHAPE;
     const GemmPlan p = make_gemm_plan(fmt, compensated != 0, M, N, K, num_sms, x_in_call != 0);
-    const int v[] = {p.bn,     p.n_tiles, p.b_tiles, p.chunks,    p.splits,          p.grid_x, p.stages,
-                     p.fused,  p.slots,   p.nacc,    p.tmem_cols, (int)p.smem_bytes, p.tuned};
+    const int fused = p.fused ? (p.qpair ? 2 : 1) : 0;
+    const int v[] = {p.bn,  p.n_tiles, p.b_tiles, p.chunks,    p.splits,          p.grid_x, p.stages,
+                     fused, p.slots,   p.nacc,    p.tmem_cols, (int)p.smem_bytes, p.tuned};
     const int n = n_out < (int)(sizeof(v) / sizeof(v[0])) ? n_out : (int)(sizeof(v) / sizeof(v[0]));
     for (int i = 0; i < n; ++i) out[i] = v[i];
     return n;
@@ -520,7 +521,7 @@ rs_status rs_debug_linear_dump(rs_format fmt, int compensated, int M, int N, int
     if (!dev->supported) return RS_ERR_UNSUPPORTED;
     const GemmPlan p = make_gemm_plan(fmt, compensated != 0, M, N, K, dev->num_sms, /*allow_fused=*/true);
     const size_t stage = plan_b_stage_bytes(p);
-    const int v[7] = {p.fused, p.bn, p.grid_x, p.splits, p.slots, (int)stage, p.chunks};
+    const int v[7] = {p.fused ? (p.qpair ? 2 : 1) : 0, p.bn, p.grid_x, p.splits, p.slots, (int)stage, p.chunks};
     for (int i = 0; i < 7; ++i) layout[i] = v[i];
     if (!dump) return RS_OK;  // layout query only
     if (!p.fused) return RS_ERR_UNSUPPORTED;

@@ -246,6 +246,11 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
+// The same with an arrival count.
+__device__ __forceinline__ void mbar_arrive_remote_cnt(uint32_t bar_cluster, uint32_t n) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cluster), "r"(n)
+                 : "memory");
+}
 
 // Bounded wait for the phase with the given parity to complete.  Gives up
 // after `limit_ns` of wall-clock time or as soon as *abort becomes non-zero;
@@ -320,6 +325,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // (TMA, tcgen05.cp, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// The same for every state space (stores into other CTAs' shared memory).
+__device__ __forceinline__ void fence_proxy_async_all() {
+    asm volatile("fence.proxy.async;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05 --
@@ -496,6 +505,17 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 
 __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_u8(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u8 [%0], %1;" ::"r"(addr), "h"((unsigned short)v) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_v2(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
 }
 
 // Asynchronous 16-byte store into another CTA's shared memory (cluster

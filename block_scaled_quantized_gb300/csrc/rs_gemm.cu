@@ -123,6 +123,7 @@ struct GemmArgs {
     int recv_bytes;         // split-K: one receive buffer (0 without split)
     int tmem_cols;
     int dyn_alpha;          // fused NVFP4: the tensor scale of X is computed here (alpha_x unused)
+    int qpair;              // fused: CTA pairs (x, x ^ 1) share the quantization of their K slice
 };
 
 template <int FMT, int BN, bool FUSED>
@@ -171,6 +172,12 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     // activation tile.  The K slice (split) of a CTA is the same for all of
     // its tiles, so fused plans quantize it once.
     const int split = blockIdx.z;
+    // Cluster ranks: (x % 2) + 2 z with CTA pairs sharing a K slice, else z.
+    const bool qpair = FUSED && g.qpair != 0;
+    const uint32_t px = qpair ? (blockIdx.x & 1u) : 0u;
+    auto krank = [&](uint32_t p) -> uint32_t { return qpair ? px + 2u * p : p; };  // split p, our pair slot
+    const int nranks = qpair ? 2 * g.splits : g.splits;
+    const uint32_t my_crank = krank((uint32_t)split);
     const int total_tiles = g.n_tiles * g.b_tiles;
     const int ntl = (total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
     const int per = g.chunks / g.splits, rem = g.chunks % g.splits;
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
         // every scale block of chunk i (all token rows) arrives once
         if (FUSED)
             for (int i = 0; i < nck; ++i) mbar_init(smem_u32(&cbar[i]), (uint32_t)(g.M * (256 / block_elems(FMT))));
-        mbar_init(smem_u32(abar), (uint32_t)g.splits);  // one slice amax per CTA of the cluster
+        mbar_init(smem_u32(abar), (uint32_t)nranks);  // one slice amax per CTA of the cluster
         *amax_cta = 0u;
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accum_full[b]), 1);
@@ -256,6 +263,16 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
         tmem_alloc(smem_u32(tmem_slot), (uint32_t)g.tmem_cols);
         tmem_relinquish();
     }
+    if (FUSED) {
+        // The quantizer leaves no byte of the slice unwritten except the padding
+        // rows and the scale bytes of a ragged K tail: zeros for those, written
+        // before any quantizer (ours or, with CTA pairs, the partner's after the
+        // cluster barrier below) stores codes, and visible to the tensor pipe.
+        const uint32_t bbytes = (uint32_t)nck * BSTAGE;
+        for (uint32_t off = threadIdx.x * 16u; off < bbytes; off += (uint32_t)kThreads * 16u)
+            *reinterpret_cast<uint4*>(bregion + off) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -270,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     const uint32_t tm_sf = tmem + (uint32_t)(nacc * BN);
     // split-K partners copy into our receive buffers and signal red_full:
     // every barrier of the cluster must be initialised before that
-    if (g.splits > 1) cluster_sync_all();
+    if (g.splits > 1 || qpair) cluster_sync_all();
 
     // Dependents may start their prologue now; they wait for our completion
     // before they touch anything we read or write.
@@ -382,7 +399,12 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 // fused plans: chunk i of the activation slice is quantized
                 // (the quantizer finishes chunks in order, so the first MMAs
                 // overlap the quantization of the later chunks)
-                if (FUSED && j == 0) landed = landed && mbar_wait_bounded(smem_u32(&cbar[i]), 0, abort_flag, g.err);
+                if (FUSED && j == 0) {
+                    // (with CTA pairs, the partner's quantizer arrives on this
+                    // barrier from its CTA: a cluster-scope acquire)
+                    landed = landed && mbar_wait_bounded(smem_u32(&cbar[i]), 0, abort_flag, g.err, 1000000000ull, qpair);
+                    if (qpair) fence_proxy_async_all();
+                }
                 if (u == 0 && lane == 0) RS_TRACE_MARK(g.trace, 11);
                 ok = __all_sync(0xFFFFFFFFu, landed);
                 if (!ok) break;
@@ -485,17 +507,13 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             // CTA's K slice of every token -> base (row 2j) and residue
             // (row 2j+1) codes in the swizzled B tiles, scales in the B atoms.
             constexpr int E = block_elems(FMT);  // 16 (NVFP4) or 32 (MXFP4)
-            const uint32_t bbytes = (uint32_t)nck * BSTAGE;
             // NVFP4 scale table (s~ and fl(1/s~) of every scale byte): built here
             // from the tensor scale as it reads before the dependency wait (one
             // thread reads it, so that every thread uses the same value), and
             // rebuilt after the wait only if the scale turns out to differ
             const bool spec_tab = FMT == 0 && !g.dyn_alpha;
             if (spec_tab && qtid == 0) *alpha_spec = *g.alpha_x;
-            for (uint32_t off = (uint32_t)qtid * 16u; off < bbytes; off += (uint32_t)kQuantThreads * 16u)
-                *reinterpret_cast<uint4*>(bregion + off) = make_uint4(0u, 0u, 0u, 0u);
-            fence_proxy_async_smem();  // the zeros are in every chunk, whoever signals it
-            named_bar_sync(2, kQuantThreads);
+            if (spec_tab) named_bar_sync(2, kQuantThreads);  // every thread builds from the value read
             auto build_table = [&](float a) {
                 for (int i = qtid; i < 128; i += kQuantThreads) {
                     float st, mul;
@@ -512,17 +530,22 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             const int kbeg = c0 * 256, kend = min(g.K, (c0 + nck) * 256);
             // flat chunk-major mapping: thread qtid takes scale blocks qtid,
             // qtid + T, ... (T = quantizer threads) of the order (chunk, token
-            // row, block), so chunks complete in order.
+            // row, block), so chunks complete in order.  With CTA pairs, this
+            // CTA's chunks are every other one of the slice, from chunk px.
             constexpr int bpc = 256 / E;    // blocks per token row in one chunk
             constexpr int kWords = E / 8;   // 16-byte words of X per block
             constexpr int kBatch = 32 / E;  // blocks per thread per batch
             const int cb = g.M * bpc;       // blocks per chunk
-            const int total = nck * cb;
+            const int my_chunks = qpair ? (nck - (int)px + 1) / 2 : nck;
+            const int total = my_chunks * cb;
+            auto chunk_of = [&](int cl) { return qpair ? 2 * cl + (int)px : cl; };  // local -> slice chunk
             auto block_pos = [&](int f, int& j, int& kk) {
-                const int ci = f / cb, rem = f - ci * cb;
+                const int cl = f / cb, rem = f - cl * cb;
                 j = rem / bpc;
-                kk = ci * 256 + (rem - j * bpc) * E;
+                kk = chunk_of(cl) * 256 + (rem - j * bpc) * E;
             };
+            // the partner's copy of this CTA's shared memory (CTA pairs)
+            const uint32_t peer = qpair ? krank((uint32_t)split) ^ 1u : 0u;
             // raw bf16 words of this thread's blocks in one batch; the first
             // batch is requested before the tensor scale is read, so that both
             // come back in one round trip
@@ -546,23 +569,43 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 // the same value rs_compute_tensor_scale gives.  Each CTA takes the
                 // max |x| of its K slice; the K splits of the cluster cover K and
                 // trade their maxima (DSMEM store + remote arrival on each CTA).
-                uint32_t m = 0;
-                const int g8 = (kend - kbeg) / 8;  // 8-element groups per token row of the slice
-                for (int t = qtid; t < g.M * g8; t += kQuantThreads) {
-                    const int j = t / g8;
-                    const uint4 v = *reinterpret_cast<const uint4*>(g.x + (size_t)j * g.K + kbeg + (t - j * g8) * 8);
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                // |x| bit patterns, two per word (integer order: NaN > Inf > finite):
+                // the words of this thread's first batch are in registers
+                // already (zeros for blocks past the slice); later batches'
+                // blocks are read here
+                uint32_t m2 = 0u;
+                if (fw0 < total)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+                    for (int r = 0; r < kBatch; ++r)
+#pragma unroll
+                        for (int q = 0; q < kWords; ++q) {
+                            m2 = __vmaxu2(m2, raw[r][q].x & 0x7FFF7FFFu);
+                            m2 = __vmaxu2(m2, raw[r][q].y & 0x7FFF7FFFu);
+                            m2 = __vmaxu2(m2, raw[r][q].z & 0x7FFF7FFFu);
+                            m2 = __vmaxu2(m2, raw[r][q].w & 0x7FFF7FFFu);
+                        }
+                for (int f = kBatch * kQuantThreads + qtid; f < total; f += kQuantThreads) {
+                    int j, kk;
+                    block_pos(f, j, kk);
+                    if (kbeg + kk >= kend) continue;
+#pragma unroll
+                    for (int q = 0; q < kWords; ++q) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(g.x + (size_t)j * g.K + kbeg + kk + 8 * q);
+                        m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+                        m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+                        m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+                        m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+                    }
                 }
+                uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
                 m = __reduce_max_sync(0xFFFFFFFFu, m);
                 if (lane == 0) atomicMax(amax_cta, m);
                 named_bar_sync(2, kQuantThreads);
                 if (qtid == 0) {
                     const uint32_t cm = *reinterpret_cast<volatile uint32_t*>(amax_cta);
-                    if (g.splits > 1) {
-                        for (int p = 0; p < g.splits; ++p) {
-                            st_dsmem_u32(map_dsmem(smem_u32(&amax_slot[split]), (uint32_t)p), cm);
+                    if (nranks > 1) {
+                        for (int p = 0; p < nranks; ++p) {
+                            st_dsmem_u32(map_dsmem(smem_u32(&amax_slot[my_crank]), (uint32_t)p), cm);
                             mbar_arrive_remote(map_dsmem(smem_u32(abar), (uint32_t)p));
                         }
                     } else {
@@ -572,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 }
                 uint32_t gm = 0;
                 if (mbar_wait_bounded(smem_u32(abar), 0, abort_flag, g.err, 1000000000ull, true))
-                    for (int r = 0; r < g.splits; ++r)
+                    for (int r = 0; r < nranks; ++r)
                         gm = max(gm, reinterpret_cast<volatile uint32_t*>(amax_slot)[r]);
                 const uint32_t bits = gm << 16;
                 if (bits >= 0x7F800000u) {  // Inf or NaN in X, as rs_compute_tensor_scale reports it
@@ -606,14 +649,19 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 const uint32_t kb = (uint32_t)(kk % 256) / (uint32_t)E;  // block within the chunk
                 uint8_t* slot = bregion + (size_t)ci * BSTAGE;
                 const uint32_t b = kb * (uint32_t)(E / 2);                // byte within the 128-byte row
-                if constexpr (E == 16) {
-                    *reinterpret_cast<uint2*>(slot + sw128_offset(rowb, b)) = make_uint2(codes[0], codes[1]);
-                } else {
-                    *reinterpret_cast<uint4*>(slot + sw128_offset(rowb, b)) =
-                        make_uint4(codes[0], codes[E / 8 - 3], codes[E / 8 - 2], codes[E / 8 - 1]);
-                }
+                uint8_t* cp = slot + sw128_offset(rowb, b);
                 // scale byte: atom kb / 4, byte (row % 32) * 16 + (row / 32 % 4) * 4 + kb % 4
-                slot[B_BYTES + (kb / 4) * 512 + (rowb % 32) * 16 + (rowb / 32) * 4 + kb % 4] = (uint8_t)sfbyte;
+                uint8_t* sp = slot + B_BYTES + (kb / 4) * 512 + (rowb % 32) * 16 + (rowb / 32) * 4 + kb % 4;
+                if constexpr (E == 16) {
+                    *reinterpret_cast<uint2*>(cp) = make_uint2(codes[0], codes[1]);
+                    if (qpair) st_dsmem_v2(map_dsmem(smem_u32(cp), peer), codes[0], codes[1]);
+                } else {
+                    const uint4 v = make_uint4(codes[0], codes[E / 8 - 3], codes[E / 8 - 2], codes[E / 8 - 1]);
+                    *reinterpret_cast<uint4*>(cp) = v;
+                    if (qpair) st_dsmem_v4(map_dsmem(smem_u32(cp), peer), v);
+                }
+                *sp = (uint8_t)sfbyte;
+                if (qpair) st_dsmem_u8(map_dsmem(smem_u32(sp), peer), sfbyte);
             };
             // the loop bound is per warp (fw): the warp-wide arrival below
             for (int fw = fw0; fw < total; fw += kBatch * kQuantThreads) {
@@ -639,15 +687,19 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
 #ifdef RS_TRACE
                     if (qtid == 0 && r == 0 && fw == fw0) RS_TRACE_MARK(g.trace, 21);
 #endif
-                    // these blocks are in shared memory: make them visible to the
-                    // tensor pipe, then one arrival per warp and chunk counts them
-                    fence_proxy_async_smem();
+                    // these blocks are in shared memory (with CTA pairs in both
+                    // CTAs'): make them visible to the tensor pipe, then one
+                    // arrival per warp and chunk counts them, on both CTAs
+                    if (qpair) fence_proxy_async_all();
+                    else fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
                         const int lo = fw + r * kQuantThreads, hi = min(lo + 32, total);
                         for (int c = lo / cb; c * cb < hi; ++c) {
                             const int n = min(hi, (c + 1) * cb) - max(lo, c * cb);
-                            mbar_arrive_cnt(smem_u32(&cbar[c]), (uint32_t)n);
+                            const uint32_t bar = smem_u32(&cbar[chunk_of(c)]);
+                            mbar_arrive_cnt(bar, (uint32_t)n);
+                            if (qpair) mbar_arrive_remote_cnt(map_dsmem(bar, peer), (uint32_t)n);
                         }
                     }
                 }
@@ -673,10 +725,10 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             uint32_t dst_buf0 = 0, dst_buf1 = 0, dst_bar0 = 0, dst_bar1 = 0;
             if (g.splits > 1 && warp == 8 && lane < g.splits) {
                 const uint32_t rb = recv_base + my_rank * slice_bytes;
-                dst_buf0 = map_dsmem(rb, (uint32_t)lane);
-                dst_bar0 = map_dsmem(smem_u32(&red_full[0]), (uint32_t)lane);
-                dst_buf1 = map_dsmem(rb + (uint32_t)g.recv_bytes, (uint32_t)lane);
-                dst_bar1 = map_dsmem(smem_u32(&red_full[1]), (uint32_t)lane);
+                dst_buf0 = map_dsmem(rb, krank((uint32_t)lane));
+                dst_bar0 = map_dsmem(smem_u32(&red_full[0]), krank((uint32_t)lane));
+                dst_buf1 = map_dsmem(rb + (uint32_t)g.recv_bytes, krank((uint32_t)lane));
+                dst_bar1 = map_dsmem(smem_u32(&red_full[1]), krank((uint32_t)lane));
             }
             for (int j = 0; j < ntl; ++j) {
                 const int b = j % nacc;
@@ -704,10 +756,10 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 auto emit4 = [&](int o0, float z0, float z1, float z2, float z3) {
                     if (!send_ok || o0 >= owners * per_cta) return;
                     const int o = o0 / per_cta;
-                    st_async_v4(map_dsmem(rbuf + (uint32_t)(o0 - o * per_cta) * 4u, (uint32_t)o),
+                    st_async_v4(map_dsmem(rbuf + (uint32_t)(o0 - o * per_cta) * 4u, krank((uint32_t)o)),
                                 make_uint4(__float_as_uint(z0), __float_as_uint(z1), __float_as_uint(z2),
                                            __float_as_uint(z3)),
-                                map_dsmem(rbar, (uint32_t)o));
+                                map_dsmem(rbar, krank((uint32_t)o)));
                 };
                 bool ok = mbar_wait_bounded(smem_u32(&accum_full[b]), use_ph, abort_flag, g.err);
                 if (j == 0 && ctid == 0) RS_TRACE_MARK(g.trace, 6);
@@ -935,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                         if (ctid == 0 && *abort_flag == 0) {
                             mbar_arrive_expect_tx(smem_u32(&red_full[b]), red_bytes);
                             for (int p = 0; p < g.splits; ++p)
-                                mbar_arrive_remote(map_dsmem(smem_u32(&recv_free[b]), (uint32_t)p));
+                                mbar_arrive_remote(map_dsmem(smem_u32(&recv_free[b]), krank((uint32_t)p)));
                         }
                     }
                 }
@@ -1023,9 +1075,12 @@ static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots, size
 
 // Complete plan for a given split count s; stages == 0 when it does not fit.
 // bn_min: the MMA width, at least the one the activation rows need (a measured
-// tactic may ask for a wider one; the extra operand rows are zero).
+// tactic may ask for a wider one; the extra operand rows are zero).  pair_ok:
+// a fused plan lets CTA pairs share the quantization of their K slice (only
+// on a measured tactic's request: on GB300 the remote stores and the wider
+// clusters cost more than the halved quantizer saves for every shape tuned).
 static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms, int s, bool allow_fused,
-                                int bn_min = 16) {
+                                int bn_min = 16, bool pair_ok = false) {
     GemmPlan p{};
     p.fmt = fmt;
     p.fold = fold ? 1 : 0;
@@ -1088,6 +1143,11 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
             --stages;
     }
     p.fused = fused ? 1 : 0;
+    // CTA pairs (fused plans with an even number of CTAs per K split): the
+    // cluster grows to two neighbouring channel tiles per split, each
+    // quantizing every other chunk of the shared slice into both CTAs'
+    // shared memory (one store to each, one arrival on each CTA's barrier).
+    p.qpair = (fused && pair_ok && p.grid_x % 2 == 0 && 2 * s <= kMaxSplits && max_chunks >= 2) ? 1 : 0;
     p.nacc = nacc;
     p.stages = stages;
     p.slots = p.fused ? max_chunks : 0;
@@ -1169,7 +1229,8 @@ GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bo
     GemmPlan p = plan_impl(fmt, fold, M, N, K, num_sms, allow_fused);
     Tactic t;
     if (num_sms > 0 && find_tactic(fmt, fold, M, N, K, num_sms, &t) && t.splits <= (K + 255) / 256) {
-        const GemmPlan q = plan_for_splits(fmt, fold, M, N, K, num_sms, t.splits, allow_fused && t.fused, t.bn);
+        const GemmPlan q =
+            plan_for_splits(fmt, fold, M, N, K, num_sms, t.splits, allow_fused && t.fused, t.bn, t.fused == 2);
         if (q.stages > 0) {
             p = q;
             p.tuned = 1;
@@ -1256,9 +1317,9 @@ static cudaError_t launch_typed(const GemmPlan& p, const CUtensorMap& tb, const 
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
-    if (p.splits > 1) {
+    if (p.splits > 1 || p.qpair) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.x = p.qpair ? 2 : 1;
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = (unsigned)p.splits;
         ++na;
@@ -1329,6 +1390,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
     a.tmem_cols = p.tmem_cols;
     a.part_bytes = p.part_bytes;
     a.dyn_alpha = c.dyn_alpha;
+    a.qpair = p.fused ? p.qpair : 0;
     a.qdump = p.fused ? static_cast<uint8_t*>(c.qdump) : nullptr;
 #define RS_CASE(F, B, FU)                                                      \
     if (p.fmt == F && p.bn == B && (p.fused != 0) == FU) return launch_typed<F, B, FU>(p, tb, a, stream);

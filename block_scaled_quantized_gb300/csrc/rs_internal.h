@@ -52,6 +52,7 @@ struct GemmPlan {
     size_t smem_bytes;
     int pair;        // large operands: the paired-CTA kernel (rs_gemm_pair.cu) runs the call
     int tuned;       // 1: a measured tactic chose splits, fused and bn
+    int qpair;       // fused: pairs of neighbouring CTAs (same K slice) quantize half of it each
 };
 
 constexpr int kMaxSplits = 8;   // portable thread-block cluster size
@@ -69,7 +70,7 @@ GemmPlan make_gemm_plan_analytic(int fmt, bool fold, int M, int N, int K, int nu
 // the width the activation rows need; wider pads the operand with zero rows).
 struct Tactic {
     int splits;  // 1..kMaxSplits
-    int fused;   // 0 or 1
+    int fused;   // 0: separate quantizer; 1: in the GEMM; 2: in the GEMM, shared by CTA pairs
     int bn;      // 16, 32, 64, 128 or 256
 };
 // Install (replace) the tactic of (fmt, fold, M, N, K, num_sms); false on an

@@ -40,7 +40,7 @@ std::vector<Entry> g_table;
 bool g_loaded = false;
 
 bool valid(const Tactic& t) {
-    return t.splits >= 1 && t.splits <= kMaxSplits && (t.fused == 0 || t.fused == 1) &&
+    return t.splits >= 1 && t.splits <= kMaxSplits && t.fused >= 0 && t.fused <= 2 &&
            (t.bn == 16 || t.bn == 32 || t.bn == 64 || t.bn == 128 || t.bn == 256);
 }
 

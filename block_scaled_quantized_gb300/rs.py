@@ -251,11 +251,11 @@ def rs_debug_pair_gemm(enable: bool):
     lib().rs_debug_pair_gemm(int(bool(enable)))
 
 
-def rs_set_tactic(fmt: int, compensated: bool, M: int, N: int, K: int, num_sms: int, splits: int, fused: bool,
+def rs_set_tactic(fmt: int, compensated: bool, M: int, N: int, K: int, num_sms: int, splits: int, fused: int,
                   bn: int):
     """Install a measured launch tactic for one shape (see rs.h)."""
     _check("rs_set_tactic", lib().rs_set_tactic(fmt, int(bool(compensated)), M, N, K, num_sms, splits,
-                                                int(bool(fused)), bn))
+                                                int(fused), bn))
 
 
 def rs_reset_tactics(builtin: bool = True):

@@ -73,7 +73,7 @@ def candidates(M: int, K: int, compensated: bool):
     chunks = (K + 255) // 256
     for bn in bns:
         for splits in range(1, min(8, chunks) + 1):
-            for fused in ((1, 0) if bn <= 32 else (0,)):
+            for fused in ((2, 1, 0) if bn <= 32 else (0,)):
                 yield splits, fused, bn
 
 

@@ -95,7 +95,7 @@ def run_dump(fmt, compensated, x_bf16, wq, aw, N, alpha_x):
     y = torch.empty((M, N), dtype=torch.float32, device=DEV)
     ws = rs.empty_workspace(fmt, M, N, K, compensated)
     lay = rs.rs_debug_linear_dump(fmt, compensated, M, N, K)
-    assert lay["fused"] == 1, "the shape must take the one-launch plan"
+    assert lay["fused"] in (1, 2), "the shape must take the one-launch plan"
     nbytes = lay["grid_x"] * lay["splits"] * lay["slots"] * lay["stage_bytes"]
     dump = torch.full((nbytes,), 0x5A, dtype=torch.uint8, device=DEV)
     lay2 = rs.rs_debug_linear_dump(fmt, compensated, M, N, K, x=x, alpha_x=alpha_x, wq=wq, alpha_w=aw, y=y,
@@ -139,12 +139,33 @@ CASES = [
 ]
 
 
+@pytest.fixture(params=["shipped", "paired", "unpaired"])
+def prologue_mode(request):
+    """Which prologue runs: the shipped tactic table's choice, the analytic
+    plan (CTA pairs share the quantization of a K slice when the grid allows),
+    or the same plan with every CTA quantizing its whole slice."""
+    yield request.param
+    rs.rs_reset_tactics(True)
+
+
+def set_mode(mode, fmt, compensated, M, N, K):
+    rs.rs_reset_tactics(mode == "shipped")
+    if mode == "unpaired":
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        p = rs.rs_plan_linear(fmt, compensated, M, N, K, sms)
+        rs.rs_set_tactic(fmt, compensated, M, N, K, sms, p["splits"], 1, p["bn"])
+    lay = rs.rs_debug_linear_dump(fmt, compensated, M, N, K)
+    if mode == "unpaired":
+        assert lay["fused"] == 1
+
+
 @pytest.mark.parametrize("own_scale", [False, True])
 @pytest.mark.parametrize("fmt,compensated,M,N,K,recipe", CASES)
-def test_fused_slices_bit_exact(fmt, compensated, M, N, K, recipe, own_scale):
+def test_fused_slices_bit_exact(fmt, compensated, M, N, K, recipe, own_scale, prologue_mode):
     import oracle
     if own_scale and fmt == 1:
         pytest.skip("MXFP4 has no tensor scale")
+    set_mode(prologue_mode, fmt, compensated, M, N, K)
     x = workloads.make_x(recipe, M, K=K, seed=M * 31 + K)
     xb = workloads.bf16_bits(x)
     ax = oracle.tensor_scale(xb) if fmt == 0 else np.float32(0)
@@ -160,7 +181,7 @@ def test_fused_slices_bit_exact(fmt, compensated, M, N, K, recipe, own_scale):
 def test_dump_layout_query_and_refusals():
     # layout only (no launch) and the documented refusals
     lay = rs.rs_debug_linear_dump(0, True, 8, 4096, 4096)
-    assert lay["fused"] == 1 and lay["splits"] * lay["grid_x"] <= 304
+    assert lay["fused"] in (1, 2) and lay["splits"] * lay["grid_x"] <= 304
     lay = rs.rs_debug_linear_dump(0, True, 512, 4096, 4096)
     assert lay["fused"] == 0
     wq, aw = make_weight(0, 256, 512, seed=3)
@@ -197,7 +218,7 @@ def test_residue_scale_boundaries_standalone_and_fused():
     opb = rs.rs_operand_bytes(0, 2, K)
     q_all = torch.full((n * opb,), 0xAB, dtype=torch.uint8, device=DEV)
     lay = rs.rs_debug_linear_dump(0, True, 1, N, K)
-    assert lay["fused"] == 1 and lay["splits"] == 1 and lay["grid_x"] == 1
+    assert lay["fused"] in (1, 2) and lay["splits"] == 1 and lay["grid_x"] == 1
     stage = lay["stage_bytes"] * lay["slots"]
     d_all = torch.full((n * stage,), 0x5A, dtype=torch.uint8, device=DEV)
     y = torch.empty((n, N), dtype=torch.float32, device=DEV)
@@ -221,3 +242,51 @@ def test_residue_scale_boundaries_standalone_and_fused():
         lsf = np.stack([q["sf_x"][0], q["sf_r"][0]])
         want = expected_image(0, lcodes, lsf, K, lay["bn"], lay["stage_bytes"], [0])
         assert np.array_equal(d_all[i * stage:i * stage + len(want)], want), ctx
+
+
+# (fmt, compensated, M, N, K, splits, recipe): CTA pairs with odd chunk counts
+# per K slice (one CTA of a pair quantizes one chunk more), a single K split
+# (clusters of one pair), and MXFP4
+PAIRED = [
+    (0, True, 3, 1024, 1280, 2, "gauss_outlier_k2048"),
+    (0, True, 8, 512, 768, 1, "attn_proj_k4096"),
+    (0, False, 6, 768, 2560, 3, "attn_proj_k4096"),
+    (1, True, 5, 768, 2560, 3, "mx_k5120_n27648"),
+    (1, False, 7, 512, 1280, 1, "gauss_outlier_k2048"),
+]
+
+
+@pytest.mark.parametrize("own_scale", [False, True])
+@pytest.mark.parametrize("fmt,compensated,M,N,K,splits,recipe", PAIRED)
+def test_paired_prologue_bit_exact(fmt, compensated, M, N, K, splits, recipe, own_scale):
+    """Tactic fused = 2 forces CTA pairs to share the quantization of each K
+    slice; every CTA's slice image still equals the oracle's codes and scale
+    bytes, and Y matches a plan without pairs exactly (same MMAs, same order)."""
+    import oracle
+    if own_scale and fmt == 1:
+        pytest.skip("MXFP4 has no tensor scale")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    x = workloads.make_x(recipe, M, K=K, seed=M + 7 * K)
+    xb = workloads.bf16_bits(x)
+    ax = oracle.tensor_scale(xb) if fmt == 0 else np.float32(0)
+    wq, aw = make_weight(fmt, N, K, seed=N + 3)
+    ax_dev = None if (fmt == 1 or own_scale) else torch.tensor([ax], dtype=torch.float32, device=DEV)
+    ys = {}
+    try:
+        for fused in (2, 1):
+            rs.rs_reset_tactics(False)
+            rs.rs_set_tactic(fmt, compensated, M, N, K, sms, splits, fused, 16)
+            lay, dump = run_dump(fmt, compensated, x, wq, aw, N, ax_dev)
+            assert lay["fused"] == fused and lay["splits"] == splits
+            codes, sf = oracle_rows(fmt, compensated, xb, ax)
+            check_slices(fmt, lay, dump, codes, sf, K)
+            y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+            fn = rs.rs_linear_compensated if compensated else rs.rs_linear_w4a4
+            fn(fmt, M, N, K, x=x.to(DEV), alpha_x=ax_dev, wq=wq, alpha_w=aw, y=y,
+               workspace=rs.empty_workspace(fmt, M, N, K, compensated))
+            torch.cuda.synchronize()
+            assert rs.rs_get_device_error() == 0
+            ys[fused] = y.cpu()
+    finally:
+        rs.rs_reset_tactics(True)
+    assert torch.equal(ys[1], ys[2])

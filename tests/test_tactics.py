@@ -75,7 +75,7 @@ def test_tactics_that_do_not_fit_fall_back():
     assert {k: v for k, v in plan(0, True, 8, 1024, 512).items()} == base
 
 
-@pytest.mark.parametrize("fields", [(0, 0, 16), (9, 0, 16), (2, 2, 16), (2, 0, 48), (2, 0, 512)])
+@pytest.mark.parametrize("fields", [(0, 0, 16), (9, 0, 16), (2, 3, 16), (2, -1, 16), (2, 0, 48), (2, 0, 512)])
 def test_out_of_range_tactics_are_refused(fields):
     assert rs.lib().rs_set_tactic(0, 1, 8, 4096, 4096, SMS, *fields) == rs.RS_ERR_INVALID_ARG
     assert rs.rs_tactic_count() == 0
@@ -170,3 +170,16 @@ def test_every_tuned_case_has_its_own_row():
         for M in Ms:
             for comp in (0, 1):
                 assert (fmt, comp, M, N, K) in rows, (fmt, comp, M, N, K)
+
+
+def test_pair_tactic_pairs_only_where_the_grid_allows():
+    """fused = 2: CTA pairs share the quantization of a K slice when the plan
+    is fused, its CTAs per split are even and two clusters' worth of splits
+    stay within 8 CTAs; otherwise the plan is the unpaired fused one."""
+    rs.rs_set_tactic(0, True, 8, 4096, 4096, SMS, 4, 2, 16)
+    assert plan(0, True, 8, 4096, 4096)["fused"] == 2          # 32 CTAs per split, 4 splits
+    rs.rs_set_tactic(0, True, 8, 4096, 4096, SMS, 8, 2, 16)
+    assert plan(0, True, 8, 4096, 4096)["fused"] == 1          # 16-CTA clusters would be needed
+    rs.rs_set_tactic(0, True, 8, 384, 4096, SMS, 4, 2, 16)
+    assert plan(0, True, 8, 384, 4096)["fused"] == 1           # 3 CTAs per split
+    assert plan(0, True, 8, 4096, 4096, x_in_call=False)["fused"] == 0
