@@ -536,11 +536,15 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             constexpr int kWords = E / 8;   // 16-byte words of X per block
             constexpr int kBatch = 32 / E;  // blocks per thread per batch
             const int cb = g.M * bpc;       // blocks per chunk
+            // f / cb as a multiply-high: with m = ceil(2^32 / cb) the quotient
+            // is exact while f cb < 2^32 (here f < 32 chunks x cb, cb <= 512)
+            const uint32_t cb_magic = 0xFFFFFFFFu / (uint32_t)cb + 1u;
+            auto div_cb = [&](int f) { return (int)__umulhi((uint32_t)f, cb_magic); };
             const int my_chunks = qpair ? (nck - (int)px + 1) / 2 : nck;
             const int total = my_chunks * cb;
             auto chunk_of = [&](int cl) { return qpair ? 2 * cl + (int)px : cl; };  // local -> slice chunk
             auto block_pos = [&](int f, int& j, int& kk) {
-                const int cl = f / cb, rem = f - cl * cb;
+                const int cl = div_cb(f), rem = f - cl * cb;
                 j = rem / bpc;
                 kk = chunk_of(cl) * 256 + (rem - j * bpc) * E;
             };
@@ -695,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                     __syncwarp();
                     if (lane == 0) {
                         const int lo = fw + r * kQuantThreads, hi = min(lo + 32, total);
-                        for (int c = lo / cb; c * cb < hi; ++c) {
+                        for (int c = div_cb(lo); c * cb < hi; ++c) {
                             const int n = min(hi, (c + 1) * cb) - max(lo, c * cb);
                             const uint32_t bar = smem_u32(&cbar[chunk_of(c)]);
                             mbar_arrive_cnt(bar, (uint32_t)n);
