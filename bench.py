@@ -43,7 +43,7 @@ WORKLOAD = "nvfp4_compensated_linear_attn_proj_M8_K4096_N4096"
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by
 # the hash of the kernel sources it was taken on (null once they change).
-TRAFFIC = {"sources_sha": "1490d2ab12ee5932", "bytes_per_launch": 9587712}
+TRAFFIC = {"sources_sha": "541d5e30eeb3dd3e", "bytes_per_launch": 9597696}
 
 
 def kernel_sources_sha() -> str:
@@ -378,23 +378,23 @@ RESATTN_CASES = [
 ]
 
 
-def resattn_leg(torch, rs, hbm) -> list:
-    """ResAttn decode steps over synthetic paged NVFP4 caches (random codes,
-    E4M3 scales in [2^-2, 2^2], every sequence full length, a shuffled block
-    table), rotated over enough copies that each step reads its cache from
-    HBM.  Algorithmic bytes: K and V of every cached token and KV head,
+class ResAttnCase:
+    """One ResAttn decode workload: synthetic paged NVFP4 caches (random
+    codes, E4M3 scales in [2^-2, 2^2], every sequence full length, a shuffled
+    block table), rotated over enough copies that each step reads its cache
+    from HBM.  Algorithmic bytes: K and V of every cached token and KV head,
     2 (D/2 + D/16) bytes (144 B at D = 128), plus Q and O."""
-    rows = []
-    gen = torch.Generator(device="cuda")
-    gen.manual_seed(0)
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    for B, Hq, Hkv, D, L in RESATTN_CASES:
+
+    def __init__(self, torch, rs, B, Hq, Hkv, D, L, gen):
+        self.rs = rs
+        self.B, self.Hq, self.Hkv, self.D, self.L = B, Hq, Hkv, D, L
         pages = (L + 31) // 32
         page_bytes = 32 * (D // 2 + D // 16)
         cache_bytes = B * pages * Hkv * page_bytes
-        copies = max(2, math.ceil(2 * l2 / (2 * cache_bytes)) + 1)
-        caches = []
-        for _ in range(copies):
+        l2 = torch.cuda.get_device_properties(0).L2_cache_size
+        self.copies = max(2, math.ceil(2 * l2 / (2 * cache_bytes)) + 1)
+        self.caches = []
+        for _ in range(self.copies):
             kv = []
             for _ in range(2):
                 c = torch.randint(0, 256, (B * pages, Hkv, page_bytes), dtype=torch.uint8, device="cuda",
@@ -403,25 +403,34 @@ def resattn_leg(torch, rs, hbm) -> list:
                                    generator=gen)
                 c[:, :, 32 * (D // 2):] = sc
                 kv.append(c)
-            caches.append(kv)
-        table = torch.randperm(B * pages, device="cuda", generator=gen).to(torch.int32).reshape(B, pages)
-        lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
-        q = (torch.randn((B, Hq, D), device="cuda", generator=gen)).to(torch.bfloat16)
-        aq = torch.empty(1, dtype=torch.float32, device="cuda")
-        rs.rs_compute_tensor_scale(q, aq)
-        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
-        ws = torch.empty(rs.rs_resattn_workspace_bytes(B, Hq, Hkv, D, L), dtype=torch.uint8, device="cuda")
+            self.caches.append(kv)
+        self.table = torch.randperm(B * pages, device="cuda", generator=gen).to(torch.int32).reshape(B, pages)
+        self.lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
+        self.q = (torch.randn((B, Hq, D), device="cuda", generator=gen)).to(torch.bfloat16)
+        self.aq = torch.empty(1, dtype=torch.float32, device="cuda")
+        rs.rs_compute_tensor_scale(self.q, self.aq)
+        self.out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+        self.ws = torch.empty(rs.rs_resattn_workspace_bytes(B, Hq, Hkv, D, L), dtype=torch.uint8, device="cuda")
+        self.algo_bytes = 2 * B * L * Hkv * (D // 2 + D // 16) + 2 * B * Hq * D * 2
 
-        def step(i):
-            k, v = caches[i % copies]
-            rs.rs_resattn_decode(q, aq, k, v, table, lens, L, out, ws, Hkv)
+    def step(self, i):
+        k, v = self.caches[i % self.copies]
+        self.rs.rs_resattn_decode(self.q, self.aq, k, v, self.table, self.lens, self.L, self.out, self.ws, self.Hkv)
 
-        us, _ = graph_time_us(torch, step, 30)
-        algo = 2 * B * L * Hkv * (D // 2 + D // 16) + 2 * B * Hq * D * 2
+
+def resattn_leg(torch, rs, hbm) -> list:
+    """ResAttn decode steps (ResAttnCase) timed in CUDA graphs."""
+    rows = []
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    for B, Hq, Hkv, D, L in RESATTN_CASES:
+        case = ResAttnCase(torch, rs, B, Hq, Hkv, D, L, gen)
+        us, _ = graph_time_us(torch, case.step, 30)
+        algo = case.algo_bytes
         rows.append({"B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "tokens": L, "us": round(us, 2),
                      "achieved_gbs": round(algo / (us * 1e-6) / 1e9, 1),
                      "hbm_frac": round(algo / (us * 1e-6) / 1e9 / hbm, 4), "kv_bytes_per_token_head": 2 * (D // 2 + D // 16)})
-        del caches, table, q, out, ws
+        del case
         torch.cuda.empty_cache()
     assert rs.rs_get_device_error() == 0
     return rows
@@ -462,6 +471,8 @@ PROFILE_CASES = {
     "mlp_down": (0, "mlp_down", 8, True),
     "mx_m1": (1, "mx_k5120_n27648", 1, True),
     "prefill_kext1": (0, "prefill_k8192", 4096, "kext1"),
+    # ResAttn decode: (B, Hq, Hkv, D, tokens per sequence)
+    "resattn_b8_l8192": ("resattn", (8, 32, 8, 128, 8192)),
 }
 
 
@@ -471,7 +482,15 @@ def run_profile_case(args) -> dict:
     import torch
     from block_scaled_quantized_gb300 import build, rs, workloads
     build.build()
-    fmt, recipe, M, comp = PROFILE_CASES[args.profile_case]
+    case = PROFILE_CASES[args.profile_case]
+    if case[0] == "resattn":
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(0)
+        att = ResAttnCase(torch, rs, *case[1], gen)
+        us, _ = graph_time_us(torch, att.step, args.steps, reps=1, warm=args.warmup)
+        assert rs.rs_get_device_error() == 0
+        return {"profile_case": args.profile_case, "us_per_call": round(us, 3), "launches_per_call": 3}
+    fmt, recipe, M, comp = case
     if comp == "kext1":
         lin = KextLinear(torch, rs, workloads, recipe, M, 1)
     else:

@@ -432,9 +432,9 @@ size_t rs_resattn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len) {
     return attn_q_bytes(B, Hq, D) + (size_t)B * Hkv * max_splits * (Hq / Hkv) * (D + 2) * sizeof(float);
 }
 
-int rs_resattn_split_tokens(int B, int Hkv, int max_len, int num_sms) {
-    if (B < 1 || Hkv < 1 || max_len < 0 || num_sms < 1) return 0;
-    return rs::resattn_split_tokens(B, Hkv, max_len, num_sms);
+int rs_resattn_split_tokens(int B, int Hkv, int D, int max_len, int num_sms) {
+    if (B < 1 || Hkv < 1 || (D != 128 && D != 256) || max_len < 0 || num_sms < 1) return 0;
+    return rs::resattn_split_tokens(B, Hkv, D, max_len, num_sms);
 }
 
 rs_status rs_resattn_decode(int B, int Hq, int Hkv, int D, int max_pages, int max_len, const void* q_bf16,
@@ -476,7 +476,7 @@ rs_status rs_resattn_decode(int B, int Hq, int Hkv, int D, int max_pages, int ma
     a.D = D;
     a.max_pages = max_pages;
     a.max_len = max_len;
-    a.split_tokens = rs::resattn_split_tokens(B, Hkv, max_len, dev->num_sms);
+    a.split_tokens = rs::resattn_split_tokens(B, Hkv, D, max_len, dev->num_sms);
     a.splits = max_len > 0 ? (max_len + a.split_tokens - 1) / a.split_tokens : 1;
     a.q_rows_pad = (2 * rows + 127) / 128 * 128;
     a.q_atoms_k = n_atoms_k_host(RS_NVFP4, D);

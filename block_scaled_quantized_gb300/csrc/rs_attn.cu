@@ -139,7 +139,9 @@ __device__ __forceinline__ float warp_max_f32(float x) {
     return __int_as_float(key >= 0 ? key : (key ^ 0x7FFFFFFF));
 }
 
-template <int D>
+// GM: the query heads per KV head the softmax and output loops cover (4 or
+// 8, at least G; groups of at most four take the shorter loops).
+template <int D, int GM>
 __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_kernel(const AttnArgs g) {
     using Ly = AttnLayout<D>;
     constexpr int CB = Ly::CB, SB = Ly::SB, NA = Ly::NA, PB = Ly::PB, S = Ly::STAGES;
@@ -261,12 +263,12 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
         const float c = __fmul_rn(*g.alpha_q, __frsqrt_rn((float)D));  // alpha_q / sqrt(D), alpha_k = 1
         const uint64_t kdesc = kmajor_sw128_desc(smem_u32(ktile)), qdesc = kmajor_sw128_desc(smem_u32(qtile));
         const uint64_t vdesc = kmajor_sw128_desc(smem_u32(vt)), pdesc = kmajor_sw128_desc(smem_u32(ptile));
-        float o[MB][8];
+        float o[MB][GM];
 #pragma unroll
         for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
-            for (int q = 0; q < 8; ++q) o[mb][q] = 0.0f;
-        float a_t[8];  // this tile's rescale factors exp(m_old - m_new)
+            for (int q = 0; q < GM; ++q) o[mb][q] = 0.0f;
+        float a_t[GM];  // this tile's rescale factors exp(m_old - m_new)
         if (warp == 1) {
             if (elect_one_sync())
                 for (int a = 0; a < NA; ++a) tc_cp_sf_atom(t_sfq + a * 4, sf_atom_desc(smem_u32(qsf + a * 512)));
@@ -379,17 +381,17 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
                 for (int e = 0; e < 16; ++e) z[e] = 0.0f;
                 if (ok) tmem_ld16(t_qk + quarter, z);
                 if (r == 0 && it < 6) RS_TRACE_MARK(g.trace, 5 * it + 2);  // QK done
-                float sc[8];
+                float sc[GM];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < GM; ++q) {
                     sc[q] = (q < G && r < nt) ? __fmul_rn(__fadd_rn(z[2 * q], z[2 * q + 1]), c) : -INFINITY;
                     const float mx = warp_max_f32(sc[q]);
                     if (lane == 0) red[(warp - 4) * 8 + q] = mx;
                 }
                 named_bar_sync(2, 128);
-                float m_new[8];
+                float m_new[GM];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+                for (int q = 0; q < GM; ++q) {
                     const float tm = fmaxf(fmaxf(red[q], red[8 + q]), fmaxf(red[16 + q], red[24 + q]));
                     const float mo = m_run[q];
                     m_new[q] = fmaxf(mo, tm);
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
                 named_bar_sync(2, 128);
                 if (r == 0)
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
+                    for (int q = 0; q < GM; ++q) {
                         const int tile_sum = (red2[q] + red2[8 + q]) + (red2[16 + q] + red2[24 + q]);
                         l_run[q] = l_run[q] * a_t[q] + __fmul_rn((float)tile_sum, 0x1p-9f);
                         m_run[q] = m_new[q];
@@ -443,7 +445,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
                     if (ok) tmem_ld16(t_pv + (uint32_t)(mb * 16) + quarter, pv);
                     if (r == 0 && mb == 0 && it < 6) RS_TRACE_MARK(g.trace, 5 * it + 4);  // PV done
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) o[mb][q] = fmaf(o[mb][q], a_t[q], pv[q]);
+                    for (int q = 0; q < GM; ++q) o[mb][q] = fmaf(o[mb][q], a_t[q], pv[q]);
                 }
             }
         }
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
 #pragma unroll
             for (int mb = 0; mb < MB; ++mb)
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
+                for (int q = 0; q < GM; ++q)
                     if (q < G) part[(size_t)q * (D + 2) + mb * 128 + r] = o[mb][q];
             if (r < G) {
                 part[(size_t)r * (D + 2) + D] = m_run[r];
@@ -515,24 +517,39 @@ __global__ void resattn_combine_kernel(const AttnArgs g, void* out, int out_f32)
 // CTAs that fit on it (two at head size 128), in multiples of the tile and
 // at least one tile per split (the preset rule of Sec. 5.2 from batch, KV
 // heads, sequence length and SM count).
-int resattn_split_tokens(int B, int Hkv, int max_len, int num_sms) {
+// Split count: the (split, KV head, sequence) CTAs run in waves of `slots`
+// (resident CTAs per SM x SMs: two at head size 128, one at 256); a CTA's
+// time is about its tiles plus one tile's worth of set-up and teardown.  The
+// split minimising waves x (tiles per split + 1) wins, the fewer splits on a
+// tie (fewer partial results to combine).
+int resattn_split_tokens(int B, int Hkv, int D, int max_len, int num_sms) {
     const int tiles = (max_len + kAttnTile - 1) / kAttnTile;
-    const int slots = 2 * num_sms;
-    int splits = (slots + B * Hkv - 1) / (B * Hkv);
-    if (splits > tiles) splits = tiles;
-    if (splits < 1) splits = 1;
-    const int tiles_per_split = (tiles + splits - 1) / splits;
-    return (tiles_per_split < 1 ? 1 : tiles_per_split) * kAttnTile;
+    if (tiles <= 1) return kAttnTile;
+    const int64_t slots = (int64_t)(D <= 128 ? 2 : 1) * num_sms;
+    const int64_t groups = (int64_t)B * Hkv;
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int s = 1; s <= tiles; ++s) {
+        const int per = (tiles + s - 1) / s;
+        if (s > 1 && (tiles + per - 1) / per < s) continue;  // the same split size as a smaller s
+        const int64_t waves = (groups * s + slots - 1) / slots;
+        const int64_t cost = waves * (per + 1);
+        if (best_cost < 0 || cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return ((tiles + best - 1) / best) * kAttnTile;
 }
 
-template <int D>
+template <int D, int GM>
 static cudaError_t launch_split(const AttnArgs& a, cudaStream_t stream) {
     static bool attr_done[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(resattn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(resattn_split_kernel<D, GM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)AttnLayout<D>::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev] = true;
@@ -547,12 +564,14 @@ static cudaError_t launch_split(const AttnArgs& a, cudaStream_t stream) {
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, resattn_split_kernel<D>, a);
+    return cudaLaunchKernelEx(&cfg, resattn_split_kernel<D, GM>, a);
 }
 
 cudaError_t launch_resattn(int D, const AttnArgs& a, void* out, int out_f32, cudaStream_t stream) {
-    cudaError_t e = D == 128 ? launch_split<128>(a, stream) : D == 256 ? launch_split<256>(a, stream)
-                                                                      : cudaErrorInvalidValue;
+    const bool g4 = a.Hq / a.Hkv <= 4;
+    cudaError_t e = D == 128   ? (g4 ? launch_split<128, 4>(a, stream) : launch_split<128, 8>(a, stream))
+                    : D == 256 ? (g4 ? launch_split<256, 4>(a, stream) : launch_split<256, 8>(a, stream))
+                               : cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)a.Hq, (unsigned)a.B, 1);

@@ -157,7 +157,7 @@ struct AttnArgs {
 };
 
 // Tokens per split of a ResAttn call, a multiple of the 128-token tile.
-int resattn_split_tokens(int B, int Hkv, int max_len, int num_sms);
+int resattn_split_tokens(int B, int Hkv, int D, int max_len, int num_sms);
 cudaError_t launch_resattn(int D, const AttnArgs& a, void* out, int out_f32, cudaStream_t stream);
 
 // Device error word of the current device.

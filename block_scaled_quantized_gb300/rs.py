@@ -78,7 +78,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_get_device_error_async": ([P, P], I),
         "rs_fold_pairs": ([I, I, P, P, I, P], I),
         "rs_resattn_workspace_bytes": ([I, I, I, I, I], SZ),
-        "rs_resattn_split_tokens": ([I, I, I, I], I),
+        "rs_resattn_split_tokens": ([I, I, I, I, I], I),
         "rs_debug_pair_gemm": ([I], None),
         "rs_set_tactic": ([I, I, I, I, I, I, I, I, I], I),
         "rs_reset_tactics": ([I], I),
@@ -228,8 +228,8 @@ def rs_resattn_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, max_len: int) 
     return lib().rs_resattn_workspace_bytes(B, Hq, Hkv, D, max_len)
 
 
-def rs_resattn_split_tokens(B: int, Hkv: int, max_len: int, num_sms: int) -> int:
-    return lib().rs_resattn_split_tokens(B, Hkv, max_len, num_sms)
+def rs_resattn_split_tokens(B: int, Hkv: int, D: int, max_len: int, num_sms: int) -> int:
+    return lib().rs_resattn_split_tokens(B, Hkv, D, max_len, num_sms)
 
 
 def rs_resattn_decode(q: torch.Tensor, alpha_q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

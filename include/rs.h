@@ -332,9 +332,11 @@ RS_API rs_status rs_linear_kext(rs_format fmt, int M, int N, int K, int k, const
 RS_API size_t rs_resattn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len);
 
 /* Tokens per sequence split that rs_resattn_decode uses on a device with
- * num_sms SMs (a multiple of 128; host only): enough (split, KV head,
- * sequence) CTAs to cover the SMs, at least one 128-token tile each. */
-RS_API int rs_resattn_split_tokens(int B, int Hkv, int max_len, int num_sms);
+ * num_sms SMs (a multiple of 128; host only; 0 for invalid arguments): the
+ * (split, KV head, sequence) CTAs run in waves of two CTAs per SM at D = 128
+ * and one at D = 256, and the split count minimises waves x (128-token
+ * tiles per split + 1), the fewer splits on a tie. */
+RS_API int rs_resattn_split_tokens(int B, int Hkv, int D, int max_len, int num_sms);
 
 /* One decode step of ResAttn (Sec. 4.3 Eq. 3, Fig. 3; Sec. 5.2 "ResAttn
  * execution").  q_bf16 [B][Hq][D] (device, bf16) is quantized with Alg. 1

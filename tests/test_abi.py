@@ -169,8 +169,14 @@ def test_resattn_sizes_and_argument_checks(librs):
     assert librs.rs_resattn_workspace_bytes(B, Hq, Hkv, D, L) == q_bytes + B * Hkv * 8 * (Hq // Hkv) * (D + 2) * 4
     assert librs.rs_resattn_workspace_bytes(B, Hq, Hkv, 64, L) == 0      # head size
     assert librs.rs_resattn_workspace_bytes(B, 18, 2, D, L) == 0         # 9 query heads per KV head
-    assert librs.rs_resattn_split_tokens(1, 8, 4096, 152) % 128 == 0
-    assert librs.rs_resattn_split_tokens(1, 1, 4096, 152) == 128        # one tile per split covers the SMs
+    assert librs.rs_resattn_split_tokens(1, 8, 128, 4096, 152) % 128 == 0
+    assert librs.rs_resattn_split_tokens(1, 1, 128, 4096, 152) == 128   # one tile per split covers the SMs
+    assert librs.rs_resattn_split_tokens(1, 8, 96, 4096, 152) == 0      # head size
+    # splits fill one wave of resident CTAs (two per SM at D = 128, one at 256)
+    # rather than spill a few CTAs into a second one
+    assert librs.rs_resattn_split_tokens(8, 8, 128, 8192, 152) == 2048  # 4 splits: 256 CTAs <= 304
+    assert librs.rs_resattn_split_tokens(4, 8, 256, 16384, 152) == 1920  # 9 splits: 2 waves x 15 tiles < 1 x 32
+    assert librs.rs_resattn_split_tokens(32, 8, 128, 2048, 152) == 2048  # 256 sequence-heads: no split
 
     def call(shape, ptrs=None, dtype=0, ws=1 << 30):
         pp = ptrs or [dummy] * 7

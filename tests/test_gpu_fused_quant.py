@@ -157,6 +157,8 @@ def set_mode(mode, fmt, compensated, M, N, K):
     lay = rs.rs_debug_linear_dump(fmt, compensated, M, N, K)
     if mode == "unpaired":
         assert lay["fused"] == 1
+    if mode == "shipped" and lay["fused"] == 0:
+        pytest.skip("the shipped tactic quantizes this shape in a separate kernel")
 
 
 @pytest.mark.parametrize("own_scale", [False, True])

@@ -82,7 +82,7 @@ def test_resattn_decode_parity(B, Hq, Hkv, D, lens):
     aq = float(oracle.tensor_scale(qb))
     out = run_gpu(q, kcache, vcache, table, lens, Hkv, L, alpha=aq)
     assert rs.rs_get_device_error() == 0
-    st = rs.rs_resattn_split_tokens(B, Hkv, L, torch.cuda.get_device_properties(0).multi_processor_count)
+    st = rs.rs_resattn_split_tokens(B, Hkv, D, L, torch.cuda.get_device_properties(0).multi_processor_count)
     ref = ra.resattn_decode(qb, aq, kc, ks, vc, vs, np.array(lens), split_tokens=st)
     got = out.cpu().numpy().astype(np.float64)
     assert np.all(np.isfinite(got))
@@ -102,7 +102,7 @@ def test_resattn_bf16_output():
     aq = float(oracle.tensor_scale(qb))
     out = run_gpu(q, kcache, vcache, table, lens, Hkv, max(lens), out_dtype=torch.bfloat16, alpha=aq)
     assert rs.rs_get_device_error() == 0
-    st = rs.rs_resattn_split_tokens(B, Hkv, max(lens), torch.cuda.get_device_properties(0).multi_processor_count)
+    st = rs.rs_resattn_split_tokens(B, Hkv, D, max(lens), torch.cuda.get_device_properties(0).multi_processor_count)
     ref = ra.resattn_decode(qb, aq, kc, ks, vc, vs, np.array(lens), split_tokens=st)
     ref_b = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).float().numpy().astype(np.float64)
     got = out.float().cpu().numpy().astype(np.float64)
@@ -119,7 +119,7 @@ def test_resattn_sequence_longer_than_max_len_is_clamped_and_reported():
     aq = float(oracle.tensor_scale(qb))
     out = run_gpu(q, kcache, vcache, table, [384 + 100], Hkv, 384, alpha=aq)  # claims 100 tokens too many
     assert rs.rs_get_device_error() == rs.RS_ERR_INVALID_ARG
-    st = rs.rs_resattn_split_tokens(B, Hkv, 384, torch.cuda.get_device_properties(0).multi_processor_count)
+    st = rs.rs_resattn_split_tokens(B, Hkv, D, 384, torch.cuda.get_device_properties(0).multi_processor_count)
     ref = ra.resattn_decode(qb, aq, kc, ks, vc, vs, np.array([384]), split_tokens=st)
     got = out.cpu().numpy().astype(np.float64)
     assert np.abs(got - ref).max() <= 1e-3 * np.abs(ref).max()
