@@ -9,11 +9,12 @@ from HBM (working set > 2x L2).  K steps are captured in one CUDA graph; the
 graph is replayed several times, each replay timed with CUDA events between
 synchronizations, and `value` is the median microseconds per step.
 
-Extra keys: the paper's protocol (a 200-call graph, median of five replays)
-and the latency of one call on its own; config 1 (M=1, K=N=2048); the M in
+Extra keys: the paper's protocol (a 200-call graph, median of five replays,
+also as the median over three fresh processes) and the latency of one call
+on its own; config 1 (M=1, K=N=2048); the M in
 {1,2,4,8} sweep of compensated vs W4A4 latency and HBM roofline fraction;
-the MLP pair, the MXFP4 sweep, the prefill TFLOP/s, the 22 projection shapes
-and the on-chip Fold ablation; the roofline of the dominant kernel; the CPU
+the MLP pair, the MXFP4 sweep, the prefill TFLOP/s, the 22 projection shapes,
+the on-chip Fold ablation and ResAttn decode attention; the roofline of the dominant kernel; the CPU
 oracle on all host cores and on one (and on a sample of the prefill rows);
 an end-to-end number through host buffers; the SM clocks sampled during the
 timed region.
@@ -471,6 +472,7 @@ PROFILE_CASES = {
     "mlp_down": (0, "mlp_down", 8, True),
     "mx_m1": (1, "mx_k5120_n27648", 1, True),
     "prefill_kext1": (0, "prefill_k8192", 4096, "kext1"),
+    "prefill_w4a4_pair": (0, "prefill_k8192", 4096, False, "pair"),
     # ResAttn decode: (B, Hq, Hkv, D, tokens per sequence)
     "resattn_b8_l8192": ("resattn", (8, 32, 8, 128, 8192)),
 }
@@ -490,7 +492,8 @@ def run_profile_case(args) -> dict:
         us, _ = graph_time_us(torch, att.step, args.steps, reps=1, warm=args.warmup)
         assert rs.rs_get_device_error() == 0
         return {"profile_case": args.profile_case, "us_per_call": round(us, 3), "launches_per_call": 3}
-    fmt, recipe, M, comp = case
+    fmt, recipe, M, comp = case[:4]
+    rs.rs_debug_pair_gemm(len(case) > 4 and case[4] == "pair")
     if comp == "kext1":
         lin = KextLinear(torch, rs, workloads, recipe, M, 1)
     else:
@@ -498,6 +501,20 @@ def run_profile_case(args) -> dict:
     us, _ = graph_time_us(torch, lin.call, args.steps, reps=1, warm=args.warmup)
     assert rs.rs_get_device_error() == 0
     return {"profile_case": args.profile_case, "us_per_call": round(us, 3), "launches_per_call": lin.launches_per_call()}
+
+
+def processes_protocol(n: int) -> dict:
+    """The headline's 200-call graph timed in n fresh processes, one after
+    the other (each: median of five replays); their median."""
+    vals = []
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--headline-only", "--steps", "200", "--warmup", "5",
+           "--soak-s", "0", "--replays", "5"]
+    for _ in range(n):
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+        if r.returncode != 0:
+            return {"error": f"process exited {r.returncode}", "us": vals}
+        vals.append(json.loads(r.stdout.strip().splitlines()[-1])["value"])
+    return {"processes": n, "graph_calls": 200, "us": vals, "median_us": round(statistics.median(vals), 3)}
 
 
 def max_over_ranks(value: float, world: int, device: str) -> float:
@@ -557,6 +574,10 @@ def run_gpu(args) -> dict:
     g200 = capture(torch, main.call, 200)
     protocol = {"graph_calls": 200, "replays": 5, "us": round(statistics.median(replay_us(torch, g200, 200, 5)), 3)}
     del g200
+    # ... and the median over independent processes (App. C.1 takes medians
+    # over at least three): the same 200-call measurement in fresh processes
+    if world == 1 and args.processes > 0:
+        protocol["processes"] = processes_protocol(args.processes)
     sampler2 = ClockSampler(local)
     sampler2.start()
     isolated = isolated_call_us(torch, main)
@@ -846,6 +867,8 @@ def main():
                     help="projection-shape sweep at M in {1, 8, 64, 512} (default: M = 8)")
     ap.add_argument("--soak-s", type=float, default=1.5)
     ap.add_argument("--replays", type=int, default=7, help="timed replays of the K-step graph (median; at least 5)")
+    ap.add_argument("--processes", type=int, default=3,
+                    help="fresh processes for the 200-call protocol figure (0: skip)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true",
