@@ -510,7 +510,7 @@ def processes_protocol(n: int) -> dict:
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--headline-only", "--steps", "200", "--warmup", "5",
            "--soak-s", "0", "--replays", "5"]
     for _ in range(n):
-        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=180, cwd=ROOT)
         if r.returncode != 0:
             return {"error": f"process exited {r.returncode}", "us": vals}
         vals.append(json.loads(r.stdout.strip().splitlines()[-1])["value"])

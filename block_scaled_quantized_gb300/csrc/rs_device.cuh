@@ -518,6 +518,15 @@ __device__ __forceinline__ void st_dsmem_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
+// Asynchronous 4-byte store into another CTA's shared memory (cluster
+// address from map_dsmem), completing 4 bytes of transaction count on that
+// CTA's mbarrier, whose waiters then see the value.
+__device__ __forceinline__ void st_async_b32(uint32_t dst_cluster, uint32_t v, uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst_cluster),
+                 "r"(v), "r"(bar_cluster)
+                 : "memory");
+}
+
 // Asynchronous 16-byte store into another CTA's shared memory (cluster
 // addresses from map_dsmem, 16-byte aligned); completes 16 bytes of
 // transaction count on that CTA's mbarrier, whose waiters then see the data.

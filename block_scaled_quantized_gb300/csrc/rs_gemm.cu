@@ -230,7 +230,9 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
         // every scale block of chunk i (all token rows) arrives once
         if (FUSED)
             for (int i = 0; i < nck; ++i) mbar_init(smem_u32(&cbar[i]), (uint32_t)(g.M * (256 / block_elems(FMT))));
-        mbar_init(smem_u32(abar), (uint32_t)nranks);  // one slice amax per CTA of the cluster
+        // one 4-byte slice amax from every CTA of the cluster (st.async bytes)
+        mbar_init(smem_u32(abar), 1);
+        if (nranks > 1) mbar_arrive_expect_tx(smem_u32(abar), 4u * (uint32_t)nranks);
         *amax_cta = 0u;
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&accum_full[b]), 1);
@@ -572,7 +574,8 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 // This call's tensor scale (App. B.2 Eq. 8): a = fl(amax(X) / 2688),
                 // the same value rs_compute_tensor_scale gives.  Each CTA takes the
                 // max |x| of its K slice; the K splits of the cluster cover K and
-                // trade their maxima (DSMEM store + remote arrival on each CTA).
+                // trade their maxima (one 4-byte st.async into every CTA's slot
+                // of this rank, completing bytes on that CTA's barrier).
                 // |x| bit patterns, two per word (integer order: NaN > Inf > finite):
                 // the words of this thread's first batch are in registers
                 // already (zeros for blocks past the slice); later batches'
@@ -605,23 +608,18 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 m = __reduce_max_sync(0xFFFFFFFFu, m);
                 if (lane == 0) atomicMax(amax_cta, m);
                 named_bar_sync(2, kQuantThreads);
-                if (qtid == 0) {
-                    const uint32_t cm = *reinterpret_cast<volatile uint32_t*>(amax_cta);
-                    if (nranks > 1) {
-                        for (int p = 0; p < nranks; ++p) {
-                            st_dsmem_u32(map_dsmem(smem_u32(&amax_slot[my_crank]), (uint32_t)p), cm);
-                            mbar_arrive_remote(map_dsmem(smem_u32(abar), (uint32_t)p));
-                        }
-                    } else {
-                        amax_slot[0] = cm;
-                        mbar_arrive(smem_u32(abar));
-                    }
+                const uint32_t cm = *reinterpret_cast<volatile uint32_t*>(amax_cta);
+                uint32_t gm = cm;
+                if (nranks > 1) {
+                    if (qtid < nranks)  // one lane per destination CTA
+                        st_async_b32(map_dsmem(smem_u32(&amax_slot[my_crank]), (uint32_t)qtid), cm,
+                                     map_dsmem(smem_u32(abar), (uint32_t)qtid));
+                    if (mbar_wait_bounded(smem_u32(abar), 0, abort_flag, g.err, 1000000000ull, true))
+                        for (int r = 0; r < nranks; ++r)
+                            gm = max(gm, reinterpret_cast<volatile uint32_t*>(amax_slot)[r]);
                 }
-                uint32_t gm = 0;
-                if (mbar_wait_bounded(smem_u32(abar), 0, abort_flag, g.err, 1000000000ull, true))
-                    for (int r = 0; r < nranks; ++r)
-                        gm = max(gm, reinterpret_cast<volatile uint32_t*>(amax_slot)[r]);
                 const uint32_t bits = gm << 16;
+                if (qtid == 0) RS_TRACE_MARK(g.trace, 8);  // the cluster's amax is known
                 if (bits >= 0x7F800000u) {  // Inf or NaN in X, as rs_compute_tensor_scale reports it
                     if (qtid == 0 && blockIdx.x == 0 && split == 0) atomicExch(g.err, kErrInvalidArg);
                     ax_val = __uint_as_float(0x7FC00000u);
@@ -633,8 +631,10 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             }
             const NvScaleConst ksc = nv_scale_const(ax_val);
             if (FMT == 0 && (g.dyn_alpha || __float_as_uint(ax_val) != __float_as_uint(*alpha_spec))) {
-                // (the same value on every thread: read after the wait, or found by the cluster)
-                named_bar_sync(2, kQuantThreads);
+                // (the same value on every thread: read after the wait, or found by the
+                // cluster; a table built before the wait may still be read until all
+                // threads are here, and without one nothing reads it yet)
+                if (!g.dyn_alpha) named_bar_sync(2, kQuantThreads);
                 build_table(ax_val);
                 named_bar_sync(2, kQuantThreads);
             }
