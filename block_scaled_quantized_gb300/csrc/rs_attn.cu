@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
     uint8_t* ksf = sm + Ly::OFF_KSF;
     uint8_t* qsf = sm + Ly::OFF_QSF;
     uint8_t* vlut = sm + Ly::OFF_LUT;
+    if (threadIdx.x == 0) RS_TRACE_MARK(g.trace, 30);  // CTA start
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + Ly::OFF_CTRL);  // [S]: a stage's pages landed
     uint64_t* empty = full + 3;                                       // [S]: a stage was read
     uint64_t* qk_done = empty + 3;                                    // the tile's QK MMAs are done
@@ -460,6 +461,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
                 part[(size_t)r * (D + 2) + D] = m_run[r];
                 part[(size_t)r * (D + 2) + D + 1] = l_run[r];
             }
+            if (r == 0) RS_TRACE_MARK(g.trace, 31);  // split written
         }
     }
 
@@ -484,28 +486,73 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
 }
 
 // O = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s (R19); empty sequences give 0.
-__global__ void resattn_combine_kernel(const AttnArgs g, void* out, int out_f32) {
+// Split combination (R19), one CTA of P x D threads per (query head,
+// sequence), P = 4 groups when there are many splits and 1 otherwise: the
+// CTA's maximum M of the splits' m_s, then group p sums w_s o_s[d] and
+// w_s l_s over the splits s = p, p + P, ... (w_s = e^(m_s - M), four splits'
+// loads in flight per thread), and the groups' sums are added in group order:
+// a fixed order, so the result does not depend on timing.
+constexpr int kCombineGroups = 4;
+
+__global__ void __launch_bounds__(kCombineGroups * 256) resattn_combine_kernel(const AttnArgs g, void* out,
+                                                                               int out_f32) {
+    __shared__ float red_m[32];
+    __shared__ float num_p[kCombineGroups][256];
+    __shared__ float den_p[kCombineGroups];
     pdl_wait_prior_grid();  // the splits' partial results
     pdl_launch_dependents();
     const int Hq = g.Hq, Hkv = g.Hkv, D = g.D, splits = g.splits, split_tokens = g.split_tokens;
-    const float* part = g.part;
     const int G = Hq / Hkv;
-    const int b = blockIdx.y, hq = blockIdx.x, d = threadIdx.x;
-    if (d >= D) return;
+    const int b = blockIdx.y, hq = blockIdx.x;
+    const int d = threadIdx.x % D, grp = threadIdx.x / D, P = (int)blockDim.x / D;
     const int h = hq / G, gg = hq % G;
     const int L = attn_len(g, b);
     const int ns = min(splits, (L + split_tokens - 1) / split_tokens);
+    const size_t stride = (size_t)G * (D + 2);  // floats from one split's row of this head to the next
+    const float* base = g.part + ((((size_t)b * Hkv + h) * splits) * G + gg) * (D + 2);
+    // M = max_s m_s over the whole CTA
+    float m = -INFINITY;
+    for (int s = threadIdx.x; s < ns; s += blockDim.x) m = fmaxf(m, base[(size_t)s * stride + D]);
+    m = warp_max_f32(m);
+    if ((threadIdx.x & 31) == 0) red_m[threadIdx.x >> 5] = m;
+    __syncthreads();
     float M = -INFINITY;
-    for (int s = 0; s < ns; ++s)
-        M = fmaxf(M, part[((((size_t)b * Hkv + h) * splits + s) * G + gg) * (D + 2) + D]);
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) M = fmaxf(M, red_m[w]);
+    // this group's splits
     float num = 0.0f, den = 0.0f;
-    for (int s = 0; s < ns; ++s) {
-        const float* p = part + ((((size_t)b * Hkv + h) * splits + s) * G + gg) * (D + 2);
+    int s = grp;
+    for (; s + 3 * P < ns; s += 4 * P) {
+        float mv[4], ov[4], lv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float* p = base + (size_t)(s + u * P) * stride;
+            mv[u] = p[D];
+            ov[u] = p[d];
+            lv[u] = p[D + 1];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float w = __expf(mv[u] - M);
+            num = fmaf(w, ov[u], num);
+            den = fmaf(w, lv[u], den);
+        }
+    }
+    for (; s < ns; s += P) {
+        const float* p = base + (size_t)s * stride;
         const float w = __expf(p[D] - M);
         num = fmaf(w, p[d], num);
         den = fmaf(w, p[D + 1], den);
     }
-    const float val = ns > 0 ? num / den : 0.0f;
+    num_p[grp][d] = num;
+    if (d == 0) den_p[grp] = den;
+    __syncthreads();
+    if (grp != 0) return;
+    float nsum = 0.0f, dsum = 0.0f;
+    for (int p = 0; p < P; ++p) {
+        nsum += num_p[p][d];
+        dsum += den_p[p];
+    }
+    const float val = ns > 0 ? nsum / dsum : 0.0f;
     const size_t idx = ((size_t)b * Hq + hq) * D + d;
     if (out_f32) reinterpret_cast<float*>(out)[idx] = val;
     else reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(val);
@@ -513,10 +560,6 @@ __global__ void resattn_combine_kernel(const AttnArgs g, void* out, int out_f32)
 
 // ---------------------------------------------------------------- launch --
 
-// Splits: enough (split, KV head, sequence) CTAs to fill every SM with the
-// CTAs that fit on it (two at head size 128), in multiples of the tile and
-// at least one tile per split (the preset rule of Sec. 5.2 from batch, KV
-// heads, sequence length and SM count).
 // Split count: the (split, KV head, sequence) CTAs run in waves of `slots`
 // (resident CTAs per SM x SMs: two at head size 128, one at 256); a CTA's
 // time is about its tiles plus one tile's worth of set-up and teardown.  The
@@ -575,7 +618,7 @@ cudaError_t launch_resattn(int D, const AttnArgs& a, void* out, int out_f32, cud
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)a.Hq, (unsigned)a.B, 1);
-    cfg.blockDim = dim3((unsigned)D, 1, 1);
+    cfg.blockDim = dim3((unsigned)((a.splits >= 2 * kCombineGroups ? kCombineGroups : 1) * D), 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
