@@ -491,7 +491,7 @@ def run_profile_case(args) -> dict:
         att = ResAttnCase(torch, rs, *case[1], gen)
         us, _ = graph_time_us(torch, att.step, args.steps, reps=1, warm=args.warmup)
         assert rs.rs_get_device_error() == 0
-        return {"profile_case": args.profile_case, "us_per_call": round(us, 3), "launches_per_call": 3}
+        return {"profile_case": args.profile_case, "us_per_call": round(us, 3), "launches_per_call": 2}
     fmt, recipe, M, comp = case[:4]
     rs.rs_debug_pair_gemm(len(case) > 4 and case[4] == "pair")
     if comp == "kext1":

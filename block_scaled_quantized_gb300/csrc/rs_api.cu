@@ -423,13 +423,12 @@ bool attn_shape_ok(int B, int Hq, int Hkv, int D, int max_pages, int max_len) {
            max_pages >= 1 && max_len >= 0 && (int64_t)max_len <= (int64_t)max_pages * 32 &&
            (int64_t)B * Hq * 2 <= 0x7FFFFFFF;
 }
-size_t attn_q_bytes(int B, int Hq, int D) { return rs::align_up(rs::operand_bytes(RS_NVFP4, 2 * B * Hq, D), 1024); }
 }  // namespace
 
 size_t rs_resattn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len) {
     if (!attn_shape_ok(B, Hq, Hkv, D, (max_len + 31) / 32 + 1, max_len)) return 0;
     const int max_splits = max_len > 0 ? (max_len + 127) / 128 : 1;
-    return attn_q_bytes(B, Hq, D) + (size_t)B * Hkv * max_splits * (Hq / Hkv) * (D + 2) * sizeof(float);
+    return (size_t)B * Hkv * max_splits * (Hq / Hkv) * (D + 2) * sizeof(float);
 }
 
 int rs_resattn_split_tokens(int B, int Hkv, int D, int max_len, int num_sms) {
@@ -453,21 +452,15 @@ rs_status rs_resattn_decode(int B, int Hq, int Hkv, int D, int max_pages, int ma
     const rs::DeviceInfo* dev = rs::current_device(&why);
     if (!dev) return RS_ERR_CUDA;
     if (!dev->supported) return RS_ERR_UNSUPPORTED;
-    // the query-quantization step (Sec. 5.2): base and residue rows of Q
-    const int rows = B * Hq;
-    uint8_t* qop = static_cast<uint8_t*>(workspace);
-    if (launch_quantize(RS_NVFP4, true, rows, D, q_bf16, D, alpha_q, qop, (cudaStream_t)stream, dev->num_sms,
-                        /*pdl=*/true) != cudaSuccess)
-        return RS_ERR_CUDA;
+    // (the query-quantization step of Sec. 5.2 runs inside the split kernel)
     rs::AttnArgs a{};
-    a.q_op = qop;
-    a.q_sf = qop + operand_sf_offset(RS_NVFP4, 2 * rows, D);
+    a.q = static_cast<const uint16_t*>(q_bf16);
     a.alpha_q = alpha_q;
     a.k_cache = static_cast<const uint8_t*>(k_cache);
     a.v_cache = static_cast<const uint8_t*>(v_cache);
     a.block_table = block_table;
     a.seq_lens = seq_lens;
-    a.part = reinterpret_cast<float*>(qop + attn_q_bytes(B, Hq, D));
+    a.part = static_cast<float*>(workspace);
     a.err = dev->err;
     a.trace = rs::trace_buffer();
     a.B = B;
@@ -478,8 +471,6 @@ rs_status rs_resattn_decode(int B, int Hq, int Hkv, int D, int max_pages, int ma
     a.max_len = max_len;
     a.split_tokens = rs::resattn_split_tokens(B, Hkv, D, max_len, dev->num_sms);
     a.splits = max_len > 0 ? (max_len + a.split_tokens - 1) / a.split_tokens : 1;
-    a.q_rows_pad = (2 * rows + 127) / 128 * 128;
-    a.q_atoms_k = n_atoms_k_host(RS_NVFP4, D);
     return from_cuda(rs::launch_resattn(D, a, out, out_dtype == RS_OUT_F32 ? 1 : 0, (cudaStream_t)stream));
 }
 

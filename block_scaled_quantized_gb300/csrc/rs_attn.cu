@@ -8,24 +8,28 @@
 // One CTA per (split, KV head, sequence); tiles of 128 tokens (four pages):
 //   * warp 0 streams the tile's K and V pages with bulk copies into a ring
 //     of stages, ahead of the compute (pages taken from the block table);
+//   * the group's G query rows are quantized in the kernel (Alg. 1: base and
+//     residue rows with the call's tensor scale), straight into the QK operand;
 //   * warps 1-7 rearrange a landed stage in shared memory: K codes into the
 //     128-byte-swizzled rows of the MMA operand, K scales into atoms, and V
-//     from NVFP4 to E4M3 (R17) in its own token-major order (128 head
-//     dimensions per 128-byte-swizzled row);
+//     from NVFP4 to E4M3 (each dequantized element rounded to nearest-even,
+//     saturating) in its own token-major order (128 head dimensions per
+//     128-byte-swizzled row);
 //   * QK on the tensor cores: kind::mxf4nvf4, A = the key tile (M = 128
-//     tokens), B = the group's 2G <= 16 query rows (base 2g, residue 2g+1,
-//     from the paired quantizer), accumulator 128 x 16 fp32;
+//     tokens), B = the group's 2G <= 16 query rows (base 2g, residue 2g+1),
+//     accumulator 128 x 16 fp32;
 //   * fold and online softmax (warps 4-7, one token per thread):
 //     s_g = fl(fl(z_2g + z_2g+1) c), the tile maximum per head, p = exp(s - m)
-//     rounded to E4M3 (R18) and written as the PV operand P [head][token];
+//     rounded to E4M3 and written as the PV operand P [head][token];
 //   * PV on the tensor cores: kind::f8f6f4 (E4M3 x E4M3, fp32 accumulation),
 //     A = V^T read as an MN-major operand (M = 128 head dimensions per MMA,
 //     contiguous in each token row), B = P (N = 16), K = 128 tokens in four
 //     steps of 32 rows; warps 4-7 add the tile's accumulator into their
 //     running outputs after rescaling them by exp(m_old - m_new), and the
-//     normalizer sums the rounded weights (R18);
+//     normalizer sums the rounded weights;
 //   * the split's o, m, l go to a workspace; a second kernel combines the
-//     splits (R19) and writes bf16 or fp32.
+//     splits (O = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s) and writes
+//     bf16 or fp32.
 // Several CTAs share an SM (head size 128), so one CTA's rearranging and
 // softmax overlap another's MMAs and copies.  Every wait is bounded.
 #include <cuda_bf16.h>
@@ -96,7 +100,7 @@ __device__ __forceinline__ int attn_len(const AttnArgs& g, int b) {
     return L < 0 ? 0 : (L > g.max_len ? g.max_len : L);
 }
 
-// V from NVFP4 to E4M3 (R17).  The E4M3 value of s~ x dec(q) depends only
+// V from NVFP4 to E4M3 (each dequantized element rounded to nearest-even, saturating).  The E4M3 value of s~ x dec(q) depends only
 // on the block's scale byte and the code's magnitude, so each CTA first
 // builds lut[byte][m] = E4M3(s~(byte) x |dec(m)|), m = 0..7: the product of an
 // E4M3 and an E2M1 value has at most five significant bits and lies within
@@ -203,22 +207,35 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
     const int L = attn_len(g, b);
     const int t0 = split * g.split_tokens, t1 = min(L, t0 + g.split_tokens);
     const int ntiles = t1 > t0 ? (t1 - t0 + kAttnTile - 1) / kAttnTile : 0;
-    // the group's 2G query rows (zero rows up to 16), P all zero (rows >= G
-    // stay zero), the query scales in atoms
+    // The query-quantization step (Sec. 5.2) inside this kernel: the
+    // group's G query rows, one 16-element block per thread (Alg. 1: base,
+    // then residue with its own block scale and the same tensor scale), into
+    // rows 2g (base) and 2g + 1 (residue) of the QK operand and its scale
+    // atoms; every other byte zero (rows up to 16, head dimensions up to the
+    // 256-element chunk), P all zero (rows >= G stay zero).
     for (int i = threadIdx.x; i < 16 * 8; i += kAttnThreads) {
-        const int r = i / 8, c = i % 8;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        const int row = 2 * (b * g.Hq + h * G) + r;
-        if (r < 2 * G && c * 16 < CB) v = *reinterpret_cast<const uint4*>(g.q_op + (size_t)row * CB + c * 16);
-        *reinterpret_cast<uint4*>(qtile + sw128_offset((uint32_t)r, (uint32_t)c * 16u)) = v;
+        *reinterpret_cast<uint4*>(qtile + (size_t)i * 16) = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(ptile + (size_t)i * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
     for (int i = threadIdx.x; i < NA * 128; i += kAttnThreads) reinterpret_cast<uint32_t*>(qsf)[i] = 0u;
     __syncthreads();
-    for (int i = threadIdx.x; i < 2 * G * SB; i += kAttnThreads) {
-        const int r = i / SB, blk = i % SB;
-        const int row = 2 * (b * g.Hq + h * G) + r;
-        qsf[(blk / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + blk % 4] = g.q_sf[sf_offset(row, blk, g.q_atoms_k)];
+    {
+        const NvScaleConst qsc = nv_scale_const(*g.alpha_q);
+        if (threadIdx.x == 0 && split == 0 && h == 0 && b == 0 && !nv_alpha_supported(qsc.alpha))
+            atomicExch(g.err, kErrInvalidArg);
+        for (int i = threadIdx.x; i < G * SB; i += kAttnThreads) {
+            const int gq = i / SB, blk = i % SB;
+            const uint16_t* src = g.q + ((size_t)b * g.Hq + h * G + gq) * D + blk * 16;
+            const uint4 raw[2] = {*reinterpret_cast<const uint4*>(src), *reinterpret_cast<const uint4*>(src + 8)};
+            uint32_t sf, sfr, codes[2], rcodes[2];
+            quant_block_raw<0, 16, true>(raw, qsc, sf, codes, sfr, rcodes);
+            const uint32_t rb = 2u * (uint32_t)gq;
+            *reinterpret_cast<uint2*>(qtile + sw128_offset(rb, (uint32_t)blk * 8u)) = make_uint2(codes[0], codes[1]);
+            *reinterpret_cast<uint2*>(qtile + sw128_offset(rb + 1u, (uint32_t)blk * 8u)) =
+                make_uint2(rcodes[0], rcodes[1]);
+            qsf[(blk / 4) * 512 + rb * 16 + blk % 4] = (uint8_t)sf;
+            qsf[(blk / 4) * 512 + (rb + 1u) * 16 + blk % 4] = (uint8_t)sfr;
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -336,7 +353,7 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
                     if (i < kAttnTile * NA)
                         *reinterpret_cast<uint32_t*>(ksf + a * 512 + (rr % 32) * 16 + (rr / 32) * 4) = ks[j];
                 }
-                // V -> E4M3 (R17): token row t holds its head dimensions, 128 per tile
+                // V -> E4M3: token row t holds its head dimensions, 128 per tile
 #pragma unroll
                 for (int j = 0; j < NV; ++j) {
                     const int i = ct + j * kAttnCompute, t = i / SB, bb = i % SB;
@@ -485,8 +502,8 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
     }
 }
 
-// O = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s (R19); empty sequences give 0.
-// Split combination (R19), one CTA of P x D threads per (query head,
+// O = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s; empty sequences give 0.
+// Split combination, one CTA of P x D threads per (query head,
 // sequence), P = 4 groups when there are many splits and 1 otherwise: the
 // CTA's maximum M of the splits' m_s, then group p sums w_s o_s[d] and
 // w_s l_s over the splits s = p, p + P, ... (w_s = e^(m_s - M), four splits'

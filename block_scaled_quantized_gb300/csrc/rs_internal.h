@@ -141,8 +141,7 @@ cudaError_t launch_fold_pairs(const float* z, void* y, int M, int N, int out_f32
 
 // Residue-compensated decode attention (rs_attn.cu).
 struct AttnArgs {
-    const uint8_t* q_op;      // paired query operand of [B*Hq] rows (rows 2j base, 2j+1 residue), K = D
-    const uint8_t* q_sf;      // its scale atoms
+    const uint16_t* q;        // bf16 query [B][Hq][D]: each CTA quantizes its group's rows (Alg. 1)
     const float* alpha_q;     // query tensor scale (device)
     const uint8_t* k_cache;   // [pages][Hkv] page blocks
     const uint8_t* v_cache;
@@ -152,8 +151,6 @@ struct AttnArgs {
     uint32_t* err;
     uint64_t* trace;          // trace builds only: 32 timer stamps per CTA
     int B, Hq, Hkv, D, max_pages, max_len, split_tokens, splits;
-    int q_rows_pad;           // paired operand rows rounded to 128 (scale atoms)
-    int q_atoms_k;            // scale atoms per 128-row tile of the query operand
 };
 
 // Tokens per split of a ResAttn call, a multiple of the 128-token tile.

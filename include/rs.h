@@ -326,9 +326,9 @@ RS_API rs_status rs_linear_kext(rs_format fmt, int M, int N, int K, int k, const
  * lives in page block_table[b][t / 32] at row t % 32.  Unused entries of a
  * page are never read. */
 
-/* Workspace of rs_resattn_decode: the quantized query and the partial
- * outputs of the sequence splits (an upper bound for any device).  0 for a
- * shape rs_resattn_decode refuses. */
+/* Workspace of rs_resattn_decode: the partial outputs of the sequence splits
+ * (fp32 o, m and l per split and query head; an upper bound for any device).
+ * 0 for a shape rs_resattn_decode refuses. */
 RS_API size_t rs_resattn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len);
 
 /* Tokens per sequence split that rs_resattn_decode uses on a device with
@@ -341,7 +341,10 @@ RS_API int rs_resattn_split_tokens(int B, int Hkv, int D, int max_len, int num_s
 /* One decode step of ResAttn (Sec. 4.3 Eq. 3, Fig. 3; Sec. 5.2 "ResAttn
  * execution").  q_bf16 [B][Hq][D] (device, bf16) is quantized with Alg. 1
  * into base and residue rows with the tensor scale *alpha_q (device; e.g.
- * rs_compute_tensor_scale over Q); query head g reads KV head g / (Hq/Hkv).
+ * rs_compute_tensor_scale over Q) inside the attention kernel, each CTA its
+ * own query group (a tensor scale outside the supported range is reported as
+ * RS_ERR_INVALID_ARG by rs_get_device_error); query head g reads KV head
+ * g / (Hq/Hkv).
  * Scores s = (<Q^, K^> + <R^, K^>) alpha_q / sqrt(D) are folded in fp32
  * before an online softmax over 128-token tiles; V goes from NVFP4 to E4M3
  * on chip; the softmax weights are rounded to E4M3 for PV with fp32

@@ -163,10 +163,9 @@ def test_resattn_sizes_and_argument_checks(librs):
     f.argtypes = [ctypes.c_int] * 6 + [P] * 7 + [ctypes.c_int, P, ctypes.c_size_t, P]
     dummy = P(1 << 20)  # aligned, never dereferenced: every call fails validation first
     ok = (2, 8, 2, 128, 4, 128)
-    # workspace: quantized query (2*B*Hq rows of D) + partials of up to ceil(max_len/128) splits
+    # workspace: partials (o, m, l) of up to ceil(max_len/128) splits
     B, Hq, Hkv, D, L = 2, 8, 2, 128, 1000
-    q_bytes = (layout.operand_bytes(0, 2 * B * Hq, D) + 1023) // 1024 * 1024
-    assert librs.rs_resattn_workspace_bytes(B, Hq, Hkv, D, L) == q_bytes + B * Hkv * 8 * (Hq // Hkv) * (D + 2) * 4
+    assert librs.rs_resattn_workspace_bytes(B, Hq, Hkv, D, L) == B * Hkv * 8 * (Hq // Hkv) * (D + 2) * 4
     assert librs.rs_resattn_workspace_bytes(B, Hq, Hkv, 64, L) == 0      # head size
     assert librs.rs_resattn_workspace_bytes(B, 18, 2, D, L) == 0         # 9 query heads per KV head
     assert librs.rs_resattn_split_tokens(1, 8, 128, 4096, 152) % 128 == 0
