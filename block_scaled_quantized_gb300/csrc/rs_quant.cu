@@ -99,7 +99,7 @@ struct QuantArgs {
     int chunks;          // ceil(K / 256)
     int early_trigger;   // release the dependent grid once the prior grid is done
     uint32_t* err;       // device error word
-    // WEIGHT with a K-Ext extension (Eq. 6, reading R13): columns k_base..K-1
+    // WEIGHT with a K-Ext extension (Eq. 6; [W | W[:, S]] in bf16): columns k_base..K-1
     // are W[:, S] -- column k_base + g*kext_k + j is the j-th selected channel
     // of group g (kext_mask[g], device)
     int k_base;
