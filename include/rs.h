@@ -462,7 +462,8 @@ RS_API rs_status rs_get_device_error_async(uint32_t *out, rs_stream_t stream);
  * rs_linear_compensated (compensated != 0) or rs_linear_w4a4 makes with a
  * bf16 input and, when its plan quantizes inside the GEMM, also copies every
  * CTA's quantized activation slice to `dump` (device), as the MMAs read it.
- * layout (host, 7 ints) receives: fused (0/1), bn (rows of the activation
+ * layout (host, 7 ints) receives: fused (0 separate quantizer, 1 in the GEMM,
+ * 2 in the GEMM with CTA pairs sharing the slice; rs_set_tactic), bn (rows of the activation
  * tile), grid_x (CTAs per K split), splits, slots (chunk stages per CTA),
  * stage_bytes, chunks (256-element K chunks of the call).  The slice of the
  * CTA (x, split z) starts at byte (z * grid_x + x) * slots * stage_bytes;
