@@ -288,7 +288,9 @@ __global__ void __launch_bounds__(kAttnThreads, D == 128 ? 2 : 1) resattn_split_
             for (int q = 0; q < GM; ++q) o[mb][q] = 0.0f;
         float a_t[GM];  // this tile's rescale factors exp(m_old - m_new)
         if (warp == 1) {
-            if (elect_one_sync())
+            // (only with tiles to process: every copy must be complete, through the
+            // last PV commit that warps 4-7 wait for, before the tensor memory is freed)
+            if (ntiles > 0 && elect_one_sync())
                 for (int a = 0; a < NA; ++a) tc_cp_sf_atom(t_sfq + a * 4, sf_atom_desc(smem_u32(qsf + a * 512)));
             __syncwarp();
         }
