@@ -230,11 +230,11 @@ int rs_plan_linear(rs_format fmt, int compensated, int M, int N, int K, int num_
 }
 
 rs_status rs_set_tactic(rs_format fmt, int compensated, int M, int N, int K, int num_sms, int splits, int fused,
-                        int bn) {
+                        int bn, int deep) {
     if (!fmt_ok(fmt) || M < 1 || N < 1 || num_sms < 1) return RS_ERR_INVALID_ARG;
     if (!k_ok(K)) return RS_ERR_SHAPE;
-    return set_tactic(fmt, compensated != 0, M, N, K, num_sms, Tactic{splits, fused, bn}) ? RS_OK
-                                                                                         : RS_ERR_INVALID_ARG;
+    return set_tactic(fmt, compensated != 0, M, N, K, num_sms, Tactic{splits, fused, bn, deep}) ? RS_OK
+                                                                                               : RS_ERR_INVALID_ARG;
 }
 
 rs_status rs_reset_tactics(int builtin) {

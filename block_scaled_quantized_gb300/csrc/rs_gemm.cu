@@ -1083,8 +1083,10 @@ static size_t plan_smem(int fmt, int bn, int stages, bool fused, int slots, size
 // a fused plan lets CTA pairs share the quantization of their K slice (only
 // on a measured tactic's request: on GB300 the remote stores and the wider
 // clusters cost more than the halved quantizer saves for every shape tuned).
+// deep: a split plan whose CTAs take one tile each keeps its deepest weight
+// ring instead of the shallower one that lets two CTAs share an SM.
 static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms, int s, bool allow_fused,
-                                int bn_min = 16, bool pair_ok = false) {
+                                int bn_min = 16, bool pair_ok = false, bool deep = false) {
     GemmPlan p{};
     p.fmt = fmt;
     p.fold = fold ? 1 : 0;
@@ -1139,7 +1141,7 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
     // two, and the rest wait for a second wave.  A split plan whose CTAs take
     // one tile each keeps three stages (or all its units) when that lets two
     // CTAs share an SM; plans that stream several tiles keep the deep ring.
-    if (s > 1 && ntl == 1) {
+    if (s > 1 && ntl == 1 && !deep) {
         const int floor_st = std::min(3, nu);
         while (stages > floor_st &&
                plan_smem(fmt, p.bn, stages, fused, fused ? max_chunks : 0, splitbuf, nacc, partbuf) > kSmemLimit / 2 &&
@@ -1234,7 +1236,8 @@ GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bo
     Tactic t;
     if (num_sms > 0 && find_tactic(fmt, fold, M, N, K, num_sms, &t) && t.splits <= (K + 255) / 256) {
         const GemmPlan q =
-            plan_for_splits(fmt, fold, M, N, K, num_sms, t.splits, allow_fused && t.fused, t.bn, t.fused == 2);
+            plan_for_splits(fmt, fold, M, N, K, num_sms, t.splits, allow_fused && t.fused, t.bn, t.fused == 2,
+                            t.deep != 0);
         if (q.stages > 0) {
             p = q;
             p.tuned = 1;

@@ -72,6 +72,7 @@ struct Tactic {
     int splits;  // 1..kMaxSplits
     int fused;   // 0: separate quantizer; 1: in the GEMM; 2: in the GEMM, shared by CTA pairs
     int bn;      // 16, 32, 64, 128 or 256
+    int deep;    // 1: split plans keep their deepest weight ring (one CTA per SM)
 };
 // Install (replace) the tactic of (fmt, fold, M, N, K, num_sms); false on an
 // out-of-range field.  Thread-safe.

@@ -1,8 +1,9 @@
 // Layout autotuning (ResServe Sec. 5.1 and Fig. 3): per-shape launch tactics
 // chosen by measurement instead of the planner's cost rules.
 //
-// A tactic fixes three choices of a linear call's plan -- the K-split count,
-// in-GEMM quantization of a bf16 input, and the MMA width -- for one
+// A tactic fixes four choices of a linear call's plan -- the K-split count,
+// in-GEMM quantization of a bf16 input, the MMA width and the weight ring
+// depth of split plans -- for one
 // (format, compensated, M, N, K) on a GPU with a given SM count.  The
 // library ships the table measured on GB300 (rs_tactics_gb300.inc, written by
 // block_scaled_quantized_gb300/tune.py, which times every candidate plan of
@@ -28,7 +29,7 @@ struct Entry {
 };
 
 struct BuiltinRow {
-    int fmt, fold, M, N, K, sms, splits, fused, bn;
+    int fmt, fold, M, N, K, sms, splits, fused, bn, deep;
 };
 
 const BuiltinRow kBuiltin[] = {
@@ -41,7 +42,7 @@ bool g_loaded = false;
 
 bool valid(const Tactic& t) {
     return t.splits >= 1 && t.splits <= kMaxSplits && t.fused >= 0 && t.fused <= 2 &&
-           (t.bn == 16 || t.bn == 32 || t.bn == 64 || t.bn == 128 || t.bn == 256);
+           (t.bn == 16 || t.bn == 32 || t.bn == 64 || t.bn == 128 || t.bn == 256) && (t.deep == 0 || t.deep == 1);
 }
 
 void put_locked(int fmt, int fold, int M, int N, int K, int sms, const Tactic& t) {
@@ -56,7 +57,7 @@ void put_locked(int fmt, int fold, int M, int N, int K, int sms, const Tactic& t
 void load_builtin_locked() {
     g_table.clear();
     for (const BuiltinRow& r : kBuiltin) {
-        const Tactic t{r.splits, r.fused, r.bn};
+        const Tactic t{r.splits, r.fused, r.bn, r.deep};
         if (valid(t)) put_locked(r.fmt, r.fold, r.M, r.N, r.K, r.sms, t);
     }
     g_loaded = true;

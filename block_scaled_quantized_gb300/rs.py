@@ -80,7 +80,7 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
         "rs_resattn_workspace_bytes": ([I, I, I, I, I], SZ),
         "rs_resattn_split_tokens": ([I, I, I, I, I], I),
         "rs_debug_pair_gemm": ([I], None),
-        "rs_set_tactic": ([I, I, I, I, I, I, I, I, I], I),
+        "rs_set_tactic": ([I, I, I, I, I, I, I, I, I, I], I),
         "rs_reset_tactics": ([I], I),
         "rs_tactic_count": ([], I),
         "rs_resattn_decode": ([I, I, I, I, I, I, P, P, P, P, P, P, P, I, P, SZ, P], I),
@@ -252,10 +252,10 @@ def rs_debug_pair_gemm(enable: bool):
 
 
 def rs_set_tactic(fmt: int, compensated: bool, M: int, N: int, K: int, num_sms: int, splits: int, fused: int,
-                  bn: int):
+                  bn: int, deep: int = 0):
     """Install a measured launch tactic for one shape (see rs.h)."""
     _check("rs_set_tactic", lib().rs_set_tactic(fmt, int(bool(compensated)), M, N, K, num_sms, splits,
-                                                int(fused), bn))
+                                                int(fused), bn, int(deep)))
 
 
 def rs_reset_tactics(builtin: bool = True):

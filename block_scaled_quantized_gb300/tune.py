@@ -2,9 +2,10 @@
 
 The paper selects a kernel layout per (M, N, K) by measuring the candidates.
 This script does that for librs's launch tactics -- K-split count, in-GEMM
-quantization of the bf16 input, and MMA width (see rs_set_tactic in
-include/rs.h) -- on the GPU it runs on, and writes the winners as the C table
-that librs compiles in (csrc/rs_tactics_gb300.inc), keyed by the GPU's SM count.
+quantization of the bf16 input, MMA width and the weight ring depth of split
+plans (see rs_set_tactic in include/rs.h) -- on the GPU it runs on, and
+writes the winners as the C table that librs compiles in
+(csrc/rs_tactics_gb300.inc), keyed by the GPU's SM count.
 
 Each candidate runs through the public entry points (rs_linear_w4a4 /
 rs_linear_compensated with a bf16 input), captured `steps` calls at a time in a
@@ -74,7 +75,8 @@ def candidates(M: int, K: int, compensated: bool):
     for bn in bns:
         for splits in range(1, min(8, chunks) + 1):
             for fused in ((2, 1, 0) if bn <= 32 else (0,)):
-                yield splits, fused, bn
+                for deep in ((0, 1) if splits > 1 else (0,)):
+                    yield splits, fused, bn, deep
 
 
 class Shape:
@@ -146,14 +148,14 @@ def plan_key(fmt, compensated, M, N, K, sms):
 
 
 def analytic_tactic(fmt, compensated, M, N, K, sms):
-    """(splits, fused, bn) of the analytic plan (host only)."""
+    """(splits, fused, bn, deep) of the analytic plan (host only)."""
     rs.rs_reset_tactics(False)
     p = rs.rs_plan_linear(fmt, compensated, M, N, K, sms)
-    return p["splits"], p["fused"], p["bn"]
+    return p["splits"], p["fused"], p["bn"], 0
 
 
 def tune_one(shape: Shape, M: int, compensated: bool, sms: int, margin: float):
-    """Tactic for one (shape, M, compensated): ((splits, fused, bn), its us,
+    """Tactic for one (shape, M, compensated): ((splits, fused, bn, deep), its us,
     analytic us, plans timed, whether the analytic plan was kept)."""
     fmt, N, K = shape.fmt, shape.N, shape.K
     steps = 32 if M <= 512 else 8
@@ -164,9 +166,9 @@ def tune_one(shape: Shape, M: int, compensated: bool, sms: int, margin: float):
     base_us = time_calls(shape, M, compensated, inp, steps, reps)
     seen = {base_key: base_us}
     best, best_us = None, base_us
-    for splits, fused, bn in candidates(M, K, compensated):
+    for splits, fused, bn, deep in candidates(M, K, compensated):
         rs.rs_reset_tactics(False)
-        rs.rs_set_tactic(fmt, compensated, M, N, K, sms, splits, fused, bn)
+        rs.rs_set_tactic(fmt, compensated, M, N, K, sms, splits, fused, bn, deep)
         p = rs.rs_plan_linear(fmt, compensated, M, N, K, sms)
         if not p["tuned"]:
             continue  # the tactic's plan does not fit
@@ -176,7 +178,7 @@ def tune_one(shape: Shape, M: int, compensated: bool, sms: int, margin: float):
         us = time_calls(shape, M, compensated, inp, steps, reps)
         seen[key] = us
         if us < best_us:
-            best, best_us = (splits, p["fused"], p["bn"]), us
+            best, best_us = (splits, p["fused"], p["bn"], deep), us
     kept = best is None or best_us > base_us * (1.0 - margin)
     if kept:
         best, best_us = analytic_tactic(fmt, compensated, M, N, K, sms), base_us
@@ -186,19 +188,19 @@ def tune_one(shape: Shape, M: int, compensated: bool, sms: int, margin: float):
 
 def write_table(path: str, sms: int, rows: list):
     lines = ["// Measured launch tactics for GB300 (%d SMs): {fmt, compensated, M, N, K," % sms,
-             "// SMs, splits, fused, bn}, each with the measured us per call of the tactic",
-             "// and of the analytic plan.  Written by block_scaled_quantized_gb300/tune.py.",
-             "{0, 1, 0, 0, 0, 0, 0, 0, 0},  // placeholder row (M = 0 never matches)"]
+             "// SMs, splits, fused, bn, deep}, each with the measured us per call of the",
+             "// tactic and of the analytic plan.  Written by block_scaled_quantized_gb300/tune.py.",
+             "{0, 1, 0, 0, 0, 0, 0, 0, 0, 0},  // placeholder row (M = 0 never matches)"]
     for (fmt, comp, M, N, K, t, us, base, kept) in rows:
         note = "analytic plan" if kept else "analytic plan %.3f us" % base
-        lines.append("{%d, %d, %d, %d, %d, %d, %d, %d, %d},  // %.3f us (%s)"
-                     % (fmt, comp, M, N, K, sms, t[0], t[1], t[2], us, note))
+        lines.append("{%d, %d, %d, %d, %d, %d, %d, %d, %d, %d},  // %.3f us (%s)"
+                     % (fmt, comp, M, N, K, sms, t[0], t[1], t[2], t[3], us, note))
     with open(path, "w") as f:
         f.write("\n".join(lines) + "\n")
 
 
 LOG_LINE = re.compile(r"fmt=(\d) comp=(\d) M=(\d+) N=(\d+) K=(\d+) sms=(\d+): analytic ([\d.]+) us, "
-                      r"best ([\d.]+) us \((\d+), (\d), (\d+)\)( analytic)?")
+                      r"best ([\d.]+) us \((\d+), (\d), (\d+)(?:, (\d))?\)( analytic)?")
 
 
 def rows_from_log(path):
@@ -209,8 +211,8 @@ def rows_from_log(path):
             continue
         fmt, comp, M, N, K, sms = (int(v) for v in m.groups()[:6])
         base, us = float(m.group(7)), float(m.group(8))
-        t = tuple(int(v) for v in m.groups()[8:11])
-        rows.append((fmt, comp, M, N, K, t, us, base, m.group(12) is not None))
+        t = tuple(int(v) for v in m.groups()[8:11]) + (int(m.group(12) or 0),)
+        rows.append((fmt, comp, M, N, K, t, us, base, m.group(13) is not None))
     return sms, rows
 
 
@@ -238,7 +240,7 @@ def main(argv=None):
             for comp in (False, True):
                 t, us, base, n, kept = tune_one(shape, M, comp, sms, a.margin)
                 line = (f"fmt={fmt} comp={int(comp)} M={M} N={N} K={K} sms={sms}: analytic {base:.3f} us, "
-                        f"best {us:.3f} us ({t[0]}, {t[1]}, {t[2]}){' analytic' if kept else ''} over {n} plans")
+                        f"best {us:.3f} us ({t[0]}, {t[1]}, {t[2]}, {t[3]}){' analytic' if kept else ''} over {n} plans")
                 print(line, flush=True)
                 log.append(line)
                 rows.append((fmt, int(comp), M, N, K, t, us, base, kept))

@@ -157,11 +157,15 @@ RS_API int rs_plan_linear(rs_format fmt, int compensated, int M, int N, int K, i
 
 /* The paper picks a kernel layout per (M, N, K) by measurement.  Here a
  * tactic fixes, for one (fmt, compensated, M, N, K) on a GPU with num_sms
- * SMs: the K-split count (1..8, the cluster size), whether a bf16 input may
- * be quantized inside the GEMM (fused, 0/1; only plans whose activation
- * tile is at most 32 rows can), and the MMA width bn (16, 32, 64, 128 or
- * 256; a width below what the activation rows need is raised to it, a wider
- * one pads the operand with zero rows).  A linear call of M rows takes the
+ * SMs: the K-split count (1..8, the cluster size); whether a bf16 input may
+ * be quantized inside the GEMM (fused: 0 no, 1 yes, 2 yes with CTA pairs
+ * sharing the quantization of a K slice; only plans whose activation tile
+ * is at most 32 rows can); the MMA width bn (16, 32, 64, 128 or 256; a
+ * width below what the activation rows need is raised to it, a wider one
+ * pads the operand with zero rows); and deep (0/1: a split plan whose CTAs
+ * take one output tile each keeps the deepest weight ring that fits, one
+ * CTA per SM, instead of the 3-stage ring that lets two CTAs share an SM).
+ * A linear call of M rows takes the
  * tactic of the same fmt, compensated, N, K and SM count with the smallest
  * tuned M' >= M; its plan replaces the analytic one when it fits the SM's
  * shared and tensor memory and splits <= ceil(K/256), else the analytic plan
@@ -172,7 +176,7 @@ RS_API int rs_plan_linear(rs_format fmt, int compensated, int M, int N, int K, i
  * graphs already captured).  RS_ERR_INVALID_ARG for a field out of range,
  * RS_ERR_SHAPE unless K % 32 == 0. */
 RS_API rs_status rs_set_tactic(rs_format fmt, int compensated, int M, int N, int K, int num_sms, int splits,
-                               int fused, int bn);
+                               int fused, int bn, int deep);
 /* builtin != 0: restore the shipped table (dropping rs_set_tactic entries);
  * builtin == 0: remove every tactic, so that every call uses the analytic plan. */
 RS_API rs_status rs_reset_tactics(int builtin);

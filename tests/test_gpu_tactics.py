@@ -54,6 +54,31 @@ def test_forced_tactic_parity(fmt, compensated, M, N, K, splits, fused, bn):
         rs.rs_reset_tactics(True)
 
 
+# deep weight rings (M, N, K, splits, fused, bn): some wrap the ring several times
+DEEP = [(8, 640, 8192, 4, 1, 16), (3, 384, 6144, 3, 0, 32), (1, 768, 12288, 2, 0, 16),
+        (16, 256, 8192, 6, 1, 16), (5, 1024, 4096, 3, 0, 16)]
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("compensated", [False, True])
+@pytest.mark.parametrize("M,N,K,splits,fused,bn", DEEP)
+def test_deep_tactic_parity(fmt, compensated, M, N, K, splits, fused, bn):
+    rs.rs_reset_tactics(False)
+    try:
+        rs.rs_set_tactic(fmt, compensated, M, N, K, sms(), splits, fused, bn, 0)
+        shallow = rs.rs_plan_linear(fmt, compensated, M, N, K, sms())
+        rs.rs_set_tactic(fmt, compensated, M, N, K, sms(), splits, fused, bn, 1)
+        plan = rs.rs_plan_linear(fmt, compensated, M, N, K, sms())
+        assert plan["tuned"] == 1 and plan["splits"] == splits and plan["stages"] >= shallow["stages"]
+        x = workloads.make_x("gauss_outlier_k2048", M, K=K, seed=M * 7 + K)
+        w = workloads.make_w("gauss_outlier_k2048", N=N, K=K, seed=N + 3 * K)
+        wp = prepare_weight(fmt, w)
+        y, _ = gpu_linear(fmt, compensated, x, wp)
+        assert_close_f32(y, oracle_linear(fmt, compensated, x, wp))
+    finally:
+        rs.rs_reset_tactics(True)
+
+
 def shipped_cases(limit):
     """Shipped table entries for this GPU, small enough for the oracle at full
     size, spread over split counts and widths."""
@@ -61,7 +86,7 @@ def shipped_cases(limit):
     path = rs.__file__.replace("rs.py", "csrc/rs_tactics_gb300.inc")
     rows = []
     for line in open(path):
-        m = re.match(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\}", line)
+        m = re.match(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\}", line)
         if m:
             v = [int(t) for t in m.groups()]
             if v[2] > 0 and v[5] == sms() and v[2] <= 16 and v[3] * v[4] <= 40_000_000:
@@ -80,7 +105,7 @@ def test_shipped_tactics_full_size():
     if not cases:
         pytest.skip("no shipped tactics for this GPU's SM count")
     rs.rs_reset_tactics(True)
-    for fmt, comp, M, N, K, _, splits, fused, bn in cases:
+    for fmt, comp, M, N, K, _, splits, fused, bn, deep in cases:
         plan = rs.rs_plan_linear(fmt, comp, M, N, K, sms())
         assert plan["tuned"] == 1 and plan["splits"] == splits
         x = workloads.make_x("proj_shapes", M, K=K, seed=M + N)

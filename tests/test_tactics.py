@@ -75,7 +75,8 @@ def test_tactics_that_do_not_fit_fall_back():
     assert {k: v for k, v in plan(0, True, 8, 1024, 512).items()} == base
 
 
-@pytest.mark.parametrize("fields", [(0, 0, 16), (9, 0, 16), (2, 3, 16), (2, -1, 16), (2, 0, 48), (2, 0, 512)])
+@pytest.mark.parametrize("fields", [(0, 0, 16, 0), (9, 0, 16, 0), (2, 3, 16, 0), (2, -1, 16, 0), (2, 0, 48, 0),
+                                    (2, 0, 512, 0), (2, 0, 16, 2), (2, 0, 16, -1)])
 def test_out_of_range_tactics_are_refused(fields):
     assert rs.lib().rs_set_tactic(0, 1, 8, 4096, 4096, SMS, *fields) == rs.RS_ERR_INVALID_ARG
     assert rs.rs_tactic_count() == 0
@@ -83,10 +84,10 @@ def test_out_of_range_tactics_are_refused(fields):
 
 def test_argument_checks():
     lib = rs.lib()
-    assert lib.rs_set_tactic(2, 1, 8, 4096, 4096, SMS, 1, 0, 16) == rs.RS_ERR_INVALID_ARG
-    assert lib.rs_set_tactic(0, 1, 0, 4096, 4096, SMS, 1, 0, 16) == rs.RS_ERR_INVALID_ARG
-    assert lib.rs_set_tactic(0, 1, 8, 4096, 4100, SMS, 1, 0, 16) == rs.RS_ERR_SHAPE
-    assert lib.rs_set_tactic(0, 1, 8, 4096, 4096, 0, 1, 0, 16) == rs.RS_ERR_INVALID_ARG
+    assert lib.rs_set_tactic(2, 1, 8, 4096, 4096, SMS, 1, 0, 16, 0) == rs.RS_ERR_INVALID_ARG
+    assert lib.rs_set_tactic(0, 1, 0, 4096, 4096, SMS, 1, 0, 16, 0) == rs.RS_ERR_INVALID_ARG
+    assert lib.rs_set_tactic(0, 1, 8, 4096, 4100, SMS, 1, 0, 16, 0) == rs.RS_ERR_SHAPE
+    assert lib.rs_set_tactic(0, 1, 8, 4096, 4096, 0, 1, 0, 16, 0) == rs.RS_ERR_INVALID_ARG
 
 
 def test_reset_restores_the_shipped_table():
@@ -104,7 +105,7 @@ def shipped_rows():
     path = rs.__file__.replace("rs.py", "csrc/rs_tactics_gb300.inc")
     rows = []
     for line in open(path):
-        m = re.match(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\}", line)
+        m = re.match(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\}", line)
         if m:
             rows.append(tuple(int(t) for t in m.groups()))
     return [r for r in rows if r[2] > 0]
@@ -115,7 +116,7 @@ def test_every_shipped_tactic_gives_its_plan():
     rows = shipped_rows()
     assert rs.rs_tactic_count() == len(rows)
     keys = set()
-    for fmt, comp, M, N, K, sms, splits, fused, bn in rows:
+    for fmt, comp, M, N, K, sms, splits, fused, bn, deep in rows:
         assert (fmt, comp, M, N, K, sms) not in keys
         keys.add((fmt, comp, M, N, K, sms))
         p = plan(fmt, comp, M, N, K, sms)
@@ -130,13 +131,13 @@ def test_candidate_set_contains_the_analytic_plan():
         for M in Ms:
             for comp in (False, True):
                 p = plan(fmt, comp, M, N, K)
-                assert (p["splits"], p["fused"], p["bn"]) in set(tune.candidates(M, K, comp)), (fmt, N, K, M, comp)
+                assert (p["splits"], p["fused"], p["bn"], 0) in set(tune.candidates(M, K, comp)), (fmt, N, K, M, comp)
 
 
 def test_no_plan_lets_two_ctas_share_more_than_the_tensor_memory():
-    for s, f, bn in tune.candidates(8, 4096, True):
+    for s, f, bn, deep in tune.candidates(8, 4096, True):
         rs.rs_reset_tactics(False)
-        rs.rs_set_tactic(0, True, 8, 4096, 4096, SMS, s, f, bn)
+        rs.rs_set_tactic(0, True, 8, 4096, 4096, SMS, s, f, bn, deep)
         p = plan(0, True, 8, 4096, 4096)
         if p["tmem_cols"] > 256:
             assert p["smem_bytes"] > 232448 // 2
@@ -149,13 +150,13 @@ def test_rows_that_kept_the_analytic_plan_reproduce_it():
     path = rs.__file__.replace("rs.py", "csrc/rs_tactics_gb300.inc")
     n = 0
     for line in open(path):
-        m = re.match(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\},.*\(analytic plan\)", line)
+        m = re.match(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\},.*\(analytic plan\)", line)
         if not m:
             continue
-        fmt, comp, M, N, K, sms, splits, fused, bn = (int(v) for v in m.groups())
+        fmt, comp, M, N, K, sms, splits, fused, bn, deep = (int(v) for v in m.groups())
         rs.rs_reset_tactics(False)
         a = plan(fmt, comp, M, N, K, sms)
-        rs.rs_set_tactic(fmt, comp, M, N, K, sms, splits, fused, bn)
+        rs.rs_set_tactic(fmt, comp, M, N, K, sms, splits, fused, bn, deep)
         t = plan(fmt, comp, M, N, K, sms)
         assert {**a, "tuned": 1} == t, (fmt, comp, M, N, K)
         n += 1
@@ -170,6 +171,26 @@ def test_every_tuned_case_has_its_own_row():
         for M in Ms:
             for comp in (0, 1):
                 assert (fmt, comp, M, N, K) in rows, (fmt, comp, M, N, K)
+
+
+def test_deep_tactic_keeps_the_deep_ring_of_a_split_plan():
+    """deep = 1: a split plan whose CTAs take one tile each keeps the deepest
+    weight ring that fits (one CTA per SM) instead of the shallow ring that
+    lets two CTAs share an SM; plans without that cap are unchanged."""
+    rs.rs_set_tactic(0, False, 1, 5120, 25600, SMS, 3, 0, 16, 0)
+    shallow = plan(0, False, 1, 5120, 25600)
+    rs.rs_set_tactic(0, False, 1, 5120, 25600, SMS, 3, 0, 16, 1)
+    deep = plan(0, False, 1, 5120, 25600)
+    assert shallow["tuned"] == deep["tuned"] == 1
+    assert deep["stages"] > shallow["stages"] and shallow["smem_bytes"] <= 232448 // 2 < deep["smem_bytes"]
+    assert deep["smem_bytes"] <= 232448
+    same = ("bn", "n_tiles", "b_tiles", "chunks", "splits", "grid_x", "fused", "slots", "nacc")
+    assert all(deep[k] == shallow[k] for k in same)
+    for t in ((1, 0, 16), (4, 1, 16)):  # one split; a fused ring already past half the SM
+        rs.rs_set_tactic(0, False, 1, 4096, 14336, SMS, *t, 0)
+        p0 = plan(0, False, 1, 4096, 14336)
+        rs.rs_set_tactic(0, False, 1, 4096, 14336, SMS, *t, 1)
+        assert plan(0, False, 1, 4096, 14336) == p0 and p0["tuned"] == 1
 
 
 def test_pair_tactic_pairs_only_where_the_grid_allows():
