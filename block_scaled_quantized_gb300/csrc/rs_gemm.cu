@@ -73,7 +73,12 @@ constexpr int kQuantThreads = kQuantWarps * 32;
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;   // 227 KB opt-in per block
 constexpr uint32_t kCtrlBytes = 2048;  // barriers and flags, then the fused NVFP4 scale table (1 KB)
-constexpr int kMaxChunkBars = 32;   // fused plans: one "quantized" mbarrier per resident chunk
+constexpr int kMaxChunkBars = 64;   // fused plans: one "quantized" mbarrier per resident chunk
+// barriers (full, empty: kMaxStages each; accumulator, reduction and receive
+// pairs; the chunk barriers; the amax barrier), then the amax slots, the
+// tensor-memory slot and the flags: all before the scale table's 1 KB
+static_assert((2 * kMaxStages + 8 + kMaxChunkBars + 1) * 8 + (kMaxSplits + 1 + 5) * 4 <= 1024,
+              "control words overlap the scale table");
 
 __host__ __device__ constexpr int b_atom_tiles(int bn) { return (bn + 127) / 128; }
 // Split-K exchange of a tile with `outs` outputs per channel.  Narrow tiles
@@ -1132,7 +1137,9 @@ static GemmPlan plan_for_splits(int fmt, bool fold, int M, int N, int K, int sms
             stages = st1;
         }
     }
-    if (fused && stages == 0) {
+    // a resident slice that leaves the weight ring fewer than three stages
+    // starves the MMAs: quantize in a separate launch then
+    if (fused && stages < std::min(3, nu)) {
         fused = false;
         stages = best_stages(false, nacc);
     }

@@ -180,6 +180,39 @@ def test_fused_slices_bit_exact(fmt, compensated, M, N, K, recipe, own_scale, pr
     check_slices(fmt, lay, dump, codes, sf, K)
 
 
+# slices of more than 32 chunks (up to the shared memory's limit) and ragged
+# K tails, forced by tactics: (fmt, compensated, M, N, K, recipe, splits, fused)
+LONG_CASES = [
+    (0, True, 4, 384, 16640, "gauss_outlier_k2048", 2, 1),     # 33 chunks per slice
+    (0, False, 1, 5120, 25600, "proj_shapes", 3, 1),           # 34
+    (1, True, 3, 256, 12320, "gauss_outlier_k2048", 1, 1),     # 49, ragged tail
+    (0, False, 5, 768, 12320, "gauss_outlier_k2048", 2, 2),    # CTA pairs, ragged tail
+    (1, False, 8, 512, 12320, "gauss_outlier_k2048", 2, 2),
+]
+
+
+@pytest.mark.parametrize("fmt,compensated,M,N,K,recipe,splits,fused", LONG_CASES)
+def test_fused_long_slices_bit_exact(fmt, compensated, M, N, K, recipe, splits, fused):
+    import oracle
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rs.rs_reset_tactics(False)
+    try:
+        rs.rs_set_tactic(fmt, compensated, M, N, K, sms, splits, fused, 16, 1)
+        lay = rs.rs_debug_linear_dump(fmt, compensated, M, N, K)
+        assert lay["fused"] == fused and lay["splits"] == splits
+        assert lay["slots"] == (lay["chunks"] + splits - 1) // splits
+        x = workloads.make_x(recipe, M, K=K, seed=M * 13 + K)
+        xb = workloads.bf16_bits(x)
+        ax = oracle.tensor_scale(xb) if fmt == 0 else np.float32(0)
+        wq, aw = make_weight(fmt, N, K, seed=N + 2 * K)
+        ax_dev = torch.tensor([ax], dtype=torch.float32, device=DEV) if fmt == 0 else None
+        lay, dump = run_dump(fmt, compensated, x, wq, aw, N, ax_dev)
+        codes, sf = oracle_rows(fmt, compensated, xb, ax)
+        check_slices(fmt, lay, dump, codes, sf, K)
+    finally:
+        rs.rs_reset_tactics(True)
+
+
 def test_dump_layout_query_and_refusals():
     # layout only (no launch) and the documented refusals
     lay = rs.rs_debug_linear_dump(0, True, 8, 4096, 4096)

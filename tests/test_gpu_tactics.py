@@ -31,7 +31,8 @@ def sms():
 FORCED = [(5, 384, 1024, 1, 1, 32), (5, 384, 1024, 3, 1, 32), (5, 384, 1024, 4, 0, 64),
           (8, 640, 2048, 8, 1, 32), (8, 640, 2048, 8, 0, 16), (8, 640, 2048, 2, 0, 128),
           (3, 200, 1280, 5, 1, 16), (16, 256, 2304, 6, 0, 64), (30, 384, 512, 2, 0, 256),
-          (64, 256, 1024, 4, 0, 256), (100, 130, 768, 3, 0, 256)]
+          (64, 256, 1024, 4, 0, 256), (100, 130, 768, 3, 0, 256),
+          (4, 384, 16640, 2, 1, 16), (3, 256, 12320, 1, 1, 16)]  # fused slices of 33 and 49 chunks
 
 
 @pytest.mark.parametrize("fmt", [0, 1])

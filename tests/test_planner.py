@@ -56,7 +56,7 @@ def test_plan_limits(sms, fmt, comp, x_in_call):
             assert p["tmem_cols"] <= 256, where
         if p["fused"]:
             assert x_in_call and p["b_tiles"] == 1 and p["bn"] <= 32, where
-            assert p["slots"] == (p["chunks"] + p["splits"] - 1) // p["splits"] <= 32, where
+            assert p["slots"] == (p["chunks"] + p["splits"] - 1) // p["splits"] <= 64, where
         else:
             assert p["slots"] == 0, where
 
