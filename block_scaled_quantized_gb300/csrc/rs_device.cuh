@@ -463,6 +463,36 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Store 8 / 16 consecutive 32-bit columns of this warp's 32 tensor-memory
+// lanes (thread l: lane l of the warp's quarter, register c: column taddr + c).
+// Asynchronous: tmem_st_wait() before another thread may read the columns.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+// N (8, 16 or 32) consecutive columns from registers.
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+    static_assert(N == 8 || N % 16 == 0, "8 or a multiple of 16 columns");
+    if constexpr (N == 8) {
+        tmem_st8(taddr, r);
+    } else {
+#pragma unroll
+        for (int h = 0; h < N / 16; ++h)
+            tmem_st16(taddr + (uint32_t)(16 * h), *reinterpret_cast<const uint32_t(*)[16]>(&r[16 * h]));
+    }
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // --------------------------------------------------- clusters and DSMEM --
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -16,11 +16,13 @@
 //    activation operand, or, for small M, from a quantizing prologue that
 //    converts the CTA's slice of the bf16 input straight into shared memory
 //    (Alg. 1 fused into the GEMM: one launch per linear layer);
-//  * scale atoms go shared memory -> tensor memory with tcgen05.cp
+//  * scale atoms go shared memory -> tensor memory, where the
+//    kind::mxf4nvf4 block-scaled MMA reads them: with tcgen05.cp
 //    (32x128b.warpx4, issued by the MMA warp ahead of the MMAs that read
-//    them), where the kind::mxf4nvf4 block-scaled MMA reads them; in fused
-//    plans the weight atoms of the prefetched stages are copied before the
-//    dependency wait.
+//    them; in fused plans the weight atoms of the prefetched stages are
+//    copied before the dependency wait), or, for 128- and 256-row activation
+//    tiles, with tcgen05.st from four scale warps, which keeps the copies out
+//    of the tensor pipe.
 //
 // Fold (Sec. 4.3 Eq. 2): with paired rows, the base and residue products of
 // token j are accumulator columns 2j and 2j+1; a 32x32b tensor-memory load
@@ -52,7 +54,9 @@
 // Warp roles (384 threads): warp 4 bulk/TMA producer; warp 5 TMEM allocator,
 // scale copies and MMA issuer; warps 8-11 (lane quarters 0-3) run the
 // epilogue, with warps 0-3 for wide tiles without split-K; in fused plans
-// warps 0-3 and 6-11 first run the quantizing prologue.  Every wait is
+// warps 0-3 and 6-11 first run the quantizing prologue.  Kernels for 128-
+// and 256-row activation tiles have 448 threads: warps 12, 13, 6 and 7 move
+// the scale atoms, and warp 5 only issues MMAs.  Every wait is
 // bounded (about one second); a wait that runs out sets the device error
 // word and an abort flag, and the CTA drains its copies and exits.
 #include <cuda.h>
@@ -68,6 +72,14 @@
 namespace rs {
 
 constexpr int kThreads = 384;       // 12 warps
+// Plans with a 128- or 256-row activation tile fed by TMA (the large-M
+// GEMMs) bring each stage's scale atoms into tensor memory with tcgen05.st
+// from four warps of their own (warps 12, 13, 6, 7: lane quarters 0-3), so
+// that the tensor pipe runs only MMAs: as tcgen05.cp from the MMA warp the
+// copies took about a third of the pipe's time at 256 rows.  Those kernels
+// have 448 threads.
+__host__ __device__ constexpr bool sf_by_warps(int bn, bool fused) { return !fused && bn >= 128; }
+__host__ __device__ constexpr int gemm_threads(int bn, bool fused) { return sf_by_warps(bn, fused) ? 448 : kThreads; }
 constexpr int kQuantWarps = 10;     // warps 0-3 and 6-11 quantize in fused plans
 constexpr int kQuantThreads = kQuantWarps * 32;
 constexpr int kMaxStages = 8;
@@ -77,7 +89,7 @@ constexpr int kMaxChunkBars = 64;   // fused plans: one "quantized" mbarrier per
 // barriers (full, empty: kMaxStages each; accumulator, reduction and receive
 // pairs; the chunk barriers; the amax barrier), then the amax slots, the
 // tensor-memory slot and the flags: all before the scale table's 1 KB
-static_assert((2 * kMaxStages + 8 + kMaxChunkBars + 1) * 8 + (kMaxSplits + 1 + 5) * 4 <= 1024,
+static_assert((3 * kMaxStages + 8 + kMaxChunkBars + 1) * 8 + (kMaxSplits + 1 + 5) * 4 <= 1024,
               "control words overlap the scale table");
 
 __host__ __device__ constexpr int b_atom_tiles(int bn) { return (bn + 127) / 128; }
@@ -132,7 +144,7 @@ struct GemmArgs {
 };
 
 template <int FMT, int BN, bool FUSED>
-__global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
+__global__ void __launch_bounds__(gemm_threads(BN, FUSED), BN >= 128 ? 1 : 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs g) {
     constexpr int APC = weight_atoms_per_block(FMT);
     constexpr int BT = b_atom_tiles(BN);
@@ -141,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     constexpr uint32_t BSTAGE = b_stage_bytes(FMT, BN);
     constexpr int SFA_COLS = sfa_cols(FMT);
     constexpr int SF_COLS = sf_cols_per_stage(FMT, BN);
+    constexpr bool SFW = sf_by_warps(BN, FUSED);
     static_assert(!FUSED || BT == 1, "fused plans keep the activation tile within one scale atom");
 
     extern __shared__ uint8_t smem_raw[];
@@ -160,7 +173,8 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
     uint64_t* recv_free = red_full + 2;            // split-K: every owner's receive buffer free again
     uint64_t* cbar = recv_free + 2;                // fused: chunk i of the slice quantized
     uint64_t* abar = cbar + kMaxChunkBars;         // dynamic tensor scale: every split's slice amax in
-    uint32_t* amax_slot = reinterpret_cast<uint32_t*>(abar + 1);  // [kMaxSplits] slice amax (bf16 |x| bits)
+    uint64_t* sfr = abar + 1;                      // scale warps: stage s's atoms are in tensor memory
+    uint32_t* amax_slot = reinterpret_cast<uint32_t*>(sfr + kMaxStages);  // [kMaxSplits] slice amax (bf16 |x| bits)
     uint32_t* amax_cta = amax_slot + kMaxSplits;   // this CTA's slice amax
     uint32_t* tmem_slot = amax_cta + 1;
     volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -231,6 +245,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
+            if (SFW) mbar_init(smem_u32(&sfr[s]), 4);  // one arrival per scale warp
         }
         // every scale block of chunk i (all token rows) arrives once
         if (FUSED)
@@ -276,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
         // before any quantizer (ours or, with CTA pairs, the partner's after the
         // cluster barrier below) stores codes, and visible to the tensor pipe.
         const uint32_t bbytes = (uint32_t)nck * BSTAGE;
-        for (uint32_t off = threadIdx.x * 16u; off < bbytes; off += (uint32_t)kThreads * 16u)
+        for (uint32_t off = threadIdx.x * 16u; off < bbytes; off += (uint32_t)gemm_threads(BN, FUSED) * 16u)
             *reinterpret_cast<uint4*>(bregion + off) = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
@@ -401,6 +416,8 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
             const int nb_tiles = min(BT, g.b_row_tiles - b_tile_of(j) * BT);
             for (int i = 0; i < nck; ++i, ++u) {
                 bool landed = mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err);
+                // (scale warps: the stage's atoms are in tensor memory)
+                if (SFW) landed = landed && mbar_wait_bounded(smem_u32(&sfr[s]), ph, abort_flag, g.err);
                 if (lane == 0 && (u == 8 || u == 16 || u == 24 || u == 31))
                     RS_TRACE_MARK(g.trace, u == 8 ? 13 : u == 16 ? 14 : u == 24 ? 28 : 30);
                 // fused plans: chunk i of the activation slice is quantized
@@ -429,11 +446,13 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 const bool a_sf = u >= npre;  // weight scales not yet in tensor memory
                 if (elect_one_sync()) {
                     if (whole) {
+                        if constexpr (!SFW) {
 #pragma unroll
-                        for (int a = 0; a < APC; ++a) {
-                            if (a_sf) tc_cp_sf_atom(tsfa + a * 4, sad + (uint32_t)a * 32u);
-                            for (int t = 0; t < nb_tiles; ++t)
-                                tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sbd + (uint32_t)(t * APC + a) * 32u);
+                            for (int a = 0; a < APC; ++a) {
+                                if (a_sf) tc_cp_sf_atom(tsfa + a * 4, sad + (uint32_t)a * 32u);
+                                for (int t = 0; t < nb_tiles; ++t)
+                                    tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sbd + (uint32_t)(t * APC + a) * 32u);
+                            }
                         }
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
@@ -450,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                         // ragged K tail: the k-steps (and scale atoms) it covers
                         const int nks = (g.K - (c0 + i) * 256 + 63) / 64;
                         const int na = FMT == 0 ? nks : (nks + 1) / 2;
-                        for (int a = 0; a < na; ++a) {
+                        for (int a = 0; !SFW && a < na; ++a) {
                             if (a_sf) tc_cp_sf_atom(tsfa + a * 4, sad + (uint32_t)a * 32u);
                             for (int t = 0; t < nb_tiles; ++t)
                                 tc_cp_sf_atom(tsfb + (a * BT + t) * 4, sbd + (uint32_t)(t * APC + a) * 32u);
@@ -501,6 +520,49 @@ __global__ void __launch_bounds__(kThreads, BN >= 128 ? 1 : 2)
                 tmem_dealloc(tmem, (uint32_t)g.tmem_cols);
                 tmem_freed = true;
                 if (lane == 0) RS_TRACE_MARK(g.trace, 10);
+            }
+        }
+    } else if (SFW && (warp == 6 || warp == 7 || warp >= 12)) {
+        // ------------------------------------------------ scale warps
+        // Once a stage has landed, each warp copies every scale atom of it
+        // (32 rows x 16 bytes) into its lane quarter of the stage's scale
+        // columns: lane l, columns c..c+3 hold row l of the atom, the image
+        // the 32x128b.warpx4 copy gives and the block-scaled MMA reads.  The
+        // columns of stage s are rewritten only after its full barrier, which
+        // the producer re-arms after that stage's previous MMAs are done.
+        const uint32_t tq = tm_sf + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint8_t* sa0 = wring + kWeightCodeBytes + lane * 16;
+        const uint8_t* sb0 = bregion + B_BYTES + lane * 16;
+        int s = 0;
+        uint32_t ph = 0;
+        for (int u = 0; u < nu; ++u) {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&full[s]), ph, abort_flag, g.err))) break;
+            tc_fence_after();
+            const uint32_t col = tq + (uint32_t)(s * SF_COLS);
+            uint32_t ra[4 * APC];  // weight atom a -> columns 4a..4a+3
+#pragma unroll
+            for (int a = 0; a < APC; ++a) {
+                const uint4 v = *reinterpret_cast<const uint4*>(sa0 + (size_t)s * WB + (size_t)a * 512);
+                ra[4 * a] = v.x, ra[4 * a + 1] = v.y, ra[4 * a + 2] = v.z, ra[4 * a + 3] = v.w;
+            }
+            uint32_t rb[4 * APC * BT];  // activation atom (a, t) -> columns SFA_COLS + 4 (a BT + t)
+#pragma unroll
+            for (int a = 0; a < APC; ++a)
+#pragma unroll
+                for (int t = 0; t < BT; ++t) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(sb0 + (size_t)s * BSTAGE + (size_t)(t * APC + a) * 512);
+                    const int c = 4 * (a * BT + t);
+                    rb[c] = v.x, rb[c + 1] = v.y, rb[c + 2] = v.z, rb[c + 3] = v.w;
+                }
+            tmem_st_cols(col, ra);
+            tmem_st_cols(col + (uint32_t)SFA_COLS, rb);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sfr[s]));
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
             }
         }
     } else {
@@ -1323,7 +1385,7 @@ static cudaError_t launch_typed(const GemmPlan& p, const CUtensorMap& tb, const 
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)p.grid_x, 1u, (unsigned)p.splits);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)gemm_threads(BN, FUSED), 1, 1);
     cfg.dynamicSmemBytes = p.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
