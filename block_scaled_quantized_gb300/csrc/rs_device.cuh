@@ -311,6 +311,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// The same 2-D load multicast to the CTAs of `mask` in the cluster: the box
+// lands at the same shared-memory offset in each, and each one's mbarrier at
+// the offset of `bar` receives the completed bytes.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar, int x, int y,
+                                               uint16_t mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(policy)
+        : "memory");
+}
+
+// Bulk copy global -> shared multicast to the CTAs of `mask` (same offsets).
+__device__ __forceinline__ void bulk_load_mc(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                             uint16_t mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4, %5;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "h"(mask), "l"(policy)
+        : "memory");
+}
+
 // Non-tensor bulk copy global -> shared (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar, uint64_t policy) {
@@ -426,6 +448,14 @@ __device__ __forceinline__ void mma_mxfp4(uint32_t d_tmem, uint64_t adesc, uint6
 
 // Arrive on `bar` once all previously issued tcgen05 async operations of
 // this thread have completed.
+// Arrive on `bar` at the same offset in each CTA of `mask` once this
+// thread's earlier tcgen05 operations are done.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

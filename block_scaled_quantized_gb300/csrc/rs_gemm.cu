@@ -64,6 +64,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include "rs_device.cuh"
 #include "rs_internal.h"
@@ -141,6 +142,9 @@ struct GemmArgs {
     int tmem_cols;
     int dyn_alpha;          // fused NVFP4: the tensor scale of X is computed here (alpha_x unused)
     int qpair;              // fused: CTA pairs (x, x ^ 1) share the quantization of their K slice
+    int mcast;              // scale-warp plans without split: CTA pairs (x, x ^ 1) of a cluster take
+                            // neighbouring channel tiles of one activation tile, each loading half of
+                            // it for both by multicast
 };
 
 template <int FMT, int BN, bool FUSED>
@@ -193,6 +197,9 @@ __global__ void __launch_bounds__(gemm_threads(BN, FUSED), BN >= 128 ? 1 : 2)
     const int split = blockIdx.z;
     // Cluster ranks: (x % 2) + 2 z with CTA pairs sharing a K slice, else z.
     const bool qpair = FUSED && g.qpair != 0;
+    // activation tile shared by multicast: cluster rank = x % 2
+    const bool mcast = SFW && g.mcast != 0;
+    const uint32_t mrank = blockIdx.x & 1u;
     const uint32_t px = qpair ? (blockIdx.x & 1u) : 0u;
     auto krank = [&](uint32_t p) -> uint32_t { return qpair ? px + 2u * p : p; };  // split p, our pair slot
     const int nranks = qpair ? 2 * g.splits : g.splits;
@@ -244,7 +251,7 @@ __global__ void __launch_bounds__(gemm_threads(BN, FUSED), BN >= 128 ? 1 : 2)
         RS_TRACE_MARK(g.trace, 31);
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&empty[s]), mcast ? 2 : 1);  // (multicast: both CTAs' MMAs)
             if (SFW) mbar_init(smem_u32(&sfr[s]), 4);  // one arrival per scale warp
         }
         // every scale block of chunk i (all token rows) arrives once
@@ -309,7 +316,8 @@ __global__ void __launch_bounds__(gemm_threads(BN, FUSED), BN >= 128 ? 1 : 2)
     const uint32_t tm_sf = tmem + (uint32_t)(nacc * BN);
     // split-K partners copy into our receive buffers and signal red_full:
     // every barrier of the cluster must be initialised before that
-    if (g.splits > 1 || qpair) cluster_sync_all();
+    // (multicast: the partner writes into our stages and arrives on our barriers)
+    if (g.splits > 1 || qpair || mcast) cluster_sync_all();
 
     // Dependents may start their prologue now; they wait for our completion
     // before they touch anything we read or write.
@@ -328,6 +336,25 @@ __global__ void __launch_bounds__(gemm_threads(BN, FUSED), BN >= 128 ? 1 : 2)
             uint8_t* st = bregion + (size_t)s * BSTAGE;
             const uint32_t fb = smem_u32(&full[s]);
             const int na = min(APC, g.n_atoms_k - chunk * APC);
+            if (mcast) {
+                // our half of the rows and our share of the scale atoms, to
+                // both CTAs (each CTA's full barrier expects the whole stage)
+                tma_load_2d_mc(smem_u32(st) + mrank * (B_BYTES / 2), &tmap_b, fb, chunk * 128,
+                               bt * BN + (int)mrank * (BN / 2), (uint16_t)3, pol_x);
+                if (BT == 2) {
+                    if ((int)mrank < nb_tiles)
+                        bulk_load_mc(smem_u32(st + B_BYTES + mrank * (uint32_t)APC * 512u),
+                                     g.sfb + ((size_t)(bt * BT + (int)mrank) * g.n_atoms_k + (size_t)chunk * APC) * 512,
+                                     (uint32_t)na * 512u, fb, (uint16_t)3, pol_x);
+                } else {
+                    const int a0 = (int)mrank * (APC / 2), a1 = min(na, a0 + APC / 2);
+                    if (a1 > a0)
+                        bulk_load_mc(smem_u32(st + B_BYTES + (uint32_t)a0 * 512u),
+                                     g.sfb + ((size_t)(bt * BT) * g.n_atoms_k + (size_t)chunk * APC + a0) * 512,
+                                     (uint32_t)(a1 - a0) * 512u, fb, (uint16_t)3, pol_x);
+                }
+                return;
+            }
             tma_load_2d(smem_u32(st), &tmap_b, fb, chunk * 128, bt * BN, pol_x);
             for (int t = 0; t < nb_tiles; ++t)
                 bulk_load(smem_u32(st + B_BYTES + (uint32_t)t * APC * 512u),
@@ -485,7 +512,10 @@ __global__ void __launch_bounds__(gemm_threads(BN, FUSED), BN >= 128 ? 1 : 2)
                                           tsfa + (ks >> 1) * 4, tsfb + (ks >> 1) * BT * 4, accum);
                         }
                     }
-                    tc_commit(smem_u32(&empty[s]));
+                    // multicast: the stage is free once both CTAs' MMAs are done
+                    // (the last S units' stages are never refilled: local only)
+                    if (mcast && u + S < nu) tc_commit_mc(smem_u32(&empty[s]), (uint16_t)3);
+                    else tc_commit(smem_u32(&empty[s]));
                 }
                 __syncwarp();
                 if (++s == S) {
@@ -1090,6 +1120,8 @@ __global__ void __launch_bounds__(gemm_threads(BN, FUSED), BN >= 128 ? 1 : 2)
         tmem_dealloc(tmem, (uint32_t)g.tmem_cols);
         if (lane == 0) RS_TRACE_MARK(g.trace, 10);
     }
+    // multicast: neither CTA leaves while the other may still write into it
+    if (mcast) cluster_sync_all();
 }
 
 // Separate Fold (Sec. 4.3 Eq. 2) for the on-chip Fold ablation (Sec. 5.1,
@@ -1379,6 +1411,56 @@ static cudaError_t ensure_smem_attr() {
     return e;
 }
 
+// The kernels with scale warps (TMA-fed, 128- or 256-row activation tiles).
+static const void* scale_warp_kernel(int fmt, int bn) {
+    if (fmt == 0) return bn == 256 ? (const void*)gemm_kernel<0, 256, false> : (const void*)gemm_kernel<0, 128, false>;
+    return bn == 256 ? (const void*)gemm_kernel<1, 256, false> : (const void*)gemm_kernel<1, 128, false>;
+}
+
+// Clusters of two CTAs of `func` that can be resident at once on the current
+// device (0 when none), per device and shared-memory size.
+static int pair_clusters_resident(const void* func, size_t smem, int threads) {
+    static std::mutex mu;
+    static int cache_dev[16] = {};
+    static size_t cache_smem[16] = {};
+    static const void* cache_fn[16] = {};
+    static int cache_n[16] = {};
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache_dev[i] == dev && cache_smem[i] == smem && cache_fn[i] == func) return cache_n[i];
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2u, 1u, 1u);
+    cfg.blockDim = dim3((unsigned)threads, 1u, 1u);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (used < 16) {
+        cache_dev[used] = dev;
+        cache_smem[used] = smem;
+        cache_fn[used] = func;
+        cache_n[used] = n;
+        ++used;
+    }
+    return n;
+}
+
 template <int FMT, int BN, bool FUSED>
 static cudaError_t launch_typed(const GemmPlan& p, const CUtensorMap& tb, const GemmArgs& args, cudaStream_t stream) {
     cudaError_t e = ensure_smem_attr<FMT, BN, FUSED>();
@@ -1393,9 +1475,9 @@ static cudaError_t launch_typed(const GemmPlan& p, const CUtensorMap& tb, const 
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
-    if (p.splits > 1 || p.qpair) {
+    if (p.splits > 1 || p.qpair || args.mcast) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = p.qpair ? 2 : 1;
+        attr[na].val.clusterDim.x = (p.qpair || args.mcast) ? 2 : 1;
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = (unsigned)p.splits;
         ++na;
@@ -1431,9 +1513,26 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
         return launch_gemm_pair(p.fmt, p.M, p.Rb, p.N, p.K, p.fold, c.xq, c.wq, c.alpha_x, c.alpha_w, c.y, c.out_f32,
                                 c.err, trace, sms, stream);
     }
+    // Scale-warp plans without split whose channel tiles pair up share each
+    // activation tile between the two CTAs of a cluster (multicast), on a
+    // persistent grid of the pair clusters that fit at once.  Prefill GEMM
+    // (M = 4096, K = N = 8192): 123.8 -> 116.2 us W4A4, 229.6 -> 212.2 us
+    // compensated.
+    GemmPlan q = p;
+    int mcast = 0;
+    if (sf_by_warps(q.bn, q.fused != 0) && q.splits == 1 && q.n_tiles % 2 == 0 && q.grid_x >= 2 &&
+        q.n_tiles * q.b_tiles >= 2 * q.grid_x) {  // (at least two tiles per CTA: one measured slower)
+        const int pairs = pair_clusters_resident(scale_warp_kernel(q.fmt, q.bn), q.smem_bytes,
+                                                 gemm_threads(q.bn, false));
+        const int grid = std::min(q.grid_x / 2, pairs) * 2;
+        if (grid >= 2) {
+            q.grid_x = grid;
+            mcast = 1;
+        }
+    }
     alignas(64) CUtensorMap tb;
     std::memset(&tb, 0, sizeof tb);
-    if (!p.fused && !encode_codes_map(&tb, c.xq, p.Rb, p.K, p.bn)) return cudaErrorInvalidValue;
+    if (!q.fused && !encode_codes_map(&tb, c.xq, q.Rb, q.K, mcast ? q.bn / 2 : q.bn)) return cudaErrorInvalidValue;
     GemmArgs a{};
     a.wq = static_cast<const uint8_t*>(c.wq);
     a.x = static_cast<const uint16_t*>(c.x);
@@ -1468,8 +1567,9 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
     a.dyn_alpha = c.dyn_alpha;
     a.qpair = p.fused ? p.qpair : 0;
     a.qdump = p.fused ? static_cast<uint8_t*>(c.qdump) : nullptr;
+    a.mcast = mcast;
 #define RS_CASE(F, B, FU)                                                      \
-    if (p.fmt == F && p.bn == B && (p.fused != 0) == FU) return launch_typed<F, B, FU>(p, tb, a, stream);
+    if (q.fmt == F && q.bn == B && (q.fused != 0) == FU) return launch_typed<F, B, FU>(q, tb, a, stream);
     RS_CASE(0, 16, true) RS_CASE(0, 32, true) RS_CASE(1, 16, true) RS_CASE(1, 32, true)
     RS_CASE(0, 16, false) RS_CASE(0, 32, false) RS_CASE(0, 64, false) RS_CASE(0, 128, false) RS_CASE(0, 256, false)
     RS_CASE(1, 16, false) RS_CASE(1, 32, false) RS_CASE(1, 64, false) RS_CASE(1, 128, false) RS_CASE(1, 256, false)
