@@ -20,9 +20,9 @@
 //    kind::mxf4nvf4 block-scaled MMA reads them: with tcgen05.cp
 //    (32x128b.warpx4, issued by the MMA warp ahead of the MMAs that read
 //    them; in fused plans the weight atoms of the prefetched stages are
-//    copied before the dependency wait), or, for 128- and 256-row activation
-//    tiles, with tcgen05.st from four scale warps, which keeps the copies out
-//    of the tensor pipe.
+//    copied before the dependency wait), or, for 256-row activation tiles,
+//    with tcgen05.st from four scale warps, which keeps the copies out of the
+//    tensor pipe.
 //
 // Fold (Sec. 4.3 Eq. 2): with paired rows, the base and residue products of
 // token j are accumulator columns 2j and 2j+1; a 32x32b tensor-memory load
@@ -54,9 +54,9 @@
 // Warp roles (384 threads): warp 4 bulk/TMA producer; warp 5 TMEM allocator,
 // scale copies and MMA issuer; warps 8-11 (lane quarters 0-3) run the
 // epilogue, with warps 0-3 for wide tiles without split-K; in fused plans
-// warps 0-3 and 6-11 first run the quantizing prologue.  Kernels for 128-
-// and 256-row activation tiles have 448 threads: warps 12, 13, 6 and 7 move
-// the scale atoms, and warp 5 only issues MMAs.  Every wait is
+// warps 0-3 and 6-11 first run the quantizing prologue.  Kernels for
+// 256-row activation tiles have 448 threads: warps 12, 13, 6 and 7 move the
+// scale atoms, and warp 5 only issues MMAs.  Every wait is
 // bounded (about one second); a wait that runs out sets the device error
 // word and an abort flag, and the CTA drains its copies and exits.
 #include <cuda.h>
@@ -73,13 +73,14 @@
 namespace rs {
 
 constexpr int kThreads = 384;       // 12 warps
-// Plans with a 128- or 256-row activation tile fed by TMA (the large-M
-// GEMMs) bring each stage's scale atoms into tensor memory with tcgen05.st
-// from four warps of their own (warps 12, 13, 6, 7: lane quarters 0-3), so
-// that the tensor pipe runs only MMAs: as tcgen05.cp from the MMA warp the
-// copies took about a third of the pipe's time at 256 rows.  Those kernels
-// have 448 threads.
-__host__ __device__ constexpr bool sf_by_warps(int bn, bool fused) { return !fused && bn >= 128; }
+// Plans with a 256-row activation tile fed by TMA (the large-M GEMMs) bring
+// each stage's scale atoms into tensor memory with tcgen05.st from four
+// warps of their own (warps 12, 13, 6, 7: lane quarters 0-3), so that the
+// tensor pipe runs only MMAs: as tcgen05.cp from the MMA warp the twelve
+// copies per chunk took about a third of the pipe's time.  With 128-row tiles
+// (six or eight copies per chunk) the extra hand-off per stage cost more than
+// it saved, so those keep tcgen05.cp.  These kernels have 448 threads.
+__host__ __device__ constexpr bool sf_by_warps(int bn, bool fused) { return !fused && bn >= 256; }
 __host__ __device__ constexpr int gemm_threads(int bn, bool fused) { return sf_by_warps(bn, fused) ? 448 : kThreads; }
 constexpr int kQuantWarps = 10;     // warps 0-3 and 6-11 quantize in fused plans
 constexpr int kQuantThreads = kQuantWarps * 32;
@@ -1411,10 +1412,9 @@ static cudaError_t ensure_smem_attr() {
     return e;
 }
 
-// The kernels with scale warps (TMA-fed, 128- or 256-row activation tiles).
-static const void* scale_warp_kernel(int fmt, int bn) {
-    if (fmt == 0) return bn == 256 ? (const void*)gemm_kernel<0, 256, false> : (const void*)gemm_kernel<0, 128, false>;
-    return bn == 256 ? (const void*)gemm_kernel<1, 256, false> : (const void*)gemm_kernel<1, 128, false>;
+// The kernels with scale warps (TMA-fed, 256-row activation tiles).
+static const void* scale_warp_kernel(int fmt) {
+    return fmt == 0 ? (const void*)gemm_kernel<0, 256, false> : (const void*)gemm_kernel<1, 256, false>;
 }
 
 // Clusters of two CTAs of `func` that can be resident at once on the current
@@ -1522,7 +1522,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
     int mcast = 0;
     if (sf_by_warps(q.bn, q.fused != 0) && q.splits == 1 && q.n_tiles % 2 == 0 && q.grid_x >= 2 &&
         q.n_tiles * q.b_tiles >= 2 * q.grid_x) {  // (at least two tiles per CTA: one measured slower)
-        const int pairs = pair_clusters_resident(scale_warp_kernel(q.fmt, q.bn), q.smem_bytes,
+        const int pairs = pair_clusters_resident(scale_warp_kernel(q.fmt), q.smem_bytes,
                                                  gemm_threads(q.bn, false));
         const int grid = std::min(q.grid_x / 2, pairs) * 2;
         if (grid >= 2) {
