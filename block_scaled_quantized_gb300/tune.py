@@ -19,6 +19,8 @@ tuned row count and not to a larger one.
     python -m block_scaled_quantized_gb300.tune            # full table (a few minutes)
     python -m block_scaled_quantized_gb300.tune --quick    # a handful of shapes, printed only
     python -m block_scaled_quantized_gb300.tune --from-log LOG   # table from an earlier run's --log
+    python -m block_scaled_quantized_gb300.tune --min-rows 64    # re-tune the cases of at least 64
+                                                                 # activation rows, keep the other rows
 """
 from __future__ import annotations
 
@@ -203,6 +205,25 @@ LOG_LINE = re.compile(r"fmt=(\d) comp=(\d) M=(\d+) N=(\d+) K=(\d+) sms=(\d+): an
                       r"best ([\d.]+) us \((\d+), (\d), (\d+)(?:, (\d))?\)( analytic)?")
 
 
+TABLE_LINE = re.compile(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+)\},  "
+                        r"// ([\d.]+) us \(analytic plan(?: ([\d.]+) us)?\)")
+
+
+def rows_from_table(path):
+    """The rows of a table written by write_table (placeholder row excluded)."""
+    rows, sms = [], None
+    for line in open(path):
+        m = TABLE_LINE.match(line)
+        if not m or int(m.group(3)) == 0:
+            continue
+        fmt, comp, M, N, K, sms, sp, fu, bn, deep = (int(v) for v in m.groups()[:10])
+        us = float(m.group(11))
+        kept = m.group(12) is None
+        base = us if kept else float(m.group(12))
+        rows.append((fmt, comp, M, N, K, (sp, fu, bn, deep), us, base, kept))
+    return sms, rows
+
+
 def rows_from_log(path):
     rows, sms = [], None
     for line in open(path):
@@ -224,6 +245,9 @@ def main(argv=None):
     ap.add_argument("--out", default=os.path.join(HERE, "csrc", "rs_tactics_gb300.inc"))
     ap.add_argument("--log", default=None, help="also write one line per tuned case to this file")
     ap.add_argument("--from-log", default=None, help="write the table from an earlier run's --log (no GPU)")
+    ap.add_argument("--min-rows", type=int, default=0,
+                    help="tune only the cases with at least this many activation rows (2M compensated, M "
+                         "plain) and keep the table's other rows")
     a = ap.parse_args(argv)
     build.build()
     if a.from_log:
@@ -234,10 +258,20 @@ def main(argv=None):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     t0 = time.time()
     rows, log = [], []
+    kept_rows = {}
+    if a.min_rows > 0 and os.path.exists(a.out):
+        _, old = rows_from_table(a.out)
+        kept_rows = {r[:5]: r for r in old}
     for fmt, N, K, Ms in tuning_set(a.quick):
-        shape = Shape(fmt, N, K)
+        shape = None
         for M in Ms:
             for comp in (False, True):
+                key = (fmt, int(comp), M, N, K)
+                if (2 * M if comp else M) < a.min_rows and key in kept_rows:
+                    rows.append(kept_rows[key])
+                    continue
+                if shape is None:
+                    shape = Shape(fmt, N, K)
                 t, us, base, n, kept = tune_one(shape, M, comp, sms, a.margin)
                 line = (f"fmt={fmt} comp={int(comp)} M={M} N={N} K={K} sms={sms}: analytic {base:.3f} us, "
                         f"best {us:.3f} us ({t[0]}, {t[1]}, {t[2]}, {t[3]}){' analytic' if kept else ''} over {n} plans")
