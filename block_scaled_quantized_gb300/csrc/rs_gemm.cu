@@ -338,22 +338,16 @@ __global__ void __launch_bounds__(gemm_threads(BN, FUSED), BN >= 128 ? 1 : 2)
             const uint32_t fb = smem_u32(&full[s]);
             const int na = min(APC, g.n_atoms_k - chunk * APC);
             if (mcast) {
-                // our half of the rows and our share of the scale atoms, to
-                // both CTAs (each CTA's full barrier expects the whole stage)
+                // our half of the 256 rows and its atom tile (if the operand
+                // has one there), to both CTAs (each CTA's full barrier
+                // expects the whole stage)
+                static_assert(!SFW || BT == 2, "scale-warp plans have 256-row tiles");
                 tma_load_2d_mc(smem_u32(st) + mrank * (B_BYTES / 2), &tmap_b, fb, chunk * 128,
                                bt * BN + (int)mrank * (BN / 2), (uint16_t)3, pol_x);
-                if (BT == 2) {
-                    if ((int)mrank < nb_tiles)
-                        bulk_load_mc(smem_u32(st + B_BYTES + mrank * (uint32_t)APC * 512u),
-                                     g.sfb + ((size_t)(bt * BT + (int)mrank) * g.n_atoms_k + (size_t)chunk * APC) * 512,
-                                     (uint32_t)na * 512u, fb, (uint16_t)3, pol_x);
-                } else {
-                    const int a0 = (int)mrank * (APC / 2), a1 = min(na, a0 + APC / 2);
-                    if (a1 > a0)
-                        bulk_load_mc(smem_u32(st + B_BYTES + (uint32_t)a0 * 512u),
-                                     g.sfb + ((size_t)(bt * BT) * g.n_atoms_k + (size_t)chunk * APC + a0) * 512,
-                                     (uint32_t)(a1 - a0) * 512u, fb, (uint16_t)3, pol_x);
-                }
+                if ((int)mrank < nb_tiles)
+                    bulk_load_mc(smem_u32(st + B_BYTES + mrank * (uint32_t)APC * 512u),
+                                 g.sfb + ((size_t)(bt * BT + (int)mrank) * g.n_atoms_k + (size_t)chunk * APC) * 512,
+                                 (uint32_t)na * 512u, fb, (uint16_t)3, pol_x);
                 return;
             }
             tma_load_2d(smem_u32(st), &tmap_b, fb, chunk * 128, bt * BN, pol_x);
