@@ -223,7 +223,8 @@ int rs_plan_linear(rs_format fmt, int compensated, int M, int N, int K, int num_
     const GemmPlan p = make_gemm_plan(fmt, compensated != 0, M, N, K, num_sms, x_in_call != 0);
     const int fused = p.fused ? (p.qpair ? 2 : 1) : 0;
     const int v[] = {p.bn,  p.n_tiles, p.b_tiles, p.chunks,    p.splits,          p.grid_x, p.stages,
-                     fused, p.slots,   p.nacc,    p.tmem_cols, (int)p.smem_bytes, p.tuned};
+                     fused, p.slots,   p.nacc,    p.tmem_cols, (int)p.smem_bytes, p.tuned,
+                     multicast_eligible(p) ? 1 : 0};
     const int n = n_out < (int)(sizeof(v) / sizeof(v[0])) ? n_out : (int)(sizeof(v) / sizeof(v[0]));
     for (int i = 0; i < n; ++i) out[i] = v[i];
     return n;

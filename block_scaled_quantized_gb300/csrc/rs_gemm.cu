@@ -1406,6 +1406,12 @@ static cudaError_t ensure_smem_attr() {
     return e;
 }
 
+bool multicast_eligible(const GemmPlan& p) {
+    // (with one tile per CTA the pair's lock step measured slower)
+    return sf_by_warps(p.bn, p.fused != 0) && p.splits == 1 && p.n_tiles % 2 == 0 && p.grid_x >= 2 &&
+           p.n_tiles * p.b_tiles >= 2 * p.grid_x;
+}
+
 // The kernels with scale warps (TMA-fed, 256-row activation tiles).
 static const void* scale_warp_kernel(int fmt) {
     return fmt == 0 ? (const void*)gemm_kernel<0, 256, false> : (const void*)gemm_kernel<1, 256, false>;
@@ -1514,8 +1520,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const GemmCall& c, cudaStream_t strea
     // compensated.
     GemmPlan q = p;
     int mcast = 0;
-    if (sf_by_warps(q.bn, q.fused != 0) && q.splits == 1 && q.n_tiles % 2 == 0 && q.grid_x >= 2 &&
-        q.n_tiles * q.b_tiles >= 2 * q.grid_x) {  // (at least two tiles per CTA: one measured slower)
+    if (multicast_eligible(q)) {
         const int pairs = pair_clusters_resident(scale_warp_kernel(q.fmt), q.smem_bytes,
                                                  gemm_threads(q.bn, false));
         const int grid = std::min(q.grid_x / 2, pairs) * 2;

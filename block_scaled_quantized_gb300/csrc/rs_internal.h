@@ -61,6 +61,12 @@ constexpr int kMaxSplits = 8;   // portable thread-block cluster size
 // small-M plans may quantize inside the GEMM.  A measured tactic for the
 // shape (below) takes precedence over the analytic choice when its plan fits.
 GemmPlan make_gemm_plan(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused);
+// Whether a plan shares each activation tile between the two CTAs of a
+// cluster by multicast: 256-row activation tiles fed by TMA, no K split, an
+// even number of channel tiles and at least two output tiles per CTA.  (A
+// launch also needs two pair clusters resident at once, else it runs the
+// plan without multicast.)
+bool multicast_eligible(const GemmPlan& p);
 // The analytic plan alone (what make_gemm_plan gives without a tactic).
 GemmPlan make_gemm_plan_analytic(int fmt, bool fold, int M, int N, int K, int num_sms, bool allow_fused);
 

@@ -150,7 +150,7 @@ def rs_debug_wait_probe(limit_ns: int, stream=None):
 
 
 PLAN_FIELDS = ("bn", "n_tiles", "b_tiles", "chunks", "splits", "grid_x", "stages", "fused", "slots", "nacc",
-               "tmem_cols", "smem_bytes", "tuned")
+               "tmem_cols", "smem_bytes", "tuned", "mcast")
 
 
 def rs_plan_linear(fmt: int, compensated: bool, M: int, N: int, K: int, num_sms: int, x_in_call: bool = True) -> dict:

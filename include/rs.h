@@ -148,8 +148,10 @@ RS_API size_t rs_workspace_bytes(rs_format fmt, int M, int N, int K, int compens
  * size), grid_x (persistent CTAs per split), stages (weight ring depth),
  * fused (1: quantized inside the GEMM), slots, nacc (accumulator buffers),
  * tmem_cols, smem_bytes (dynamic shared memory per CTA), tuned (1: a
- * measured tactic below chose splits, fused and bn).  Returns the number
- * written, or minus an rs_status code on bad arguments. */
+ * measured tactic below chose splits, fused and bn), mcast (1: the two CTAs
+ * of a cluster share each 256-row activation tile by multicast, when two
+ * such clusters fit at once on the GPU).  Returns the number written, or
+ * minus an rs_status code on bad arguments. */
 RS_API int rs_plan_linear(rs_format fmt, int compensated, int M, int N, int K, int num_sms, int x_in_call,
                           int *out, int n_out);
 

@@ -101,3 +101,25 @@ def test_plan_rejects_bad_arguments():
         rs.rs_plan_linear(0, True, 8, 4096, 100, 152)
     with pytest.raises(rs.RsError):
         rs.rs_plan_linear(3, True, 8, 4096, 4096, 152)
+
+
+def test_multicast_rule(tactics):
+    """The activation tile is shared by multicast only by 256-row TMA-fed
+    plans without K split, with an even number of channel tiles and at least
+    two output tiles per CTA; every other plan loads its own."""
+    for sms in (152, 148, 132):
+        for fmt, comp, M, N, K in [(0, False, 4096, 8192, 8192), (0, True, 4096, 8192, 8192),
+                                   (1, True, 512, 27648, 5120), (0, False, 1024, 4096, 4096),
+                                   (1, True, 128, 27648, 5120), (0, True, 64, 4096, 4096),
+                                   (0, True, 8, 4096, 4096), (0, False, 4096, 8320, 8192)]:
+            p = rs.rs_plan_linear(fmt, comp, M, N, K, sms)
+            tiles = p["n_tiles"] * p["b_tiles"]
+            want = (p["bn"] == 256 and not p["fused"] and p["splits"] == 1 and p["n_tiles"] % 2 == 0
+                    and tiles >= 2 * p["grid_x"])
+            assert p["mcast"] == int(want), (fmt, comp, M, N, K, sms, p)
+    # the prefill shape shares it; one tile per CTA (W4A4 M = 1024, K = N = 4096:
+    # 128 tiles) and an odd channel-tile count (N = 8320) do not
+    assert rs.rs_plan_linear(0, False, 4096, 8192, 8192, 152)["mcast"] == 1
+    assert rs.rs_plan_linear(0, True, 4096, 8192, 8192, 152)["mcast"] == 1
+    assert rs.rs_plan_linear(0, False, 1024, 4096, 4096, 152)["mcast"] == 0
+    assert rs.rs_plan_linear(0, False, 4096, 8320, 8192, 152)["mcast"] == 0
