@@ -204,3 +204,21 @@ def test_pair_tactic_pairs_only_where_the_grid_allows():
     rs.rs_set_tactic(0, True, 8, 384, 4096, SMS, 4, 2, 16)
     assert plan(0, True, 8, 384, 4096)["fused"] == 1           # 3 CTAs per split
     assert plan(0, True, 8, 4096, 4096, x_in_call=False)["fused"] == 0
+
+
+def test_shipped_table_round_trips_through_the_tuner(tmp_path):
+    """tune.py --min-rows reads the shipped table back to keep the rows it does
+    not re-measure: parsing and writing it again gives the same file, and the
+    rows it would keep for --min-rows 64 are exactly those under 64 rows."""
+    import os
+    src = os.path.join(os.path.dirname(tune.__file__), "csrc", "rs_tactics_gb300.inc")
+    sms, rows = tune.rows_from_table(src)
+    assert sms == SMS and len(rows) == sum(1 for line in open(src) if line.startswith("{")) - 1
+    out = tmp_path / "table.inc"
+    tune.write_table(str(out), sms, rows)
+    assert out.read_text() == open(src).read()
+    kept = [r for r in rows if (2 * r[2] if r[1] else r[2]) < 64]
+    assert kept and all((2 * r[2] if r[1] else r[2]) < 64 for r in kept)
+    retuned = sum(1 for _, _, _, Ms in tune.tuning_set(False) for M in Ms for comp in (0, 1)
+                  if (2 * M if comp else M) >= 64)
+    assert len(kept) + retuned == len(rows)
